@@ -1,0 +1,140 @@
+"""Seeded synthetic operands for C = A*B.
+
+This module only draws random numbers and lays them out; it holds none of the
+product's arithmetic.  The CUDA path (through the C ABI) and the CPU oracle
+both consume exactly the tensors made here.
+
+Recipe (the pages give seeds and distributions but no generator):
+  * ``g = torch.Generator("cpu").manual_seed(seed)``;
+  * A's M x K values are drawn first, then B's values in its storage
+    orientation (K x N for layout KN, N x K for layout NK), both in float32;
+  * uniform(a, b) is ``a + (b - a) * torch.rand``; normal(mu, sigma) is
+    ``mu + sigma * torch.randn``; ints(lo, hi) is ``torch.randint(lo, hi + 1)``;
+  * the float32 draws are rounded to FP16/BF16 with ``Tensor.to`` (RNE);
+  * a leading dimension larger than the row length pads each row; the pad
+    holds ``pad_value`` (NaN by default for the poison tests), never data.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+F16, BF16, F32 = 0, 1, 2
+B_KN, B_NK = 0, 1
+
+TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}
+DTYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32"}
+DTYPE_SIZE = {F16: 2, BF16: 2, F32: 4}
+
+
+@dataclass(frozen=True)
+class Dist:
+    """A value distribution: kind in {"uniform", "normal", "ints"}."""
+    kind: str
+    a: float
+    b: float
+
+    def draw(self, shape, g: torch.Generator) -> torch.Tensor:
+        if self.kind == "uniform":
+            return self.a + (self.b - self.a) * torch.rand(shape, generator=g, dtype=torch.float32)
+        if self.kind == "normal":
+            return self.a + self.b * torch.randn(shape, generator=g, dtype=torch.float32)
+        if self.kind == "ints":
+            return torch.randint(int(self.a), int(self.b) + 1, shape, generator=g).to(torch.float32)
+        raise ValueError("unknown distribution %r" % (self.kind,))
+
+
+def uniform(a: float, b: float) -> Dist:
+    return Dist("uniform", a, b)
+
+
+def normal(mu: float, sigma: float) -> Dist:
+    return Dist("normal", mu, sigma)
+
+
+def ints(lo: int, hi: int) -> Dist:
+    return Dist("ints", lo, hi)
+
+
+def _pad(values: torch.Tensor, ld: int, pad_value: float) -> torch.Tensor:
+    rows, cols = values.shape
+    if ld == cols:
+        return values.contiguous()
+    out = torch.full((rows, ld), pad_value, dtype=values.dtype)
+    out[:, :cols] = values
+    return out
+
+
+def make_operands(M: int, N: int, K: int, in_dtype: int, b_layout: int,
+                  dist_a: Dist, dist_b: Optional[Dist], seed: int,
+                  lda: Optional[int] = None, ldb: Optional[int] = None,
+                  pad_value: float = float("nan")) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Seeded CPU operands: A stored M x lda, B stored K x ldb (KN) or N x ldb (NK)."""
+    dist_b = dist_b or dist_a
+    lda = K if lda is None else lda
+    b_rows, b_cols = (K, N) if b_layout == B_KN else (N, K)
+    ldb = b_cols if ldb is None else ldb
+    if lda < K or ldb < b_cols:
+        raise ValueError("leading dimension shorter than the row")
+    g = torch.Generator("cpu").manual_seed(seed)
+    a = dist_a.draw((M, K), g)
+    b = dist_b.draw((b_rows, b_cols), g)
+    t = TORCH_DTYPE[in_dtype]
+    return _pad(a.to(t), lda, pad_value), _pad(b.to(t), ldb, pad_value)
+
+
+def b_logical(B: torch.Tensor, N: int, K: int, b_layout: int) -> torch.Tensor:
+    """The K x N logical view of a stored B (a view, no arithmetic)."""
+    return B[:K, :N] if b_layout == B_KN else B[:N, :K].t()
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One named synthetic GEMM problem."""
+    name: str
+    M: int
+    N: int
+    K: int
+    in_dtype: int
+    out_dtype: int
+    b_layout: int
+    dist_a: Dist
+    dist_b: Dist
+    seed: int
+
+    def operands(self, **kw):
+        return make_operands(self.M, self.N, self.K, self.in_dtype, self.b_layout,
+                             self.dist_a, self.dist_b, self.seed, **kw)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """A and B read once, C written once: the method's minimum traffic."""
+        e_in, e_out = DTYPE_SIZE[self.in_dtype], DTYPE_SIZE[self.out_dtype]
+        return self.M * self.K * e_in + self.K * self.N * e_in + self.M * self.N * e_out
+
+
+# The five problem families the benchmark configuration lists, by shape.
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("gemm_256x256x256_f16_kn_f32", 256, 256, 256, F16, F32, B_KN,
+                 uniform(-1, 1), uniform(-1, 1), 0),
+        Workload("gemm_256x256x256_f16_kn_f32_ints", 256, 256, 256, F16, F32, B_KN,
+                 ints(-2, 2), ints(-2, 2), 0),
+        Workload("gemm_4000x3000x5000_bf16_nk_bf16", 4000, 3000, 5000, BF16, BF16, B_NK,
+                 normal(0, 1), normal(0, 1), 1),
+        Workload("gemm_4096x4096x4096_f16_kn_f16", 4096, 4096, 4096, F16, F16, B_KN,
+                 uniform(-1, 1), uniform(-1, 1), 2),
+        Workload("gemm_8192x8192x8192_f16_nk_f16", 8192, 8192, 8192, F16, F16, B_NK,
+                 uniform(-0.5, 0.5), uniform(-0.5, 0.5), 3),
+        Workload("proj_16384x14336x4096_bf16_nk_bf16", 16384, 14336, 4096, BF16, BF16, B_NK,
+                 normal(0, 1), normal(0, 0.02), 4),
+        Workload("proj_16x4096x4096_bf16_nk_bf16", 16, 4096, 4096, BF16, BF16, B_NK,
+                 normal(0, 1), normal(0, 0.02), 4),
+    ]
+}

@@ -1,0 +1,19 @@
+"""CPU oracle for C = A*B (test infrastructure only).
+
+Only the tests, the package smoke entry and the benchmark's CPU-baseline leg
+may import this package.  The product path never does.
+"""
+from .oracle import (  # noqa: F401
+    build,
+    gemm,
+    gemm_rows,
+    gemm_elements,
+    round_bits,
+    ulp,
+    decode,
+    F16,
+    BF16,
+    F32,
+    B_KN,
+    B_NK,
+)

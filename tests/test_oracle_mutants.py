@@ -1,0 +1,51 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each case compiles a copy of the oracle source with one plausible slip (a
+dropped term, a wrong sign, a transposed or mis-strided operand, an exponent
+bias off by one, ties rounded away from zero, a spacing off by a factor of
+two) and runs the pin suite against it in a child process.  The suite has to
+fail for every mutant.  Everything runs on the CPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "tgemm_oracle.c")
+
+MUTANTS = {
+    "dropped_last_term_nk": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[bcol[k]];",
+                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[bcol[k]];"),
+    "dropped_last_term_kn": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[p->B[k * p->ldb + j]];",
+                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[p->B[k * p->ldb + j]];"),
+    "wrong_sign": ("            s += a * b;\n            r += fabs(a) * fabs(b);\n        }\n    } else {",
+                   "            s -= a * b;\n            r += fabs(a) * fabs(b);\n        }\n    } else {"),
+    "transposed_b_kn": ("p->B[k * p->ldb + j]", "p->B[j * p->ldb + k]"),
+    "wrong_row_nk": ("p->B + j * p->ldb", "p->B + i * p->ldb"),
+    "ignores_lda": ("p->A + i * p->lda", "p->A + i * p->K"),
+    "f16_bias_off_by_one": ("expo - 25); /* 1.frac", "expo - 24); /* 1.frac"),
+    "bf16_fraction_width": ("(frac | 0x80), expo - 134)", "(frac | 0x80), expo - 133)"),
+    "ties_away_from_zero": ("double r = nearbyint(a / q) * q;", "double r = round(a / q) * q;"),
+    "ulp_factor_two": ("return ldexp(1.0, e - p + 1);", "return ldexp(1.0, e - p);"),
+    "bound_signed": ("r += fabs(a) * fabs(b);\n        }\n    } else {", "r += a * fabs(b);\n        }\n    } else {"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor missing: %s" % name
+    mutated = src.replace(old, new, 1)
+    c_path = tmp_path / "mutant.c"
+    so_path = tmp_path / "libmutant.so"
+    c_path.write_text(mutated)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so_path), str(c_path),
+                    "-lpthread", "-lm"], check=True)
+    env = dict(os.environ, TGEMM_ORACLE_LIB=str(so_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "pins did not catch mutant %s:\n%s" % (name, r.stdout[-2000:])

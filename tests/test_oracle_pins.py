@@ -1,0 +1,310 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test ties one oracle routine to what the pages or the mathematics fix:
+exact rational brute force (the defining sum of "Writing high-performance
+matrix multiplication with NVIDIA CUDA Tile", "What is matrix
+multiplication?"), identity and permutation matrices, integer inputs whose
+result is exact, linearity in B, numpy's float64 matmul, and numpy/torch
+conversions for the decoding, rounding and spacing routines.
+"""
+import math
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from dense_tiled_gemm_persistent_gb300 import inputs as gen
+
+F16, BF16, F32 = 0, 1, 2
+KN, NK = 0, 1
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def exact_value(bits: int, dtype: int) -> Fraction:
+    """Exact value of a 16-bit pattern via the standard library / torch."""
+    if dtype == F16:
+        return Fraction(struct.unpack("<e", struct.pack("<H", bits))[0])
+    f = struct.unpack("<f", struct.pack("<I", bits << 16))[0]   # bf16 = top half of an f32
+    return Fraction(f)
+
+
+def fraction_gemm(A, B, M, N, K, lda, ldb, layout, dtype):
+    """C and the bound as exact rationals, straight from the definition."""
+    a = A.reshape(-1)
+    b = B.reshape(-1)
+    C = [[Fraction(0)] * N for _ in range(M)]
+    R = [[Fraction(0)] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s, r = Fraction(0), Fraction(0)
+            for k in range(K):
+                x = exact_value(int(a[i * lda + k]), dtype)
+                y = exact_value(int(b[k * ldb + j] if layout == KN else b[j * ldb + k]), dtype)
+                s += x * y
+                r += abs(x) * abs(y)
+            C[i][j], R[i][j] = s, r
+    return C, R
+
+
+# --- decoding ------------------------------------------------------------
+
+def test_decode_f16_all_patterns_match_numpy(orc):
+    bits = np.arange(65536, dtype=np.uint32)
+    got = orc.decode(bits, F16)
+    ref = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_decode_bf16_all_patterns_match_torch(orc):
+    bits = np.arange(65536, dtype=np.uint32)
+    got = orc.decode(bits, BF16)
+    ref = torch.from_numpy(bits.astype(np.uint16).view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+# --- rounding to the output format (round-to-nearest-even) ----------------
+
+def _probe_values(rng, lo_exp, hi_exp, n=20000):
+    mant = rng.random(n) + 1.0
+    expo = rng.integers(lo_exp, hi_exp, n)
+    sign = rng.choice([-1.0, 1.0], n)
+    return sign * np.ldexp(mant, expo)
+
+
+def test_round_f16_matches_numpy(orc):
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        _probe_values(rng, -30, 18),
+        # exact ties between neighbouring binary16 values, incl. subnormals and overflow edge
+        (np.arange(-2048, 2048) + 0.5) * 2.0 ** -24,
+        (np.arange(1024, 2048) + 0.5) * 2.0 ** 5,
+        [0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 1e6, np.inf, -np.inf, 2.0 ** -25, 2.0 ** -26],
+    ])
+    got = orc.round_bits(x, F16).astype(np.uint16)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_round_f32_matches_numpy(orc):
+    rng = np.random.default_rng(12)
+    x = np.concatenate([_probe_values(rng, -160, 130),
+                        [0.0, -0.0, 3.4028235677973366e38, 3.5e38, 1e-46, 2.0 ** -150]])
+    got = orc.round_bits(x, F32)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float32).view(np.uint32)
+    assert np.array_equal(got, ref)
+
+
+def test_round_bf16_matches_torch(orc):
+    # float32-representable inputs, so torch's float32 -> bfloat16 rounding is a
+    # single correct rounding of the same value
+    rng = np.random.default_rng(13)
+    x = _probe_values(rng, -140, 127).astype(np.float32)
+    ties = ((np.arange(-256, 256, dtype=np.float64) + 0.5) * 2.0 ** -7).astype(np.float32)
+    x = np.concatenate([x, ties, np.float32([0.0, 3.3895314e38, 3.39e38, 1e-40])])
+    got = orc.round_bits(x.astype(np.float64), BF16).astype(np.uint16)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# --- unit in the last place ------------------------------------------------
+
+def test_ulp_f16_f32_match_numpy_spacing(orc):
+    rng = np.random.default_rng(14)
+    h = rng.integers(1, 0x7BFF, 5000).astype(np.uint16).view(np.float16)   # positive finite
+    assert np.array_equal(orc.ulp(h.astype(np.float64), F16), np.spacing(h).astype(np.float64))
+    f = np.abs(rng.standard_normal(5000).astype(np.float32)) * np.float32(2.0 ** 20)
+    assert np.array_equal(orc.ulp(f.astype(np.float64), F32), np.spacing(f).astype(np.float64))
+    assert orc.ulp(np.array([0.0]), F16)[0] == 2.0 ** -24
+    assert orc.ulp(np.array([0.0]), F32)[0] == 2.0 ** -149
+
+
+def test_ulp_bf16_is_the_gap_to_the_next_pattern(orc):
+    bits = np.arange(1, 0x7F7F, 37, dtype=np.uint32)          # positive finite bf16 patterns
+    v = orc.decode(bits, BF16)
+    gap = orc.decode(bits + 1, BF16) - v
+    assert np.array_equal(orc.ulp(v, BF16), gap)
+
+
+# --- the defining sum, exactly ----------------------------------------------
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_brute_force_rational_exact_inputs(orc, dtype, layout):
+    """Inputs on a 2^-10 grid in [-1, 1): every double sum is exact, so the
+    oracle must equal the rational result bit for bit."""
+    rng = np.random.default_rng(100 + 2 * dtype + layout)
+    for trial in range(6):
+        M, N, K = (int(v) for v in rng.integers(1, 7, 3))
+        lda, ldb = K + int(rng.integers(0, 3)), (N if layout == KN else K) + int(rng.integers(0, 3))
+        t = gen.TORCH_DTYPE[dtype]
+        a = torch.from_numpy(rng.integers(-1024, 1024, (M, lda)) / 1024.0).to(t)
+        b = torch.from_numpy(rng.integers(-1024, 1024, ((K if layout == KN else N), ldb)) / 1024.0).to(t)
+        A, B = bits16(a), bits16(b)
+        C, R = orc.gemm(A, B, M, N, K, lda, ldb, layout, dtype)
+        Cf, Rf = fraction_gemm(A, B, M, N, K, lda, ldb, layout, dtype)
+        for i in range(M):
+            for j in range(N):
+                assert C[i, j] == float(Cf[i][j]) and Fraction(C[i, j]) == Cf[i][j]
+                assert R[i, j] == float(Rf[i][j])
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_brute_force_rational_random_bits(orc, dtype, layout):
+    """Arbitrary finite patterns (wide exponent range): the oracle is within
+    its double-precision error bound K * 2^-53 * sum|a||b| of the exact sum."""
+    rng = np.random.default_rng(200 + 2 * dtype + layout)
+    for trial in range(6):
+        M, N, K = (int(v) for v in rng.integers(1, 9, 3))
+        def finite_bits(shape):
+            v = rng.integers(0, 65536, shape).astype(np.uint16)
+            expo_mask = 0x7C00 if dtype == F16 else 0x7F80
+            v[(v & expo_mask) == expo_mask] &= np.uint16(0x83FF if dtype == F16 else 0x807F)
+            return v
+        A = finite_bits((M, K))
+        B = finite_bits((K, N) if layout == KN else (N, K))
+        ldb = N if layout == KN else K
+        C, R = orc.gemm(A, B, M, N, K, K, ldb, layout, dtype)
+        Cf, Rf = fraction_gemm(A, B, M, N, K, K, ldb, layout, dtype)
+        for i in range(M):
+            for j in range(N):
+                err = abs(Fraction(C[i, j]) - Cf[i][j])
+                assert err <= Fraction(K) * Fraction(2) ** -53 * Rf[i][j]
+
+
+# --- special cases ----------------------------------------------------------
+
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_identity_right_and_left(orc, layout):
+    M, K = 37, 29
+    a, _ = gen.make_operands(M, K, K, F16, layout, gen.uniform(-4, 4), None, seed=5)
+    I = torch.eye(K, dtype=torch.float16)   # symmetric: same store in KN and NK
+    C, _ = orc.gemm(bits16(a), bits16(I), M, K, K, K, K, layout, F16)
+    assert np.array_equal(C, a.double().numpy())
+    # I * B = B for a K x N right operand
+    N = 23
+    _, b = gen.make_operands(K, N, K, BF16, layout, gen.uniform(-4, 4), None, seed=6)
+    Ik = torch.eye(K, dtype=torch.bfloat16)
+    C2, _ = orc.gemm(bits16(Ik), bits16(b), K, N, K, K, b.shape[1], layout, BF16)
+    assert np.array_equal(C2, gen.b_logical(b, N, K, layout).double().numpy())
+
+
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_permutation_matrices_permute_exactly(orc, layout):
+    rng = np.random.default_rng(7)
+    M, N, K = 19, 31, 31
+    a, _ = gen.make_operands(M, N, K, F16, layout, gen.normal(0, 3), None, seed=8)
+    perm = rng.permutation(K)
+    P = torch.zeros(K, K, dtype=torch.float16)
+    P[np.arange(K), perm] = 1.0                # (A P)[:, perm[k]] = A[:, k]
+    store = P if layout == KN else P.t().contiguous()
+    C, _ = orc.gemm(bits16(a), bits16(store), M, K, K, K, K, layout, F16)
+    ref = np.empty((M, K))
+    ref[:, perm] = a.double().numpy()
+    assert np.array_equal(C, ref)
+    # P^T B permutes the rows of B: (P^T B)[perm[k], :] = B[k, :]
+    _, b = gen.make_operands(K, N, K, F16, layout, gen.normal(0, 3), None, seed=9)
+    Pt = P.t().contiguous()
+    C2, _ = orc.gemm(bits16(Pt), bits16(b), K, N, K, K, b.shape[1], layout, F16)
+    bl = gen.b_logical(b, N, K, layout).double().numpy()
+    ref2 = np.empty((K, N))
+    ref2[perm, :] = bl
+    assert np.array_equal(C2, ref2)
+
+
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_integer_inputs_exact_against_integer_arithmetic(orc, layout):
+    M, N, K = 24, 20, 33
+    a, b = gen.make_operands(M, N, K, BF16, layout, gen.ints(-2, 2), None, seed=0)
+    C, R = orc.gemm(bits16(a), bits16(b), M, N, K, K, b.shape[1], layout, BF16)
+    ai = a.to(torch.int64).tolist()
+    bi = gen.b_logical(b, N, K, layout).to(torch.int64).tolist()
+    for i in range(M):
+        for j in range(N):
+            assert C[i, j] == sum(ai[i][k] * bi[k][j] for k in range(K))
+            assert R[i, j] == sum(abs(ai[i][k] * bi[k][j]) for k in range(K))
+
+
+def test_linearity_in_b(orc):
+    M, N, K = 40, 36, 50
+    a, b1 = gen.make_operands(M, N, K, F16, NK, gen.ints(-2, 2), None, seed=21)
+    _, b2 = gen.make_operands(M, N, K, F16, NK, gen.ints(-2, 2), None, seed=22)
+    s = (b1.float() + b2.float()).to(torch.float16)          # exact: small integers
+    C1, _ = orc.gemm(bits16(a), bits16(b1), M, N, K, K, K, NK, F16)
+    C2, _ = orc.gemm(bits16(a), bits16(b2), M, N, K, K, K, NK, F16)
+    C3, _ = orc.gemm(bits16(a), bits16(s), M, N, K, K, K, NK, F16)
+    assert np.array_equal(C3, C1 + C2)
+
+
+@pytest.mark.parametrize("layout", [KN, NK])
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_numpy_float64_matmul_crosscheck(orc, layout, dtype):
+    M, N, K = 128, 96, 256
+    a, b = gen.make_operands(M, N, K, dtype, layout, gen.normal(0, 1), None, seed=31)
+    C, R = orc.gemm(bits16(a), bits16(b), M, N, K, K, b.shape[1], layout, dtype)
+    ref = a.double().numpy() @ gen.b_logical(b, N, K, layout).double().numpy()
+    assert np.all(np.abs(C - ref) <= 1e-12 * R)
+    assert np.all(R >= np.abs(C))
+
+
+def test_transposed_operand_is_detected(orc):
+    """Reading B with the wrong layout changes the result on a non-square case."""
+    M, N, K = 8, 12, 12
+    a, b = gen.make_operands(M, N, K, F16, NK, gen.ints(-2, 2), None, seed=41)
+    C_nk, _ = orc.gemm(bits16(a), bits16(b), M, N, K, K, K, NK, F16)
+    C_kn, _ = orc.gemm(bits16(a), bits16(b), M, N, K, K, K, KN, F16)
+    assert not np.array_equal(C_nk, C_kn)
+    ref = a.double().numpy() @ b.double().numpy().T
+    assert np.array_equal(C_nk, ref)
+
+
+def test_padding_is_never_read(orc):
+    M, N, K = 17, 9, 21
+    a, b = gen.make_operands(M, N, K, F16, KN, gen.uniform(-1, 1), None, seed=51,
+                             lda=K + 11, ldb=N + 7, pad_value=float("nan"))
+    C, R = orc.gemm(bits16(a), bits16(b), M, N, K, K + 11, N + 7, KN, F16)
+    assert np.all(np.isfinite(C)) and np.all(np.isfinite(R))
+
+
+def test_elements_and_row_ranges_agree_with_full(orc):
+    M, N, K = 33, 45, 70
+    a, b = gen.make_operands(M, N, K, BF16, NK, gen.normal(0, 1), None, seed=61)
+    C, R = orc.gemm(bits16(a), bits16(b), M, N, K, K, K, NK, BF16, threads=3)
+    rng = np.random.default_rng(0)
+    ii, jj = rng.integers(0, M, 200), rng.integers(0, N, 200)
+    e, eb = orc.gemm_elements(bits16(a), bits16(b), M, N, K, K, K, NK, BF16, ii, jj)
+    assert np.array_equal(e, C[ii, jj]) and np.array_equal(eb, R[ii, jj])
+    Cr, Rr = orc.gemm_rows(bits16(a), bits16(b), M, N, K, K, K, NK, BF16, 5, 19, threads=4)
+    assert np.array_equal(Cr, C[5:19]) and np.array_equal(Rr, R[5:19])
+    # thread count never changes a result
+    C1, _ = orc.gemm(bits16(a), bits16(b), M, N, K, K, K, NK, BF16, threads=1)
+    assert np.array_equal(C1, C)
+
+
+def test_empty_sum_and_empty_shapes(orc):
+    """K = 0 is the empty sum: C = 0.  M = 0 or N = 0 give empty results."""
+    a = np.zeros((4, 1), np.uint16)
+    b = np.zeros((1, 5), np.uint16)
+    C, R = orc.gemm(a, b, 4, 5, 0, 1, 5, KN, F16)
+    assert C.shape == (4, 5) and not C.any() and not R.any()
+    C0, _ = orc.gemm(a, b, 0, 5, 1, 1, 5, KN, F16)
+    assert C0.shape == (0, 5)
+
+
+def test_bad_arguments_rejected(orc):
+    a = np.zeros((4, 4), np.uint16)
+    with pytest.raises(ValueError):
+        orc.gemm(a, a, 4, 4, 4, 3, 4, KN, F16)      # lda < K
+    with pytest.raises(ValueError):
+        orc.gemm(a, a, 4, 4, 4, 4, 4, KN, F32)      # FP32 is not an input format
