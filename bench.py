@@ -1,0 +1,362 @@
+"""Benchmark: device-timed TFLOPS of the tiled GEMM on one GB300.
+
+Workload: C = A * B with M = N = K = 8192, A (M x K) and B stored N x K, both
+FP16 drawn uniform on [-0.5, 0.5) from seed 3, FP32 accumulation, FP16
+output -- the 8192^3 FP16 problem of the pages' headline table (the Croqtile
+tutorial, "Performance at a glance").  A step is one tgemm_run call on the
+whole problem; the operands (128 MiB each) and C (128 MiB) together exceed
+the 129 MB L2, so back-to-back steps do not run from L2.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
+plain FP64 triple loop) on a bounded sample of the same workload instead.
+Several GPUs under torchrun run independent replicas (no collective on the
+data path); value is the FLOPs of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gemm_8192x8192x8192_f16_nk_f16"
+METRIC = "GEMM TFLOPS (device-timed) and fraction of GB300 dense FP16/BF16 tensor peak"
+PUBLISHED_TFLOPS = 489.9      # Croqtile v4 on H800 PCIe, same shape and B layout (context, other GPU)
+FALLBACK_TENSOR_TFLOPS = 1900.0
+KERNEL_SOURCES = ["tgemm_kernel.cuh", "tgemm_ptx.cuh", "tgemm_wait.cuh", "tgemm_sched.h", "tgemm_params.h"]
+
+
+def tflops(M: int, N: int, K: int, ms: float) -> float:
+    """2*M*N*K floating-point operations over `ms` milliseconds, in TFLOP/s."""
+    return 2.0 * M * N * K / (ms * 1e-3) / 1e12
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_tiled_gemm_persistent_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    digest = kernel_digest()
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) == 3 and not ln.startswith("#") and parts[0] == workload and parts[1] == digest:
+            return int(parts[2])
+    return None
+
+
+# ---- clocks --------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_uuid=None):
+        self.proc = None
+        self.path = None
+        self.gpu_uuid = gpu_uuid
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_uuid:
+            cmd += ["-i", self.gpu_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path).read().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]), hw=f[5], hw_th=f[6],
+                                 sw_th=f[7], pcap=f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        smax = max(r["max"] for r in rows)
+        loaded = [r for r in rows if r["power"] > 200] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_th", "hw_thermal_slowdown"),
+                              ("sw_th", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---- workload --------------------------------------------------------------------
+
+def workload():
+    from dense_tiled_gemm_persistent_gb300 import inputs as gen
+    return gen.WORKLOADS[WORKLOAD]
+
+
+def cpu_oracle_sample(wl, a, b, budget_s: float, threads: int):
+    """Time the oracle on rows [0, r) of C, r a multiple of the thread count
+    chosen to fill about budget_s seconds; returns (TFLOPS, seconds, rows)."""
+    import oracle
+    lda, ldb = a.shape[1], b.shape[1]
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, oracle.B_NK, oracle.F16, 0, threads, False, threads)
+    t_wave = time.perf_counter() - t0                     # one row per thread
+    rows = min(wl.M, max(1, int(budget_s / max(t_wave, 1e-9))) * threads)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, oracle.B_NK, oracle.F16, 0, rows, False, threads)
+    dt = time.perf_counter() - t0
+    return tflops(rows, wl.N, wl.K, dt * 1e3), dt, rows
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, rank 0 only."""
+    if rank != 0:
+        return
+    wl = workload()
+    a, b = wl.operands()
+    threads = os.cpu_count() or 1
+    total_budget = 120.0
+    per_step = max(0.05, min(20.0, total_budget / max(args.steps + args.warmup, 1)))
+    import oracle
+    oracle.build()
+    # rows per step: calibrate on one row per thread
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], oracle.B_NK, oracle.F16, 0,
+                     threads, False, threads)
+    t_wave = time.perf_counter() - t0
+    rows = max(1, min(wl.M, int(per_step / max(t_wave, 1e-9)) * threads))
+    if rows < threads:
+        rows = max(1, int(per_step / max(t_wave, 1e-9) * threads))
+    used = min(threads, rows)
+    times = []
+    for step in range(args.warmup + args.steps):
+        r0 = (step * rows) % max(wl.M - rows + 1, 1)
+        t0 = time.perf_counter()
+        oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], oracle.B_NK, oracle.F16, r0,
+                         r0 + rows, False, threads)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = tflops(rows * len(times), wl.N, wl.K, total * 1e3)
+    sample = "%d rows of C per step (%d x %d outputs, K = %d), FP64 dot products on %d threads" % (
+        rows, rows, wl.N, wl.K, used)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / max(len(times), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(wl, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": used, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl, world):
+    return {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "in_dtype": "f16", "out_dtype": "f16",
+            "accumulate": "f32", "b_layout": "NxK", "values": "uniform[-0.5,0.5) seed 3",
+            "l2": "operands+output 384 MiB > 129 MB L2 (no flush needed)",
+            "parallelism": "replicas%d" % world if world > 1 else "single-gpu"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="tgemm", choices=["tgemm", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from dense_tiled_gemm_persistent_gb300 import build as libbuild
+    from dense_tiled_gemm_persistent_gb300 import inputs as gen
+    from dense_tiled_gemm_persistent_gb300 import tgemm
+    import ctypes
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    libbuild.build()
+    tgemm.load()
+
+    wl = workload()
+    a_cpu, b_cpu = wl.operands()
+    A, B = a_cpu.to(dev), b_cpu.to(dev)
+    C = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    lda, ldb, ldc = A.shape[1], B.shape[1], wl.N
+
+    def step(c_ptr=None, a_ptr=None, b_ptr=None):
+        rc = tgemm.tgemm_run(wl.M, wl.N, wl.K, a_ptr or A.data_ptr(), lda, b_ptr or B.data_ptr(), ldb,
+                             gen.B_NK, c_ptr or C.data_ptr(), ldc, gen.F16, gen.F16, sh)
+        if rc != 0:
+            raise RuntimeError("tgemm_run: " + tgemm.status_string(rc))
+
+    for _ in range(args.warmup):
+        step()
+    rc = tgemm.tgemm_check(sh)
+    if rc != 0:
+        raise RuntimeError("warm-up failed: " + tgemm.status_string(rc))
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+
+    # per-launch events for the kernel's own duration, plus the whole region
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    rc = tgemm.tgemm_check(sh)
+    if rc != 0:
+        raise RuntimeError("timed region failed: " + tgemm.status_string(rc))
+    total_ms = ev[0].elapsed_time(ev[-1])
+    launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    ms_per_step = total_ms / args.steps
+    value = tflops(wl.M, wl.N, wl.K, ms_per_step) * world
+    avg_launch = statistics.mean(launch_ms)
+
+    peaks = measured_peaks()
+    if peaks and peaks.get("bf16_tflops"):
+        peak, peak_src = float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate equals bf16)"
+    else:
+        peak, peak_src = FALLBACK_TENSOR_TFLOPS, "fallback"
+    achieved = tflops(wl.M, wl.N, wl.K, avg_launch)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
+                "algorithmic_bytes": wl.algorithmic_bytes, "flops_per_launch": wl.flops}
+    if peaks and peaks.get("bf16_tflops_sustained"):
+        roofline["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+
+    # end to end through the C ABI with host buffers: H2D of A and B from
+    # pinned memory, the GEMM, D2H of C into pinned memory, every step
+    e2e = None
+    if not args.no_e2e:
+        ha = a_cpu.pin_memory()
+        hb = b_cpu.pin_memory()
+        hc = torch.empty((wl.M, wl.N), dtype=torch.float16).pin_memory()
+        A2, B2 = torch.empty_like(A), torch.empty_like(B)
+        C2 = torch.empty_like(C)
+        for _ in range(2):
+            A2.copy_(ha, non_blocking=True)
+            B2.copy_(hb, non_blocking=True)
+            step(C2.data_ptr(), A2.data_ptr(), B2.data_ptr())
+            hc.copy_(C2, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            A2.copy_(ha, non_blocking=True)
+            B2.copy_(hb, non_blocking=True)
+            step(C2.data_ptr(), A2.data_ptr(), B2.data_ptr())
+            hc.copy_(C2, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        e2e = {"value": tflops(wl.M, wl.N, wl.K, e2e_ms) * world, "unit": "TFLOPS",
+               "h2d_bytes_per_step": a_cpu.numel() * 2 + b_cpu.numel() * 2,
+               "d2h_bytes_per_step": hc.numel() * 2, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = os.cpu_count() or 1
+        v, dt, rows = cpu_oracle_sample(wl, a_cpu, b_cpu, 15.0, threads)
+        cpu = {"value": v, "unit": "TFLOPS", "cores": min(threads, rows), "kind": "oracle",
+               "sample": "rows 0..%d of C (%d x %d outputs, K = %d), FP64 dot products, %.1f s" % (
+                   rows - 1, rows, wl.N, wl.K, dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / PUBLISHED_TFLOPS, "dtype": "f16", "data": "synthetic",
+            "config": config_dict(wl, world), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": args.steps,
+            "kernel_ms": {"mean": avg_launch, "median": statistics.median(launch_ms), "min": min(launch_ms)},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,421 @@
+// Host side of the C ABI declared in include/tgemm.h: argument validation,
+// configuration choice, tensor-map encoding and the launch of the persistent
+// kernels.  Nothing here computes any part of C; every element of the result
+// is produced by the device kernels (or, for K = 0, by a device memset that
+// writes the empty sum).
+#include "tgemm.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "tgemm_kernel.cuh"
+#include "tgemm_params.h"
+#include "tgemm_sched.h"
+
+#define TGEMM_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace tgemm {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultGroupM = 8;   // GROUP_SIZE_M of the cuTile tutorial's matmul example
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *status = nullptr;     // device status word, lazily allocated
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint32_t> g_last_fault{0};   // last non-zero status word seen by tgemm_check
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+uint64_t wait_timeout_ns()
+{
+    static uint64_t ns = [] {
+        const char *s = std::getenv("TGEMM_WAIT_TIMEOUT_MS");
+        long ms = s ? std::strtol(s, nullptr, 10) : 0;
+        if (ms <= 0) ms = 2000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+size_t elem_size(int dt) { return dt == TGEMM_F32 ? 4 : 2; }
+
+// Current device's state; allocates the status word on first use.
+tgemm_status device_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return TGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        d.ready = true;
+    }
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return TGEMM_ERR_ARCH;
+    if (!d.status) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_OOM;
+        }
+        if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) {
+            cudaFree(p);
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        d.status = static_cast<uint32_t *>(p);
+    }
+    *out = &d;
+    return TGEMM_OK;
+}
+
+// Host-only checks (no CUDA call).  Returns TGEMM_OK with *noop set when
+// there is nothing to compute (M = 0 or N = 0).
+tgemm_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                      int64_t ldb, int b_layout, const void *C, int64_t ldc, int in_dtype, int out_dtype,
+                      bool *noop)
+{
+    *noop = false;
+    if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
+    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16 && in_dtype != TGEMM_F32)
+        return TGEMM_ERR_INVALID_ARG;
+    if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
+        return TGEMM_ERR_INVALID_ARG;
+    if (in_dtype == TGEMM_F32) return TGEMM_ERR_UNSUPPORTED;   // FP32 operands are not provided
+    if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
+    // Tensor coordinates are signed 32-bit.
+    const int64_t kMax = (int64_t)1 << 31;
+    if (M >= kMax || N >= kMax || K >= kMax) return TGEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) {
+        *noop = true;
+        return TGEMM_OK;
+    }
+    if (ldc < N) return TGEMM_ERR_INVALID_ARG;
+    if (C == nullptr) return TGEMM_ERR_INVALID_ARG;
+    const size_t ei = elem_size(in_dtype), eo = elem_size(out_dtype);
+    if (((uintptr_t)C % 16) != 0 || ((uint64_t)ldc * eo) % 16 != 0) return TGEMM_ERR_MISALIGNED;
+    if (K == 0) return TGEMM_OK;
+    if (lda < K) return TGEMM_ERR_INVALID_ARG;
+    if (ldb < (b_layout == TGEMM_B_KN ? N : K)) return TGEMM_ERR_INVALID_ARG;
+    if (A == nullptr || B == nullptr) return TGEMM_ERR_INVALID_ARG;
+    if (((uintptr_t)A % 16) != 0 || ((uintptr_t)B % 16) != 0) return TGEMM_ERR_MISALIGNED;
+    if (((uint64_t)lda * ei) % 16 != 0 || ((uint64_t)ldb * ei) % 16 != 0) return TGEMM_ERR_MISALIGNED;
+    return TGEMM_OK;
+}
+
+const KernelVariant *find_variant(int bn, int stages, int out, int b_mn)
+{
+    const KernelVariant *tab = nullptr;
+    int n = 0;
+    switch (out) {
+    case TGEMM_F16: tab = kVariantsF16; n = kNumVariantsF16; break;
+    case TGEMM_BF16: tab = kVariantsBF16; n = kNumVariantsBF16; break;
+    case TGEMM_F32: tab = kVariantsF32; n = kNumVariantsF32; break;
+    default: return nullptr;
+    }
+    for (int i = 0; i < n; ++i)
+        if (tab[i].bn == bn && tab[i].stages == stages && tab[i].b_mn == b_mn) return &tab[i];
+    return nullptr;
+}
+
+int default_stages(int bn) { return bn == 256 ? 4 : 6; }
+
+// Tile-width choice.  A 128 x 256 tile does twice the MMA work of a 128 x 128
+// tile for 1.5x the shared-memory operand traffic, so it is preferred; the
+// narrower tile wins when it needs fewer waves of persistent CTAs.  The cost
+// model is waves * tile-time with tile-time ~ bn * (1 + 64 / bn).
+void choose_config(int64_t M, int64_t N, int sm_count, tgemm_config *cfg)
+{
+    int best_bn = 0;
+    double best_cost = 0;
+    for (int bn : {256, 128}) {
+        const TileGrid g(M, N, kBM, bn);
+        const int64_t waves = ceil_div(g.count(), sm_count);
+        const double cost = (double)waves * (bn + 64);
+        if (best_bn == 0 || cost < best_cost) {
+            best_bn = bn;
+            best_cost = cost;
+        }
+    }
+    const TileGrid g(M, N, kBM, best_bn);
+    cfg->bm = kBM;
+    cfg->bn = best_bn;
+    cfg->bk = kBK;
+    cfg->stages = default_stages(best_bn);
+    cfg->cluster_m = 1;
+    cfg->group_m = kDefaultGroupM;
+    cfg->split_k = 1;
+    cfg->swap_ab = 0;
+    cfg->grid = (int)(g.count() < sm_count ? g.count() : sm_count);
+}
+
+CUtensorMapDataType map_dtype(int dt)
+{
+    switch (dt) {
+    case TGEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case TGEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    }
+}
+
+// 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
+// `ld` elements between rows; boxes of box_inner x box_outer, 128-byte swizzle,
+// zero fill outside the tensor.
+bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld * elem_size(dt)};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, map_dtype(dt), 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+tgemm_status legal_config(const tgemm_config &c, int out_dtype, int b_layout, const KernelVariant **v)
+{
+    if (c.bm != kBM || c.bk != kBK || c.cluster_m != 1 || c.split_k != 1 || c.swap_ab != 0)
+        return TGEMM_ERR_UNSUPPORTED;
+    if (c.group_m < 1 || c.grid < 0) return TGEMM_ERR_UNSUPPORTED;
+    *v = find_variant(c.bn, c.stages, out_dtype, b_layout == TGEMM_B_KN ? 1 : 0);
+    return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+}
+
+tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                      int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
+                      void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags)
+{
+    bool noop = false;
+    tgemm_status st = validate(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, &noop);
+    if (st != TGEMM_OK) return st;
+    tgemm_config cfg;
+    const KernelVariant *var = nullptr;
+    if (forced) {
+        cfg = *forced;
+        st = legal_config(cfg, out_dtype, b_layout, &var);
+        if (st != TGEMM_OK) return st;
+    }
+    if (noop) return TGEMM_OK;
+    DeviceState *dev = nullptr;
+    st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const size_t eo = elem_size(out_dtype);
+    if (K == 0) {
+        // The empty sum: C = 0 (all-zero bits are +0 in every output type).
+        if (cudaMemset2DAsync(C, (size_t)ldc * eo, 0, (size_t)N * eo, (size_t)M, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        return TGEMM_OK;
+    }
+    if (!forced) {
+        choose_config(M, N, dev->sm_count, &cfg);
+        st = legal_config(cfg, out_dtype, b_layout, &var);
+        if (st != TGEMM_OK) return st;
+    }
+    const bool b_mn = b_layout == TGEMM_B_KN;
+    const TileGrid grid(M, N, kBM, cfg.bn);
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    bool ok = encode_2d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kBK, kBM);
+    if (b_mn)
+        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, kBK);
+    else
+        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kBK,
+                             (uint32_t)cfg.bn);
+    ok = ok && encode_2d(&p.tma_c, out_dtype, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc,
+                         (uint32_t)(128 / eo), 32);
+    if (!ok) return TGEMM_ERR_CUDA;
+    p.M = (int32_t)M;
+    p.N = (int32_t)N;
+    p.K = (int32_t)K;
+    p.tiles_m = (int32_t)grid.tiles_m;
+    p.tiles_n = (int32_t)grid.tiles_n;
+    p.num_tiles = (int32_t)grid.count();
+    p.num_kb = (int32_t)ceil_div(K, kBK);
+    p.group_m = cfg.group_m;
+    p.idesc = make_idesc(in_dtype == TGEMM_BF16, b_mn, kBM, cfg.bn);
+    p.debug_flags = debug_flags;
+    p.status = dev->status;
+    p.timeout_ns = wait_timeout_ns();
+
+    int g = cfg.grid > 0 ? cfg.grid : dev->sm_count;
+    if (g > p.num_tiles) g = p.num_tiles;
+    if (g < 1) g = 1;
+    if (var->launch(p, g, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
+}  // namespace
+}  // namespace tgemm
+
+using namespace tgemm;
+
+TGEMM_EXPORT tgemm_status tgemm_run(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                                    const void *B, int64_t ldb, tgemm_b_layout b_layout, void *C,
+                                    int64_t ldc, tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream)
+{
+    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, nullptr, 0);
+}
+
+TGEMM_EXPORT tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                                           const void *B, int64_t ldb, tgemm_b_layout b_layout, void *C,
+                                           int64_t ldc, tgemm_dtype in_dtype, tgemm_dtype out_dtype,
+                                           void *stream, const tgemm_config *cfg)
+{
+    if (!cfg) return TGEMM_ERR_INVALID_ARG;
+    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0);
+}
+
+TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
+                                             tgemm_dtype in_dtype, tgemm_dtype out_dtype,
+                                             tgemm_config *out_cfg)
+{
+    if (!out_cfg) return TGEMM_ERR_INVALID_ARG;
+    if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
+    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16) return TGEMM_ERR_UNSUPPORTED;
+    if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
+        return TGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
+    DeviceState *dev = nullptr;
+    tgemm_status st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, dev->sm_count, out_cfg);
+    return TGEMM_OK;
+}
+
+TGEMM_EXPORT tgemm_status tgemm_check(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    uint32_t *status = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        status = g_dev[dev].status;
+    }
+    if (!status) return TGEMM_OK;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    if (word == 0) return TGEMM_OK;
+    g_last_fault.store(word);
+    if (cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return (word >> 28) == kFaultTimeout ? TGEMM_ERR_TIMEOUT : TGEMM_ERR_CUDA;
+}
+
+TGEMM_EXPORT uint32_t tgemm_last_fault_code(void) { return g_last_fault.load(); }
+
+TGEMM_EXPORT const char *tgemm_status_string(tgemm_status s)
+{
+    switch (s) {
+    case TGEMM_OK: return "ok";
+    case TGEMM_ERR_INVALID_ARG: return "invalid argument (negative size, NULL pointer, short leading dimension or bad enum)";
+    case TGEMM_ERR_UNSUPPORTED: return "unsupported dtype, size or configuration";
+    case TGEMM_ERR_MISALIGNED: return "pointer or leading dimension not 16-byte aligned";
+    case TGEMM_ERR_ARCH: return "current device is not sm_103 (GB300)";
+    case TGEMM_ERR_CUDA: return "CUDA runtime or driver error";
+    case TGEMM_ERR_OOM: return "out of device memory for library workspace";
+    case TGEMM_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+TGEMM_EXPORT void tgemm_shutdown(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = -1;
+    cudaGetDevice(&cur);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_dev[d].status) {
+            cudaSetDevice(d);
+            cudaFree(g_dev[d].status);
+        }
+        g_dev[d] = DeviceState();
+    }
+    if (cur >= 0) cudaSetDevice(cur);
+    cudaGetLastError();
+}
+
+TGEMM_EXPORT tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn, int group_m, int64_t bid,
+                                           int64_t *bid_m, int64_t *bid_n)
+{
+    if (M <= 0 || N <= 0 || bm <= 0 || bn <= 0 || group_m <= 0 || !bid_m || !bid_n)
+        return TGEMM_ERR_INVALID_ARG;
+    const TileGrid g(M, N, bm, bn);
+    if (bid < 0 || bid >= g.count()) return TGEMM_ERR_INVALID_ARG;
+    grouped_tile(g.tiles_m, g.tiles_n, group_m, bid, *bid_m, *bid_n);
+    return TGEMM_OK;
+}
+
+TGEMM_EXPORT tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream)
+{
+    DeviceState *dev = nullptr;
+    tgemm_status st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return TGEMM_ERR_INVALID_ARG;
+    if (launch_wait_timeout_probe(dev->status, (uint64_t)timeout_us * 1000ull,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}

@@ -1,0 +1,16 @@
+// Compiled variants of the persistent GEMM kernel with F32 output.
+// Each entry: output tile width BN, ring depth STAGES, output type, B layout
+// (0 = B stored N x K, K-major; 1 = B stored K x N, MN-major).
+#include "tgemm_kernel.cuh"
+
+namespace tgemm {
+
+const KernelVariant kVariantsF32[] = {
+    TGEMM_VARIANT(256, 4, OUT_F32, 0),
+    TGEMM_VARIANT(256, 4, OUT_F32, 1),
+    TGEMM_VARIANT(128, 6, OUT_F32, 0),
+    TGEMM_VARIANT(128, 6, OUT_F32, 1),
+};
+const int kNumVariantsF32 = (int)(sizeof(kVariantsF32) / sizeof(kVariantsF32[0]));
+
+}  // namespace tgemm

@@ -1,0 +1,382 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a: C = A * B.
+//
+// The dataflow is the tile lifecycle the pages describe (load a BM x BK tile
+// of A and a BK x BN tile of B, multiply-accumulate over the K loop, cast and
+// write back; the double-buffered prefetch of the wmrh.cn essay "the parallel
+// secret of a CUDA tile", section 2.2; the producer/consumer ring with full
+// and empty events of the Croqtile tutorial's "Kernel 3: warp
+// specialisation"), rebuilt on Blackwell hardware:
+//
+//   warp 0  producer  one thread issues TMA loads of A and B k-blocks into a
+//                     STAGES-deep shared-memory ring (128-byte swizzle) and
+//                     arms the stage's "full" mbarrier with the byte count;
+//   warp 1  MMA       one thread waits on "full", issues BK/16 tcgen05.mma
+//                     (M = 128, N = BN, K = 16) into an FP32 accumulator in
+//                     tensor memory, and commits the stage back to "empty";
+//                     after the last k-block it commits "tmem_full";
+//   warps 2-5 epilogue  wait "tmem_full", read the accumulator with
+//                     tcgen05.ld (warp w owns TMEM lanes 32*(w%4)..+31, i.e.
+//                     tile rows), release the buffer ("tmem_empty"), cast
+//                     FP32 -> output type with round-to-nearest-even, stage
+//                     128-byte rows in swizzled shared memory and write them
+//                     with TMA stores, which drop out-of-range rows/columns.
+//
+// Two accumulator buffers in tensor memory let the epilogue of tile i run
+// while the MMAs of tile i+1 proceed.  The CTA loops over tiles
+// bid = blockIdx.x, blockIdx.x + gridDim.x, ... in the grouped order of
+// tgemm_sched.h, so the grid is one CTA per SM.
+//
+// Tails follow the CUDA Programming Guide 13.4.2 (unofficial Chinese
+// translation), section 2.4.9.1: ceil(K/BK) k-blocks with the partial block
+// zero-filled (TMA fills out-of-range elements with zeros), and partial M/N
+// tiles clipped at the store.  A store whose box would start past the end of
+// C is not issued at all.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <string.h>
+
+#include "tgemm_params.h"
+#include "tgemm_ptx.cuh"
+#include "tgemm_sched.h"
+#include "tgemm_wait.cuh"
+
+namespace tgemm {
+
+constexpr int kBM = 128;           // rows of one CTA tile = TMEM lanes
+constexpr int kBK = 64;            // K depth of one stage: 64 x 2 bytes = one 128-byte swizzle row
+constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
+constexpr int kThreads = 192;      // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kStageCBytes = 32 * 128;   // one staged 32-row x 128-byte block of C
+
+// ---- shared-memory matrix descriptors (tcgen05, 128-byte swizzle) -----------
+//
+// Bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4,
+// 32-45 stride-dimension byte offset >> 4, 46-47 version (1), 49-51 base
+// offset (0: every swizzle atom starts 1024-byte aligned), 61-63 layout
+// (2 = 128-byte swizzle).
+__host__ __device__ constexpr uint64_t desc_sw128(uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    return ((uint64_t)((lbo_bytes >> 4) & 0x3fffu) << 16) |
+           ((uint64_t)((sbo_bytes >> 4) & 0x3fffu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ uint64_t desc_at(uint64_t tmpl, uint32_t smem_byte_addr)
+{
+    return tmpl | (uint64_t)((smem_byte_addr >> 4) & 0x3fffu);
+}
+
+// K-major operand (rows of 64 K-elements = 128 bytes, 8-row swizzle atoms
+// 1024 bytes apart).  The leading offset is unused for swizzled K-major
+// layouts; the usual value 16 bytes is kept.
+constexpr uint64_t kDescKMajor = desc_sw128(16, 1024);
+// MN-major operand (B stored K x N): each 64-wide column block is 64 k-rows
+// of 128 bytes (8 KiB); the leading offset steps between 64-wide column
+// blocks, the stride offset between 8-row K groups.
+constexpr uint64_t kDescMNMajor = desc_sw128(kBK * 128, 1024);
+
+// ---- instruction descriptor (kind::f16) -------------------------------------
+//
+// Bits 4-5 D type (1 = F32), 7-9 A type and 10-12 B type (0 = F16, 1 = BF16),
+// 15 A major (0 = K), 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, bool b_mn_major, int m, int n)
+{
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// ---- shared-memory plan ---------------------------------------------------
+template <int BN, int STAGES>
+struct SmemPlan {
+    static constexpr uint32_t a_stage = kBM * kBK * 2;
+    static constexpr uint32_t b_stage = BN * kBK * 2;
+    static constexpr uint32_t a_off = 0;
+    static constexpr uint32_t b_off = a_off + STAGES * a_stage;
+    static constexpr uint32_t c_off = b_off + STAGES * b_stage;
+    static constexpr uint32_t bar_off = c_off + kEpiWarps * 2 * kStageCBytes;
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    static constexpr uint32_t n_bars = 2 * STAGES + 5;
+    static constexpr uint32_t slot_off = bar_off + 8 * n_bars;   // TMEM address
+    static constexpr uint32_t abort_off = slot_off + 4;
+    static constexpr uint32_t bytes = abort_off + 4;
+    static constexpr uint32_t alloc_bytes = bytes + 1024;        // slack to align the base to 1024
+};
+
+template <int BN>
+struct TmemCols {
+    static constexpr uint32_t value = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                      : (2 * BN <= 256) ? 256 : 512;
+};
+
+__device__ __forceinline__ uint32_t pack_out(float lo, float hi, int out)
+{
+    uint32_t u;
+    if (out == OUT_F16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        memcpy(&u, &h, 4);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        memcpy(&u, &h, 4);
+    }
+    return u;
+}
+
+template <int BN, int STAGES, int OUT, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p)
+{
+    using Plan = SmemPlan<BN, STAGES>;
+    constexpr uint32_t kStageBytes = Plan::a_stage + Plan::b_stage;
+    constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;          // columns of one 128-byte staged row
+    constexpr int kChunks = BN / kChunkCols;
+    constexpr uint32_t kTmemCols = TmemCols<BN>::value;
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+    static_assert(2 * BN <= 512, "two accumulator buffers must fit in tensor memory");
+    static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base + Plan::a_off;
+    const uint32_t sB = base + Plan::b_off;
+    const uint32_t sC = base + Plan::c_off;
+    const uint32_t bar = base + Plan::bar_off;
+    auto full_bar = [&](int s) { return bar + 8u * s; };
+    auto empty_bar = [&](int s) { return bar + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar + 8u * (2 * STAGES + 4);
+    const uint32_t slot = base + Plan::slot_off;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&p.tma_a);
+        ptx::prefetch_tensormap(&p.tma_b);
+        ptx::prefetch_tensormap(&p.tma_c);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(slot, kTmemCols);
+        ptx::tmem_relinquish();
+        ptx::tc_fence_before_sync();
+    }
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
+
+    const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
+    const int num_tiles = p.num_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;   // latest load per stage, for wind-down
+            bool ok = true;
+            bool first = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int64_t tr, tc;
+                grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+                const int32_t m0 = (int32_t)tr * kBM;
+                const int32_t n0 = (int32_t)tc * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool skip = first && (p.debug_flags & 1u);
+                    first = false;
+                    if (!skip) {
+                        const uint32_t fb = full_bar(s);
+                        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                        const int32_t k0 = kb * kBK;
+                        ptx::tma_load_2d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0);
+                        if (B_MN) {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                ptx::tma_load_2d(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
+                                                 n0 + 64 * j, k0);
+                        } else {
+                            ptx::tma_load_2d(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0);
+                        }
+                        issued_mask |= 1u << s;
+                        issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Wind down: wait for the copies still in flight into our ring.
+                for (int t = 0; t < STAGES; ++t)
+                    if (issued_mask & (1u << t))
+                        wait_bounded(full_bar(t), (issued_parity >> t) & 1u, wc, SITE_DRAIN_LOADS, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t local = 0;      // tiles done by this CTA
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+                const uint32_t buf = local & 1u;
+                const uint32_t bph = (local >> 1) & 1u;
+                if (!wait_bounded(tempty_bar(buf), bph ^ 1u, wc, SITE_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a_addr = sA + s * Plan::a_stage;
+                    const uint32_t b_addr = sB + s * Plan::b_stage;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
+                        const uint64_t bd = B_MN ? desc_at(kDescMNMajor, b_addr + k * (kUmmaK * 128))
+                                                 : desc_at(kDescKMajor, b_addr + k * (kUmmaK * 2));
+                        ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(s));       // stage reusable once these MMAs finish
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull_bar(buf));         // accumulator ready for the epilogue
+            }
+            if (!ok) {
+                // Wind down: every MMA issued so far must finish before the
+                // tensor memory is released.
+                ptx::mma_commit(drain_bar);
+                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;                         // staging slot 0..3
+        const int q = warp & 3;                          // TMEM lane quarter = tile rows 32q..32q+31
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
+        uint32_t local = 0, cc = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            const uint32_t buf = local & 1u;
+            const uint32_t bph = (local >> 1) & 1u;
+            const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
+            if (!__all_sync(0xffffffffu, got)) break;
+            ptx::tc_fence_after_sync();
+
+            int64_t tr, tc;
+            grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+            const int32_t row0 = (int32_t)tr * kBM + 32 * q;
+            const int32_t col0 = (int32_t)tc * BN;
+            const uint32_t t_acc = tmem_base + lane_base + buf * BN;
+
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c) {
+                uint32_t v0[32], v1[32];
+                ptx::tmem_ld_32x32b_x32(t_acc + c * kChunkCols, v0);
+                if constexpr (kChunkCols == 64) ptx::tmem_ld_32x32b_x32(t_acc + c * kChunkCols + 32, v1);
+                ptx::tmem_ld_wait();
+                if (c == kChunks - 1) {
+                    // The accumulator buffer is fully read: hand it back to the MMA warp.
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+                }
+                const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
+                if (lane == 0) ptx::bulk_wait_group_read<1>();   // the store that last used sbuf is done reading
+                __syncwarp();
+                const uint32_t row_addr = sbuf + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w0, w1, w2, w3;
+                    if constexpr (OUT == OUT_F32) {
+                        w0 = v0[4 * j + 0];
+                        w1 = v0[4 * j + 1];
+                        w2 = v0[4 * j + 2];
+                        w3 = v0[4 * j + 3];
+                    } else {
+                        // columns 8j .. 8j+7 of the 64-column chunk
+                        const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+                        w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
+                        w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);
+                        w2 = pack_out(__uint_as_float(src[4]), __uint_as_float(src[5]), OUT);
+                        w3 = pack_out(__uint_as_float(src[6]), __uint_as_float(src[7]), OUT);
+                    }
+                    // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
+                    ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int32_t x = col0 + c * kChunkCols;
+                    if (x < p.N && row0 < p.M) ptx::tma_store_2d(&p.tma_c, sbuf, x, row0);
+                    ptx::bulk_commit_group();
+                }
+                ++cc;
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int BN, int STAGES, int OUT, bool B_MN>
+cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
+{
+    auto kern = gemm_persistent_kernel<BN, STAGES, OUT, B_MN>;
+    constexpr uint32_t smem = SmemPlan<BN, STAGES>::alloc_bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+#define TGEMM_VARIANT(BN, ST, OUT, BMN) \
+    {BN, ST, OUT, BMN, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, (BMN) != 0>}
+
+}  // namespace tgemm

@@ -1,0 +1,63 @@
+// Kernel parameter block and launch declarations shared by the host API and
+// the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tgemm {
+
+enum OutType { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
+
+// Fault codes written to the device status word: bits 31..28 hold the
+// status (7 = timeout), bits 27..20 the wait site, bits 19..0 the CTA.
+enum WaitSite : uint32_t {
+    SITE_PRODUCER_EMPTY = 1,
+    SITE_MMA_TMEM_EMPTY = 2,
+    SITE_MMA_FULL = 3,
+    SITE_EPI_TMEM_FULL = 4,
+    SITE_DRAIN_LOADS = 5,
+    SITE_DRAIN_MMA = 6,
+    SITE_DEBUG = 7,
+    SITE_SPLITK_COUNTER = 8,
+};
+
+constexpr uint32_t kFaultTimeout = 7u;
+
+// Everything one persistent GEMM launch needs.  The three tensor maps must
+// stay 128-byte aligned (CUtensorMap) inside the parameter space.
+struct alignas(128) GemmParams {
+    CUtensorMap tma_a;      // A: dims {K, M}, box {64, 128}, 128-byte swizzle
+    CUtensorMap tma_b;      // B: NK dims {K, N} box {64, bn}; KN dims {N, K} box {64, 64}
+    CUtensorMap tma_c;      // C: dims {N, M}, box {128 bytes of columns, 32}, 128-byte swizzle
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n, num_tiles, num_kb;
+    int32_t group_m;
+    uint32_t idesc;         // tcgen05 instruction descriptor (kind::f16)
+    uint32_t debug_flags;   // bit 0: the producer skips its first load (timeout test)
+    uint32_t *status;       // device status word (first fault wins)
+    uint64_t timeout_ns;    // limit of every pipeline wait
+};
+
+using LaunchFn = cudaError_t (*)(const GemmParams &, int grid, cudaStream_t);
+
+// One compiled kernel variant.
+struct KernelVariant {
+    int bn, stages, out, b_mn;
+    size_t smem_bytes;
+    LaunchFn launch;
+};
+
+// Defined in the kernel translation units (one per output type).
+extern const KernelVariant kVariantsF16[];
+extern const int kNumVariantsF16;
+extern const KernelVariant kVariantsBF16[];
+extern const int kNumVariantsBF16;
+extern const KernelVariant kVariantsF32[];
+extern const int kNumVariantsF32;
+
+// The bounded-wait self test kernel launcher (tgemm_debug.cu).
+cudaError_t launch_wait_timeout_probe(uint32_t *status, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace tgemm

@@ -1,0 +1,55 @@
+// Tile-space arithmetic shared by the kernels (device) and the host API.
+//
+// The output C (M x N) is cut into a grid of bm x bn tiles, the partition
+// view of the CUDA Programming Guide 13.4.2 (unofficial Chinese translation),
+// section 2.4.6.1 "Tile-space load and store", Figure 19: tile (i, j) covers
+// rows [i*bm, i*bm + bm) and columns [j*bn, j*bn + bn), clipped to the array;
+// the grid is ceil(M/bm) x ceil(N/bn).
+//
+// A persistent CTA walks tile numbers bid = blockIdx.x, blockIdx.x + gridDim.x,
+// ... and maps each to a tile with the grouped ("swizzled") order of "Writing
+// high-performance matrix multiplication with NVIDIA CUDA Tile", section
+// "Performance optimisation: Swizzle": tile numbers are dealt out in bands of
+// group_m tile rows; within a band consecutive numbers go down the band's rows
+// first and then move one tile column to the right, so CTAs running at the
+// same time share A row-blocks and B column-blocks in L2.  The row inside the
+// band is taken from the tile number itself (not from its offset inside the
+// band), as that tutorial does; in the last, shorter band this rotates the
+// rows but keeps the mapping one-to-one.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define TGEMM_HD __host__ __device__ __forceinline__
+#else
+#define TGEMM_HD inline
+#endif
+
+namespace tgemm {
+
+TGEMM_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct TileGrid {
+    int64_t tiles_m, tiles_n;
+
+    TGEMM_HD TileGrid(int64_t M, int64_t N, int bm, int bn)
+        : tiles_m(ceil_div(M, bm)), tiles_n(ceil_div(N, bn)) {}
+
+    TGEMM_HD int64_t count() const { return tiles_m * tiles_n; }
+};
+
+// Tile number -> (tile row, tile column) in grouped order.
+TGEMM_HD void grouped_tile(int64_t tiles_m, int64_t tiles_n, int group_m, int64_t bid,
+                           int64_t &tile_row, int64_t &tile_col)
+{
+    const int64_t band_tiles = (int64_t)group_m * tiles_n;     // tiles in one full band
+    const int64_t band = bid / band_tiles;
+    const int64_t row0 = band * group_m;                         // first tile row of the band
+    int64_t rows = tiles_m - row0;                               // the last band may be shorter
+    if (rows > group_m) rows = group_m;
+    tile_row = row0 + bid % rows;
+    tile_col = (bid - band * band_tiles) / rows;
+}
+
+}  // namespace tgemm

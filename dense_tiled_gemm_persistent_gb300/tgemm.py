@@ -1,0 +1,168 @@
+"""Python binding of the C ABI in include/tgemm.h (libtgemm.so).
+
+Argument marshalling only: every element of C is computed by the library's
+CUDA kernels.  There is no CPU fallback; if the library is missing, every
+call raises.  The raw functions mirror the C names and take integer device
+pointers and a stream handle; ``matmul`` is a thin convenience that derives
+sizes and leading dimensions from torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+F16, BF16, F32 = 0, 1, 2
+B_KN, B_NK = 0, 1
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_OOM, ERR_TIMEOUT = range(8)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libtgemm.so")
+
+# Every symbol include/tgemm.h declares.
+EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
+           "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
+           "tgemm_debug_wait_timeout")
+
+
+class TgemmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (status %d)" % (where, status_string(code), code))
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("bm", "bn", "bk", "stages", "cluster_m", "group_m", "split_k", "swap_ab", "grid")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+_i64, _p, _i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+
+
+def load(path: str = LIB_PATH):
+    """Load libtgemm.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError("libtgemm.so is not built (%s); run "
+                               "dense_tiled_gemm_persistent_gb300.build.build()" % path)
+        lib = ctypes.CDLL(path)
+        run_args = [_i64, _i64, _i64, _p, _i64, _p, _i64, _i, _p, _i64, _i, _i, _p]
+        lib.tgemm_run.argtypes = run_args
+        lib.tgemm_run.restype = _i
+        lib.tgemm_run_config.argtypes = run_args + [ctypes.POINTER(Config)]
+        lib.tgemm_run_config.restype = _i
+        lib.tgemm_query_config.argtypes = [_i64, _i64, _i64, _i, _i, _i, ctypes.POINTER(Config)]
+        lib.tgemm_query_config.restype = _i
+        lib.tgemm_check.argtypes = [_p]
+        lib.tgemm_check.restype = _i
+        lib.tgemm_last_fault_code.argtypes = []
+        lib.tgemm_last_fault_code.restype = ctypes.c_uint32
+        lib.tgemm_status_string.argtypes = [_i]
+        lib.tgemm_status_string.restype = ctypes.c_char_p
+        lib.tgemm_shutdown.argtypes = []
+        lib.tgemm_shutdown.restype = None
+        lib.tgemm_tile_coord.argtypes = [_i64, _i64, _i, _i, _i, _i64, ctypes.POINTER(_i64),
+                                         ctypes.POINTER(_i64)]
+        lib.tgemm_tile_coord.restype = _i
+        lib.tgemm_debug_wait_timeout.argtypes = [ctypes.c_uint32, _p]
+        lib.tgemm_debug_wait_timeout.restype = _i
+        _lib = lib
+        return lib
+
+
+# ---- raw C ABI ---------------------------------------------------------------
+
+def tgemm_run(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None) -> int:
+    return load().tgemm_run(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream)
+
+
+def tgemm_run_config(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream,
+                     cfg: Config) -> int:
+    return load().tgemm_run_config(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype,
+                                   stream, ctypes.byref(cfg))
+
+
+def tgemm_query_config(M, N, K, b_layout, in_dtype, out_dtype):
+    cfg = Config()
+    rc = load().tgemm_query_config(M, N, K, b_layout, in_dtype, out_dtype, ctypes.byref(cfg))
+    return rc, cfg
+
+
+def tgemm_check(stream=None) -> int:
+    return load().tgemm_check(stream)
+
+
+def tgemm_last_fault_code() -> int:
+    return load().tgemm_last_fault_code()
+
+
+def status_string(code: int) -> str:
+    return load().tgemm_status_string(code).decode()
+
+
+def tgemm_shutdown() -> None:
+    load().tgemm_shutdown()
+
+
+def tgemm_tile_coord(M, N, bm, bn, group_m, bid):
+    r, c = _i64(), _i64()
+    rc = load().tgemm_tile_coord(M, N, bm, bn, group_m, bid, ctypes.byref(r), ctypes.byref(c))
+    return rc, r.value, c.value
+
+
+def tgemm_debug_wait_timeout(timeout_us: int, stream=None) -> int:
+    return load().tgemm_debug_wait_timeout(timeout_us, stream)
+
+
+# ---- torch convenience ------------------------------------------------------
+
+def _dtype_code(t):
+    import torch
+    return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32}[t]
+
+
+def _ld(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("operands must be 2-D with unit column stride (row-major)")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def matmul(A, B, b_layout: int = B_NK, out_dtype=None, C=None, stream=None, config: Config = None):
+    """C = A @ B on the GPU through tgemm_run (or tgemm_run_config).
+
+    A: (M, K) row-major CUDA tensor, FP16 or BF16.  B: (K, N) for B_KN or
+    (N, K) for B_NK, same dtype.  C: optional (M, N) output (allocated with
+    torch.empty when omitted, dtype out_dtype or A.dtype).
+    """
+    import torch
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("operands must be CUDA tensors")
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must have the same dtype")
+    M, K = A.shape
+    N = B.shape[1] if b_layout == B_KN else B.shape[0]
+    kb = B.shape[0] if b_layout == B_KN else B.shape[1]
+    if kb != K:
+        raise ValueError("inner dimensions differ")
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype or A.dtype, device=A.device)
+    args = (M, N, K, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), b_layout, C.data_ptr(), _ld(C),
+            _dtype_code(A.dtype), _dtype_code(C.dtype), _stream_handle(stream))
+    rc = tgemm_run(*args) if config is None else tgemm_run_config(*args, config)
+    if rc != OK:
+        raise TgemmError(rc, "tgemm_run")
+    return C

@@ -1,0 +1,139 @@
+/*
+ * tgemm: tiled dense matrix multiply C = A * B for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the defining sum of "Writing high-performance matrix
+ * multiplication with NVIDIA CUDA Tile" (juejin.cn, section "What is matrix
+ * multiplication?"):  C[i][j] = sum_k A[i][k] * B[k][j],  with the precision
+ * contract of the CUDA Programming Guide 13.4.2 (unofficial Chinese
+ * translation), section 2.4.9.1 "Matrix multiplication": FP16 or BF16
+ * operands, an FP32 accumulator, one cast to the output type at the store.
+ * Tails follow the same section: the K loop runs ceil(K / tile_k) times with
+ * the partial K tile zero-padded, and partial M/N edge tiles drop their
+ * out-of-range elements at the store.
+ *
+ * Conventions shared by every entry point:
+ *   - All matrices are row-major.  A is M x K: A[i*lda + k].  C is M x N:
+ *     C[i*ldc + j].  B is K x N stored either as B[k*ldb + j]
+ *     (TGEMM_B_KN) or as its transpose, N x K: B[j*ldb + k] (TGEMM_B_NK).
+ *   - Leading dimensions are in elements.  ld * element size must be a
+ *     multiple of 16 bytes and every base pointer 16-byte aligned (the tensor
+ *     memory accelerator addresses rows in 16-byte units; CUDA Programming
+ *     Guide 13.4.2, section 2.4.12.2 "Mark array pointers as 16-byte
+ *     aligned").  There is no unaligned fallback.
+ *   - A, B and C are device memory owned by the caller and must not overlap
+ *     (section 2.4.12.1 of the same guide: __restrict__ arrays).  C is
+ *     overwritten, never accumulated into.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream).  Argument errors are detected on the host
+ *     before anything is launched and leave C untouched.
+ *   - The library owns only a 4-byte device status word per device, its
+ *     split-K workspace and a host cache of tensor descriptors; all are freed
+ *     by tgemm_shutdown().  Entry points are thread-safe.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TGEMM_B_KN = 0, TGEMM_B_NK = 1 } tgemm_b_layout;
+
+typedef enum { TGEMM_F16 = 0, TGEMM_BF16 = 1, TGEMM_F32 = 2 } tgemm_dtype;
+
+typedef enum {
+    TGEMM_OK = 0,
+    TGEMM_ERR_INVALID_ARG = 1,   /* negative size, NULL pointer, ld shorter than a row, bad enum  */
+    TGEMM_ERR_UNSUPPORTED = 2,   /* dtype combination or configuration the kernels do not provide */
+    TGEMM_ERR_MISALIGNED = 3,    /* pointer not 16-byte aligned or ld*elem not a multiple of 16   */
+    TGEMM_ERR_ARCH = 4,          /* current device is not compute capability 10.3 (sm_103)         */
+    TGEMM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed                               */
+    TGEMM_ERR_OOM = 6,           /* library-owned workspace could not be allocated                 */
+    TGEMM_ERR_TIMEOUT = 7        /* a kernel gave up on a pipeline wait and recorded it (see check) */
+} tgemm_status;
+
+/*
+ * A kernel configuration.  bm x bn is the output tile of one CTA pair
+ * (cluster_m = 2) or one CTA (cluster_m = 1); bk is the K depth of one
+ * pipeline stage; stages is the shared-memory ring depth; group_m is the
+ * GROUP_SIZE_M of the grouped rasterisation ("Performance optimisation:
+ * Swizzle" of the cuTile matrix multiplication tutorial); split_k > 1 splits
+ * the K loop over CTAs with an FP32 workspace; swap_ab != 0 computes
+ * C^T = B^T A^T so a short M becomes the MMA's N; grid is the number of
+ * persistent CTAs launched (0 = the library's choice).
+ */
+typedef struct {
+    int bm, bn, bk, stages, cluster_m, group_m, split_k, swap_ab, grid;
+} tgemm_config;
+
+/*
+ * C = A * B.  in_dtype (TGEMM_F16 or TGEMM_BF16) is the type of both A and
+ * B; out_dtype is TGEMM_F16, TGEMM_BF16 or TGEMM_F32.  M, N or K may be 0:
+ * M = 0 or N = 0 is a no-op; K = 0 writes zeros (the empty sum).
+ * Returns TGEMM_OK once the work is enqueued on `stream`.
+ */
+tgemm_status tgemm_run(int64_t M, int64_t N, int64_t K,
+                       const void *A, int64_t lda,
+                       const void *B, int64_t ldb, tgemm_b_layout b_layout,
+                       void *C, int64_t ldc,
+                       tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream);
+
+/* The configuration tgemm_run would use for this problem (no device work,
+ * but it reads the current device's SM count and compute capability). */
+tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
+                                tgemm_dtype in_dtype, tgemm_dtype out_dtype,
+                                tgemm_config *out_cfg);
+
+/* tgemm_run with an explicit configuration, for tuning and tests.  A
+ * configuration the kernels do not provide returns TGEMM_ERR_UNSUPPORTED. */
+tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K,
+                              const void *A, int64_t lda,
+                              const void *B, int64_t ldb, tgemm_b_layout b_layout,
+                              void *C, int64_t ldc,
+                              tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
+                              const tgemm_config *cfg);
+
+/* Synchronise `stream`, then report the first failure since the last check:
+ * a pending CUDA error (TGEMM_ERR_CUDA) or a kernel that timed out on a
+ * pipeline wait (TGEMM_ERR_TIMEOUT; the status word is then cleared). */
+tgemm_status tgemm_check(void *stream);
+
+/* The device status word's last recorded value for the current device
+ * (0 = none), without clearing it; for diagnostics after tgemm_check. */
+uint32_t tgemm_last_fault_code(void);
+
+/* A short English description of a status code (never NULL). */
+const char *tgemm_status_string(tgemm_status s);
+
+/* Free every library-owned resource on every device it touched. */
+void tgemm_shutdown(void);
+
+/*
+ * The grouped tile rasterisation used by the persistent scheduler, exposed
+ * for host-side tests: tile number `bid` of a grid of ceil(M/bm) x ceil(N/bn)
+ * output tiles maps to (tile row *bid_m, tile column *bid_n).  This is the
+ * swizzle_2d_from_bid mapping of "Writing high-performance matrix
+ * multiplication with NVIDIA CUDA Tile", section "Performance optimisation:
+ * Swizzle".  Returns TGEMM_ERR_INVALID_ARG if bid is outside the grid.
+ */
+tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn, int group_m, int64_t bid,
+                              int64_t *bid_m, int64_t *bid_n);
+
+/*
+ * Diagnostic: launch one block that waits on a pipeline barrier nobody
+ * signals, with a wait limit of `timeout_us` microseconds.  The kernel gives
+ * up, records TGEMM_ERR_TIMEOUT's fault code in the status word and returns;
+ * tgemm_check(stream) must then report TGEMM_ERR_TIMEOUT and the context
+ * stays usable.  This exercises the same bounded-wait routine the GEMM
+ * kernels use (the pipeline's "silent deadlock" risk named by the Croqtile
+ * tutorial's summary).
+ */
+tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

@@ -1,0 +1,179 @@
+"""Host-side tests of the C-ABI library (no GPU needed).
+
+The library must load, export every entry point include/tgemm.h declares, and
+reject bad arguments on the host before touching the device.  The scheduler's
+tile mapping is checked against the pages' worked examples.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from dense_tiled_gemm_persistent_gb300 import build as libbuild
+from dense_tiled_gemm_persistent_gb300 import tgemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return tgemm.load()
+
+
+def read_golden(name):
+    out = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, v = (s.strip() for s in line.split("=", 1))
+        out[k] = [float(x) if "." in x else int(x) for x in v.split()]
+    return out
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "tgemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tgemm_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = header_functions()
+    assert set(declared) == set(tgemm.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    nm = os.popen("nm -D --defined-only %s" % tgemm.LIB_PATH).read()
+    exported = set(re.findall(r" T (tgemm_\w+)", nm))
+    assert set(declared) <= exported
+    # nothing else leaks out of the library under our prefix
+    assert exported == set(declared)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = tgemm.status_string(code)
+        assert isinstance(s, str) and s
+    assert tgemm.status_string(0) == "ok"
+    assert "unknown" in tgemm.status_string(99)
+
+
+FAKE = 1 << 20   # a 16-byte aligned non-null address, never dereferenced by host checks
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(M=-1), tgemm.ERR_INVALID_ARG),
+    (dict(K=-5), tgemm.ERR_INVALID_ARG),
+    (dict(lda=63), tgemm.ERR_INVALID_ARG),            # lda < K
+    (dict(ldb=63), tgemm.ERR_INVALID_ARG),            # NK: ldb < K
+    (dict(ldc=95), tgemm.ERR_INVALID_ARG),            # ldc < N
+    (dict(A=0), tgemm.ERR_INVALID_ARG),
+    (dict(C=0), tgemm.ERR_INVALID_ARG),
+    (dict(A=FAKE + 8), tgemm.ERR_MISALIGNED),
+    (dict(C=FAKE + 4), tgemm.ERR_MISALIGNED),
+    (dict(lda=68), tgemm.ERR_MISALIGNED),             # 68 * 2 bytes is not a multiple of 16
+    (dict(ldc=98, out=tgemm.F32), tgemm.ERR_MISALIGNED),   # 392 bytes
+    (dict(layout=7), tgemm.ERR_INVALID_ARG),
+    (dict(ind=5), tgemm.ERR_INVALID_ARG),
+    (dict(out=9), tgemm.ERR_INVALID_ARG),
+    (dict(ind=tgemm.F32), tgemm.ERR_UNSUPPORTED),     # FP32 operands are not provided
+    (dict(M=1 << 31), tgemm.ERR_UNSUPPORTED),
+])
+def test_host_argument_checks(lib, case, expect):
+    a = dict(M=128, N=96, K=64, A=FAKE, lda=64, B=FAKE, ldb=64, layout=tgemm.B_NK, C=FAKE, ldc=96,
+             ind=tgemm.F16, out=tgemm.F16)
+    a.update(case)
+    rc = tgemm.tgemm_run(a["M"], a["N"], a["K"], a["A"], a["lda"], a["B"], a["ldb"], a["layout"],
+                         a["C"], a["ldc"], a["ind"], a["out"], None)
+    assert rc == expect, tgemm.status_string(rc)
+
+
+def test_empty_output_is_a_noop_without_device(lib):
+    # M = 0 or N = 0: nothing to do, not even a device query; NULL pointers are fine
+    assert tgemm.tgemm_run(0, 10, 10, 0, 10, 0, 10, tgemm.B_NK, 0, 10, tgemm.F16, tgemm.F16, None) == 0
+    assert tgemm.tgemm_run(10, 0, 10, 0, 10, 0, 10, tgemm.B_NK, 0, 0, tgemm.F16, tgemm.F16, None) == 0
+
+
+def test_run_config_rejects_unknown_configuration(lib):
+    cfg = tgemm.Config(bm=128, bn=200, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)
+    rc = tgemm.tgemm_run_config(128, 96, 64, FAKE, 64, FAKE, 64, tgemm.B_NK, FAKE, 96, tgemm.F16,
+                                tgemm.F16, None, cfg)
+    assert rc == tgemm.ERR_UNSUPPORTED
+
+
+# ---- tile space and grouped order ---------------------------------------------
+
+def coords(M, N, bm, bn, g):
+    rc, _, _ = tgemm.tgemm_tile_coord(M, N, bm, bn, g, 0)
+    assert rc == 0
+    tm, tn = -(-M // bm), -(-N // bn)
+    out = []
+    for bid in range(tm * tn):
+        rc, r, c = tgemm.tgemm_tile_coord(M, N, bm, bn, g, bid)
+        assert rc == 0
+        out.append((r, c))
+    assert tgemm.tgemm_tile_coord(M, N, bm, bn, g, tm * tn)[0] == tgemm.ERR_INVALID_ARG
+    return out
+
+
+def test_tile_space_of_figure_19(lib):
+    """CUDA Programming Guide 13.4.2, section 2.4.6.1, Figure 19."""
+    g = read_golden("tile_space_fig19.txt")
+    rows, cols = g["array_shape"]
+    th, tw = g["tile_shape"]
+    tiles = coords(rows, cols, th, tw, 1)
+    assert len(tiles) == g["tile_grid"][0] * g["tile_grid"][1]
+    assert max(r for r, _ in tiles) + 1 == g["tile_grid"][0]
+    assert max(c for _, c in tiles) + 1 == g["tile_grid"][1]
+    ti, tj = g["tile_index"]
+    assert (ti, tj) in tiles
+    first = (ti * th, tj * tw)
+    last = (min(ti * th + th, rows) - 1, min(tj * tw + tw, cols) - 1)
+    assert list(first) == g["first_element"] and list(last) == g["last_element"]
+
+
+def test_grouped_order_reads_of_figure_2(lib):
+    """cuTile tutorial, "Performance optimisation: Swizzle", Figure 2: the
+    first four tiles in row order touch 4 + 16 blocks, grouped 2 x 2 order
+    touches 8 + 8."""
+    g = read_golden("swizzle_fig2.txt")
+    gm, gn = g["grid"]
+    kb = g["k_blocks"][0]
+    n_out = g["outputs"][0]
+
+    def reads(group):
+        first = coords(gm, gn, 1, 1, group)[:n_out]
+        left = {(r, k) for r, _ in first for k in range(kb)}
+        right = {(k, c) for _, c in first for k in range(kb)}
+        return len(left), len(right)
+
+    assert reads(1) == (g["linear_left"][0], g["linear_right"][0])
+    assert sum(reads(1)) == g["linear_reads"][0]
+    assert reads(g["group_size_m"][0]) == (g["grouped_left"][0], g["grouped_right"][0])
+    assert sum(reads(g["group_size_m"][0])) == g["grouped_reads"][0]
+
+
+@pytest.mark.parametrize("group", [1, 2, 3, 4, 8, 16])
+def test_grouped_order_is_a_bijection(lib, group):
+    rng = np.random.default_rng(group)
+    shapes = [(1, 1), (5, 2), (7, 3), (64, 32), (33, 17)] + [tuple(rng.integers(1, 40, 2)) for _ in range(6)]
+    for tm, tn in shapes:
+        tiles = coords(int(tm), int(tn), 1, 1, group)
+        assert sorted(tiles) == [(r, c) for r in range(tm) for c in range(tn)]
+
+
+def test_grouped_order_within_full_bands(lib):
+    # In a full band, consecutive tile numbers walk down the band's rows first.
+    tiles = coords(16 * 128, 4 * 256, 128, 256, 8)
+    assert tiles[:10] == [(0, 0), (1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (6, 0), (7, 0), (0, 1), (1, 1)]
+    assert tiles[32] == (8, 0)
+
+
+def test_last_short_band_uses_the_tile_number(lib):
+    # 5 x 2 tiles, bands of 3 rows: the last band has 2 rows.  The row inside
+    # the band comes from the tile number (6 % 2 = 0), giving (3, 0) for tile 6.
+    tiles = coords(5, 2, 1, 1, 3)
+    assert tiles[6] == (3, 0)
+    assert tiles[7] == (4, 0)

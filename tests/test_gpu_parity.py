@@ -1,0 +1,196 @@
+"""GPU parity: the tcgen05 kernels against the FP64 CPU oracle, element by
+element, through the C ABI.
+
+Sizes span several tiles and ragged tails in M, N and K (the tail rules of
+the CUDA Programming Guide 13.4.2, section 2.4.9.1: zero-padded partial K
+tile, out-of-range M/N elements dropped at the store).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_tiled_gemm_persistent_gb300 import inputs as gen
+from dense_tiled_gemm_persistent_gb300 import tgemm
+
+from gpu_util import check_full, ensure_built, run_gpu, bits, values, assert_close, operands
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = [gen.B_NK, gen.B_KN]
+LNAME = {gen.B_NK: "nk", gen.B_KN: "kn"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def cfg(bn, stages=None, group_m=8, grid=0):
+    return tgemm.Config(bm=128, bn=bn, bk=64, stages=stages or (4 if bn == 256 else 6), cluster_m=1,
+                        group_m=group_m, split_k=1, swap_ab=0, grid=grid)
+
+
+# ---- one tile, exact integers: descriptor and layout sanity ------------------
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("bn", [256, 128])
+def test_one_tile_integers_exact(layout, bn):
+    M, N, K = 128, bn, 64
+    a, b = operands(M, N, K, gen.F16, layout, gen.ints(-2, 2), seed=1)
+    check_full(a, b, M, N, K, layout, gen.F16, gen.F32, exact=True, config=cfg(bn),
+               what="one tile %s bn=%d" % (LNAME[layout], bn))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_one_hot_products_land_in_place(layout):
+    """A single 1 in A at (i, k) and in B at (k, j): C is zero except C[i, j] = 1."""
+    M, N, K = 256, 512, 192
+    rng = np.random.default_rng(3)
+    for _ in range(4):
+        i, k, j = int(rng.integers(M)), int(rng.integers(K)), int(rng.integers(N))
+        a = torch.zeros(M, K, dtype=torch.bfloat16)
+        a[i, k] = 1
+        b = torch.zeros((K, N) if layout == gen.B_KN else (N, K), dtype=torch.bfloat16)
+        if layout == gen.B_KN:
+            b[k, j] = 1
+        else:
+            b[j, k] = 1
+        C = run_gpu(a, b, M, N, K, layout, gen.BF16, gen.F32)
+        v = values(C, gen.F32)
+        want = np.zeros((M, N))
+        want[i, j] = 1
+        assert np.array_equal(v, want), "one-hot (%d,%d,%d) misplaced: nonzeros at %s" % (
+            i, k, j, np.argwhere(v != 0)[:4].tolist())
+
+
+# ---- full comparisons over shapes, layouts, dtypes and tile widths --------------
+
+SHAPES = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (1, 1, 1), (640, 384, 1000), (17, 700, 130)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("in_dtype", [gen.F16, gen.BF16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("out_dtype", [gen.F32, gen.F16, gen.BF16], ids=["o32", "o16", "obf16"])
+def test_full_compare(shape, layout, in_dtype, out_dtype):
+    M, N, K = shape
+    seed = hash((M, N, K, layout, in_dtype, out_dtype)) % 1000
+    a, b = operands(M, N, K, in_dtype, layout, gen.normal(0, 1), seed=seed)
+    for bn in (256, 128):
+        check_full(a, b, M, N, K, layout, in_dtype, out_dtype, config=cfg(bn),
+                   what="%s %s bn=%d" % (shape, LNAME[layout], bn))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("out_dtype", [gen.F32, gen.F16, gen.BF16], ids=["o32", "o16", "obf16"])
+def test_integers_bit_exact_all_outputs(layout, out_dtype):
+    M, N, K = 384, 640, 520
+    a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=5)
+    for bn in (256, 128):
+        check_full(a, b, M, N, K, layout, gen.BF16, out_dtype, exact=True, config=cfg(bn),
+                   what="ints %s bn=%d" % (LNAME[layout], bn))
+
+
+@pytest.mark.parametrize("K", [1, 15, 16, 63, 64, 65, 127, 129, 1000])
+def test_k_tails(K):
+    M, N = 200, 300
+    for layout in LAYOUTS:
+        a, b = operands(M, N, K, gen.F16, layout, gen.uniform(-1, 1), seed=K)
+        check_full(a, b, M, N, K, layout, gen.F16, gen.F32, what="K=%d %s" % (K, LNAME[layout]))
+
+
+# ---- the persistent loop: many tiles per CTA -----------------------------------
+
+@pytest.mark.parametrize("grid", [1, 3, 0])
+@pytest.mark.parametrize("group_m", [1, 3, 8, 16])
+def test_persistent_tile_loop(grid, group_m):
+    """More tiles than CTAs, so each CTA runs the stage ring and both
+    accumulator buffers through several phases; the result may not depend on
+    the grid size or the tile order."""
+    M, N, K = 1100, 1300, 300
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.ints(-2, 2), seed=9)
+    for bn in (256, 128):
+        check_full(a, b, M, N, K, gen.B_NK, gen.BF16, gen.BF16, exact=True,
+                   config=cfg(bn, group_m=group_m, grid=grid),
+                   what="grid=%d group=%d bn=%d" % (grid, group_m, bn))
+
+
+def test_more_tiles_than_sms_default_config():
+    M, N, K = 4096, 2304, 256
+    a, b = operands(M, N, K, gen.F16, gen.B_KN, gen.uniform(-1, 1), seed=11)
+    check_full(a, b, M, N, K, gen.B_KN, gen.F16, gen.F16, what="4096x2304x256 default")
+
+
+# ---- padding, poison and degenerate sizes ---------------------------------------
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+def test_poisoned_padding_is_never_read_or_written(layout):
+    M, N, K = 300, 200, 150
+    b_cols = N if layout == gen.B_KN else K
+    lda, ldb, ldc = 152 + 24, -(-b_cols // 8) * 8 + 40, N + 56     # every row 16-byte aligned
+    a, b = gen.make_operands(M, N, K, gen.F16, layout, gen.normal(0, 1), None, seed=13,
+                             lda=lda, ldb=ldb, pad_value=float("nan"))
+    A, B = a.to("cuda:0"), b.to("cuda:0")
+    C = torch.full((M + 5, ldc), 12345.0, dtype=torch.float32, device="cuda:0")
+    rc = tgemm.tgemm_run(M, N, K, A.data_ptr(), lda, B.data_ptr(), b.shape[1], layout, C.data_ptr(), ldc,
+                         gen.F16, gen.F32, None)
+    assert rc == 0
+    assert tgemm.tgemm_check() == 0
+    Cc = C.cpu().double().numpy()
+    ref, bound = oracle.gemm(a, b, M, N, K, lda, b.shape[1], layout, gen.F16)
+    assert_close(Cc[:M, :N], ref, bound, gen.F32, "padded")
+    assert np.all(Cc[:M, N:] == 12345.0), "columns beyond N were written"
+    assert np.all(Cc[M:, :] == 12345.0), "rows beyond M were written"
+
+
+def test_k_zero_writes_the_empty_sum():
+    M, N = 70, 96
+    C = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda:0")
+    A = torch.empty(16, device="cuda:0", dtype=torch.bfloat16)
+    rc = tgemm.tgemm_run(M, N, 0, A.data_ptr(), 8, A.data_ptr(), 8, gen.B_NK, C.data_ptr(), N,
+                         gen.BF16, gen.BF16, None)
+    assert rc == 0 and tgemm.tgemm_check() == 0
+    assert torch.count_nonzero(C).item() == 0
+
+
+def test_empty_m_or_n_leaves_c_untouched():
+    C = torch.full((8, 8), 3.0, dtype=torch.float16, device="cuda:0")
+    assert tgemm.tgemm_run(0, 8, 8, 0, 8, 0, 8, gen.B_NK, C.data_ptr(), 8, gen.F16, gen.F16, None) == 0
+    assert tgemm.tgemm_run(8, 0, 8, 0, 8, 0, 8, gen.B_NK, C.data_ptr(), 8, gen.F16, gen.F16, None) == 0
+    assert tgemm.tgemm_check() == 0
+    assert torch.all(C == 3.0)
+
+
+# ---- streams, query and failure reporting -----------------------------------------
+
+def test_runs_on_a_side_stream():
+    M, N, K = 512, 768, 256
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.ints(-2, 2), seed=17)
+    s = torch.cuda.Stream()
+    C = run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F16, stream=s)
+    ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.F16)
+    assert np.array_equal(bits(C[:M, :N], gen.F16), oracle.round_bits(ref, gen.F16))
+
+
+def test_query_config_matches_what_runs():
+    rc, c = tgemm.tgemm_query_config(8192, 8192, 8192, gen.B_NK, gen.F16, gen.F16)
+    assert rc == 0
+    assert c.bm == 128 and c.bk == 64 and c.bn in (128, 256) and c.grid >= 1
+    assert c.grid <= torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on a barrier nothing signals gives up after ~1 ms; the host sees
+    TGEMM_ERR_TIMEOUT and the next GEMM still runs correctly."""
+    assert tgemm.tgemm_check() == 0
+    assert tgemm.tgemm_debug_wait_timeout(1000) == 0
+    assert tgemm.tgemm_check() == tgemm.ERR_TIMEOUT
+    code = tgemm.tgemm_last_fault_code()
+    assert code >> 28 == 7 and (code >> 20) & 0xff == 7
+    assert tgemm.tgemm_check() == 0
+    M, N, K = 256, 256, 128
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.ints(-2, 2), seed=19)
+    check_full(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, exact=True, what="after timeout")
