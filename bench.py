@@ -212,6 +212,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--config", default="auto", choices=["auto", "pair", "1cta256", "1cta128"],
+                    help="tile shape: the library's pick, or a forced one (tuning)")
+    ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -246,9 +249,22 @@ def main():
     sh = ctypes.c_void_p(stream.cuda_stream)
     lda, ldb, ldc = A.shape[1], B.shape[1], wl.N
 
+    rc, picked = tgemm.tgemm_query_config(wl.M, wl.N, wl.K, gen.B_NK, gen.F16, gen.F16)
+    if rc != 0:
+        raise RuntimeError("tgemm_query_config: " + tgemm.status_string(rc))
+    forced = None
+    if args.config != "auto" or args.group_m:
+        shapes = {"pair": (256, 256, 6, 2), "1cta256": (128, 256, 4, 1), "1cta128": (128, 128, 6, 1)}
+        bm, bn, st, cl = shapes[args.config] if args.config != "auto" else (
+            picked.bm, picked.bn, picked.stages, picked.cluster_m)
+        forced = tgemm.Config(bm=bm, bn=bn, bk=64, stages=st, cluster_m=cl,
+                              group_m=args.group_m or picked.group_m, split_k=1, swap_ab=0, grid=0)
+        picked = forced
+
     def step(c_ptr=None, a_ptr=None, b_ptr=None):
-        rc = tgemm.tgemm_run(wl.M, wl.N, wl.K, a_ptr or A.data_ptr(), lda, b_ptr or B.data_ptr(), ldb,
-                             gen.B_NK, c_ptr or C.data_ptr(), ldc, gen.F16, gen.F16, sh)
+        args_ = (wl.M, wl.N, wl.K, a_ptr or A.data_ptr(), lda, b_ptr or B.data_ptr(), ldb,
+                 gen.B_NK, c_ptr or C.data_ptr(), ldc, gen.F16, gen.F16, sh)
+        rc = tgemm.tgemm_run(*args_) if forced is None else tgemm.tgemm_run_config(*args_, forced)
         if rc != 0:
             raise RuntimeError("tgemm_run: " + tgemm.status_string(rc))
 
@@ -349,7 +365,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": value / PUBLISHED_TFLOPS, "dtype": "f16", "data": "synthetic",
-            "config": config_dict(wl, world), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "config": dict(config_dict(wl, world), kernel=picked.as_dict()), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": args.steps,
             "kernel_ms": {"mean": avg_launch, "median": statistics.median(launch_ms), "min": min(launch_ms)},
         }

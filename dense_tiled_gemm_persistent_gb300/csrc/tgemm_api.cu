@@ -11,9 +11,10 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 
-#include "tgemm_kernel.cuh"
+#include "tgemm_kernel_pair.cuh"
 #include "tgemm_params.h"
 #include "tgemm_sched.h"
 
@@ -30,6 +31,7 @@ struct DeviceState {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     uint32_t *status = nullptr;     // device status word, lazily allocated
+    std::map<const void *, int> pairs;   // resident CTA pairs per pair-kernel variant
 };
 
 std::mutex g_mu;
@@ -141,7 +143,7 @@ tgemm_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     return TGEMM_OK;
 }
 
-const KernelVariant *find_variant(int bn, int stages, int out, int b_mn)
+const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int cluster)
 {
     const KernelVariant *tab = nullptr;
     int n = 0;
@@ -152,39 +154,51 @@ const KernelVariant *find_variant(int bn, int stages, int out, int b_mn)
     default: return nullptr;
     }
     for (int i = 0; i < n; ++i)
-        if (tab[i].bn == bn && tab[i].stages == stages && tab[i].b_mn == b_mn) return &tab[i];
+        if (tab[i].bn == bn && tab[i].stages == stages && tab[i].b_mn == b_mn && tab[i].cluster == cluster)
+            return &tab[i];
     return nullptr;
 }
 
-int default_stages(int bn) { return bn == 256 ? 4 : 6; }
-
-// Tile-width choice.  A 128 x 256 tile does twice the MMA work of a 128 x 128
-// tile for 1.5x the shared-memory operand traffic, so it is preferred; the
-// narrower tile wins when it needs fewer waves of persistent CTAs.  The cost
-// model is waves * tile-time with tile-time ~ bn * (1 + 64 / bn).
-void choose_config(int64_t M, int64_t N, int sm_count, tgemm_config *cfg)
+void fill_config(tgemm_config *cfg, int cluster, int bn, int64_t tiles, int units)
 {
-    int best_bn = 0;
-    double best_cost = 0;
-    for (int bn : {256, 128}) {
-        const TileGrid g(M, N, kBM, bn);
-        const int64_t waves = ceil_div(g.count(), sm_count);
-        const double cost = (double)waves * (bn + 64);
-        if (best_bn == 0 || cost < best_cost) {
-            best_bn = bn;
-            best_cost = cost;
-        }
-    }
-    const TileGrid g(M, N, kBM, best_bn);
-    cfg->bm = kBM;
-    cfg->bn = best_bn;
+    cfg->bm = cluster == 2 ? kPairBM : kBM;
+    cfg->bn = bn;
     cfg->bk = kBK;
-    cfg->stages = default_stages(best_bn);
-    cfg->cluster_m = 1;
+    cfg->stages = cluster == 2 ? 6 : (bn == 256 ? 4 : 6);
+    cfg->cluster_m = cluster;
     cfg->group_m = kDefaultGroupM;
     cfg->split_k = 1;
     cfg->swap_ab = 0;
-    cfg->grid = (int)(g.count() < sm_count ? g.count() : sm_count);
+    const int64_t ctas = (tiles < units ? tiles : units) * cluster;
+    cfg->grid = (int)ctas;
+}
+
+// Tile-shape choice by a wave cost model: time ~ waves * (per-SM time of one
+// tile).  A CTA of the pair kernel and a 128 x 256 one-CTA tile do the same
+// MMA work per SM, but the pair moves a third fewer operand bytes per SM;
+// a 128 x 128 tile halves the work per SM for 2/3 of the bytes of a
+// 128 x 256 one and keeps the tensor pipe less busy.
+void choose_config(int64_t M, int64_t N, int sm_count, tgemm_config *cfg)
+{
+    struct Cand { int cluster, bn; double per_tile; };
+    const Cand cands[] = {{2, 256, 0.85 * 256}, {1, 256, 256}, {1, 128, 1.25 * 128}};
+    double best = 0;
+    const Cand *pick = nullptr;
+    int64_t pick_tiles = 0;
+    int pick_units = 0;
+    for (const Cand &c : cands) {
+        const int bm = c.cluster == 2 ? kPairBM : kBM;
+        const TileGrid g(M, N, bm, c.bn);
+        const int units = c.cluster == 2 ? sm_count / 2 : sm_count;
+        const double cost = (double)ceil_div(g.count(), units) * c.per_tile;
+        if (!pick || cost < best) {
+            pick = &c;
+            best = cost;
+            pick_tiles = g.count();
+            pick_units = units;
+        }
+    }
+    fill_config(cfg, pick->cluster, pick->bn, pick_tiles, pick_units);
 }
 
 CUtensorMapDataType map_dtype(int dt)
@@ -215,11 +229,24 @@ bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64
 
 tgemm_status legal_config(const tgemm_config &c, int out_dtype, int b_layout, const KernelVariant **v)
 {
-    if (c.bm != kBM || c.bk != kBK || c.cluster_m != 1 || c.split_k != 1 || c.swap_ab != 0)
+    if (c.bk != kBK || c.split_k != 1 || c.swap_ab != 0) return TGEMM_ERR_UNSUPPORTED;
+    if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
         return TGEMM_ERR_UNSUPPORTED;
     if (c.group_m < 1 || c.grid < 0) return TGEMM_ERR_UNSUPPORTED;
-    *v = find_variant(c.bn, c.stages, out_dtype, b_layout == TGEMM_B_KN ? 1 : 0);
+    *v = find_variant(c.bn, c.stages, out_dtype, b_layout == TGEMM_B_KN ? 1 : 0, c.cluster_m);
     return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+}
+
+// Resident CTA pairs for a pair-kernel variant on this device (cached).
+int resident_pairs(DeviceState *dev, const KernelVariant *v)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = dev->pairs.find((const void *)v);
+    if (it != dev->pairs.end()) return it->second;
+    int n = v->max_active ? v->max_active() : 0;
+    if (n <= 0) n = dev->sm_count / 2;
+    dev->pairs[(const void *)v] = n;
+    return n;
 }
 
 tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -256,7 +283,10 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         if (st != TGEMM_OK) return st;
     }
     const bool b_mn = b_layout == TGEMM_B_KN;
-    const TileGrid grid(M, N, kBM, cfg.bn);
+    const bool pair = cfg.cluster_m == 2;
+    const TileGrid grid(M, N, cfg.bm, cfg.bn);
+    // Rows of A and columns of B one CTA stages per k-block.
+    const uint32_t b_box_rows = pair ? (uint32_t)(cfg.bn / 2) : (uint32_t)cfg.bn;
 
     GemmParams p;
     std::memset(&p, 0, sizeof p);
@@ -264,8 +294,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     if (b_mn)
         ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, kBK);
     else
-        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kBK,
-                             (uint32_t)cfg.bn);
+        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kBK, b_box_rows);
     ok = ok && encode_2d(&p.tma_c, out_dtype, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc,
                          (uint32_t)(128 / eo), 32);
     if (!ok) return TGEMM_ERR_CUDA;
@@ -277,14 +306,26 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     p.num_tiles = (int32_t)grid.count();
     p.num_kb = (int32_t)ceil_div(K, kBK);
     p.group_m = cfg.group_m;
-    p.idesc = make_idesc(in_dtype == TGEMM_BF16, b_mn, kBM, cfg.bn);
+    p.idesc = make_idesc(in_dtype == TGEMM_BF16, b_mn, cfg.bm, cfg.bn);
     p.debug_flags = debug_flags;
     p.status = dev->status;
     p.timeout_ns = wait_timeout_ns();
 
-    int g = cfg.grid > 0 ? cfg.grid : dev->sm_count;
-    if (g > p.num_tiles) g = p.num_tiles;
-    if (g < 1) g = 1;
+    int g;
+    if (pair) {
+        // grid counts CTAs: an even number, at most two per tile and two per
+        // resident pair
+        int pairs = cfg.grid > 0 ? cfg.grid / 2 : dev->sm_count / 2;
+        const int resident = resident_pairs(dev, var);
+        if (pairs > resident) pairs = resident;
+        if (pairs > p.num_tiles) pairs = p.num_tiles;
+        if (pairs < 1) pairs = 1;
+        g = 2 * pairs;
+    } else {
+        g = cfg.grid > 0 ? cfg.grid : dev->sm_count;
+        if (g > p.num_tiles) g = p.num_tiles;
+        if (g < 1) g = 1;
+    }
     if (var->launch(p, g, stream) != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;

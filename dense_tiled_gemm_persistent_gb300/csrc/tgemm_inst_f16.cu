@@ -1,7 +1,8 @@
 // Compiled variants of the persistent GEMM kernel with F16 output.
 // Each entry: output tile width BN, ring depth STAGES, output type, B layout
-// (0 = B stored N x K, K-major; 1 = B stored K x N, MN-major).
-#include "tgemm_kernel.cuh"
+// (0 = B stored N x K, K-major; 1 = B stored K x N, MN-major); the pair
+// entries run 256 x 256 tiles on CTA pairs.
+#include "tgemm_kernel_pair.cuh"
 
 namespace tgemm {
 
@@ -10,6 +11,8 @@ const KernelVariant kVariantsF16[] = {
     TGEMM_VARIANT(256, 4, OUT_F16, 1),
     TGEMM_VARIANT(128, 6, OUT_F16, 0),
     TGEMM_VARIANT(128, 6, OUT_F16, 1),
+    TGEMM_PAIR_VARIANT(6, OUT_F16, 0),
+    TGEMM_PAIR_VARIANT(6, OUT_F16, 1),
 };
 const int kNumVariantsF16 = (int)(sizeof(kVariantsF16) / sizeof(kVariantsF16[0]));
 

@@ -123,14 +123,71 @@ __device__ __forceinline__ uint32_t pack_out(float lo, float hi, int out)
     return u;
 }
 
+// Drain one accumulator buffer held in this warp's TMEM lane quarter: tile
+// rows [row0, row0 + 32), columns [col0, col0 + BN).  Each 128-byte-wide
+// column chunk is read with tcgen05.ld, cast, written to one of this warp's
+// two swizzled staging blocks and stored with TMA.  `release()` runs on lane 0
+// once the last chunk is in registers, handing the buffer back to the MMA
+// issuer.  `cc` counts chunks (it selects the staging block).
+template <int BN, int OUT, typename Release>
+__device__ __forceinline__ void epilogue_drain(const GemmParams &p, uint32_t t_acc, uint32_t stage_base,
+                                               uint32_t &cc, int32_t row0, int32_t col0, int lane,
+                                               Release release)
+{
+    constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;          // columns of one 128-byte staged row
+    constexpr int kChunks = BN / kChunkCols;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+        uint32_t v0[32], v1[32];
+        ptx::tmem_ld_32x32b_x32(t_acc + c * kChunkCols, v0);
+        if constexpr (kChunkCols == 64) ptx::tmem_ld_32x32b_x32(t_acc + c * kChunkCols + 32, v1);
+        ptx::tmem_ld_wait();
+        if (c == kChunks - 1) {
+            // The accumulator buffer is fully read: hand it back.
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+        const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
+        if (lane == 0) ptx::bulk_wait_group_read<1>();   // the store that last used sbuf is done reading
+        __syncwarp();
+        const uint32_t row_addr = sbuf + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t w0, w1, w2, w3;
+            if constexpr (OUT == OUT_F32) {
+                w0 = v0[4 * j + 0];
+                w1 = v0[4 * j + 1];
+                w2 = v0[4 * j + 2];
+                w3 = v0[4 * j + 3];
+            } else {
+                // columns 8j .. 8j+7 of the 64-column chunk
+                const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+                w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
+                w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);
+                w2 = pack_out(__uint_as_float(src[4]), __uint_as_float(src[5]), OUT);
+                w3 = pack_out(__uint_as_float(src[6]), __uint_as_float(src[7]), OUT);
+            }
+            // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
+            ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const int32_t x = col0 + c * kChunkCols;
+            if (x < p.N && row0 < p.M) ptx::tma_store_2d(&p.tma_c, sbuf, x, row0);
+            ptx::bulk_commit_group();
+        }
+        ++cc;
+    }
+}
+
 template <int BN, int STAGES, int OUT, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p)
 {
     using Plan = SmemPlan<BN, STAGES>;
     constexpr uint32_t kStageBytes = Plan::a_stage + Plan::b_stage;
-    constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
-    constexpr int kChunkCols = 128 / kOutBytes;          // columns of one 128-byte staged row
-    constexpr int kChunks = BN / kChunkCols;
     constexpr uint32_t kTmemCols = TmemCols<BN>::value;
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
     static_assert(2 * BN <= 512, "two accumulator buffers must fit in tensor memory");
@@ -303,51 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             const int32_t row0 = (int32_t)tr * kBM + 32 * q;
             const int32_t col0 = (int32_t)tc * BN;
             const uint32_t t_acc = tmem_base + lane_base + buf * BN;
-
-#pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t v0[32], v1[32];
-                ptx::tmem_ld_32x32b_x32(t_acc + c * kChunkCols, v0);
-                if constexpr (kChunkCols == 64) ptx::tmem_ld_32x32b_x32(t_acc + c * kChunkCols + 32, v1);
-                ptx::tmem_ld_wait();
-                if (c == kChunks - 1) {
-                    // The accumulator buffer is fully read: hand it back to the MMA warp.
-                    ptx::tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
-                }
-                const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
-                if (lane == 0) ptx::bulk_wait_group_read<1>();   // the store that last used sbuf is done reading
-                __syncwarp();
-                const uint32_t row_addr = sbuf + lane * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t w0, w1, w2, w3;
-                    if constexpr (OUT == OUT_F32) {
-                        w0 = v0[4 * j + 0];
-                        w1 = v0[4 * j + 1];
-                        w2 = v0[4 * j + 2];
-                        w3 = v0[4 * j + 3];
-                    } else {
-                        // columns 8j .. 8j+7 of the 64-column chunk
-                        const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
-                        w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
-                        w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);
-                        w2 = pack_out(__uint_as_float(src[4]), __uint_as_float(src[5]), OUT);
-                        w3 = pack_out(__uint_as_float(src[6]), __uint_as_float(src[7]), OUT);
-                    }
-                    // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
-                    ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int32_t x = col0 + c * kChunkCols;
-                    if (x < p.N && row0 < p.M) ptx::tma_store_2d(&p.tma_c, sbuf, x, row0);
-                    ptx::bulk_commit_group();
-                }
-                ++cc;
-            }
+            const uint32_t release_bar = tempty_bar(buf);
+            epilogue_drain<BN, OUT>(p, t_acc, stage_base, cc, row0, col0, lane,
+                                    [&] { ptx::mbar_arrive(release_bar); });
         }
         if (lane == 0) ptx::bulk_wait_group_all();
         __syncwarp();
@@ -377,6 +392,6 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
 }
 
 #define TGEMM_VARIANT(BN, ST, OUT, BMN) \
-    {BN, ST, OUT, BMN, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, (BMN) != 0>}
+    {BN, ST, OUT, BMN, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, (BMN) != 0>, 1, nullptr}
 
 }  // namespace tgemm

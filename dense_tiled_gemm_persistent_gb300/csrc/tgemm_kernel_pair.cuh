@@ -1,0 +1,294 @@
+// Persistent GEMM on CTA pairs (tcgen05 cta_group::2): one 256 x 256 output
+// tile per cluster of two CTAs on neighbouring SMs.
+//
+// Each CTA of the pair stages its own half of both operands: the leader
+// (rank 0) rows [m0, m0 + 128) of A and B columns [n0, n0 + 128); the peer
+// (rank 1) the next 128 rows of A and the next 128 columns of B.  The leader's
+// single MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16),
+// which reads A and B from both CTAs' shared memory and writes each CTA's 128
+// rows of D into that CTA's tensor memory.  Per CTA and k-block that is 32 KiB
+// of operands for a 128 x 256 x 64 share of the work, against 48 KiB in the
+// one-CTA kernel: a third less L2 -> SM traffic, and a 6-stage ring fits.
+// Operand tiles are never multicast; every byte is loaded by the CTA that
+// holds it.  The tile lifecycle is the one of tgemm_kernel.cuh.
+//
+// Synchronisation across the pair:
+//   full[s]       leader only; the leader's producer arms it with the bytes of
+//                 both CTAs, both producers' TMA loads complete on it;
+//   empty[s]      in both CTAs; the leader's commit arrives on both;
+//   tmem_full[b]  in both CTAs; the leader's commit arrives on both;
+//   tmem_empty[b] leader only; all eight epilogue warps of the pair arrive.
+// A cluster barrier after barrier initialisation and another before the
+// tensor memory is freed keep either CTA from running ahead of the other.
+#pragma once
+
+#include "tgemm_kernel.cuh"
+
+namespace tgemm {
+
+constexpr int kPairBM = 256;        // rows of a pair tile (128 per CTA)
+constexpr int kPairBN = 256;        // columns of a pair tile (B split 128 + 128)
+
+template <int STAGES, int OUT, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p)
+{
+    constexpr int kHalfN = kPairBN / 2;
+    using Plan = SmemPlan<kHalfN, STAGES>;                 // A 16 KiB + B 16 KiB per stage
+    constexpr uint32_t kPairStageBytes = 2 * (Plan::a_stage + Plan::b_stage);
+    constexpr uint32_t kTmemCols = 512;                     // two 256-column accumulators
+    static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base + Plan::a_off;
+    const uint32_t sB = base + Plan::b_off;
+    const uint32_t sC = base + Plan::c_off;
+    const uint32_t bar = base + Plan::bar_off;
+    auto full_bar = [&](int s) { return bar + 8u * s; };
+    auto empty_bar = [&](int s) { return bar + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar + 8u * (2 * STAGES + 4);
+    const uint32_t slot = base + Plan::slot_off;
+    const uint32_t abort_addr = base + Plan::abort_off;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();           // 0 = leader, 1 = peer
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&p.tma_a);
+        ptx::prefetch_tensormap(&p.tma_b);
+        ptx::prefetch_tensormap(&p.tma_c);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(slot, kTmemCols);
+        ptx::tmem_relinquish_pair();
+        ptx::tc_fence_before_sync();
+    }
+    __syncthreads();
+    ptx::cluster_sync();          // both CTAs' barriers initialised, pair TMEM allocated
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
+
+    WaitCtx wc{p.status, abort_flag, p.timeout_ns};
+    wc.peer_abort = ptx::map_to_cta(abort_addr, rank ^ 1u);
+    const int num_tiles = p.num_tiles;
+    const int cluster_id = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+    bool aborted = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+                int64_t tr, tc;
+                grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+                const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank;
+                const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ptx::map_to_cta(full_bar(s), 0);   // the leader's barrier
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);
+                    const int32_t k0 = kb * kBK;
+                    ptx::tma_load_2d_pair(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0);
+                    if (B_MN) {
+#pragma unroll
+                        for (int j = 0; j < kHalfN / 64; ++j)
+                            ptx::tma_load_2d_pair(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
+                                                  n0 + 64 * j, k0);
+                    } else {
+                        ptx::tma_load_2d_pair(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0);
+                    }
+                    issued_mask |= 1u << s;
+                    issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                aborted = true;
+                // Wind down: the leader waits for the loads of both CTAs that
+                // complete on its barriers (bounded; a phase the peer never
+                // issued simply runs out).
+                if (leader)
+                    for (int t = 0; t < STAGES; ++t)
+                        if (issued_mask & (1u << t))
+                            wait_bounded(full_bar(t), (issued_parity >> t) & 1u, wc, SITE_DRAIN_LOADS, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA (leader)
+        if (lane == 0 && leader) {
+            const uint64_t kDescB = B_MN ? kDescMNMajor : kDescKMajor;
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t local = 0;
+            bool ok = true;
+            for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
+                const uint32_t buf = local & 1u;
+                const uint32_t bph = (local >> 1) & 1u;
+                if (!wait_bounded(tempty_bar(buf), bph ^ 1u, wc, SITE_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * kPairBN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a_addr = sA + s * Plan::a_stage;
+                    const uint32_t b_addr = sB + s * Plan::b_stage;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
+                        const uint64_t bd = desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
+                        ptx::mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit_pair(empty_bar(s), 0x3);   // stage s free in both CTAs
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(tfull_bar(buf), 0x3);     // both halves of the accumulator ready
+            }
+            if (!ok) {
+                aborted = true;
+                ptx::mma_commit_pair(drain_bar, 0x1);
+                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
+        uint32_t local = 0, cc = 0;
+        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+            const uint32_t buf = local & 1u;
+            const uint32_t bph = (local >> 1) & 1u;
+            const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
+            if (!__all_sync(0xffffffffu, got)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+
+            int64_t tr, tc;
+            grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+            const int32_t row0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 32 * q;
+            const int32_t col0 = (int32_t)tc * kPairBN;
+            const uint32_t t_acc = tmem_base + lane_base + buf * kPairBN;
+            const uint32_t release_bar = ptx::map_to_cta(tempty_bar(buf), 0);
+            epilogue_drain<kPairBN, OUT>(p, t_acc, stage_base, cc, row0, col0, lane,
+                                         [&] { ptx::mbar_arrive_cluster(release_bar); });
+        }
+        if (lane == 0) ptx::bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    if (aborted || *abort_flag) {
+        // After a timeout, give copies issued by either CTA of the pair (their
+        // completion may be signalled in the other CTA) time to land before
+        // the shared memory is released: about 200 us, far above a TMA round trip.
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::cluster_sync();          // neither CTA frees TMEM or exits while its partner still works
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <int STAGES, int OUT, bool B_MN>
+cudaError_t launch_gemm_pair(const GemmParams &p, int grid, cudaStream_t stream)
+{
+    auto kern = gemm_pair_kernel<STAGES, OUT, B_MN>;
+    constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Number of CTA pairs of this kernel that can be resident at once.
+template <int STAGES, int OUT, bool B_MN>
+int max_active_pairs()
+{
+    auto kern = gemm_pair_kernel<STAGES, OUT, B_MN>;
+    constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+#define TGEMM_PAIR_VARIANT(ST, OUT, BMN)                                                              \
+    {256, ST, OUT, BMN, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_pair<ST, OUT, (BMN) != 0>, \
+     2, &max_active_pairs<ST, OUT, (BMN) != 0>}
+
+}  // namespace tgemm

@@ -41,12 +41,17 @@ struct alignas(128) GemmParams {
 };
 
 using LaunchFn = cudaError_t (*)(const GemmParams &, int grid, cudaStream_t);
+using OccupancyFn = int (*)();
 
-// One compiled kernel variant.
+// One compiled kernel variant.  cluster = 1: one CTA per 128 x bn tile;
+// cluster = 2: a CTA pair per 256 x bn tile, and max_active reports how many
+// pairs fit on the device at once.
 struct KernelVariant {
     int bn, stages, out, b_mn;
     size_t smem_bytes;
     LaunchFn launch;
+    int cluster;
+    OccupancyFn max_active;
 };
 
 // Defined in the kernel translation units (one per output type).

@@ -21,12 +21,15 @@ struct WaitCtx {
     uint32_t *status;            // device status word
     volatile int *abort_flag;    // in shared memory, one per CTA
     uint64_t timeout_ns;
+    uint32_t peer_abort = 0;     // shared::cluster address of the pair partner's flag (0: none)
 };
 
 __device__ __forceinline__ void record_fault(const WaitCtx &w, uint32_t site)
 {
     const uint32_t code = (kFaultTimeout << 28) | ((site & 0xffu) << 20) | (blockIdx.x & 0xfffffu);
     *w.abort_flag = 1;
+    if (w.peer_abort)   // the partner CTA of a pair winds down too
+        asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(w.peer_abort), "r"(1) : "memory");
     if (w.status) atomicCAS(w.status, 0u, code);
 }
 

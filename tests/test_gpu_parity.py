@@ -28,20 +28,27 @@ def gpu():
     ensure_built()
 
 
-def cfg(bn, stages=None, group_m=8, grid=0):
+def cfg(bn, stages=None, group_m=8, grid=0, pair=False):
+    if pair:
+        return tgemm.Config(bm=256, bn=256, bk=64, stages=stages or 6, cluster_m=2, group_m=group_m,
+                            split_k=1, swap_ab=0, grid=grid)
     return tgemm.Config(bm=128, bn=bn, bk=64, stages=stages or (4 if bn == 256 else 6), cluster_m=1,
                         group_m=group_m, split_k=1, swap_ab=0, grid=grid)
+
+
+# every compiled tile shape: 128 x 256 and 128 x 128 on one CTA, 256 x 256 on a CTA pair
+SHAPE_CFGS = [("1cta_128x256", dict(bn=256)), ("1cta_128x128", dict(bn=128)), ("pair_256x256", dict(bn=256, pair=True))]
 
 
 # ---- one tile, exact integers: descriptor and layout sanity ------------------
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-@pytest.mark.parametrize("bn", [256, 128])
-def test_one_tile_integers_exact(layout, bn):
-    M, N, K = 128, bn, 64
+@pytest.mark.parametrize("name,kw", SHAPE_CFGS, ids=[n for n, _ in SHAPE_CFGS])
+def test_one_tile_integers_exact(layout, name, kw):
+    M, N, K = (256 if kw.get("pair") else 128), kw["bn"], 64
     a, b = operands(M, N, K, gen.F16, layout, gen.ints(-2, 2), seed=1)
-    check_full(a, b, M, N, K, layout, gen.F16, gen.F32, exact=True, config=cfg(bn),
-               what="one tile %s bn=%d" % (LNAME[layout], bn))
+    check_full(a, b, M, N, K, layout, gen.F16, gen.F32, exact=True, config=cfg(**kw),
+               what="one tile %s %s" % (LNAME[layout], name))
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
@@ -79,9 +86,9 @@ def test_full_compare(shape, layout, in_dtype, out_dtype):
     M, N, K = shape
     seed = hash((M, N, K, layout, in_dtype, out_dtype)) % 1000
     a, b = operands(M, N, K, in_dtype, layout, gen.normal(0, 1), seed=seed)
-    for bn in (256, 128):
-        check_full(a, b, M, N, K, layout, in_dtype, out_dtype, config=cfg(bn),
-                   what="%s %s bn=%d" % (shape, LNAME[layout], bn))
+    for name, kw in SHAPE_CFGS:
+        check_full(a, b, M, N, K, layout, in_dtype, out_dtype, config=cfg(**kw),
+                   what="%s %s %s" % (shape, LNAME[layout], name))
 
 
 @pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
@@ -89,9 +96,9 @@ def test_full_compare(shape, layout, in_dtype, out_dtype):
 def test_integers_bit_exact_all_outputs(layout, out_dtype):
     M, N, K = 384, 640, 520
     a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=5)
-    for bn in (256, 128):
-        check_full(a, b, M, N, K, layout, gen.BF16, out_dtype, exact=True, config=cfg(bn),
-                   what="ints %s bn=%d" % (LNAME[layout], bn))
+    for name, kw in SHAPE_CFGS:
+        check_full(a, b, M, N, K, layout, gen.BF16, out_dtype, exact=True, config=cfg(**kw),
+                   what="ints %s %s" % (LNAME[layout], name))
 
 
 @pytest.mark.parametrize("K", [1, 15, 16, 63, 64, 65, 127, 129, 1000])
@@ -99,29 +106,34 @@ def test_k_tails(K):
     M, N = 200, 300
     for layout in LAYOUTS:
         a, b = operands(M, N, K, gen.F16, layout, gen.uniform(-1, 1), seed=K)
-        check_full(a, b, M, N, K, layout, gen.F16, gen.F32, what="K=%d %s" % (K, LNAME[layout]))
+        for name, kw in SHAPE_CFGS:
+            check_full(a, b, M, N, K, layout, gen.F16, gen.F32, config=cfg(**kw),
+                       what="K=%d %s %s" % (K, LNAME[layout], name))
 
 
 # ---- the persistent loop: many tiles per CTA -----------------------------------
 
-@pytest.mark.parametrize("grid", [1, 3, 0])
+@pytest.mark.parametrize("grid", [2, 6, 0])
 @pytest.mark.parametrize("group_m", [1, 3, 8, 16])
 def test_persistent_tile_loop(grid, group_m):
     """More tiles than CTAs, so each CTA runs the stage ring and both
     accumulator buffers through several phases; the result may not depend on
     the grid size or the tile order."""
     M, N, K = 1100, 1300, 300
-    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.ints(-2, 2), seed=9)
-    for bn in (256, 128):
-        check_full(a, b, M, N, K, gen.B_NK, gen.BF16, gen.BF16, exact=True,
-                   config=cfg(bn, group_m=group_m, grid=grid),
-                   what="grid=%d group=%d bn=%d" % (grid, group_m, bn))
+    for layout in LAYOUTS:
+        a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=9)
+        for name, kw in SHAPE_CFGS:
+            check_full(a, b, M, N, K, layout, gen.BF16, gen.BF16, exact=True,
+                       config=cfg(group_m=group_m, grid=grid, **kw),
+                       what="grid=%d group=%d %s %s" % (grid, group_m, LNAME[layout], name))
 
 
-def test_more_tiles_than_sms_default_config():
-    M, N, K = 4096, 2304, 256
+@pytest.mark.parametrize("name,kw", SHAPE_CFGS + [("default", None)], ids=[n for n, _ in SHAPE_CFGS] + ["default"])
+def test_more_tiles_than_sms(name, kw):
+    M, N, K = 4096, 2304 + 256 * 12, 256
     a, b = operands(M, N, K, gen.F16, gen.B_KN, gen.uniform(-1, 1), seed=11)
-    check_full(a, b, M, N, K, gen.B_KN, gen.F16, gen.F16, what="4096x2304x256 default")
+    check_full(a, b, M, N, K, gen.B_KN, gen.F16, gen.F16, config=None if kw is None else cfg(**kw),
+               what="%dx%dx%d %s" % (M, N, K, name))
 
 
 # ---- padding, poison and degenerate sizes ---------------------------------------
