@@ -190,7 +190,9 @@ def test_runs_on_a_side_stream():
 def test_query_config_matches_what_runs():
     rc, c = tgemm.tgemm_query_config(8192, 8192, 8192, gen.B_NK, gen.F16, gen.F16)
     assert rc == 0
-    assert c.bm == 128 and c.bk == 64 and c.bn in (128, 256) and c.grid >= 1
+    assert c.bk == 64 and c.bn in (128, 256) and c.grid >= 1
+    assert (c.cluster_m, c.bm) in ((1, 128), (2, 256))
+    assert c.grid % c.cluster_m == 0
     assert c.grid <= torch.cuda.get_device_properties(0).multi_processor_count
 
 
