@@ -32,6 +32,8 @@ WORKLOAD = "gemm_8192x8192x8192_f16_nk_f16"
 METRIC = "GEMM TFLOPS (device-timed) and fraction of GB300 dense FP16/BF16 tensor peak"
 PUBLISHED_TFLOPS = 489.9      # Croqtile v4 on H800 PCIe, same shape and B layout (context, other GPU)
 FALLBACK_TENSOR_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1000 * 1000
 KERNEL_SOURCES = ["tgemm_kernel.cuh", "tgemm_ptx.cuh", "tgemm_wait.cuh", "tgemm_sched.h", "tgemm_params.h"]
 
 
@@ -133,9 +135,9 @@ class ClockSampler:
 
 # ---- workload --------------------------------------------------------------------
 
-def workload():
+def workload(name=WORKLOAD):
     from dense_tiled_gemm_persistent_gb300 import inputs as gen
-    return gen.WORKLOADS[WORKLOAD]
+    return gen.WORKLOADS[name]
 
 
 def cpu_oracle_sample(wl, a, b, budget_s: float, threads: int):
@@ -197,9 +199,14 @@ def run_reference(args, rank, world):
 
 
 def config_dict(wl, world):
-    return {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "in_dtype": "f16", "out_dtype": "f16",
-            "accumulate": "f32", "b_layout": "NxK", "values": "uniform[-0.5,0.5) seed 3",
-            "l2": "operands+output 384 MiB > 129 MB L2 (no flush needed)",
+    from dense_tiled_gemm_persistent_gb300 import inputs as gen
+    flush = wl.algorithmic_bytes < 2 * L2_BYTES
+    return {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+            "in_dtype": gen.DTYPE_NAME[wl.in_dtype], "out_dtype": gen.DTYPE_NAME[wl.out_dtype],
+            "accumulate": "f32", "b_layout": "NxK" if wl.b_layout == gen.B_NK else "KxN",
+            "values": "A %s, B %s, seed %d" % (wl.dist_a.describe(), wl.dist_b.describe(), wl.seed),
+            "l2": ("512 MiB L2 scrub between timed launches (inputs %.1f MB)" % (wl.algorithmic_bytes / 1e6))
+            if flush else ("operands+output %.0f MB > 129 MB L2, back to back" % (wl.algorithmic_bytes / 1e6)),
             "parallelism": "replicas%d" % world if world > 1 else "single-gpu"}
 
 
@@ -215,6 +222,8 @@ def main():
     ap.add_argument("--config", default="auto", choices=["auto", "pair", "1cta256", "1cta128"],
                     help="tile shape: the library's pick, or a forced one (tuning)")
     ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="another named workload (parity-test configurations; not the headline line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -241,15 +250,15 @@ def main():
     libbuild.build()
     tgemm.load()
 
-    wl = workload()
+    wl = workload(args.workload)
     a_cpu, b_cpu = wl.operands()
     A, B = a_cpu.to(dev), b_cpu.to(dev)
-    C = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+    C = torch.empty((wl.M, wl.N), dtype=gen.TORCH_DTYPE[wl.out_dtype], device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
     lda, ldb, ldc = A.shape[1], B.shape[1], wl.N
 
-    rc, picked = tgemm.tgemm_query_config(wl.M, wl.N, wl.K, gen.B_NK, gen.F16, gen.F16)
+    rc, picked = tgemm.tgemm_query_config(wl.M, wl.N, wl.K, wl.b_layout, wl.in_dtype, wl.out_dtype)
     if rc != 0:
         raise RuntimeError("tgemm_query_config: " + tgemm.status_string(rc))
     forced = None
@@ -263,7 +272,7 @@ def main():
 
     def step(c_ptr=None, a_ptr=None, b_ptr=None):
         args_ = (wl.M, wl.N, wl.K, a_ptr or A.data_ptr(), lda, b_ptr or B.data_ptr(), ldb,
-                 gen.B_NK, c_ptr or C.data_ptr(), ldc, gen.F16, gen.F16, sh)
+                 wl.b_layout, c_ptr or C.data_ptr(), ldc, wl.in_dtype, wl.out_dtype, sh)
         rc = tgemm.tgemm_run(*args_) if forced is None else tgemm.tgemm_run_config(*args_, forced)
         if rc != 0:
             raise RuntimeError("tgemm_run: " + tgemm.status_string(rc))
@@ -282,15 +291,28 @@ def main():
     sampler = ClockSampler(uuid)
     sampler.start()
 
-    # per-launch events for the kernel's own duration, plus the whole region
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # Inputs smaller than twice the L2 are timed launch by launch with a
+    # 512 MiB write between launches that evicts them from L2; larger ones
+    # back to back (they cannot stay in L2 anyway).
+    flush = wl.algorithmic_bytes < 2 * L2_BYTES
+    scrub = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
+    if flush:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            scrub.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    else:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step()
+            ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -298,8 +320,12 @@ def main():
     rc = tgemm.tgemm_check(sh)
     if rc != 0:
         raise RuntimeError("timed region failed: " + tgemm.status_string(rc))
-    total_ms = ev[0].elapsed_time(ev[-1])
-    launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    if flush:
+        launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        total_ms = sum(launch_ms)          # launches only; the L2 scrub between them is not counted
+    else:
+        total_ms = ev[0].elapsed_time(ev[-1])
+        launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -311,15 +337,27 @@ def main():
 
     peaks = measured_peaks()
     if peaks and peaks.get("bf16_tflops"):
-        peak, peak_src = float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate equals bf16)"
+        peak_t, src_t = float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate equals bf16)"
     else:
-        peak, peak_src = FALLBACK_TENSOR_TFLOPS, "fallback"
-    achieved = tflops(wl.M, wl.N, wl.K, avg_launch)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
-                "algorithmic_bytes": wl.algorithmic_bytes, "flops_per_launch": wl.flops}
-    if peaks and peaks.get("bf16_tflops_sustained"):
-        roofline["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+        peak_t, src_t = FALLBACK_TENSOR_TFLOPS, "fallback"
+    if peaks and peaks.get("hbm_gbs"):
+        peak_h, src_h = float(peaks["hbm_gbs"]), "measured (copy)"
+    else:
+        peak_h, src_h = FALLBACK_HBM_GBS, "fallback"
+    ridge = peak_t * 1e12 / (peak_h * 1e9)          # FLOP per byte where the two roofs meet
+    ai = wl.flops / wl.algorithmic_bytes
+    if ai >= ridge:
+        achieved = tflops(wl.M, wl.N, wl.K, avg_launch)
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                    "frac": achieved / peak_t, "peak_source": src_t}
+        if peaks and peaks.get("bf16_tflops_sustained"):
+            roofline["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+    else:
+        achieved = wl.algorithmic_bytes / (avg_launch * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_h, "unit": "GB/s",
+                    "frac": achieved / peak_h, "peak_source": src_h}
+    roofline.update({"traffic": recorded_traffic(wl.name), "algorithmic_bytes": wl.algorithmic_bytes,
+                     "flops_per_launch": wl.flops, "arithmetic_intensity": ai})
 
     # end to end through the C ABI with host buffers: H2D of A and B from
     # pinned memory, the GEMM, D2H of C into pinned memory, every step
@@ -327,7 +365,7 @@ def main():
     if not args.no_e2e:
         ha = a_cpu.pin_memory()
         hb = b_cpu.pin_memory()
-        hc = torch.empty((wl.M, wl.N), dtype=torch.float16).pin_memory()
+        hc = torch.empty((wl.M, wl.N), dtype=gen.TORCH_DTYPE[wl.out_dtype]).pin_memory()
         A2, B2 = torch.empty_like(A), torch.empty_like(B)
         C2 = torch.empty_like(C)
         for _ in range(2):
@@ -348,10 +386,10 @@ def main():
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
         e2e = {"value": tflops(wl.M, wl.N, wl.K, e2e_ms) * world, "unit": "TFLOPS",
                "h2d_bytes_per_step": a_cpu.numel() * 2 + b_cpu.numel() * 2,
-               "d2h_bytes_per_step": hc.numel() * 2, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": hc.numel() * hc.element_size(), "ms_per_step": e2e_ms}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
         import oracle
         oracle.build()
         threads = os.cpu_count() or 1
@@ -364,7 +402,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": value / PUBLISHED_TFLOPS, "dtype": "f16", "data": "synthetic",
+            "vs_baseline": value / PUBLISHED_TFLOPS if wl.name == WORKLOAD else None,
+            "dtype": gen.DTYPE_NAME[wl.in_dtype], "data": "synthetic",
             "config": dict(config_dict(wl, world), kernel=picked.as_dict()), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": args.steps,
             "kernel_ms": {"mean": avg_launch, "median": statistics.median(launch_ms), "min": min(launch_ms)},

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "tgemm_kernel_pair.cuh"
+#include "tgemm_kernel_skinny.cuh"
 #include "tgemm_params.h"
 #include "tgemm_sched.h"
 
@@ -36,6 +37,16 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Split-K workspace, one per (device, stream) so that calls on different
+// streams never share partial sums: [counters: kCounterBytes][partials].
+constexpr size_t kCounterBytes = 64 * 1024;        // 16384 tile counters
+constexpr int kMaxSkinnyTiles = (int)(kCounterBytes / 4);
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, void *>, Workspace> g_ws;
 std::atomic<uint32_t> g_last_fault{0};   // last non-zero status word seen by tgemm_check
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -173,13 +184,43 @@ void fill_config(tgemm_config *cfg, int cluster, int bn, int64_t tiles, int unit
     cfg->grid = (int)ctas;
 }
 
+int skinny_npad(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
+// Splits of the K loop for the swap-AB path: about two CTAs per SM stream
+// the weights, every split keeps at least one k-block.
+int skinny_splits(int64_t N, int64_t K, int sm_count)
+{
+    const int64_t tiles = ceil_div(N, kSkinnyRows);
+    const int64_t kb = ceil_div(K, kBK);
+    if (tiles > kMaxSkinnyTiles) return 1;
+    int64_t s = (2 * sm_count + tiles / 2) / tiles;
+    if (s > kb) s = kb;
+    if (s > 32) s = 32;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
 // Tile-shape choice by a wave cost model: time ~ waves * (per-SM time of one
 // tile).  A CTA of the pair kernel and a 128 x 256 one-CTA tile do the same
 // MMA work per SM, but the pair moves a third fewer operand bytes per SM;
 // a 128 x 128 tile halves the work per SM for 2/3 of the bytes of a
-// 128 x 256 one and keeps the tensor pipe less busy.
-void choose_config(int64_t M, int64_t N, int sm_count, tgemm_config *cfg)
+// 128 x 256 one and keeps the tensor pipe less busy.  At most 64 rows of A
+// go to the swap-AB split-K path instead.
+void choose_config(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg)
 {
+    if (M <= 64) {
+        const int s = skinny_splits(N, K, sm_count);
+        cfg->bm = kSkinnyRows;
+        cfg->bn = skinny_npad(M);
+        cfg->bk = kBK;
+        cfg->stages = kSkinnyStages;
+        cfg->cluster_m = 1;
+        cfg->group_m = 1;
+        cfg->split_k = s;
+        cfg->swap_ab = 1;
+        cfg->grid = (int)(ceil_div(N, kSkinnyRows) * s);
+        return;
+    }
     struct Cand { int cluster, bn; double per_tile; };
     const Cand cands[] = {{2, 256, 0.85 * 256}, {1, 256, 256}, {1, 128, 1.25 * 128}};
     double best = 0;
@@ -227,14 +268,56 @@ bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-tgemm_status legal_config(const tgemm_config &c, int out_dtype, int b_layout, const KernelVariant **v)
+tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_dtype, int b_layout,
+                          const KernelVariant **v)
 {
-    if (c.bk != kBK || c.split_k != 1 || c.swap_ab != 0) return TGEMM_ERR_UNSUPPORTED;
+    if (c.bk != kBK || c.grid < 0 || c.group_m < 1) return TGEMM_ERR_UNSUPPORTED;
+    const int b_mn = b_layout == TGEMM_B_KN ? 1 : 0;
+    if (c.swap_ab) {
+        // swap-AB: bm weight rows per CTA, bn = padded token count >= M
+        if (c.bm != kSkinnyRows || c.cluster_m != 1 || c.stages != kSkinnyStages) return TGEMM_ERR_UNSUPPORTED;
+        if (c.bn < M || c.split_k < 1 || c.split_k > 1024 || c.split_k > ceil_div(K > 0 ? K : 1, kBK))
+            return TGEMM_ERR_UNSUPPORTED;
+        *v = find_variant(c.bn, c.stages, out_dtype, b_mn, 0);
+        return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+    }
+    if (c.split_k != 1) return TGEMM_ERR_UNSUPPORTED;
     if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
         return TGEMM_ERR_UNSUPPORTED;
-    if (c.group_m < 1 || c.grid < 0) return TGEMM_ERR_UNSUPPORTED;
-    *v = find_variant(c.bn, c.stages, out_dtype, b_layout == TGEMM_B_KN ? 1 : 0, c.cluster_m);
+    *v = find_variant(c.bn, c.stages, out_dtype, b_mn, c.cluster_m);
     return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+}
+
+// The split-K workspace of (current device, stream), grown on demand; the
+// counter region is zeroed (stream-ordered) whenever it is (re)allocated and
+// is kept zero by the kernels themselves.
+tgemm_status split_workspace(int dev, void *stream, size_t partial_bytes, uint32_t **counters, float **partials)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_ws[std::make_pair(dev, stream)];
+    const size_t need = kCounterBytes + partial_bytes;
+    if (w.bytes < need) {
+        if (w.ptr) {
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        void *p = nullptr;
+        if (cudaMalloc(&p, need) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_OOM;
+        }
+        if (cudaMemsetAsync(p, 0, kCounterBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+            cudaFree(p);
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        w.ptr = p;
+        w.bytes = need;
+    }
+    *counters = static_cast<uint32_t *>(w.ptr);
+    *partials = reinterpret_cast<float *>(static_cast<char *>(w.ptr) + kCounterBytes);
+    return TGEMM_OK;
 }
 
 // Resident CTA pairs for a pair-kernel variant on this device (cached).
@@ -249,6 +332,54 @@ int resident_pairs(DeviceState *dev, const KernelVariant *v)
     return n;
 }
 
+// C^T = B^T A^T on the swap-AB split-K kernel (M <= 64).
+tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                        int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype, void *stream_ptr,
+                        const tgemm_config &cfg, const KernelVariant *var, DeviceState *dev)
+{
+    const bool w_mn = b_layout == TGEMM_B_KN;
+    const int npad = cfg.bn;
+    const int64_t tiles_n = ceil_div(N, kSkinnyRows);
+    int splits = cfg.split_k;
+    if (tiles_n > kMaxSkinnyTiles) splits = 1;
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    bool ok = encode_2d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kBK, (uint32_t)npad);
+    if (w_mn)
+        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, kBK);
+    else
+        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kBK, kSkinnyRows);
+    if (!ok) return TGEMM_ERR_CUDA;
+    p.M = (int32_t)M;
+    p.N = (int32_t)N;
+    p.K = (int32_t)K;
+    p.tiles_m = 1;
+    p.tiles_n = (int32_t)tiles_n;
+    p.num_tiles = (int32_t)tiles_n;
+    p.num_kb = (int32_t)ceil_div(K, kBK);
+    p.group_m = 1;
+    p.idesc = make_idesc(in_dtype == TGEMM_BF16, false, kSkinnyRows, npad, w_mn);
+    p.status = dev->status;
+    p.timeout_ns = wait_timeout_ns();
+    p.c_ptr = C;
+    p.ldc = ldc;
+    p.splits = splits;
+    if (splits > 1) {
+        int devno = 0;
+        cudaGetDevice(&devno);
+        const size_t part = (size_t)splits * (size_t)tiles_n * (size_t)npad * kSkinnyRows * sizeof(float);
+        tgemm_status st = split_workspace(devno, stream_ptr, part, &p.counters, &p.partials);
+        if (st != TGEMM_OK) return st;
+    }
+    const int64_t grid = tiles_n * splits;
+    if (grid > INT32_MAX) return TGEMM_ERR_UNSUPPORTED;
+    if (var->launch(p, (int)grid, static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
 tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                       int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
                       void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags)
@@ -260,7 +391,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     const KernelVariant *var = nullptr;
     if (forced) {
         cfg = *forced;
-        st = legal_config(cfg, out_dtype, b_layout, &var);
+        st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
         if (st != TGEMM_OK) return st;
     }
     if (noop) return TGEMM_OK;
@@ -278,10 +409,13 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         return TGEMM_OK;
     }
     if (!forced) {
-        choose_config(M, N, dev->sm_count, &cfg);
-        st = legal_config(cfg, out_dtype, b_layout, &var);
+        choose_config(M, N, K, dev->sm_count, &cfg);
+        st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
         if (st != TGEMM_OK) return st;
     }
+    if (cfg.swap_ab)
+        return run_skinny(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream_ptr, cfg, var,
+                          dev);
     const bool b_mn = b_layout == TGEMM_B_KN;
     const bool pair = cfg.cluster_m == 2;
     const TileGrid grid(M, N, cfg.bm, cfg.bn);
@@ -367,7 +501,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     DeviceState *dev = nullptr;
     tgemm_status st = device_state(&dev);
     if (st != TGEMM_OK) return st;
-    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, dev->sm_count, out_cfg);
+    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, dev->sm_count, out_cfg);
     return TGEMM_OK;
 }
 
@@ -396,6 +530,13 @@ TGEMM_EXPORT tgemm_status tgemm_check(void *stream)
     }
     if (word == 0) return TGEMM_OK;
     g_last_fault.store(word);
+    {
+        // A kernel gave up part-way: split-K arrival counters may be left
+        // non-zero; clear them so the next call starts clean.
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (auto &kv : g_ws)
+            if (kv.first.first == dev && kv.second.ptr) cudaMemset(kv.second.ptr, 0, kCounterBytes);
+    }
     if (cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
@@ -425,6 +566,13 @@ TGEMM_EXPORT void tgemm_shutdown(void)
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = -1;
     cudaGetDevice(&cur);
+    for (auto &kv : g_ws) {
+        if (kv.second.ptr) {
+            cudaSetDevice(kv.first.first);
+            cudaFree(kv.second.ptr);
+        }
+    }
+    g_ws.clear();
     for (int d = 0; d < kMaxDevices; ++d) {
         if (g_dev[d].status) {
             cudaSetDevice(d);

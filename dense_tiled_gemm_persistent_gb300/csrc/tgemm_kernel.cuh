@@ -80,11 +80,13 @@ constexpr uint64_t kDescMNMajor = desc_sw128(kBK * 128, 1024);
 // ---- instruction descriptor (kind::f16) -------------------------------------
 //
 // Bits 4-5 D type (1 = F32), 7-9 A type and 10-12 B type (0 = F16, 1 = BF16),
-// 15 A major (0 = K), 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16, bool b_mn_major, int m, int n)
+// 15 A major and 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, bool b_mn_major, int m, int n,
+                                                  bool a_mn_major = false)
 {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+           ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
 }
 
 // ---- shared-memory plan ---------------------------------------------------

@@ -1,0 +1,269 @@
+// Skinny GEMM (a handful of rows of A, e.g. 16 tokens through a projection):
+// swap-AB plus split-K.
+//
+// With M = 16 a 128-row tile would leave 7/8 of every MMA empty and only
+// N/BN CTAs would stream the weights.  Instead the kernel computes
+// C^T = B^T * A^T: the weight rows (N) feed the MMA's M = 128 side and the
+// M tokens, padded to NPAD (16, 32 or 64), become the MMA's N.  K is cut into
+// `splits` runs of whole 64-deep k-blocks so that tiles_n * splits CTAs (two
+// to three per SM) stream the weight matrix from HBM at once.  This is a
+// memory-bound shape: about 16 FLOP per byte, far under the tensor ridge
+// (the roofline argument of the wmrh.cn essay on GEMM tiling, sections 1.1
+// and 3.3); splitting K is this library's own choice, not from the pages.
+//
+// Every CTA accumulates its partial D (128 weight rows x NPAD tokens, FP32)
+// in tensor memory.  With one split it casts and stores C directly.
+// Otherwise it writes the partial to a workspace, fences, and bumps the
+// tile's arrival counter; the CTA that arrives last sums the `splits`
+// partials in split order 0, 1, ..., splits-1 (a fixed order, so results do
+// not depend on which CTA finishes last), casts with round-to-nearest-even,
+// writes C and resets the counter to zero for the next call.  Nobody waits
+// for another CTA.
+#pragma once
+
+#include "tgemm_kernel.cuh"
+
+namespace tgemm {
+
+constexpr int kSkinnyStages = 4;
+constexpr int kSkinnyRows = 128;      // weight rows (C columns) per CTA
+
+template <int NPAD>
+struct SkinnyPlan {
+    static constexpr uint32_t w_stage = kSkinnyRows * kBK * 2;   // 16 KiB
+    static constexpr uint32_t x_stage = NPAD * kBK * 2;          // 2, 4 or 8 KiB
+    static constexpr uint32_t w_off = 0;
+    static constexpr uint32_t x_off = w_off + kSkinnyStages * w_stage;
+    static constexpr uint32_t bar_off = x_off + kSkinnyStages * x_stage;
+    static constexpr uint32_t n_bars = 2 * kSkinnyStages + 2;     // full, empty, tmem_full, drain
+    static constexpr uint32_t slot_off = bar_off + 8 * n_bars;
+    static constexpr uint32_t abort_off = slot_off + 4;
+    static constexpr uint32_t last_off = abort_off + 4;
+    static constexpr uint32_t fail_off = last_off + 4;
+    static constexpr uint32_t bytes = fail_off + 4;
+    static constexpr uint32_t alloc_bytes = bytes + 1024;
+};
+
+template <int OUT>
+__device__ __forceinline__ void store_out(void *c, int64_t idx, float v)
+{
+    if constexpr (OUT == OUT_F32) {
+        static_cast<float *>(c)[idx] = v;
+    } else if constexpr (OUT == OUT_F16) {
+        static_cast<__half *>(c)[idx] = __float2half_rn(v);
+    } else {
+        static_cast<__nv_bfloat16 *>(c)[idx] = __float2bfloat16_rn(v);
+    }
+}
+
+template <int NPAD, int OUT, bool W_MN>
+__global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_constant__ GemmParams p)
+{
+    using Plan = SkinnyPlan<NPAD>;
+    constexpr int S = kSkinnyStages;
+    constexpr uint32_t kStageBytes = Plan::w_stage + Plan::x_stage;
+    constexpr uint32_t kTmemCols = NPAD < 32 ? 32 : NPAD;
+    static_assert(NPAD == 16 || NPAD == 32 || NPAD == 64, "NPAD must be 16, 32 or 64");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+    const uint32_t sW = base + Plan::w_off;
+    const uint32_t sX = base + Plan::x_off;
+    const uint32_t bar = base + Plan::bar_off;
+    auto full_bar = [&](int s) { return bar + 8u * s; };
+    auto empty_bar = [&](int s) { return bar + 8u * (S + s); };
+    const uint32_t tfull_bar = bar + 8u * (2 * S);
+    const uint32_t drain_bar = bar + 8u * (2 * S + 1);
+    const uint32_t slot = base + Plan::slot_off;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::last_off);
+    volatile int *epi_fail = reinterpret_cast<volatile int *>(base_ptr + Plan::fail_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nt = blockIdx.x % p.tiles_n;
+    const int split = blockIdx.x / p.tiles_n;
+    const int kb0 = (int)((int64_t)split * p.num_kb / p.splits);
+    const int kb1 = (int)((int64_t)(split + 1) * p.num_kb / p.splits);
+    const int32_t n0 = nt * kSkinnyRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        ptx::mbar_init(tfull_bar, 1);
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        *epi_fail = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&p.tma_a);
+        ptx::prefetch_tensormap(&p.tma_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(slot, kTmemCols);
+        ptx::tmem_relinquish();
+        ptx::tc_fence_before_sync();
+    }
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
+    const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar(s);
+                ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                const int32_t k0 = kb * kBK;
+                if (W_MN) {
+#pragma unroll
+                    for (int j = 0; j < kSkinnyRows / 64; ++j)
+                        ptx::tma_load_2d(sW + s * Plan::w_stage + j * (kBK * 128), &p.tma_b, fb, n0 + 64 * j, k0);
+                } else {
+                    ptx::tma_load_2d(sW + s * Plan::w_stage, &p.tma_b, fb, k0, n0);
+                }
+                ptx::tma_load_2d(sX + s * Plan::x_stage, &p.tma_a, fb, k0, 0);
+                issued_mask |= 1u << s;
+                issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok)
+                for (int t = 0; t < S; ++t)
+                    if (issued_mask & (1u << t))
+                        wait_bounded(full_bar(t), (issued_parity >> t) & 1u, wc, SITE_DRAIN_LOADS, false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t w_addr = sW + s * Plan::w_stage;
+                const uint32_t x_addr = sX + s * Plan::x_stage;
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k) {
+                    const uint64_t ad = W_MN ? desc_at(kDescMNMajor, w_addr + k * (kUmmaK * 128))
+                                             : desc_at(kDescKMajor, w_addr + k * (kUmmaK * 2));
+                    const uint64_t bd = desc_at(kDescKMajor, x_addr + k * (kUmmaK * 2));
+                    ptx::mma_f16_ss(tmem_base, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(empty_bar(s));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (ok) {
+                ptx::mma_commit(tfull_bar);
+            } else {
+                ptx::mma_commit(drain_bar);
+                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                   // TMEM lanes 32q..32q+31 = weight rows
+        const int nl = 32 * q + lane;             // row inside the 128-row tile
+        const int64_t n = (int64_t)n0 + nl;
+        const int M = p.M;
+        const bool got = wait_bounded(tfull_bar, 0, wc, SITE_EPI_TMEM_FULL);
+        if (!__all_sync(0xffffffffu, got) && lane == 0) *epi_fail = 1;
+        ptx::named_barrier(1, 4 * 32);   // the four epilogue warps take one decision together
+        if (!*epi_fail) {
+            ptx::tc_fence_after_sync();
+            float v[NPAD];
+#pragma unroll
+            for (int c = 0; c < NPAD / 16; ++c) {
+                uint32_t r[16];
+                ptx::tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * q) << 16) + 16 * c, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[16 * c + j] = __uint_as_float(r[j]);
+            }
+            if (p.splits == 1) {
+                if (n < p.N)
+#pragma unroll
+                    for (int m = 0; m < NPAD; ++m)
+                        if (m < M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v[m]);
+            } else {
+                // partial of this split: [split][nt][m][row]
+                float *part = p.partials + ((int64_t)split * p.tiles_n + nt) * NPAD * kSkinnyRows;
+#pragma unroll
+                for (int m = 0; m < NPAD; ++m)
+                    if (m < M) part[m * kSkinnyRows + nl] = v[m];
+                __threadfence();
+                ptx::named_barrier(1, 4 * 32);
+                if (warp == 2 && lane == 0) {
+                    const uint32_t prev = atomicAdd(&p.counters[nt], 1u);
+                    *last_flag = prev == (uint32_t)(p.splits - 1) ? 1 : 0;
+                }
+                ptx::named_barrier(1, 4 * 32);
+                if (*last_flag) {
+                    __threadfence();
+                    if (n < p.N) {
+                        for (int m = 0; m < M && m < NPAD; ++m) {
+                            float acc = 0.f;
+                            for (int j = 0; j < p.splits; ++j)   // fixed order: split 0, 1, 2, ...
+                                acc += __ldcg(p.partials + (((int64_t)j * p.tiles_n + nt) * NPAD + m) * kSkinnyRows + nl);
+                            store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, acc);
+                        }
+                    }
+                    if (warp == 2 && lane == 0) p.counters[nt] = 0u;   // every split of this tile has arrived
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int NPAD, int OUT, bool W_MN>
+cudaError_t launch_gemm_skinny(const GemmParams &p, int grid, cudaStream_t stream)
+{
+    auto kern = gemm_skinny_kernel<NPAD, OUT, W_MN>;
+    constexpr uint32_t smem = SkinnyPlan<NPAD>::alloc_bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// bn carries NPAD for the swap-AB entries; cluster = 0 marks them.
+#define TGEMM_SKINNY_VARIANT(NPAD, OUT, BMN) \
+    {NPAD, kSkinnyStages, OUT, BMN, SkinnyPlan<NPAD>::alloc_bytes, &launch_gemm_skinny<NPAD, OUT, (BMN) != 0>, 0, nullptr}
+
+}  // namespace tgemm

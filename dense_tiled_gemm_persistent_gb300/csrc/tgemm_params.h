@@ -38,6 +38,12 @@ struct alignas(128) GemmParams {
     uint32_t debug_flags;   // bit 0: the producer skips its first load (timeout test)
     uint32_t *status;       // device status word (first fault wins)
     uint64_t timeout_ns;    // limit of every pipeline wait
+    // swap-AB / split-K path only
+    void *c_ptr;            // C, row-major M x ldc (written with plain stores)
+    int64_t ldc;
+    float *partials;        // [splits][tiles_n][npad][128] FP32 partial sums
+    uint32_t *counters;     // [tiles_n] arrival counters, zero between calls
+    int32_t splits;         // K is cut into `splits` runs of whole k-blocks
 };
 
 using LaunchFn = cudaError_t (*)(const GemmParams &, int grid, cudaStream_t);

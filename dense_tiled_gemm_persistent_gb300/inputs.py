@@ -36,6 +36,13 @@ class Dist:
     a: float
     b: float
 
+    def describe(self) -> str:
+        if self.kind == "uniform":
+            return "uniform[%g,%g)" % (self.a, self.b)
+        if self.kind == "normal":
+            return "normal(%g,%g)" % (self.a, self.b)
+        return "ints{%d..%d}" % (int(self.a), int(self.b))
+
     def draw(self, shape, g: torch.Generator) -> torch.Tensor:
         if self.kind == "uniform":
             return self.a + (self.b - self.a) * torch.rand(shape, generator=g, dtype=torch.float32)

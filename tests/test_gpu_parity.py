@@ -208,3 +208,61 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     M, N, K = 256, 256, 128
     a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.ints(-2, 2), seed=19)
     check_full(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, exact=True, what="after timeout")
+
+
+# ---- the swap-AB split-K path (at most 64 rows of A) -------------------------------
+
+def skinny_cfg(npad, splits):
+    return tgemm.Config(bm=128, bn=npad, bk=64, stages=4, cluster_m=1, group_m=1, split_k=splits, swap_ab=1,
+                        grid=0)
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 33, 64])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+def test_skinny_default_pick(M, layout):
+    rc, c = tgemm.tgemm_query_config(M, 4096, 512, layout, gen.BF16, gen.BF16)
+    assert rc == 0 and c.swap_ab == 1 and c.bn >= M
+    for (N, K) in [(300, 1000), (4096, 512), (129, 4160)]:
+        for out in (gen.F32, gen.BF16):
+            a, b = operands(M, N, K, gen.BF16, layout, gen.normal(0, 1), seed=M + N + K, dist_b=gen.normal(0, 0.02))
+            check_full(a, b, M, N, K, layout, gen.BF16, out, what="skinny M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 32])
+def test_skinny_forced_splits_integers_exact(layout, splits):
+    M, N, K = 16, 640, 2048
+    a, b = operands(M, N, K, gen.F16, layout, gen.ints(-2, 2), seed=23)
+    for npad in (16, 32, 64):
+        check_full(a, b, M, N, K, layout, gen.F16, gen.F16, exact=True, config=skinny_cfg(npad, splits),
+                   what="splits=%d npad=%d" % (splits, npad))
+
+
+def test_skinny_repeated_calls_are_bitwise_identical():
+    """The arrival counters return to zero after every call and the partials
+    are summed in a fixed order, so repeating a call reproduces C exactly."""
+    M, N, K = 16, 4096, 4096
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=29, dist_b=gen.normal(0, 0.02))
+    outs = [run_gpu(a, b, M, N, K, gen.B_NK, gen.BF16, gen.F32) for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    ref, bound = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.BF16)
+    assert_close(values(outs[0][:M, :N], gen.F32), ref, bound, gen.F32, "16x4096x4096")
+
+
+def test_skinny_concurrent_streams_do_not_share_partials():
+    M, N, K = 32, 2048, 3072
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ops = [operands(M, N, K, gen.BF16, gen.B_NK, gen.ints(-2, 2), seed=s) for s in (31, 37)]
+    dev = [(a.to("cuda:0"), b.to("cuda:0")) for a, b in ops]
+    Cs = [torch.empty((M, N), dtype=torch.float32, device="cuda:0") for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        for (A, B), C, s in zip(dev, Cs, (s1, s2)):
+            rc = tgemm.tgemm_run(M, N, K, A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1], gen.B_NK,
+                                 C.data_ptr(), N, gen.BF16, gen.F32, tgemm.ctypes.c_void_p(s.cuda_stream))
+            assert rc == 0
+    torch.cuda.synchronize()
+    assert tgemm.tgemm_check() == 0
+    for (a, b), C in zip(ops, Cs):
+        ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.BF16)
+        assert np.array_equal(C.cpu().double().numpy(), ref)
