@@ -211,11 +211,13 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
                     for (int m = 0; m < NPAD; ++m)
                         if (m < M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v[m]);
             } else {
-                // partial of this split: [split][nt][m][row]
-                float *part = p.partials + ((int64_t)split * p.tiles_n + nt) * NPAD * kSkinnyRows;
+                // Partial of this split, [split][nt][row][NPAD]: each thread
+                // owns one weight row and writes its NPAD sums contiguously.
+                float4 *part = reinterpret_cast<float4 *>(
+                    p.partials + (((int64_t)split * p.tiles_n + nt) * kSkinnyRows + nl) * NPAD);
 #pragma unroll
-                for (int m = 0; m < NPAD; ++m)
-                    if (m < M) part[m * kSkinnyRows + nl] = v[m];
+                for (int c = 0; c < NPAD / 4; ++c)
+                    part[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
                 __threadfence();
                 ptx::named_barrier(1, 4 * 32);
                 if (warp == 2 && lane == 0) {
@@ -225,14 +227,44 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
                 ptx::named_barrier(1, 4 * 32);
                 if (*last_flag) {
                     __threadfence();
-                    if (n < p.N) {
-                        for (int m = 0; m < M && m < NPAD; ++m) {
-                            float acc = 0.f;
-                            for (int j = 0; j < p.splits; ++j)   // fixed order: split 0, 1, 2, ...
-                                acc += __ldcg(p.partials + (((int64_t)j * p.tiles_n + nt) * NPAD + m) * kSkinnyRows + nl);
-                            store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, acc);
-                        }
+                    float acc[NPAD];
+#pragma unroll
+                    for (int m = 0; m < NPAD; ++m) acc[m] = 0.f;
+                    const int64_t split_stride = (int64_t)p.tiles_n * kSkinnyRows * NPAD / 4;   // in float4
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.partials + ((int64_t)nt * kSkinnyRows + nl) * NPAD);
+                    // Sum the partials in split order 0, 1, 2, ...; loads of up
+                    // to four splits are issued before their additions.
+                    int j = 0;
+                    for (; j + 4 <= p.splits; j += 4) {
+                        float4 t[4][NPAD / 4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int c = 0; c < NPAD / 4; ++c) t[u][c] = __ldcg(src + (j + u) * split_stride + c);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int c = 0; c < NPAD / 4; ++c) {
+                                acc[4 * c] += t[u][c].x;
+                                acc[4 * c + 1] += t[u][c].y;
+                                acc[4 * c + 2] += t[u][c].z;
+                                acc[4 * c + 3] += t[u][c].w;
+                            }
                     }
+                    for (; j < p.splits; ++j)
+#pragma unroll
+                        for (int c = 0; c < NPAD / 4; ++c) {
+                            const float4 t = __ldcg(src + j * split_stride + c);
+                            acc[4 * c] += t.x;
+                            acc[4 * c + 1] += t.y;
+                            acc[4 * c + 2] += t.z;
+                            acc[4 * c + 3] += t.w;
+                        }
+                    if (n < p.N)
+#pragma unroll
+                        for (int m = 0; m < NPAD; ++m)
+                            if (m < M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, acc[m]);
                     if (warp == 2 && lane == 0) p.counters[nt] = 0u;   // every split of this tile has arrived
                 }
             }

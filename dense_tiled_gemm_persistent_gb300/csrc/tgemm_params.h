@@ -41,7 +41,7 @@ struct alignas(128) GemmParams {
     // swap-AB / split-K path only
     void *c_ptr;            // C, row-major M x ldc (written with plain stores)
     int64_t ldc;
-    float *partials;        // [splits][tiles_n][npad][128] FP32 partial sums
+    float *partials;        // [splits][tiles_n][128 rows][npad] FP32 partial sums
     uint32_t *counters;     // [tiles_n] arrival counters, zero between calls
     int32_t splits;         // K is cut into `splits` runs of whole k-blocks
 };
