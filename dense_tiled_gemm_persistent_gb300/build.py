@@ -26,6 +26,7 @@ SOURCES = [
     "tgemm_inst_bf16.cu",
     "tgemm_inst_f32.cu",
     "tgemm_debug.cu",
+    "tgemm_noalloc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 # Every symbol include/tgemm.h declares.
 EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
-           "tgemm_debug_wait_timeout")
+           "tgemm_debug_wait_timeout", "tgemm_run_noalloc")
 
 
 class TgemmError(RuntimeError):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
         lib.tgemm_tile_coord.argtypes = [_i64, _i64, _i, _i, _i, _i64, ctypes.POINTER(_i64),
                                          ctypes.POINTER(_i64)]
         lib.tgemm_tile_coord.restype = _i
+        lib.tgemm_run_noalloc.argtypes = run_args
+        lib.tgemm_run_noalloc.restype = _i
         lib.tgemm_debug_wait_timeout.argtypes = [ctypes.c_uint32, _p]
         lib.tgemm_debug_wait_timeout.restype = _i
         _lib = lib
@@ -82,6 +84,12 @@ def load(path: str = LIB_PATH):
 
 def tgemm_run(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None) -> int:
     return load().tgemm_run(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream)
+
+
+def tgemm_run_noalloc(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None) -> int:
+    """tgemm_run for at most 64 rows of A without any device allocation (a
+    fixed scratch array inside the library; calls that overlap on the GPU race)."""
+    return load().tgemm_run_noalloc(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream)
 
 
 def tgemm_run_config(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream,

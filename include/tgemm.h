@@ -132,6 +132,37 @@ tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn, int group_m,
  */
 tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream);
 
+/*
+ * tgemm_run without any device allocation, for a skinny A (1..64 rows).
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that may not allocate device memory at call time -- code whose device
+ * memory is owned by a pool or budgeted allocator that must see every byte,
+ * or that runs where a cudaMalloc would be an error.  tgemm_run allocates a
+ * split-K workspace and a status word on first use; this entry point uses a
+ * fixed 4 MiB array built into the library instead (reserved on every GPU
+ * that loads the library, until the process exits) and never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Same arguments and result as tgemm_run (C = A * B, same layouts, dtypes
+ * and alignment rules), computed by the same swap-AB split-K kernel, with
+ * these limits:
+ *   - 0 <= M <= 64 and N <= 524288 (4096 column tiles of 128); larger sizes
+ *     return TGEMM_ERR_UNSUPPORTED before anything is launched;
+ *   - every call shares the one array, so calls whose work overlaps on the
+ *     GPU (e.g. on two streams without ordering) race and corrupt each
+ *     other's results: order them;
+ *   - the first call on each device looks up the array's device address
+ *     (once); make that first call outside CUDA stream capture;
+ *   - a pipeline-wait timeout stops the kernel early but is not reported by
+ *     tgemm_check.
+ */
+tgemm_status tgemm_run_noalloc(int64_t M, int64_t N, int64_t K,
+                               const void *A, int64_t lda,
+                               const void *B, int64_t ldb, tgemm_b_layout b_layout,
+                               void *C, int64_t ldc,
+                               tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
