@@ -200,13 +200,14 @@ def run_reference(args, rank, world):
 
 def config_dict(wl, world):
     from dense_tiled_gemm_persistent_gb300 import inputs as gen
-    flush = wl.algorithmic_bytes < 2 * L2_BYTES
+    reps = -(-3 * L2_BYTES // wl.algorithmic_bytes) if wl.algorithmic_bytes < 3 * L2_BYTES else 1
     return {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
             "in_dtype": gen.DTYPE_NAME[wl.in_dtype], "out_dtype": gen.DTYPE_NAME[wl.out_dtype],
             "accumulate": "f32", "b_layout": "NxK" if wl.b_layout == gen.B_NK else "KxN",
             "values": "A %s, B %s, seed %d" % (wl.dist_a.describe(), wl.dist_b.describe(), wl.seed),
-            "l2": ("512 MiB L2 scrub between timed launches (inputs %.1f MB)" % (wl.algorithmic_bytes / 1e6))
-            if flush else ("operands+output %.0f MB > 129 MB L2, back to back" % (wl.algorithmic_bytes / 1e6)),
+            "l2": ("back to back over %d copies of A, B, C (%.0f MB > 3 x 129 MB L2)"
+                   % (reps, reps * wl.algorithmic_bytes / 1e6)) if reps > 1 else
+                  ("operands+output %.0f MB > 129 MB L2, back to back" % (wl.algorithmic_bytes / 1e6)),
             "parallelism": "replicas%d" % world if world > 1 else "single-gpu"}
 
 
@@ -219,9 +220,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--config", default="auto", choices=["auto", "pair", "1cta256", "1cta128"],
+    ap.add_argument("--config", default="auto", choices=["auto", "pair", "1cta256", "1cta128", "workspace"],
                     help="tile shape: the library's pick, or a forced one (tuning)")
     ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
+    ap.add_argument("--split-k", type=int, default=0, help="split count override for the swap-AB path (tuning)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another named workload (parity-test configurations; not the headline line)")
     args = ap.parse_args()
@@ -262,7 +264,16 @@ def main():
     if rc != 0:
         raise RuntimeError("tgemm_query_config: " + tgemm.status_string(rc))
     forced = None
-    if args.config != "auto" or args.group_m:
+    if args.config == "workspace" and picked.swap_ab:
+        forced = tgemm.Config(bm=picked.bm, bn=picked.bn, bk=64, stages=4, cluster_m=1, group_m=1,
+                              split_k=args.split_k or picked.split_k, swap_ab=1, grid=0)
+        picked = forced
+    elif args.split_k and picked.swap_ab:
+        forced = tgemm.Config(bm=picked.bm, bn=picked.bn, bk=64, stages=picked.stages,
+                              cluster_m=args.split_k if picked.swap_ab == 2 else 1, group_m=1,
+                              split_k=args.split_k, swap_ab=picked.swap_ab, grid=0)
+        picked = forced
+    elif args.config != "auto" or args.group_m:
         shapes = {"pair": (256, 256, 6, 2), "1cta256": (128, 256, 4, 1), "1cta128": (128, 128, 6, 1)}
         bm, bn, st, cl = shapes[args.config] if args.config != "auto" else (
             picked.bm, picked.bn, picked.stages, picked.cluster_m)
@@ -291,28 +302,25 @@ def main():
     sampler = ClockSampler(uuid)
     sampler.start()
 
-    # Inputs smaller than twice the L2 are timed launch by launch with a
-    # 512 MiB write between launches that evicts them from L2; larger ones
-    # back to back (they cannot stay in L2 anyway).
-    flush = wl.algorithmic_bytes < 2 * L2_BYTES
-    scrub = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
+    # Workloads whose operands fit in L2 cycle through R copies of A, B and C
+    # (R * bytes > 3 x L2), so every launch streams its operands from HBM;
+    # launches run back to back either way.
+    reps = 1
+    if wl.algorithmic_bytes < 3 * L2_BYTES:
+        reps = -(-3 * L2_BYTES // wl.algorithmic_bytes)
+    copies = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(reps - 1)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    if flush:
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for i in range(args.steps):
-            scrub.fill_(float(i))
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-    else:
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        ev[0].record(stream)
-        for i in range(args.steps):
-            step()
-            ev[i + 1].record(stream)
+    # Two events bracket the whole timed loop: the average launch duration is
+    # the loop time over the launch count (an event after every launch would
+    # add its own overhead to kernels of a few microseconds).
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for i in range(args.steps):
+        a_, b_, c_ = copies[i % reps]
+        step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
+    e_end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -320,12 +328,7 @@ def main():
     rc = tgemm.tgemm_check(sh)
     if rc != 0:
         raise RuntimeError("timed region failed: " + tgemm.status_string(rc))
-    if flush:
-        launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-        total_ms = sum(launch_ms)          # launches only; the L2 scrub between them is not counted
-    else:
-        total_ms = ev[0].elapsed_time(ev[-1])
-        launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = e_start.elapsed_time(e_end)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -333,7 +336,7 @@ def main():
 
     ms_per_step = total_ms / args.steps
     value = tflops(wl.M, wl.N, wl.K, ms_per_step) * world
-    avg_launch = statistics.mean(launch_ms)
+    avg_launch = total_ms / args.steps
 
     peaks = measured_peaks()
     if peaks and peaks.get("bf16_tflops"):
@@ -406,7 +409,7 @@ def main():
             "dtype": gen.DTYPE_NAME[wl.in_dtype], "data": "synthetic",
             "config": dict(config_dict(wl, world), kernel=picked.as_dict()), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": args.steps,
-            "kernel_ms": {"mean": avg_launch, "median": statistics.median(launch_ms), "min": min(launch_ms)},
+            "kernel_ms": {"mean": avg_launch},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -16,6 +16,7 @@
 
 #include "tgemm_kernel_pair.cuh"
 #include "tgemm_kernel_skinny.cuh"
+#include "tgemm_kernel_splitk_cluster.cuh"
 #include "tgemm_params.h"
 #include "tgemm_sched.h"
 
@@ -206,19 +207,43 @@ int skinny_splits(int64_t N, int64_t K, int sm_count)
 // a 128 x 128 tile halves the work per SM for 2/3 of the bytes of a
 // 128 x 256 one and keeps the tensor pipe less busy.  At most 64 rows of A
 // go to the swap-AB split-K path instead.
+int cluster_splits_limit(int npad) { return npad == 16 ? ClusterSplitPlan<16>::max_splits
+                                           : npad == 32 ? ClusterSplitPlan<32>::max_splits
+                                                        : ClusterSplitPlan<64>::max_splits; }
+int cluster_stages(int npad) { return npad == 16 ? ClusterSplitPlan<16>::stages
+                                    : npad == 32 ? ClusterSplitPlan<32>::stages : ClusterSplitPlan<64>::stages; }
+
 void choose_config(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg)
 {
     if (M <= 64) {
-        const int s = skinny_splits(N, K, sm_count);
+        const int npad = skinny_npad(M);
+        const int64_t tiles = ceil_div(N, kSkinnyRows);
+        const int64_t kb = ceil_div(K, kBK);
+        // In-cluster split-K: one CTA per SM, the splits of a tile reduce
+        // through distributed shared memory.  Used unless the tiles are so few
+        // that the cluster limit leaves most SMs idle.
+        int64_t cs = sm_count / (tiles > 0 ? tiles : 1);
+        if (cs > cluster_splits_limit(npad)) cs = cluster_splits_limit(npad);
+        if (cs > kb) cs = kb;
+        if (cs < 1) cs = 1;
         cfg->bm = kSkinnyRows;
-        cfg->bn = skinny_npad(M);
+        cfg->bn = npad;
         cfg->bk = kBK;
+        cfg->group_m = 1;
+        if (2 * tiles * cs >= sm_count || cs == kb) {
+            cfg->stages = cluster_stages(npad);
+            cfg->cluster_m = (int)cs;
+            cfg->split_k = (int)cs;
+            cfg->swap_ab = 2;
+            cfg->grid = (int)(tiles * cs);
+            return;
+        }
+        const int s = skinny_splits(N, K, sm_count);
         cfg->stages = kSkinnyStages;
         cfg->cluster_m = 1;
-        cfg->group_m = 1;
         cfg->split_k = s;
         cfg->swap_ab = 1;
-        cfg->grid = (int)(ceil_div(N, kSkinnyRows) * s);
+        cfg->grid = (int)(tiles * s);
         return;
     }
     struct Cand { int cluster, bn; double per_tile; };
@@ -273,14 +298,25 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
 {
     if (c.bk != kBK || c.grid < 0 || c.group_m < 1) return TGEMM_ERR_UNSUPPORTED;
     const int b_mn = b_layout == TGEMM_B_KN ? 1 : 0;
-    if (c.swap_ab) {
-        // swap-AB: bm weight rows per CTA, bn = padded token count >= M
+    if (c.swap_ab == 1) {
+        // swap-AB, split-K through a global workspace: bm weight rows per
+        // CTA, bn = padded row count of A (>= M)
         if (c.bm != kSkinnyRows || c.cluster_m != 1 || c.stages != kSkinnyStages) return TGEMM_ERR_UNSUPPORTED;
         if (c.bn < M || c.split_k < 1 || c.split_k > 1024 || c.split_k > ceil_div(K > 0 ? K : 1, kBK))
             return TGEMM_ERR_UNSUPPORTED;
         *v = find_variant(c.bn, c.stages, out_dtype, b_mn, 0);
         return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
     }
+    if (c.swap_ab == 2) {
+        // swap-AB, split-K inside a cluster of split_k CTAs
+        if (c.bm != kSkinnyRows || c.bn < M || c.cluster_m != c.split_k || c.split_k < 1 ||
+            c.split_k > ceil_div(K > 0 ? K : 1, kBK))
+            return TGEMM_ERR_UNSUPPORTED;
+        *v = find_variant(c.bn, c.stages, out_dtype, b_mn, 3);
+        if (!*v || c.split_k > (*v)->max_active()) return TGEMM_ERR_UNSUPPORTED;
+        return TGEMM_OK;
+    }
+    if (c.swap_ab != 0) return TGEMM_ERR_UNSUPPORTED;
     if (c.split_k != 1) return TGEMM_ERR_UNSUPPORTED;
     if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
         return TGEMM_ERR_UNSUPPORTED;
@@ -332,7 +368,8 @@ int resident_pairs(DeviceState *dev, const KernelVariant *v)
     return n;
 }
 
-// C^T = B^T A^T on the swap-AB split-K kernel (M <= 64).
+// C^T = B^T A^T on a swap-AB split-K kernel (M <= 64): the workspace
+// reduction (swap_ab = 1) or the in-cluster one (swap_ab = 2).
 tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
                         int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype, void *stream_ptr,
                         const tgemm_config &cfg, const KernelVariant *var, DeviceState *dev)
@@ -341,7 +378,7 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     const int npad = cfg.bn;
     const int64_t tiles_n = ceil_div(N, kSkinnyRows);
     int splits = cfg.split_k;
-    if (tiles_n > kMaxSkinnyTiles) splits = 1;
+    if (cfg.swap_ab == 1 && tiles_n > kMaxSkinnyTiles) splits = 1;
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     bool ok = encode_2d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kBK, (uint32_t)npad);
@@ -364,7 +401,7 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     p.c_ptr = C;
     p.ldc = ldc;
     p.splits = splits;
-    if (splits > 1) {
+    if (splits > 1 && cfg.swap_ab == 1) {
         int devno = 0;
         cudaGetDevice(&devno);
         const size_t part = (size_t)splits * (size_t)tiles_n * (size_t)npad * kSkinnyRows * sizeof(float);

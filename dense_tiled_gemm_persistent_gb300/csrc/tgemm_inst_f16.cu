@@ -2,9 +2,11 @@
 // Each entry: output tile width BN, ring depth STAGES, output type, B layout
 // (0 = B stored N x K, K-major; 1 = B stored K x N, MN-major); the pair
 // entries run 256 x 256 tiles on CTA pairs; the skinny entries are the
-// swap-AB split-K kernel for at most 64 rows of A, by padded row count.
+// swap-AB split-K kernels for at most 64 rows of A (global-workspace and
+// in-cluster reductions), by padded row count.
 #include "tgemm_kernel_pair.cuh"
 #include "tgemm_kernel_skinny.cuh"
+#include "tgemm_kernel_splitk_cluster.cuh"
 
 namespace tgemm {
 
@@ -21,6 +23,12 @@ const KernelVariant kVariantsF16[] = {
     TGEMM_SKINNY_VARIANT(32, OUT_F16, 1),
     TGEMM_SKINNY_VARIANT(64, OUT_F16, 0),
     TGEMM_SKINNY_VARIANT(64, OUT_F16, 1),
+    TGEMM_CLUSTER_SPLIT_VARIANT(16, OUT_F16, 0),
+    TGEMM_CLUSTER_SPLIT_VARIANT(16, OUT_F16, 1),
+    TGEMM_CLUSTER_SPLIT_VARIANT(32, OUT_F16, 0),
+    TGEMM_CLUSTER_SPLIT_VARIANT(32, OUT_F16, 1),
+    TGEMM_CLUSTER_SPLIT_VARIANT(64, OUT_F16, 0),
+    TGEMM_CLUSTER_SPLIT_VARIANT(64, OUT_F16, 1),
 };
 const int kNumVariantsF16 = (int)(sizeof(kVariantsF16) / sizeof(kVariantsF16[0]));
 

@@ -1,0 +1,275 @@
+// Skinny GEMM with split-K reduced inside a thread-block cluster.
+//
+// Same swap-AB formulation as tgemm_kernel_skinny.cuh (C^T = B^T * A^T: 128
+// weight rows on the MMA's M side, the <= 64 rows of A padded to NPAD on its N
+// side), but the S CTAs that split the K loop of one 128-column tile of C
+// form one cluster and add their partial sums through distributed shared
+// memory instead of a global workspace:
+//
+//   1. every CTA runs its K range through a STAGES-deep TMA ring (one CTA per
+//      SM, so the whole shared memory keeps weight bytes in flight) and reads
+//      its 128 x NPAD FP32 partial from tensor memory into registers;
+//   2. cluster barrier: every CTA of the cluster has finished its MMAs, so the
+//      leader's (rank 0) operand ring is free;
+//   3. ranks 1..S-1 store their partials into the leader's ring with
+//      st.shared::cluster;
+//   4. cluster barrier: the partials are visible to the leader;
+//   5. the leader adds them to its own in rank order 0, 1, ..., S-1 (fixed,
+//      so results do not depend on timing), casts with round-to-nearest-even
+//      and writes C.
+//
+// No device memory besides A, B and C is touched, no atomics, no counters.
+// S is limited by the cluster size (8) and by the leader's ring holding
+// S-1 partials.
+#pragma once
+
+#include "tgemm_kernel_skinny.cuh"
+
+namespace tgemm {
+
+constexpr int kMaxClusterSplits = 8;
+
+template <int NPAD>
+struct ClusterSplitPlan {
+    static constexpr uint32_t w_stage = kSkinnyRows * kBK * 2;
+    static constexpr uint32_t x_stage = NPAD * kBK * 2;
+    static constexpr uint32_t stage_bytes = w_stage + x_stage;
+    static constexpr int stages = (int)((216u * 1024u) / stage_bytes);     // 12, 11, 9 for NPAD 16, 32, 64
+    static constexpr uint32_t w_off = 0;
+    static constexpr uint32_t x_off = w_off + stages * w_stage;
+    static constexpr uint32_t bar_off = x_off + stages * x_stage;
+    static constexpr uint32_t n_bars = 2 * stages + 2;                   // full, empty, tmem_full, drain
+    static constexpr uint32_t slot_off = bar_off + 8 * n_bars;
+    static constexpr uint32_t abort_off = slot_off + 4;
+    static constexpr uint32_t bytes = abort_off + 4;
+    static constexpr uint32_t alloc_bytes = bytes + 1024;
+    static constexpr uint32_t partial_bytes = kSkinnyRows * NPAD * 4;   // one CTA's 128 x NPAD partial
+    // The leader's ring (from offset 0) receives the partials of ranks 1..S-1.
+    static constexpr int max_splits_by_ring = 1 + (int)((stages * stage_bytes) / partial_bytes);
+    static constexpr int max_splits = max_splits_by_ring < kMaxClusterSplits ? max_splits_by_ring : kMaxClusterSplits;
+};
+
+template <int NPAD, int OUT, bool W_MN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_splitk_cluster_kernel(const __grid_constant__ GemmParams p)
+{
+    using Plan = ClusterSplitPlan<NPAD>;
+    constexpr int S = Plan::stages;
+    constexpr uint32_t kTmemCols = NPAD < 32 ? 32 : NPAD;
+    static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+    const uint32_t sW = base + Plan::w_off;
+    const uint32_t sX = base + Plan::x_off;
+    const uint32_t bar = base + Plan::bar_off;
+    auto full_bar = [&](int s) { return bar + 8u * s; };
+    auto empty_bar = [&](int s) { return bar + 8u * (S + s); };
+    const uint32_t tfull_bar = bar + 8u * (2 * S);
+    const uint32_t drain_bar = bar + 8u * (2 * S + 1);
+    const uint32_t slot = base + Plan::slot_off;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int splits = p.splits;                   // = cluster size
+    const uint32_t rank = ptx::cluster_ctarank();  // = split index
+    const int nt = blockIdx.x / splits;
+    const int kb0 = (int)((int64_t)rank * p.num_kb / splits);
+    const int kb1 = (int)((int64_t)(rank + 1) * p.num_kb / splits);
+    const int32_t n0 = nt * kSkinnyRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        ptx::mbar_init(tfull_bar, 1);
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&p.tma_a);
+        ptx::prefetch_tensormap(&p.tma_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(slot, kTmemCols);
+        ptx::tmem_relinquish();
+        ptx::tc_fence_before_sync();
+    }
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
+    const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
+
+    float v[NPAD];
+    bool have = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar(s);
+                ptx::mbar_arrive_expect_tx(fb, Plan::stage_bytes);
+                const int32_t k0 = kb * kBK;
+                if (W_MN) {
+#pragma unroll
+                    for (int j = 0; j < kSkinnyRows / 64; ++j)
+                        ptx::tma_load_2d(sW + s * Plan::w_stage + j * (kBK * 128), &p.tma_b, fb, n0 + 64 * j, k0);
+                } else {
+                    ptx::tma_load_2d(sW + s * Plan::w_stage, &p.tma_b, fb, k0, n0);
+                }
+                ptx::tma_load_2d(sX + s * Plan::x_stage, &p.tma_a, fb, k0, 0);
+                issued_mask |= 1u << s;
+                issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok)
+                for (int t = 0; t < S; ++t)
+                    if (issued_mask & (1u << t))
+                        wait_bounded(full_bar(t), (issued_parity >> t) & 1u, wc, SITE_DRAIN_LOADS, false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t w_addr = sW + s * Plan::w_stage;
+                const uint32_t x_addr = sX + s * Plan::x_stage;
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k) {
+                    const uint64_t ad = W_MN ? desc_at(kDescMNMajor, w_addr + k * (kUmmaK * 128))
+                                             : desc_at(kDescKMajor, w_addr + k * (kUmmaK * 2));
+                    const uint64_t bd = desc_at(kDescKMajor, x_addr + k * (kUmmaK * 2));
+                    ptx::mma_f16_ss(tmem_base, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(empty_bar(s));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (ok) {
+                ptx::mma_commit(tfull_bar);
+                // The leader's ring is reused for the partials of the other
+                // ranks: make sure every MMA of this CTA is done reading it.
+                wait_bounded(tfull_bar, 0, wc, SITE_MMA_FULL, false);
+            } else {
+                ptx::mma_commit(drain_bar);
+                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
+            }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------- epilogue: TMEM -> registers
+        const int q = warp & 3;
+        const bool got = wait_bounded(tfull_bar, 0, wc, SITE_EPI_TMEM_FULL);
+        if (__all_sync(0xffffffffu, got)) {
+            ptx::tc_fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < NPAD / 16; ++c) {
+                uint32_t r[16];
+                ptx::tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * q) << 16) + 16 * c, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[16 * c + j] = __uint_as_float(r[j]);
+            }
+            have = true;
+        }
+    }
+
+    // Every CTA of the cluster is past its mainloop; the leader's ring is free.
+    __syncthreads();
+    ptx::cluster_sync();
+    const bool epi = warp >= 2;
+    const int nl = 32 * (warp & 3) + lane;           // weight row inside the tile (epilogue warps)
+    const bool failed = *abort_flag != 0;
+    if (epi && rank != 0 && have && !failed) {
+        const uint32_t dst = ptx::map_to_cta(sW + ((rank - 1) * kSkinnyRows + nl) * (NPAD * 4), 0);
+#pragma unroll
+        for (int c = 0; c < NPAD / 4; ++c)
+            ptx::st_cluster_v4(dst + 16 * c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+    ptx::cluster_sync();                              // partials visible in the leader
+    if (epi && rank == 0 && have && !failed) {
+        for (int r = 1; r < splits; ++r) {            // fixed order: rank 0 (own), 1, 2, ...
+            const uint32_t src = sW + ((r - 1) * kSkinnyRows + nl) * (NPAD * 4);
+#pragma unroll
+            for (int c = 0; c < NPAD / 4; ++c) {
+                const float4 t = ptx::ld_shared_v4(src + 16 * c);
+                v[4 * c] += t.x;
+                v[4 * c + 1] += t.y;
+                v[4 * c + 2] += t.z;
+                v[4 * c + 3] += t.w;
+            }
+        }
+        const int64_t n = (int64_t)n0 + nl;
+        if (n < p.N)
+#pragma unroll
+            for (int m = 0; m < NPAD; ++m)
+                if (m < p.M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v[m]);
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int NPAD, int OUT, bool W_MN>
+cudaError_t launch_gemm_splitk_cluster(const GemmParams &p, int grid, cudaStream_t stream)
+{
+    auto kern = gemm_splitk_cluster_kernel<NPAD, OUT, W_MN>;
+    constexpr uint32_t smem = ClusterSplitPlan<NPAD>::alloc_bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int NPAD>
+int cluster_max_splits()
+{
+    return ClusterSplitPlan<NPAD>::max_splits;
+}
+
+// stages carries the ring depth; cluster = 3 marks these entries; max_active
+// reports the largest split count the leader's ring can receive.
+#define TGEMM_CLUSTER_SPLIT_VARIANT(NPAD, OUT, BMN)                                                             \
+    {NPAD, ClusterSplitPlan<NPAD>::stages, OUT, BMN, ClusterSplitPlan<NPAD>::alloc_bytes,                      \
+     &launch_gemm_splitk_cluster<NPAD, OUT, (BMN) != 0>, 3, &cluster_max_splits<NPAD>}
+
+}  // namespace tgemm

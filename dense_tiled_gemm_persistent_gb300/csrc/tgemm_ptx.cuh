@@ -239,6 +239,23 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t cta)
     return r;
 }
 
+// 16-byte store into the shared memory of another CTA of the cluster
+// (a shared::cluster address from map_to_cta).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier given by a shared::cluster address (possibly in a
 // peer CTA), with release semantics at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)

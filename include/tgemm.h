@@ -59,10 +59,12 @@ typedef enum {
  * (cluster_m = 2) or one CTA (cluster_m = 1); bk is the K depth of one
  * pipeline stage; stages is the shared-memory ring depth; group_m is the
  * GROUP_SIZE_M of the grouped rasterisation ("Performance optimisation:
- * Swizzle" of the cuTile matrix multiplication tutorial); split_k > 1 splits
- * the K loop over CTAs with an FP32 workspace; swap_ab != 0 computes
- * C^T = B^T A^T so a short M becomes the MMA's N; grid is the number of
- * persistent CTAs launched (0 = the library's choice).
+ * Swizzle" of the cuTile matrix multiplication tutorial); swap_ab != 0
+ * computes C^T = B^T A^T so a short M (<= 64, padded to bn) becomes the MMA's
+ * N, with the K loop split over split_k CTAs whose partial sums are added
+ * through a global FP32 workspace (swap_ab = 1) or inside a thread-block
+ * cluster of split_k CTAs (swap_ab = 2, cluster_m = split_k); grid is the
+ * number of CTAs launched (0 = the library's choice).
  */
 typedef struct {
     int bm, bn, bk, stages, cluster_m, group_m, split_k, swap_ab, grid;

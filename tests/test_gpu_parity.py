@@ -221,7 +221,7 @@ def skinny_cfg(npad, splits):
 @pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
 def test_skinny_default_pick(M, layout):
     rc, c = tgemm.tgemm_query_config(M, 4096, 512, layout, gen.BF16, gen.BF16)
-    assert rc == 0 and c.swap_ab == 1 and c.bn >= M
+    assert rc == 0 and c.swap_ab in (1, 2) and c.bn >= M
     for (N, K) in [(300, 1000), (4096, 512), (129, 4160)]:
         for out in (gen.F32, gen.BF16):
             a, b = operands(M, N, K, gen.BF16, layout, gen.normal(0, 1), seed=M + N + K, dist_b=gen.normal(0, 0.02))
@@ -236,6 +236,46 @@ def test_skinny_forced_splits_integers_exact(layout, splits):
     for npad in (16, 32, 64):
         check_full(a, b, M, N, K, layout, gen.F16, gen.F16, exact=True, config=skinny_cfg(npad, splits),
                    what="splits=%d npad=%d" % (splits, npad))
+
+
+CLUSTER_STAGES = {16: 12, 32: 10, 64: 9}
+CLUSTER_MAX_SPLITS = {16: 8, 32: 8, 64: 7}
+
+
+def cluster_cfg(npad, splits):
+    return tgemm.Config(bm=128, bn=npad, bk=64, stages=CLUSTER_STAGES[npad], cluster_m=splits, group_m=1,
+                        split_k=splits, swap_ab=2, grid=0)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("npad", [16, 32, 64])
+def test_cluster_split_k_integers_exact(layout, npad):
+    """Split-K reduced through distributed shared memory inside a cluster, for
+    every cluster size the leader can receive."""
+    M, N, K = min(npad, 40), 700, 1600
+    a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=41 + npad)
+    for splits in range(1, CLUSTER_MAX_SPLITS[npad] + 1):
+        check_full(a, b, M, N, K, layout, gen.BF16, gen.F32, exact=True, config=cluster_cfg(npad, splits),
+                   what="cluster splits=%d npad=%d" % (splits, npad))
+
+
+def test_cluster_split_k_rejects_too_many_splits():
+    x = torch.empty(1 << 16, dtype=torch.bfloat16, device="cuda:0")
+    p = x.data_ptr()
+    for npad, too_many in ((16, 9), (64, 8)):
+        rc = tgemm.tgemm_run_config(16, 256, 1024, p, 1024, p, 1024, gen.B_NK, p, 256, gen.BF16, gen.BF16, None,
+                                    cluster_cfg(npad, too_many))
+        assert rc == tgemm.ERR_UNSUPPORTED
+
+
+def test_cluster_and_workspace_reductions_agree_bitwise():
+    """Both reductions add the same partials in the same split order."""
+    M, N, K = 16, 1024, 2048
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=43, dist_b=gen.normal(0, 0.02))
+    for splits in (2, 4, 8):
+        c1 = run_gpu(a, b, M, N, K, gen.B_NK, gen.BF16, gen.F32, config=cluster_cfg(16, splits))
+        c2 = run_gpu(a, b, M, N, K, gen.B_NK, gen.BF16, gen.F32, config=skinny_cfg(16, splits))
+        assert torch.equal(c1, c2), "splits=%d" % splits
 
 
 def test_skinny_repeated_calls_are_bitwise_identical():
