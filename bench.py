@@ -34,6 +34,7 @@ PUBLISHED_TFLOPS = 489.9      # Croqtile v4 on H800 PCIe, same shape and B layou
 FALLBACK_TENSOR_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
+GRAPH_FLOPS = 1e11
 KERNEL_SOURCES = ["tgemm_kernel.cuh", "tgemm_ptx.cuh", "tgemm_wait.cuh", "tgemm_sched.h", "tgemm_params.h"]
 
 
@@ -224,6 +225,8 @@ def main():
                     help="tile shape: the library's pick, or a forced one (tuning)")
     ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
     ap.add_argument("--split-k", type=int, default=0, help="split count override for the swap-AB path (tuning)")
+    ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
+                    help="replay the timed launches from a CUDA graph (auto: problems under 1e11 FLOP)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another named workload (parity-test configurations; not the headline line)")
     args = ap.parse_args()
@@ -281,9 +284,9 @@ def main():
                               group_m=args.group_m or picked.group_m, split_k=1, swap_ab=0, grid=0)
         picked = forced
 
-    def step(c_ptr=None, a_ptr=None, b_ptr=None):
+    def step(c_ptr=None, a_ptr=None, b_ptr=None, stream_handle=None):
         args_ = (wl.M, wl.N, wl.K, a_ptr or A.data_ptr(), lda, b_ptr or B.data_ptr(), ldb,
-                 wl.b_layout, c_ptr or C.data_ptr(), ldc, wl.in_dtype, wl.out_dtype, sh)
+                 wl.b_layout, c_ptr or C.data_ptr(), ldc, wl.in_dtype, wl.out_dtype, stream_handle or sh)
         rc = tgemm.tgemm_run(*args_) if forced is None else tgemm.tgemm_run_config(*args_, forced)
         if rc != 0:
             raise RuntimeError("tgemm_run: " + tgemm.status_string(rc))
@@ -314,12 +317,37 @@ def main():
     torch.cuda.synchronize(dev)
     # Two events bracket the whole timed loop: the average launch duration is
     # the loop time over the launch count (an event after every launch would
-    # add its own overhead to kernels of a few microseconds).
+    # add its own overhead to kernels of a few microseconds).  Small problems
+    # replay the loop from a captured CUDA graph so that the host's per-call
+    # cost does not starve the GPU; the graph holds the same launches.
+    use_graph = args.graph == "on" or (args.graph == "auto" and wl.flops < GRAPH_FLOPS)
+    graph = None
+    if use_graph:
+        cap = torch.cuda.Stream(dev)
+        cap_h = ctypes.c_void_p(cap.cuda_stream)
+        with torch.cuda.stream(cap):
+            for i in range(reps):                      # per-stream set-up outside capture
+                a_, b_, c_ = copies[i]
+                step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr(), cap_h)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                a_, b_, c_ = copies[i % reps]
+                step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr(), cap_h)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for i in range(args.steps):
-        a_, b_, c_ = copies[i % reps]
-        step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            a_, b_, c_ = copies[i % reps]
+            step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -407,7 +435,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": value / PUBLISHED_TFLOPS if wl.name == WORKLOAD else None,
             "dtype": gen.DTYPE_NAME[wl.in_dtype], "data": "synthetic",
-            "config": dict(config_dict(wl, world), kernel=picked.as_dict()), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "config": dict(config_dict(wl, world), kernel=picked.as_dict(),
+                           launch="cuda_graph" if graph is not None else "stream"), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": args.steps,
             "kernel_ms": {"mean": avg_launch},
         }

@@ -42,7 +42,7 @@ def _nvcc() -> str:
 
 
 def _headers():
-    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".inc"))]
     hs.append(os.path.join(INCLUDE, "tgemm.h"))
     return sorted(hs)
 

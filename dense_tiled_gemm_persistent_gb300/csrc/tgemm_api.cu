@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -207,13 +208,86 @@ int skinny_splits(int64_t N, int64_t K, int sm_count)
 // a 128 x 128 tile halves the work per SM for 2/3 of the bytes of a
 // 128 x 256 one and keeps the tensor pipe less busy.  At most 64 rows of A
 // go to the swap-AB split-K path instead.
+// Measured winners per grid point (tune_picker.py); the last row is a sentinel.
+struct PickRow {
+    int em, en, ek, layout;
+    struct { int bm, bn, stages, cluster_m, group_m, split_k, swap_ab; } c;
+    float us;
+};
+const PickRow kPickTable[] = {
+#include "tgemm_picker_table.inc"
+    {-1, -1, -1, -1, {0, 0, 0, 0, 0, 0, 0}, 0.f},
+};
+
+int round_log2(int64_t x)
+{
+    int e = 0;
+    while (((int64_t)1 << (e + 1)) <= x) ++e;            // floor(log2 x)
+    // round: x >= 2^(e + 0.5)  <=>  x^2 >= 2^(2e + 1)
+    const double xd = (double)x;
+    return (xd * xd >= (double)((int64_t)1 << (2 * e + 1))) ? e + 1 : e;
+}
+
+// The measured winner at the grid point nearest (in log2) to this shape, if
+// the table has one; its tile shape and split are kept, sizes re-derived.
+bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, tgemm_config *cfg)
+{
+    const int em = round_log2(M), en = round_log2(N), ek = round_log2(K);
+    for (const PickRow &r : kPickTable) {
+        if (r.em < 0) break;
+        if (r.em != em || r.en != en || r.ek != ek || r.layout != b_layout) continue;
+        cfg->bm = r.c.bm;
+        cfg->bn = r.c.bn;
+        cfg->bk = kBK;
+        cfg->stages = r.c.stages;
+        cfg->cluster_m = r.c.cluster_m;
+        cfg->group_m = r.c.group_m;
+        cfg->split_k = r.c.split_k;
+        cfg->swap_ab = r.c.swap_ab;
+        cfg->grid = 0;
+        if (cfg->swap_ab) {
+            if (M > 64) return false;
+            const int npad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+            if (npad != cfg->bn) return false;          // grid point of another padding class
+        } else if (M <= 64) {
+            return false;
+        }
+        (void)sm_count;
+        return true;
+    }
+    return false;
+}
+
 int cluster_splits_limit(int npad) { return npad == 16 ? ClusterSplitPlan<16>::max_splits
                                            : npad == 32 ? ClusterSplitPlan<32>::max_splits
                                                         : ClusterSplitPlan<64>::max_splits; }
 int cluster_stages(int npad) { return npad == 16 ? ClusterSplitPlan<16>::stages
                                     : npad == 32 ? ClusterSplitPlan<32>::stages : ClusterSplitPlan<64>::stages; }
 
-void choose_config(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg)
+void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg);
+
+// The configuration tgemm_run uses: the measured table where it covers the
+// shape and its entry is legal for it, the wave cost model otherwise.
+void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, tgemm_config *cfg)
+{
+    if (table_config(M, N, K, b_layout, sm_count, cfg)) {
+        const int64_t kb = ceil_div(K, kBK);
+        bool ok = cfg->split_k <= kb;
+        if (ok && cfg->swap_ab == 2) ok = cfg->split_k <= cluster_splits_limit(cfg->bn);
+        if (ok) {
+            if (cfg->swap_ab)
+                cfg->grid = (int)(ceil_div(N, kSkinnyRows) * cfg->split_k);
+            else if (cfg->cluster_m == 2)
+                cfg->grid = (int)(2 * std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(), sm_count / 2));
+            else
+                cfg->grid = (int)std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(), sm_count);
+            return;
+        }
+    }
+    choose_config_model(M, N, K, sm_count, cfg);
+}
+
+void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg)
 {
     if (M <= 64) {
         const int npad = skinny_npad(M);
@@ -279,8 +353,8 @@ CUtensorMapDataType map_dtype(int dt)
 // 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
 // `ld` elements between rows; boxes of box_inner x box_outer, 128-byte swizzle,
 // zero fill outside the tensor.
-bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-               uint32_t box_inner, uint32_t box_outer)
+bool encode_2d_uncached(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                        uint32_t box_inner, uint32_t box_outer)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -291,6 +365,55 @@ bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64
     return enc(map, map_dtype(dt), 2, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A small direct-mapped cache of encoded tensor maps: a descriptor depends
+// only on (address, type, extents, row pitch, box), so repeated calls on the
+// same buffers skip the driver's encoder.
+struct MapKey {
+    const void *ptr;
+    int dt;
+    uint64_t inner, outer, ld;
+    uint32_t box_inner, box_outer;
+    bool operator==(const MapKey &o) const
+    {
+        return ptr == o.ptr && dt == o.dt && inner == o.inner && outer == o.outer && ld == o.ld &&
+               box_inner == o.box_inner && box_outer == o.box_outer;
+    }
+};
+struct MapSlot {
+    bool valid = false;
+    MapKey key;
+    CUtensorMap map;
+};
+constexpr int kMapSlots = 256;
+std::mutex g_map_mu;
+MapSlot g_maps[kMapSlots];
+
+// 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
+// `ld` elements between rows; boxes of box_inner x box_outer, 128-byte swizzle,
+// zero fill outside the tensor.
+bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer)
+{
+    const MapKey key{ptr, dt, inner, outer, ld, box_inner, box_outer};
+    uint64_t h = (uint64_t)(uintptr_t)ptr * 0x9E3779B97F4A7C15ull;
+    h ^= (inner * 31 + outer) * 0xC2B2AE3D27D4EB4Full;
+    h ^= (ld + ((uint64_t)box_inner << 20) + ((uint64_t)box_outer << 40) + (uint64_t)dt) * 0x165667B19E3779F9ull;
+    MapSlot &slot = g_maps[(h >> 32) % kMapSlots];
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        if (slot.valid && slot.key == key) {
+            *map = slot.map;
+            return true;
+        }
+    }
+    if (!encode_2d_uncached(map, dt, ptr, inner, outer, ld, box_inner, box_outer)) return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    slot.valid = true;
+    slot.key = key;
+    slot.map = *map;
+    return true;
 }
 
 tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_dtype, int b_layout,
@@ -446,7 +569,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         return TGEMM_OK;
     }
     if (!forced) {
-        choose_config(M, N, K, dev->sm_count, &cfg);
+        choose_config(M, N, K, b_layout, dev->sm_count, &cfg);
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
         if (st != TGEMM_OK) return st;
     }
@@ -538,7 +661,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     DeviceState *dev = nullptr;
     tgemm_status st = device_state(&dev);
     if (st != TGEMM_OK) return st;
-    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, dev->sm_count, out_cfg);
+    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, dev->sm_count, out_cfg);
     return TGEMM_OK;
 }
 

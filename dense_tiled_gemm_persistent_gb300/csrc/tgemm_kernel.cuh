@@ -383,7 +383,8 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
 {
     auto kern = gemm_persistent_kernel<BN, STAGES, OUT, B_MN>;
     constexpr uint32_t smem = SmemPlan<BN, STAGES>::alloc_bytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

@@ -243,7 +243,8 @@ cudaError_t launch_gemm_pair(const GemmParams &p, int grid, cudaStream_t stream)
 {
     auto kern = gemm_pair_kernel<STAGES, OUT, B_MN>;
     constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -284,7 +284,8 @@ cudaError_t launch_gemm_skinny(const GemmParams &p, int grid, cudaStream_t strea
 {
     auto kern = gemm_skinny_kernel<NPAD, OUT, W_MN>;
     constexpr uint32_t smem = SkinnyPlan<NPAD>::alloc_bytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

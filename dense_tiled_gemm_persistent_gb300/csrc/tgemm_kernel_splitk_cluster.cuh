@@ -243,7 +243,8 @@ cudaError_t launch_gemm_splitk_cluster(const GemmParams &p, int grid, cudaStream
 {
     auto kern = gemm_splitk_cluster_kernel<NPAD, OUT, W_MN>;
     constexpr uint32_t smem = ClusterSplitPlan<NPAD>::alloc_bytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

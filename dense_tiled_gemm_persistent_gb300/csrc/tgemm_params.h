@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace tgemm {
 
 enum OutType { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
@@ -67,6 +69,21 @@ extern const KernelVariant kVariantsBF16[];
 extern const int kNumVariantsBF16;
 extern const KernelVariant kVariantsF32[];
 extern const int kNumVariantsF32;
+
+// Raise a kernel's dynamic shared-memory limit once per device (the
+// attribute is per device and costs a driver call; launches are frequent).
+template <class Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, unsigned smem, std::atomic<unsigned long long> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // The bounded-wait self test kernel launcher (tgemm_debug.cu).
 cudaError_t launch_wait_timeout_probe(uint32_t *status, uint64_t timeout_ns, cudaStream_t st);

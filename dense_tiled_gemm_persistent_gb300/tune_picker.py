@@ -1,0 +1,177 @@
+"""Measure every kernel configuration over a grid of shapes and write the
+picker table the library compiles in.
+
+For each grid point (M, N, K, B layout) the script times each candidate
+configuration through tgemm_run_config on the current GPU (FP16 in, FP16
+out, back-to-back launches over enough rotating operand copies to exceed L2),
+keeps the fastest, and writes
+
+  * picker_table.csv              every measurement (committed, for review);
+  * csrc/tgemm_picker_table.inc   the winner per grid point, as a C array.
+
+Launches are timed from a replayed CUDA graph.  tgemm_run rounds log2 of
+each of M, N and K to the nearest grid exponent and
+uses the winner there; off the grid it falls back to its wave cost model.
+
+Usage (on the GPU machine):  python -m dense_tiled_gemm_persistent_gb300.tune_picker
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import ctypes
+import math
+import os
+import sys
+import time
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+
+CSV_PATH = os.path.join(HERE, "picker_table.csv")
+INC_PATH = os.path.join(HERE, "csrc", "tgemm_picker_table.inc")
+
+# grid exponents: large shapes and the skinny (M <= 64) band
+BIG_M = [8, 9, 10, 11, 12, 13, 14]          # 256 .. 16384
+BIG_N = [8, 9, 10, 11, 12, 13, 14]
+BIG_K = [10, 12, 13]                        # 1024, 4096, 8192
+SKINNY_M = [0, 3, 4, 5, 6]                  # 1, 8, 16, 32, 64
+SKINNY_N = [10, 12, 14]                     # 1024, 4096, 16384
+SKINNY_K = [10, 12, 13]
+
+L2 = 129 * 1000 * 1000
+
+
+def candidates(tg, M):
+    """(kind, Config) pairs valid for M rows of A."""
+    C = tg.Config
+    out = []
+    if M <= 64:
+        npad = 16 if M <= 16 else (32 if M <= 32 else 64)
+        st = {16: 12, 32: 10, 64: 9}[npad]
+        mx = {16: 8, 32: 8, 64: 7}[npad]
+        for s in (1, 2, 3, 4, 6, 8):
+            if s <= mx:
+                out.append(("cluster%d" % s, C(bm=128, bn=npad, bk=64, stages=st, cluster_m=s, group_m=1,
+                                             split_k=s, swap_ab=2, grid=0)))
+        for s in (4, 8, 16):
+            out.append(("workspace%d" % s, C(bm=128, bn=npad, bk=64, stages=4, cluster_m=1, group_m=1,
+                                             split_k=s, swap_ab=1, grid=0)))
+    out.append(("pair256", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=1, swap_ab=0, grid=0)))
+    out.append(("cta256", C(bm=128, bn=256, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
+    out.append(("cta128", C(bm=128, bn=128, bk=64, stages=6, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
+    return out
+
+
+def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters):
+    """Microseconds per launch, replaying `iters` launches from a CUDA graph
+    (so the host's per-call cost does not hide the kernel's own time)."""
+    n = len(copies)
+    cap = torch.cuda.Stream()
+    sh = ctypes.c_void_p(cap.cuda_stream)
+
+    def run(i):
+        A, B, C = copies[i % n]
+        return tg.tgemm_run_config(M, N, K, A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1], layout,
+                                   C.data_ptr(), C.shape[1], 0, 0, sh, cfg)
+
+    with torch.cuda.stream(cap):
+        for i in range(3):
+            if run(i) != 0:
+                return None
+    torch.cuda.synchronize()
+    if tg.tgemm_check(sh) != 0:
+        return None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(iters):
+            if run(i) != 0:
+                return None
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if tg.tgemm_check(ctypes.c_void_p(stream.cuda_stream)) != 0:
+        return None
+    return e0.elapsed_time(e1) / iters * 1000.0   # microseconds
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--quick", action="store_true", help="a few grid points only (smoke)")
+    ap.add_argument("--csv", default=CSV_PATH)
+    ap.add_argument("--inc", default=INC_PATH)
+    args = ap.parse_args()
+
+    import torch
+    from dense_tiled_gemm_persistent_gb300 import build as lb
+    from dense_tiled_gemm_persistent_gb300 import tgemm as tg
+    lb.build()
+    tg.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+
+    points = []
+    for layout in (tg.B_NK, tg.B_KN):
+        for em in BIG_M:
+            for en in BIG_N:
+                for ek in BIG_K:
+                    points.append((em, en, ek, layout))
+        for em in SKINNY_M:
+            for en in SKINNY_N:
+                for ek in SKINNY_K:
+                    points.append((em, en, ek, layout))
+    if args.quick:
+        points = points[::37]
+
+    rows, winners = [], []
+    t0 = time.time()
+    for (em, en, ek, layout) in points:
+        M, N, K = 1 << em, 1 << en, 1 << ek
+        bytes_ = 2 * (M * K + K * N + M * N)
+        reps = max(1, -(-3 * L2 // bytes_))
+        reps = min(reps, 64)
+        flops = 2.0 * M * N * K
+        iters = int(min(200, max(10, 2e13 / flops)))
+        copies = []
+        for _ in range(reps):
+            A = torch.randn(M, K, device=dev).to(torch.float16)
+            B = torch.randn(*((N, K) if layout == tg.B_NK else (K, N)), device=dev).to(torch.float16)
+            Cc = torch.empty(M, N, device=dev, dtype=torch.float16)
+            copies.append((A, B, Cc))
+        best = None
+        for kind, cfg in candidates(tg, M):
+            us = time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters)
+            if us is None:
+                continue
+            rows.append(dict(em=em, en=en, ek=ek, layout=layout, kind=kind, us=round(us, 3),
+                             tflops=round(flops / us / 1e6, 1)))
+            if best is None or us < best[0]:
+                best = (us, kind, cfg)
+        del copies
+        if best:
+            winners.append((em, en, ek, layout, best))
+        print("%5d %5d %5d %s -> %s %.2f us" % (M, N, K, "nk" if layout else "kn", best[1] if best else None,
+                                                 best[0] if best else -1), flush=True)
+    print("sweep took %.0f s" % (time.time() - t0))
+
+    with open(args.csv, "w", newline="") as f:
+        w = csv.DictWriter(f, fieldnames=["em", "en", "ek", "layout", "kind", "us", "tflops"])
+        w.writeheader()
+        w.writerows(rows)
+    gpu = torch.cuda.get_device_name(dev)
+    with open(args.inc, "w") as f:
+        f.write("// Generated by dense_tiled_gemm_persistent_gb300/tune_picker.py on %s.\n" % gpu)
+        f.write("// log2 M, log2 N, log2 K, B layout (0 = KxN, 1 = NxK) -> fastest measured configuration\n")
+        f.write("// {bm, bn, stages, cluster_m, group_m, split_k, swap_ab}, and its time in us.\n")
+        for em, en, ek, layout, (us, kind, c) in winners:
+            f.write("{%d, %d, %d, %d, {%d, %d, %d, %d, %d, %d, %d}, %.3ff},  // %s\n" % (
+                em, en, ek, layout, c.bm, c.bn, c.stages, c.cluster_m, c.group_m, c.split_k, c.swap_ab, us, kind))
+    print("wrote", args.csv, "and", args.inc)
+
+
+if __name__ == "__main__":
+    main()
