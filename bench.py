@@ -43,6 +43,21 @@ def tflops(M: int, N: int, K: int, ms: float) -> float:
     return 2.0 * M * N * K / (ms * 1e-3) / 1e12
 
 
+def aggregate(total_ms_local: float, steps: int, flops_per_step: float, world: int, device="cpu"):
+    """Whole-job throughput of `world` replicas: every rank ran `steps` steps
+    of `flops_per_step`; the job's time is the slowest rank's.  Returns
+    (max_ms, ms_per_step, TFLOPS over all ranks)."""
+    total = float(total_ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    ms_per_step = total / steps
+    return total, ms_per_step, flops_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def kernel_digest() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -357,14 +372,9 @@ def main():
     if rc != 0:
         raise RuntimeError("timed region failed: " + tgemm.status_string(rc))
     total_ms = e_start.elapsed_time(e_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
-    ms_per_step = total_ms / args.steps
-    value = tflops(wl.M, wl.N, wl.K, ms_per_step) * world
-    avg_launch = total_ms / args.steps
+    local_ms = total_ms
+    total_ms, ms_per_step, value = aggregate(local_ms, args.steps, wl.flops, world, dev)
+    avg_launch = local_ms / args.steps
 
     peaks = measured_peaks()
     if peaks and peaks.get("bf16_tflops"):

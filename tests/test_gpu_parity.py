@@ -306,3 +306,12 @@ def test_skinny_concurrent_streams_do_not_share_partials():
     for (a, b), C in zip(ops, Cs):
         ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.BF16)
         assert np.array_equal(C.cpu().double().numpy(), ref)
+
+
+def test_query_config_follows_the_measured_table():
+    # 8192^3 with B stored N x K is a grid point of the table: the CTA pair won there
+    rc, c = tgemm.tgemm_query_config(8192, 8192, 8192, gen.B_NK, gen.F16, gen.F16)
+    assert rc == 0 and (c.cluster_m, c.bm, c.bn) == (2, 256, 256)
+    # 16 x 4096 x 4096: the in-cluster split-K path
+    rc, c = tgemm.tgemm_query_config(16, 4096, 4096, gen.B_NK, gen.BF16, gen.BF16)
+    assert rc == 0 and c.swap_ab == 2 and c.split_k == c.cluster_m

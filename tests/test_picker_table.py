@@ -1,0 +1,59 @@
+"""The compiled-in picker table (measured on a GB300 by tune_picker.py)."""
+import csv
+import os
+import re
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+PKG = os.path.join(os.path.dirname(HERE), "dense_tiled_gemm_persistent_gb300")
+INC = os.path.join(PKG, "csrc", "tgemm_picker_table.inc")
+CSV = os.path.join(PKG, "picker_table.csv")
+
+ROW = re.compile(r"\{(-?\d+), (-?\d+), (-?\d+), (\d+), \{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}, "
+                 r"([0-9.]+)f\},\s*// (\w+)")
+
+
+def rows():
+    out = []
+    for line in open(INC):
+        m = ROW.match(line.strip())
+        if m:
+            v = [int(x) for x in m.groups()[:11]]
+            out.append(dict(em=v[0], en=v[1], ek=v[2], layout=v[3], bm=v[4], bn=v[5], stages=v[6], cluster_m=v[7],
+                            group_m=v[8], split_k=v[9], swap_ab=v[10], us=float(m.group(12)), kind=m.group(13)))
+    return out
+
+
+def test_every_row_is_a_legal_configuration():
+    r = rows()
+    assert len(r) > 100
+    seen = set()
+    for e in r:
+        key = (e["em"], e["en"], e["ek"], e["layout"])
+        assert key not in seen, key
+        seen.add(key)
+        if e["swap_ab"]:
+            M = 1 << e["em"]
+            assert M <= 64 and e["bn"] >= M and e["bm"] == 128
+            if e["swap_ab"] == 2:
+                assert e["cluster_m"] == e["split_k"] and e["stages"] == {16: 12, 32: 10, 64: 9}[e["bn"]]
+        else:
+            assert (e["cluster_m"], e["bm"]) in ((1, 128), (2, 256))
+            assert e["split_k"] == 1
+
+
+def test_table_rows_are_the_fastest_measurement_of_their_point():
+    best = {}
+    for m in csv.DictReader(open(CSV)):
+        key = (int(m["em"]), int(m["en"]), int(m["ek"]), int(m["layout"]))
+        if key not in best or float(m["us"]) < best[key][0]:
+            best[key] = (float(m["us"]), m["kind"])
+    for e in rows():
+        us, kind = best[(e["em"], e["en"], e["ek"], e["layout"])]
+        assert kind == e["kind"] and us == pytest.approx(e["us"], abs=1e-3)
+
+
+def test_large_square_problems_pick_the_cta_pair():
+    big = [e for e in rows() if e["em"] >= 13 and e["en"] >= 13 and e["ek"] >= 12]
+    assert big and all(e["kind"] == "pair256" for e in big)
