@@ -440,7 +440,8 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
         return TGEMM_OK;
     }
     if (c.swap_ab != 0) return TGEMM_ERR_UNSUPPORTED;
-    if (c.split_k != 1) return TGEMM_ERR_UNSUPPORTED;
+    // split_k = 0 asks the pair kernel for a stream-K tail
+    if (!(c.split_k == 1 || (c.split_k == 0 && c.cluster_m == 2))) return TGEMM_ERR_UNSUPPORTED;
     if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
         return TGEMM_ERR_UNSUPPORTED;
     *v = find_variant(c.bn, c.stages, out_dtype, b_mn, c.cluster_m);
@@ -489,6 +490,51 @@ int resident_pairs(DeviceState *dev, const KernelVariant *v)
     if (n <= 0) n = dev->sm_count / 2;
     dev->pairs[(const void *)v] = n;
     return n;
+}
+
+// Stream-K tail for the pair kernel: when the tiles leave the last wave of
+// pairs partly idle, the last one or two waves' tiles are shared out by
+// k-block iterations (at least kMinSkIters per pair, at most kMaxSegments
+// tiles touched per pair).  Fills p.dp_tiles/sk_tiles/sk_units, the FP32
+// partial-tile workspace and its tensor map; sk_units = 0 keeps whole tiles.
+constexpr int64_t kMinSkIters = 8;
+
+tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *stream_ptr)
+{
+    (void)dev;
+    const int64_t T = p->num_tiles, KB = p->num_kb, P = pairs;
+    p->dp_tiles = (int32_t)T;
+    p->sk_tiles = 0;
+    p->sk_units = 0;
+    const int64_t full = T / P, rem = T % P;
+    if (rem == 0) return TGEMM_OK;
+    const int64_t dp = full >= 1 ? (full - 1) * P : 0;
+    const int64_t sk_tiles = T - dp;
+    const int64_t total = sk_tiles * KB;
+    int64_t units = total / kMinSkIters;
+    if (units > P) units = P;
+    if (units <= sk_tiles && full == 0) return TGEMM_OK;   // no more pairs than tiles to share with
+    if (units < 2) return TGEMM_OK;
+    if (2 * sk_tiles * 4 > (int64_t)kCounterBytes) return TGEMM_OK;
+    const StreamK sk{sk_tiles, units, KB};
+    for (int64_t u = 0; u < units; ++u) {
+        if (sk.bound(u + 1) <= sk.bound(u)) return TGEMM_OK;                 // empty share
+        const int64_t segs = (sk.bound(u + 1) - 1) / KB - sk.bound(u) / KB + 1;
+        if (segs > kMaxSegments) return TGEMM_OK;
+    }
+    const int64_t slots = units * kMaxSegments;
+    const size_t part = (size_t)slots * kPairBM * kPairBN * sizeof(float);
+    int devno = 0;
+    cudaGetDevice(&devno);
+    tgemm_status st = split_workspace(devno, stream_ptr, part, &p->counters, &p->partials);
+    if (st != TGEMM_OK) return st;
+    if (!encode_2d(&p->tma_ws, TGEMM_F32, p->partials, (uint64_t)kPairBN, (uint64_t)(slots * kPairBM),
+                   (uint64_t)kPairBN, 32, 32))
+        return TGEMM_ERR_CUDA;
+    p->dp_tiles = (int32_t)dp;
+    p->sk_tiles = (int32_t)sk_tiles;
+    p->sk_units = (int32_t)units;
+    return TGEMM_OK;
 }
 
 // C^T = B^T A^T on a swap-AB split-K kernel (M <= 64): the workspace
@@ -606,15 +652,22 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     p.timeout_ns = wait_timeout_ns();
 
     int g;
+    p.dp_tiles = p.num_tiles;
     if (pair) {
         // grid counts CTAs: an even number, at most two per tile and two per
         // resident pair
         int pairs = cfg.grid > 0 ? cfg.grid / 2 : dev->sm_count / 2;
         const int resident = resident_pairs(dev, var);
         if (pairs > resident) pairs = resident;
-        if (pairs > p.num_tiles) pairs = p.num_tiles;
+        if (cfg.split_k != 0 && pairs > p.num_tiles) pairs = p.num_tiles;
         if (pairs < 1) pairs = 1;
         g = 2 * pairs;
+        if (cfg.split_k == 0) {
+            tgemm_status st2 = plan_stream_k(&p, pairs, dev, stream_ptr);
+            if (st2 != TGEMM_OK) return st2;
+            if (p.sk_units == 0 && pairs > p.num_tiles) g = 2 * p.num_tiles;
+            if (p.sk_units > 0 && p.dp_tiles == 0) g = 2 * p.sk_units;   // only the sharing pairs have work
+        }
     } else {
         g = cfg.grid > 0 ? cfg.grid : dev->sm_count;
         if (g > p.num_tiles) g = p.num_tiles;

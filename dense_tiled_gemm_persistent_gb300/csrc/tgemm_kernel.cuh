@@ -102,7 +102,8 @@ struct SmemPlan {
     static constexpr uint32_t n_bars = 2 * STAGES + 5;
     static constexpr uint32_t slot_off = bar_off + 8 * n_bars;   // TMEM address
     static constexpr uint32_t abort_off = slot_off + 4;
-    static constexpr uint32_t bytes = abort_off + 4;
+    static constexpr uint32_t flag_off = abort_off + 4;          // epilogue broadcast word
+    static constexpr uint32_t bytes = flag_off + 4;
     static constexpr uint32_t alloc_bytes = bytes + 1024;        // slack to align the base to 1024
 };
 
@@ -125,16 +126,58 @@ __device__ __forceinline__ uint32_t pack_out(float lo, float hi, int out)
     return u;
 }
 
+// Cast one 128-byte-wide column chunk of this warp's 32 rows (v0, plus v1
+// for 16-bit output: 64 columns), stage it in one of the warp's two swizzled
+// staging blocks and store it with TMA at (x, row0) of `map`; rows >= rows_lim
+// or a chunk starting at x >= cols_lim are not written (TMA clips the rest).
+// `cc` counts chunks and selects the staging block.
+template <int OUT>
+__device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_t rows_lim, int32_t cols_lim,
+                                                  uint32_t stage_base, uint32_t &cc, int32_t row0, int32_t x,
+                                                  int lane, const uint32_t (&v0)[32], const uint32_t (&v1)[32])
+{
+    const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
+    if (lane == 0) ptx::bulk_wait_group_read<1>();   // the store that last used sbuf is done reading
+    __syncwarp();
+    const uint32_t row_addr = sbuf + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w0, w1, w2, w3;
+        if constexpr (OUT == OUT_F32) {
+            w0 = v0[4 * j + 0];
+            w1 = v0[4 * j + 1];
+            w2 = v0[4 * j + 2];
+            w3 = v0[4 * j + 3];
+        } else {
+            // columns 8j .. 8j+7 of the 64-column chunk
+            const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+            w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
+            w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);
+            w2 = pack_out(__uint_as_float(src[4]), __uint_as_float(src[5]), OUT);
+            w3 = pack_out(__uint_as_float(src[6]), __uint_as_float(src[7]), OUT);
+        }
+        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
+        ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (x < cols_lim && row0 < rows_lim) ptx::tma_store_2d(map, sbuf, x, row0);
+        ptx::bulk_commit_group();
+    }
+    ++cc;
+}
+
 // Drain one accumulator buffer held in this warp's TMEM lane quarter: tile
-// rows [row0, row0 + 32), columns [col0, col0 + BN).  Each 128-byte-wide
-// column chunk is read with tcgen05.ld, cast, written to one of this warp's
-// two swizzled staging blocks and stored with TMA.  `release()` runs on lane 0
+// rows [row0, row0 + 32), columns [col0, col0 + BN), into `map` (C, or the
+// FP32 partial-tile workspace).  Each 128-byte-wide column chunk is read with
+// tcgen05.ld and handed to stage_store_chunk.  `release()` runs on lane 0
 // once the last chunk is in registers, handing the buffer back to the MMA
-// issuer.  `cc` counts chunks (it selects the staging block).
+// issuer.
 template <int BN, int OUT, typename Release>
-__device__ __forceinline__ void epilogue_drain(const GemmParams &p, uint32_t t_acc, uint32_t stage_base,
-                                               uint32_t &cc, int32_t row0, int32_t col0, int lane,
-                                               Release release)
+__device__ __forceinline__ void epilogue_drain(const CUtensorMap *map, int32_t rows_lim, int32_t cols_lim,
+                                               uint32_t t_acc, uint32_t stage_base, uint32_t &cc, int32_t row0,
+                                               int32_t col0, int lane, Release release)
 {
     constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
     constexpr int kChunkCols = 128 / kOutBytes;          // columns of one 128-byte staged row
@@ -151,37 +194,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams &p, uint32_t t_a
             __syncwarp();
             if (lane == 0) release();
         }
-        const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
-        if (lane == 0) ptx::bulk_wait_group_read<1>();   // the store that last used sbuf is done reading
-        __syncwarp();
-        const uint32_t row_addr = sbuf + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t w0, w1, w2, w3;
-            if constexpr (OUT == OUT_F32) {
-                w0 = v0[4 * j + 0];
-                w1 = v0[4 * j + 1];
-                w2 = v0[4 * j + 2];
-                w3 = v0[4 * j + 3];
-            } else {
-                // columns 8j .. 8j+7 of the 64-column chunk
-                const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
-                w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
-                w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);
-                w2 = pack_out(__uint_as_float(src[4]), __uint_as_float(src[5]), OUT);
-                w3 = pack_out(__uint_as_float(src[6]), __uint_as_float(src[7]), OUT);
-            }
-            // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
-            ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            const int32_t x = col0 + c * kChunkCols;
-            if (x < p.N && row0 < p.M) ptx::tma_store_2d(&p.tma_c, sbuf, x, row0);
-            ptx::bulk_commit_group();
-        }
-        ++cc;
+        stage_store_chunk<OUT>(map, rows_lim, cols_lim, stage_base, cc, row0, col0 + c * kChunkCols, lane, v0, v1);
     }
 }
 
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             const int32_t col0 = (int32_t)tc * BN;
             const uint32_t t_acc = tmem_base + lane_base + buf * BN;
             const uint32_t release_bar = tempty_bar(buf);
-            epilogue_drain<BN, OUT>(p, t_acc, stage_base, cc, row0, col0, lane,
+            epilogue_drain<BN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
                                     [&] { ptx::mbar_arrive(release_bar); });
         }
         if (lane == 0) ptx::bulk_wait_group_all();

@@ -20,6 +20,17 @@
 //   tmem_empty[b] leader only; all eight epilogue warps of the pair arrive.
 // A cluster barrier after barrier initialisation and another before the
 // tensor memory is freed keep either CTA from running ahead of the other.
+//
+// Stream-K tail (sk_units > 0).  When the tiles do not fill whole waves of
+// pairs, the tiles of the last one or two waves are not dealt out whole: their
+// k-block iterations are shared evenly among the pairs (StreamK in
+// tgemm_sched.h).  A pair whose share covers a tile only in part writes its
+// FP32 partial tile to a workspace slot and bumps that tile's arrival counter
+// (one counter per CTA half); the CTA that arrives last adds the partials in
+// k order -- a fixed order, independent of timing -- casts, stores C and
+// resets the counter.  Nobody waits for another pair.  Splitting work by
+// iterations instead of tiles is this library's choice; the pages deal whole
+// tiles to blocks.
 #pragma once
 
 #include "tgemm_kernel.cuh"
@@ -28,6 +39,57 @@ namespace tgemm {
 
 constexpr int kPairBM = 256;        // rows of a pair tile (128 per CTA)
 constexpr int kPairBN = 256;        // columns of a pair tile (B split 128 + 128)
+
+// One work item of a CTA pair: a k-block range of one tile.
+struct PairWork {
+    int tile;          // tile number in grouped order
+    int k0, k1;        // k-blocks [k0, k1)
+    bool partial;      // a stream-K segment: the tile is shared with other pairs
+    int64_t t_sk;      // tail tile index (partial segments)
+    int64_t slot;      // workspace slot (partial segments)
+};
+
+// The items of pair `cid` of `P`: whole tiles cid, cid + P, ... below
+// dp_tiles, then the segments of its stream-K share of the tail.
+struct PairWorkIter {
+    int next_dp, dp_tiles, P, kb;
+    StreamK sk;
+    int64_t unit, it, end;
+
+    __device__ PairWorkIter(const GemmParams &p, int cid, int num_pairs)
+        : next_dp(cid), dp_tiles(p.dp_tiles), P(num_pairs), kb(p.num_kb),
+          sk{p.sk_tiles, p.sk_units > 0 ? p.sk_units : 1, p.num_kb}, unit(cid), it(0), end(0)
+    {
+        if (p.sk_units > 0 && cid < p.sk_units) {
+            it = sk.bound(cid);
+            end = sk.bound(cid + 1);
+        }
+    }
+
+    __device__ bool next(PairWork &w)
+    {
+        if (next_dp < dp_tiles) {
+            w.tile = next_dp;
+            w.k0 = 0;
+            w.k1 = kb;
+            w.partial = false;
+            next_dp += P;
+            return true;
+        }
+        if (it >= end) return false;
+        const int64_t t = it / kb;
+        const int64_t tile_end = (t + 1) * kb;
+        const int64_t stop = end < tile_end ? end : tile_end;
+        w.tile = (int)(dp_tiles + t);
+        w.k0 = (int)(it - t * kb);
+        w.k1 = (int)(stop - t * kb);
+        w.partial = !(w.k0 == 0 && w.k1 == kb);
+        w.t_sk = t;
+        w.slot = sk.slot(unit, t);
+        it = stop;
+        return true;
+    }
+};
 
 template <int STAGES, int OUT, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p)
@@ -91,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
 
     WaitCtx wc{p.status, abort_flag, p.timeout_ns};
     wc.peer_abort = ptx::map_to_cta(abort_addr, rank ^ 1u);
-    const int num_tiles = p.num_tiles;
     const int cluster_id = blockIdx.x >> 1;
     const int num_clusters = gridDim.x >> 1;
     bool aborted = false;
@@ -103,12 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+            PairWorkIter items(p, cluster_id, num_clusters);
+            PairWork w;
+            while (ok && items.next(w)) {
                 int64_t tr, tc;
-                grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+                grouped_tile(p.tiles_m, p.tiles_n, p.group_m, w.tile, tr, tc);
                 const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank;
                 const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = w.k0; kb < w.k1; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
@@ -153,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             uint32_t ph = 0;
             uint32_t local = 0;
             bool ok = true;
-            for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
+            PairWorkIter items(p, cluster_id, num_clusters);
+            PairWork w;
+            for (; ok && items.next(w); ++local) {
                 const uint32_t buf = local & 1u;
                 const uint32_t bph = (local >> 1) & 1u;
                 if (!wait_bounded(tempty_bar(buf), bph ^ 1u, wc, SITE_MMA_TMEM_EMPTY)) {
@@ -162,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * kPairBN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = w.k0; kb < w.k1; ++kb) {
                     if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
                         ok = false;
                         break;
@@ -174,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
                         const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
                         const uint64_t bd = desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
-                        ptx::mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        ptx::mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(empty_bar(s), 0x3);   // stage s free in both CTAs
                     if (++s == STAGES) {
@@ -198,25 +263,85 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
+        volatile int *last_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::flag_off);
         uint32_t local = 0, cc = 0;
-        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+        PairWorkIter items(p, cluster_id, num_clusters);
+        PairWork w;
+        for (; items.next(w); ++local) {
             const uint32_t buf = local & 1u;
             const uint32_t bph = (local >> 1) & 1u;
             const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
-            if (!__all_sync(0xffffffffu, got)) {
+            // The four epilogue warps decide together (the stream-K hand-off
+            // below synchronises them, so none may leave alone).
+            if (!ptx::named_barrier_and(2, kEpiWarps * 32, got)) {
                 aborted = true;
                 break;
             }
             ptx::tc_fence_after_sync();
 
             int64_t tr, tc;
-            grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+            grouped_tile(p.tiles_m, p.tiles_n, p.group_m, w.tile, tr, tc);
             const int32_t row0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 32 * q;
             const int32_t col0 = (int32_t)tc * kPairBN;
             const uint32_t t_acc = tmem_base + lane_base + buf * kPairBN;
             const uint32_t release_bar = ptx::map_to_cta(tempty_bar(buf), 0);
-            epilogue_drain<kPairBN, OUT>(p, t_acc, stage_base, cc, row0, col0, lane,
-                                         [&] { ptx::mbar_arrive_cluster(release_bar); });
+            if (!w.partial) {
+                epilogue_drain<kPairBN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
+                                             [&] { ptx::mbar_arrive_cluster(release_bar); });
+                continue;
+            }
+            // ---- stream-K segment: FP32 partial tile into the workspace
+            const int32_t prow = (int32_t)(w.slot * kPairBM) + 128 * (int32_t)rank + 32 * q;
+            epilogue_drain<kPairBN, OUT_F32>(&p.tma_ws, INT32_MAX, kPairBN, t_acc, stage_base, cc, prow, 0, lane,
+                                             [&] { ptx::mbar_arrive_cluster(release_bar); });
+            if (lane == 0) {
+                ptx::bulk_wait_group_all();          // this warp's partial rows are written
+                ptx::fence_proxy_async_global();
+            }
+            __syncwarp();
+            __threadfence();
+            const StreamK sk{p.sk_tiles, p.sk_units, p.num_kb};
+            const int64_t first = w.t_sk * p.num_kb, stop = first + p.num_kb;
+            const int64_t u0 = sk.unit_of(first);
+            ptx::named_barrier(1, kEpiWarps * 32);
+            if (ew == 0 && lane == 0) {
+                uint32_t segs = 0;
+                for (int64_t u = u0; u < sk.sk_units && sk.bound(u) < stop; ++u) ++segs;
+                const uint32_t prev = atomicAdd(&p.counters[2 * w.t_sk + rank], 1u);
+                *last_flag = (prev + 1 == segs) ? 1 : 0;
+            }
+            ptx::named_barrier(1, kEpiWarps * 32);
+            if (*last_flag) {
+                // Every segment of this tile half is in: add them in k order.
+                __threadfence();
+                constexpr int kCols = OUT == OUT_F32 ? 32 : 64;
+                const int64_t my_row = 128 * (int64_t)rank + 32 * q + lane;   // row inside the pair tile
+#pragma unroll 1
+                for (int c = 0; c < kPairBN / kCols; ++c) {
+                    float acc[kCols];
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
+                    for (int64_t u = u0; u < sk.sk_units && sk.bound(u) < stop; ++u) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.partials + ((sk.slot(u, w.t_sk) * kPairBM + my_row) * kPairBN + c * kCols));
+#pragma unroll
+                        for (int j = 0; j < kCols / 4; ++j) {
+                            const float4 t = __ldcg(src + j);
+                            acc[4 * j] += t.x;
+                            acc[4 * j + 1] += t.y;
+                            acc[4 * j + 2] += t.z;
+                            acc[4 * j + 3] += t.w;
+                        }
+                    }
+                    uint32_t v0[32], v1[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v0[j] = __float_as_uint(acc[j]);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v1[j] = kCols == 64 ? __float_as_uint(acc[(32 + j) % kCols]) : 0u;
+                    stage_store_chunk<OUT>(&p.tma_c, p.M, p.N, stage_base, cc, row0, col0 + c * kCols, lane, v0, v1);
+                }
+                if (ew == 0 && lane == 0) p.counters[2 * w.t_sk + rank] = 0u;   // ready for the next call
+            }
         }
         if (lane == 0) ptx::bulk_wait_group_all();
         __syncwarp();

@@ -33,6 +33,7 @@ struct alignas(128) GemmParams {
     CUtensorMap tma_a;      // A: dims {K, M}, box {64, 128}, 128-byte swizzle
     CUtensorMap tma_b;      // B: NK dims {K, N} box {64, bn}; KN dims {N, K} box {64, 64}
     CUtensorMap tma_c;      // C: dims {N, M}, box {128 bytes of columns, 32}, 128-byte swizzle
+    CUtensorMap tma_ws;     // stream-K partial tiles (FP32): dims {256, slots * 256}, box {32, 32}
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_tiles, num_kb;
     int32_t group_m;
@@ -46,6 +47,10 @@ struct alignas(128) GemmParams {
     float *partials;        // [splits][tiles_n][128 rows][npad] FP32 partial sums
     uint32_t *counters;     // [tiles_n] arrival counters, zero between calls
     int32_t splits;         // K is cut into `splits` runs of whole k-blocks
+    // stream-K tail of the CTA-pair kernel (sk_units = 0: whole tiles only)
+    int32_t dp_tiles;       // tiles [0, dp_tiles) are processed whole
+    int32_t sk_tiles;       // tiles [dp_tiles, dp_tiles + sk_tiles) are spread over
+    int32_t sk_units;       // the first sk_units pairs, evenly by k-block
 };
 
 using LaunchFn = cudaError_t (*)(const GemmParams &, int grid, cudaStream_t);

@@ -106,6 +106,13 @@ __device__ __forceinline__ void bulk_wait_group_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Order completed async-proxy (TMA) global writes with later generic-proxy
+// accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Order generic-proxy shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -208,6 +215,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier for `count` threads that also ANDs a predicate over them:
+// every participant gets true only if all passed true.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void tmem_ld_wait()

@@ -52,4 +52,32 @@ TGEMM_HD void grouped_tile(int64_t tiles_m, int64_t tiles_n, int group_m, int64_
     tile_col = (bid - band * band_tiles) / rows;
 }
 
+// Stream-K split of the last tiles ("Stream-K" work decomposition: equal
+// shares of multiply-accumulate iterations instead of whole tiles).  The
+// sk_tiles tail tiles hold sk_tiles * kb k-block iterations, numbered tile by
+// tile; unit u (a persistent CTA pair) takes iterations [bound(u),
+// bound(u+1)).  A unit's share is cut at tile boundaries into segments; a
+// tile covered by several units is summed from their partial results.  Every
+// unit's share touches at most kMaxSegments tiles (the host keeps the share
+// under two tiles' worth).
+constexpr int kMaxSegments = 3;
+
+struct StreamK {
+    int64_t sk_tiles, sk_units, kb;
+
+    TGEMM_HD int64_t total() const { return sk_tiles * kb; }
+    TGEMM_HD int64_t bound(int64_t u) const { return u * total() / sk_units; }
+    // The unit whose share contains iteration x (every share is non-empty).
+    TGEMM_HD int64_t unit_of(int64_t x) const
+    {
+        int64_t u = x * sk_units / total();
+        while (u + 1 < sk_units && bound(u + 1) <= x) ++u;
+        while (u > 0 && bound(u) > x) --u;
+        return u;
+    }
+    // Workspace slot of unit u's segment of tail tile t (unit-major, one slot
+    // per segment in the order the unit meets its tiles).
+    TGEMM_HD int64_t slot(int64_t u, int64_t t) const { return u * kMaxSegments + (t - bound(u) / kb); }
+};
+
 }  // namespace tgemm

@@ -315,3 +315,37 @@ def test_query_config_follows_the_measured_table():
     # 16 x 4096 x 4096: the in-cluster split-K path
     rc, c = tgemm.tgemm_query_config(16, 4096, 4096, gen.B_NK, gen.BF16, gen.BF16)
     assert rc == 0 and c.swap_ab == 2 and c.split_k == c.cluster_m
+
+
+# ---- stream-K tail of the CTA-pair kernel -------------------------------------------
+
+def sk_cfg(pairs=0, group_m=8):
+    return tgemm.Config(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=group_m, split_k=0, swap_ab=0,
+                        grid=2 * pairs)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("pairs", [3, 4, 7, 13, 0])
+def test_stream_k_tail_integers_exact(layout, pairs):
+    """1100 x 1300 pair tiles (5 x 6 = 30) over 3, 4, 7, 13 or all pairs: the
+    last waves' tiles are shared out by k-block and summed from partials."""
+    M, N, K = 1100, 1300, 1500
+    a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=47)
+    check_full(a, b, M, N, K, layout, gen.BF16, gen.F32, exact=True, config=sk_cfg(pairs),
+               what="stream-K pairs=%d %s" % (pairs, LNAME[layout]))
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 8192), (300, 520, 4000), (1000, 700, 3000), (2304, 1280, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out_dtype", [gen.F32, gen.BF16], ids=["o32", "obf16"])
+def test_stream_k_random_values(shape, out_dtype):
+    M, N, K = shape
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=53)
+    check_full(a, b, M, N, K, gen.B_NK, gen.BF16, out_dtype, config=sk_cfg(), what="stream-K %s" % (shape,))
+
+
+def test_stream_k_is_deterministic_across_calls():
+    M, N, K = 640, 1280, 6000
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.normal(0, 1), seed=59)
+    outs = [run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, config=sk_cfg()) for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
