@@ -236,7 +236,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--config", default="auto", choices=["auto", "pair", "1cta256", "1cta128", "workspace"],
+    ap.add_argument("--config", default="auto", choices=["auto", "pair", "pairsk", "1cta256", "1cta128", "workspace"],
                     help="tile shape: the library's pick, or a forced one (tuning)")
     ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
     ap.add_argument("--split-k", type=int, default=0, help="split count override for the swap-AB path (tuning)")
@@ -292,11 +292,12 @@ def main():
                               split_k=args.split_k, swap_ab=picked.swap_ab, grid=0)
         picked = forced
     elif args.config != "auto" or args.group_m:
-        shapes = {"pair": (256, 256, 6, 2), "1cta256": (128, 256, 4, 1), "1cta128": (128, 128, 6, 1)}
-        bm, bn, st, cl = shapes[args.config] if args.config != "auto" else (
-            picked.bm, picked.bn, picked.stages, picked.cluster_m)
+        shapes = {"pair": (256, 256, 6, 2, 1), "pairsk": (256, 256, 6, 2, 0), "1cta256": (128, 256, 4, 1, 1),
+                  "1cta128": (128, 128, 6, 1, 1)}
+        bm, bn, st, cl, sk = shapes[args.config] if args.config != "auto" else (
+            picked.bm, picked.bn, picked.stages, picked.cluster_m, picked.split_k)
         forced = tgemm.Config(bm=bm, bn=bn, bk=64, stages=st, cluster_m=cl,
-                              group_m=args.group_m or picked.group_m, split_k=1, swap_ab=0, grid=0)
+                              group_m=args.group_m or picked.group_m, split_k=sk, swap_ab=0, grid=0)
         picked = forced
 
     def step(c_ptr=None, a_ptr=None, b_ptr=None, stream_handle=None):

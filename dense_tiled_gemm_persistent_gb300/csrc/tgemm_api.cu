@@ -278,7 +278,9 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, 
             if (cfg->swap_ab)
                 cfg->grid = (int)(ceil_div(N, kSkinnyRows) * cfg->split_k);
             else if (cfg->cluster_m == 2)
-                cfg->grid = (int)(2 * std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(), sm_count / 2));
+                cfg->grid = cfg->split_k == 0 ? 2 * (sm_count / 2)
+                                              : (int)(2 * std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(),
+                                                                            sm_count / 2));
             else
                 cfg->grid = (int)std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(), sm_count);
             return;
@@ -339,6 +341,12 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         }
     }
     fill_config(cfg, pick->cluster, pick->bn, pick_tiles, pick_units);
+    // Few pair tiles over a deep K leave most pairs idle: share the K loop
+    // out (stream-K) when at most half the pairs would get a tile.
+    if (pick->cluster == 2 && 2 * pick_tiles <= pick_units && ceil_div(K, kBK) >= 64) {
+        cfg->split_k = 0;
+        cfg->grid = 2 * pick_units;
+    }
 }
 
 CUtensorMapDataType map_dtype(int dt)

@@ -49,8 +49,10 @@ struct PairWork {
     int64_t slot;      // workspace slot (partial segments)
 };
 
-// The items of pair `cid` of `P`: whole tiles cid, cid + P, ... below
-// dp_tiles, then the segments of its stream-K share of the tail.
+// The items of pair `cid` of `P`: first the segments of its stream-K share
+// of the tail tiles, then whole tiles cid, cid + P, ... below dp_tiles.
+// Doing the shared tiles first lets their partial-sum hand-off and final
+// additions run in the epilogue warps while the whole tiles' MMAs proceed.
 struct PairWorkIter {
     int next_dp, dp_tiles, P, kb;
     StreamK sk;
@@ -68,6 +70,19 @@ struct PairWorkIter {
 
     __device__ bool next(PairWork &w)
     {
+        if (it < end) {
+            const int64_t t = it / kb;
+            const int64_t tile_end = (t + 1) * kb;
+            const int64_t stop = end < tile_end ? end : tile_end;
+            w.tile = (int)(dp_tiles + t);
+            w.k0 = (int)(it - t * kb);
+            w.k1 = (int)(stop - t * kb);
+            w.partial = !(w.k0 == 0 && w.k1 == kb);
+            w.t_sk = t;
+            w.slot = sk.slot(unit, t);
+            it = stop;
+            return true;
+        }
         if (next_dp < dp_tiles) {
             w.tile = next_dp;
             w.k0 = 0;
@@ -76,18 +91,7 @@ struct PairWorkIter {
             next_dp += P;
             return true;
         }
-        if (it >= end) return false;
-        const int64_t t = it / kb;
-        const int64_t tile_end = (t + 1) * kb;
-        const int64_t stop = end < tile_end ? end : tile_end;
-        w.tile = (int)(dp_tiles + t);
-        w.k0 = (int)(it - t * kb);
-        w.k1 = (int)(stop - t * kb);
-        w.partial = !(w.k0 == 0 && w.k1 == kb);
-        w.t_sk = t;
-        w.slot = sk.slot(unit, t);
-        it = stop;
-        return true;
+        return false;
     }
 };
 
@@ -314,31 +318,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             if (*last_flag) {
                 // Every segment of this tile half is in: add them in k order.
                 __threadfence();
+                // Column-parallel over this warp's 32 rows: per store chunk (32
+                // FP32 or 64 16-bit columns) each lane owns 4 columns of a row,
+                // so every load of the warp reads whole row segments.  The sums
+                // go straight into the warp's swizzled staging block, which a
+                // TMA store then writes to C.
                 constexpr int kCols = OUT == OUT_F32 ? 32 : 64;
-                const int64_t my_row = 128 * (int64_t)rank + 32 * q + lane;   // row inside the pair tile
+                constexpr int kLanesPerRow = kCols / 4;
+                constexpr int kRowsPerPass = 32 / kLanesPerRow;
+                constexpr int kPasses = 32 / kRowsPerPass;
+                const int sub_row = lane / kLanesPerRow, col4 = lane % kLanesPerRow;
+                int64_t u_end = u0;
+                while (u_end < sk.sk_units && sk.bound(u_end) < stop) ++u_end;
+                const int64_t warp_row = 128 * (int64_t)rank + 32 * q;       // first row of this warp in the tile
 #pragma unroll 1
                 for (int c = 0; c < kPairBN / kCols; ++c) {
-                    float acc[kCols];
+                    float4 acc[kPasses];
 #pragma unroll
-                    for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
-                    for (int64_t u = u0; u < sk.sk_units && sk.bound(u) < stop; ++u) {
+                    for (int i = 0; i < kPasses; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int64_t u = u0; u < u_end; ++u) {                    // k order: unit u0, u0 + 1, ...
                         const float4 *src = reinterpret_cast<const float4 *>(
-                            p.partials + ((sk.slot(u, w.t_sk) * kPairBM + my_row) * kPairBN + c * kCols));
+                            p.partials + ((sk.slot(u, w.t_sk) * kPairBM + warp_row + sub_row) * kPairBN + c * kCols) +
+                            col4 * 4);
+                        float4 t[kPasses];
 #pragma unroll
-                        for (int j = 0; j < kCols / 4; ++j) {
-                            const float4 t = __ldcg(src + j);
-                            acc[4 * j] += t.x;
-                            acc[4 * j + 1] += t.y;
-                            acc[4 * j + 2] += t.z;
-                            acc[4 * j + 3] += t.w;
+                        for (int i = 0; i < kPasses; ++i) t[i] = __ldcg(src + (int64_t)i * kRowsPerPass * (kPairBN / 4));
+#pragma unroll
+                        for (int i = 0; i < kPasses; ++i) {
+                            acc[i].x += t[i].x;
+                            acc[i].y += t[i].y;
+                            acc[i].z += t[i].z;
+                            acc[i].w += t[i].w;
                         }
                     }
-                    uint32_t v0[32], v1[32];
+                    const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v0[j] = __float_as_uint(acc[j]);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v1[j] = kCols == 64 ? __float_as_uint(acc[(32 + j) % kCols]) : 0u;
-                    stage_store_chunk<OUT>(&p.tma_c, p.M, p.N, stage_base, cc, row0, col0 + c * kCols, lane, v0, v1);
+                    for (int i = 0; i < kPasses; ++i) {
+                        const uint32_t r = (uint32_t)(i * kRowsPerPass + sub_row);
+                        if constexpr (OUT == OUT_F32) {
+                            ptx::st_shared_v4(sbuf + r * 128 + (((uint32_t)col4 ^ (r & 7)) << 4), __float_as_uint(acc[i].x),
+                                              __float_as_uint(acc[i].y), __float_as_uint(acc[i].z),
+                                              __float_as_uint(acc[i].w));
+                        } else {
+                            const uint32_t a0 = pack_out(acc[i].x, acc[i].y, OUT);
+                            const uint32_t a1 = pack_out(acc[i].z, acc[i].w, OUT);
+                            const uint32_t off = r * 128 + ((((uint32_t)col4 >> 1) ^ (r & 7)) << 4) + (col4 & 1) * 8;
+                            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(sbuf + off), "r"(a0), "r"(a1) : "memory");
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int32_t x = col0 + c * kCols;
+                        if (x < p.N && row0 < p.M) ptx::tma_store_2d(&p.tma_c, sbuf, x, row0);
+                        ptx::bulk_commit_group();
+                    }
+                    ++cc;
                 }
                 if (ew == 0 && lane == 0) p.counters[2 * w.t_sk + rank] = 0u;   // ready for the next call
             }

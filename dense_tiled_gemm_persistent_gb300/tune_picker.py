@@ -58,6 +58,8 @@ def candidates(tg, M):
             out.append(("workspace%d" % s, C(bm=128, bn=npad, bk=64, stages=4, cluster_m=1, group_m=1,
                                              split_k=s, swap_ab=1, grid=0)))
     out.append(("pair256", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=1, swap_ab=0, grid=0)))
+    out.append(("pair256sk", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=0, swap_ab=0,
+                               grid=0)))
     out.append(("cta256", C(bm=128, bn=256, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
     out.append(("cta128", C(bm=128, bn=128, bk=64, stages=6, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
     return out
