@@ -11,6 +11,10 @@ from .oracle import (  # noqa: F401
     round_bits,
     ulp,
     decode,
+    epilogue,
+    ACT_NONE,
+    ACT_RELU,
+    ACT_GELU_TANH,
     F16,
     BF16,
     F32,

@@ -63,6 +63,9 @@ def _load():
             lib.oracle_round_bits_n.argtypes = [_p, _i64, ctypes.c_int, _p]
             lib.oracle_ulp_n.argtypes = [_p, _i64, ctypes.c_int, _p]
             lib.oracle_decode_n.argtypes = [_p, _i64, ctypes.c_int, _p]
+            lib.oracle_epilogue.argtypes = [_i64, _i64, _p, _i64, ctypes.c_double, ctypes.c_double, _p, _i64,
+                                            _p, ctypes.c_int]
+            lib.oracle_epilogue.restype = None
             _lib = lib
     return _lib
 
@@ -144,6 +147,24 @@ def ulp(x, dtype) -> np.ndarray:
     out = np.zeros(x.shape, dtype=np.float64)
     lib.oracle_ulp_n(x.ctypes.data, x.size, dtype, out.ctypes.data)
     return out
+
+
+ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
+
+
+def epilogue(C, alpha=1.0, beta=0.0, cin=None, bias=None, act=ACT_NONE) -> np.ndarray:
+    """act(alpha * C + beta * cin + bias[None, :]) in float64 (a new array).
+
+    C and cin are float64 (rows x cols); bias float64 (cols,) or None."""
+    lib = _load()
+    D = np.ascontiguousarray(C, dtype=np.float64).copy()
+    rows, cols = D.shape
+    cin_a = None if cin is None else np.ascontiguousarray(cin, dtype=np.float64)
+    bias_a = None if bias is None else np.ascontiguousarray(bias, dtype=np.float64)
+    lib.oracle_epilogue(rows, cols, D.ctypes.data, cols, float(alpha), float(beta),
+                        None if cin_a is None else cin_a.ctypes.data, cols,
+                        None if bias_a is None else bias_a.ctypes.data, act)
+    return D
 
 
 def decode(bits, dtype) -> np.ndarray:

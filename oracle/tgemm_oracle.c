@@ -326,6 +326,37 @@ uint32_t oracle_round_bits(double x, int dtype)
     return sign_bit | ((uint32_t)(er + bias) << fbits) | frac;
 }
 
+/* ---- fused epilogue ----------------------------------------------------
+ *
+ * D[i][j] = act(alpha * C[i][j] + beta * Cin[i][j] + bias[j]), with C the
+ * exact product from above, all in double.  act: 0 none, 1 ReLU max(x, 0),
+ * 2 GELU in its tanh form, 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ * The pages name epilogue fusion (the Croqtile tutorial's comparison with
+ * cuBLAS) without defining one; this is the usual affine-plus-activation
+ * form.  cin or bias may be NULL (treated as zero).  In place on D.
+ */
+static double act_apply(double x, int act)
+{
+    if (act == 1) return x > 0.0 ? x : 0.0;
+    if (act == 2) {
+        const double c = 0.7978845608028654;     /* sqrt(2 / pi) */
+        return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+    }
+    return x;
+}
+
+void oracle_epilogue(int64_t rows, int64_t cols, double *D, int64_t ldd, double alpha, double beta,
+                     const double *cin, int64_t ldcin, const double *bias, int act)
+{
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j) {
+            double x = alpha * D[i * ldd + j];
+            if (cin) x += beta * cin[i * ldcin + j];
+            if (bias) x += bias[j];
+            D[i * ldd + j] = act_apply(x, act);
+        }
+}
+
 /* Vector forms for the test harness. */
 void oracle_round_bits_n(const double *x, int64_t n, int dtype, uint32_t *out)
 {

@@ -30,6 +30,9 @@ MUTANTS = {
     "ties_away_from_zero": ("double r = nearbyint(a / q) * q;", "double r = round(a / q) * q;"),
     "ulp_factor_two": ("return ldexp(1.0, e - p + 1);", "return ldexp(1.0, e - p);"),
     "bound_signed": ("r += fabs(a) * fabs(b);\n        }\n    } else {", "r += a * fabs(b);\n        }\n    } else {"),
+    "gelu_constant": ("0.044715 * x * x * x", "0.047715 * x * x * x"),
+    "bias_row_index": ("x += bias[j];", "x += bias[i % cols];"),
+    "beta_dropped": ("if (cin) x += beta * cin[i * ldcin + j];", "if (cin) x += cin[i * ldcin + j];"),
 }
 
 

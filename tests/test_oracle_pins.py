@@ -308,3 +308,38 @@ def test_bad_arguments_rejected(orc):
         orc.gemm(a, a, 4, 4, 4, 3, 4, KN, F16)      # lda < K
     with pytest.raises(ValueError):
         orc.gemm(a, a, 4, 4, 4, 4, 4, KN, F32)      # FP32 is not an input format
+
+
+# --- fused epilogue ---------------------------------------------------------
+
+def test_epilogue_identity_scaling_and_bias(orc):
+    rng = np.random.default_rng(71)
+    C = rng.standard_normal((9, 13))
+    assert np.array_equal(orc.epilogue(C), C)                       # alpha 1, nothing else
+    assert np.array_equal(orc.epilogue(C, alpha=2.0), 2.0 * C)      # exact doubling
+    bias = rng.standard_normal(13)
+    assert np.array_equal(orc.epilogue(C, bias=bias), C + bias[None, :])
+    cin = rng.standard_normal((9, 13))
+    assert np.array_equal(orc.epilogue(C, alpha=0.0, beta=1.0, cin=cin), cin)
+    # beta * C_in with C_in = C gives (alpha + beta) C for exact small values
+    Ci = rng.integers(-50, 50, (9, 13)).astype(np.float64)
+    assert np.array_equal(orc.epilogue(Ci, alpha=3.0, beta=-2.0, cin=Ci), Ci)
+
+
+def test_epilogue_relu_is_max_with_zero(orc):
+    C = np.array([[-2.0, -0.0, 0.0, 1.5, -1e-300, 7.0]])
+    assert np.array_equal(orc.epilogue(C, act=orc.ACT_RELU), np.maximum(C, 0.0))
+
+
+def test_epilogue_gelu_tanh_odd_part_and_torch(orc):
+    x = np.linspace(-8, 8, 4001)
+    g = orc.epilogue(x[None, :], act=orc.ACT_GELU_TANH)[0]
+    gm = orc.epilogue(-x[None, :], act=orc.ACT_GELU_TANH)[0]
+    # tanh is odd, so gelu(x) - gelu(-x) = x exactly in the tanh form
+    assert np.allclose(g - gm, x, rtol=0, atol=1e-15)
+    assert g[2000] == 0.0                                           # gelu(0) = 0
+    # the library's tanh-approximated GELU (float64) agrees
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    assert np.allclose(g, ref, rtol=1e-14, atol=1e-14)
+    # far from zero it is the identity or zero
+    assert abs(g[-1] - 8.0) < 1e-12 and abs(g[0]) < 1e-12
