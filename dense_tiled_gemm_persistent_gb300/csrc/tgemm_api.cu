@@ -545,11 +545,64 @@ tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *str
     return TGEMM_OK;
 }
 
+// K = 0 with a fused epilogue: D = act(beta * C_in + bias), elementwise.
+template <int OUT>
+__global__ void epilogue_only_kernel(const __grid_constant__ GemmParams p)
+{
+    const int64_t total = (int64_t)p.M * p.N;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(e / p.N);
+        const int64_t n = e - (int64_t)m * p.N;
+        float cin = 0.f;
+        if (p.epi & 2) {
+            const int64_t ci = (int64_t)m * p.ldc_in + n;
+            if (OUT == OUT_F32) cin = static_cast<const float *>(p.cin_ptr)[ci];
+            else if (OUT == OUT_F16) cin = __half2float(static_cast<const __half *>(p.cin_ptr)[ci]);
+            else cin = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.cin_ptr)[ci]);
+        }
+        store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, epi_value(p, 0.f, cin, n));
+    }
+}
+
+// Epilogue arguments: host checks and the kernel parameter fields.
+tgemm_status epilogue_params(const tgemm_epilogue *ep, int64_t M, int64_t N, int out_dtype, GemmParams *p)
+{
+    p->alpha = 1.f;
+    p->beta = 0.f;
+    p->epi = 0;
+    if (!ep) return TGEMM_OK;
+    if (ep->act != TGEMM_ACT_NONE && ep->act != TGEMM_ACT_RELU && ep->act != TGEMM_ACT_GELU_TANH)
+        return TGEMM_ERR_INVALID_ARG;
+    if (ep->bias && ep->bias_dtype != TGEMM_F16 && ep->bias_dtype != TGEMM_BF16 && ep->bias_dtype != TGEMM_F32)
+        return TGEMM_ERR_INVALID_ARG;
+    p->alpha = ep->alpha;
+    p->beta = ep->beta;
+    p->bias = ep->bias;
+    p->bias_dtype = ep->bias_dtype;
+    p->act = ep->act;
+    const bool identity = ep->alpha == 1.f && ep->beta == 0.f && !ep->bias && ep->act == TGEMM_ACT_NONE;
+    p->epi = identity ? 0 : 1;
+    if (ep->beta != 0.f) {
+        const size_t eo = elem_size(out_dtype);
+        if (!ep->c_in || ep->ldc_in < N) return TGEMM_ERR_INVALID_ARG;
+        if (((uintptr_t)ep->c_in % 16) != 0 || ((uint64_t)ep->ldc_in * eo) % 16 != 0) return TGEMM_ERR_MISALIGNED;
+        p->epi |= 2;
+        p->cin_ptr = ep->c_in;
+        p->ldc_in = ep->ldc_in;
+        if (M > 0 && N > 0 &&
+            !encode_2d(&p->tma_cin, out_dtype, ep->c_in, (uint64_t)N, (uint64_t)M, (uint64_t)ep->ldc_in,
+                       (uint32_t)(128 / eo), 32))
+            return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
 // C^T = B^T A^T on a swap-AB split-K kernel (M <= 64): the workspace
 // reduction (swap_ab = 1) or the in-cluster one (swap_ab = 2).
 tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
                         int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype, void *stream_ptr,
-                        const tgemm_config &cfg, const KernelVariant *var, DeviceState *dev)
+                        const tgemm_config &cfg, const KernelVariant *var, DeviceState *dev,
+                        const tgemm_epilogue *ep)
 {
     const bool w_mn = b_layout == TGEMM_B_KN;
     const int npad = cfg.bn;
@@ -578,6 +631,8 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     p.c_ptr = C;
     p.ldc = ldc;
     p.splits = splits;
+    tgemm_status est = epilogue_params(ep, M, N, out_dtype, &p);
+    if (est != TGEMM_OK) return est;
     if (splits > 1 && cfg.swap_ab == 1) {
         int devno = 0;
         cudaGetDevice(&devno);
@@ -596,7 +651,8 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
 
 tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                       int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
-                      void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags)
+                      void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags,
+                      const tgemm_epilogue *ep = nullptr)
 {
     bool noop = false;
     tgemm_status st = validate(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, &noop);
@@ -614,6 +670,30 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     if (st != TGEMM_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const size_t eo = elem_size(out_dtype);
+    {
+        // epilogue arguments are checked before anything is launched
+        GemmParams probe;
+        std::memset(&probe, 0, sizeof probe);
+        tgemm_status est = epilogue_params(ep, 0, N, out_dtype, &probe);
+        if (est != TGEMM_OK) return est;
+        if (K == 0 && probe.epi) {
+            // The empty sum under the epilogue: D = act(beta * C_in + bias).
+            GemmParams q;
+            std::memset(&q, 0, sizeof q);
+            epilogue_params(ep, 0, N, out_dtype, &q);
+            q.M = (int32_t)M;
+            q.N = (int32_t)N;
+            q.c_ptr = C;
+            q.ldc = ldc;
+            const int64_t total = M * N;
+            const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * (int64_t)dev->sm_count);
+            if (out_dtype == TGEMM_F32) epilogue_only_kernel<OUT_F32><<<blocks, 256, 0, stream>>>(q);
+            else if (out_dtype == TGEMM_F16) epilogue_only_kernel<OUT_F16><<<blocks, 256, 0, stream>>>(q);
+            else epilogue_only_kernel<OUT_BF16><<<blocks, 256, 0, stream>>>(q);
+            if (cudaGetLastError() != cudaSuccess) return TGEMM_ERR_CUDA;
+            return TGEMM_OK;
+        }
+    }
     if (K == 0) {
         // The empty sum: C = 0 (all-zero bits are +0 in every output type).
         if (cudaMemset2DAsync(C, (size_t)ldc * eo, 0, (size_t)N * eo, (size_t)M, stream) != cudaSuccess) {
@@ -629,7 +709,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     }
     if (cfg.swap_ab)
         return run_skinny(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream_ptr, cfg, var,
-                          dev);
+                          dev, ep);
     const bool b_mn = b_layout == TGEMM_B_KN;
     const bool pair = cfg.cluster_m == 2;
     const TileGrid grid(M, N, cfg.bm, cfg.bn);
@@ -658,6 +738,8 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     p.debug_flags = debug_flags;
     p.status = dev->status;
     p.timeout_ns = wait_timeout_ns();
+    st = epilogue_params(ep, M, N, out_dtype, &p);
+    if (st != TGEMM_OK) return st;
 
     int g;
     p.dp_tiles = p.num_tiles;
@@ -707,6 +789,14 @@ TGEMM_EXPORT tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K, cons
 {
     if (!cfg) return TGEMM_ERR_INVALID_ARG;
     return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0);
+}
+
+TGEMM_EXPORT tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                                       int64_t ldb, tgemm_b_layout b_layout, void *C, int64_t ldc,
+                                       tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
+                                       const tgemm_epilogue *ep, const tgemm_config *cfg)
+{
+    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0, ep);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,

@@ -98,8 +98,8 @@ struct SmemPlan {
     static constexpr uint32_t b_off = a_off + STAGES * a_stage;
     static constexpr uint32_t c_off = b_off + STAGES * b_stage;
     static constexpr uint32_t bar_off = c_off + kEpiWarps * 2 * kStageCBytes;
-    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-    static constexpr uint32_t n_bars = 2 * STAGES + 5;
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain, C_in loads[4 epilogue warps]
+    static constexpr uint32_t n_bars = 2 * STAGES + 5 + kEpiWarps;
     static constexpr uint32_t slot_off = bar_off + 8 * n_bars;   // TMEM address
     static constexpr uint32_t abort_off = slot_off + 4;
     static constexpr uint32_t flag_off = abort_off + 4;          // epilogue broadcast word
@@ -126,6 +126,76 @@ __device__ __forceinline__ uint32_t pack_out(float lo, float hi, int out)
     return u;
 }
 
+// ---- fused epilogue ----------------------------------------------------------
+//
+// D = act(alpha * acc + beta * C_in + bias[col]) in FP32 before the cast: the
+// epilogue fusion the Croqtile tutorial credits cuBLAS with (its comparison
+// with cuBLAS), in the usual affine-plus-activation form.  GELU uses its tanh
+// form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float load_bias(const void *b, int dt, int64_t j)
+{
+    if (dt == OUT_F32) return __ldg(static_cast<const float *>(b) + j);
+    if (dt == OUT_F16) return __half2float(__ldg(static_cast<const __half *>(b) + j));
+    return __bfloat162float(__ldg(static_cast<const __nv_bfloat16 *>(b) + j));
+}
+
+__device__ __forceinline__ float act_apply(float x, int act)
+{
+    if (act == 1) return fmaxf(x, 0.f);
+    if (act == 2) return 0.5f * x * (1.f + tanhf(0.7978845608f * (x + 0.044715f * x * x * x)));
+    return x;
+}
+
+__device__ __forceinline__ float epi_value(const GemmParams &p, float acc, float cin, int64_t col)
+{
+    float r = p.alpha * acc;
+    if (p.epi & 2) r = fmaf(p.beta, cin, r);
+    if (p.bias && col < p.N) r += load_bias(p.bias, p.bias_dtype, col);
+    return act_apply(r, p.act);
+}
+
+// Unpack two 16-bit output-type values (low, high) to floats.
+__device__ __forceinline__ float2 unpack_out(uint32_t u, int out)
+{
+    if (out == OUT_F16) {
+        __half2 h;
+        memcpy(&h, &u, 4);
+        return __half22float2(h);
+    }
+    __nv_bfloat162 h;
+    memcpy(&h, &u, 4);
+    return __bfloat1622float2(h);
+}
+
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Per-warp state for reading C_in through the staging block.
+struct EpiCtx {
+    const GemmParams *p;    // null: write the raw FP32 values (stream-K partials)
+    uint32_t cin_bar;       // this warp's mbarrier for C_in loads
+    uint32_t cin_phase;     // loads issued so far (parity)
+    WaitCtx wc;
+};
+
+// Fetch the C_in block (x, row0) of this warp into the staging block `sbuf`
+// and wait for it.  Returns false if the wait timed out.
+__device__ __forceinline__ bool fetch_cin(EpiCtx &e, uint32_t sbuf, int32_t x, int32_t row0, int lane)
+{
+    if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(e.cin_bar, kStageCBytes);
+        ptx::tma_load_2d(sbuf, &e.p->tma_cin, e.cin_bar, x, row0);
+    }
+    const bool ok = wait_bounded(e.cin_bar, e.cin_phase & 1u, e.wc, SITE_EPI_CIN);
+    ++e.cin_phase;
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Cast one 128-byte-wide column chunk of this warp's 32 rows (v0, plus v1
 // for 16-bit output: 64 columns), stage it in one of the warp's two swizzled
 // staging blocks and store it with TMA at (x, row0) of `map`; rows >= rows_lim
@@ -134,30 +204,55 @@ __device__ __forceinline__ uint32_t pack_out(float lo, float hi, int out)
 template <int OUT>
 __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_t rows_lim, int32_t cols_lim,
                                                   uint32_t stage_base, uint32_t &cc, int32_t row0, int32_t x,
-                                                  int lane, const uint32_t (&v0)[32], const uint32_t (&v1)[32])
+                                                  int lane, uint32_t (&v0)[32], uint32_t (&v1)[32], EpiCtx &e)
 {
     const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
     if (lane == 0) ptx::bulk_wait_group_read<1>();   // the store that last used sbuf is done reading
     __syncwarp();
     const uint32_t row_addr = sbuf + lane * 128;
+    const bool fused = e.p != nullptr && (e.p->epi & 1);
+    const bool with_cin = fused && (e.p->epi & 2) && fetch_cin(e, sbuf, x, row0, lane);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+        const uint32_t addr = row_addr + ((uint32_t)(j ^ (lane & 7)) << 4);   // 128-byte swizzle
         uint32_t w0, w1, w2, w3;
         if constexpr (OUT == OUT_F32) {
+            if (fused) {
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                if (with_cin) {
+                    const uint4 q = ld_shared_u4(addr);
+                    c[0] = __uint_as_float(q.x), c[1] = __uint_as_float(q.y);
+                    c[2] = __uint_as_float(q.z), c[3] = __uint_as_float(q.w);
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    v0[4 * j + t] = __float_as_uint(epi_value(*e.p, __uint_as_float(v0[4 * j + t]), c[t], x + 4 * j + t));
+            }
             w0 = v0[4 * j + 0];
             w1 = v0[4 * j + 1];
             w2 = v0[4 * j + 2];
             w3 = v0[4 * j + 3];
         } else {
             // columns 8j .. 8j+7 of the 64-column chunk
-            const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+            uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+            if (fused) {
+                float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (with_cin) {
+                    const uint4 q = ld_shared_u4(addr);
+                    const float2 c0 = unpack_out(q.x, OUT), c1 = unpack_out(q.y, OUT);
+                    const float2 c2 = unpack_out(q.z, OUT), c3 = unpack_out(q.w, OUT);
+                    c[0] = c0.x, c[1] = c0.y, c[2] = c1.x, c[3] = c1.y, c[4] = c2.x, c[5] = c2.y, c[6] = c3.x, c[7] = c3.y;
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    src[t] = __float_as_uint(epi_value(*e.p, __uint_as_float(src[t]), c[t], x + 8 * j + t));
+            }
             w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
             w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);
             w2 = pack_out(__uint_as_float(src[4]), __uint_as_float(src[5]), OUT);
             w3 = pack_out(__uint_as_float(src[6]), __uint_as_float(src[7]), OUT);
         }
-        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
-        ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+        ptx::st_shared_v4(addr, w0, w1, w2, w3);
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
@@ -177,7 +272,7 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
 template <int BN, int OUT, typename Release>
 __device__ __forceinline__ void epilogue_drain(const CUtensorMap *map, int32_t rows_lim, int32_t cols_lim,
                                                uint32_t t_acc, uint32_t stage_base, uint32_t &cc, int32_t row0,
-                                               int32_t col0, int lane, Release release)
+                                               int32_t col0, int lane, Release release, EpiCtx &e)
 {
     constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
     constexpr int kChunkCols = 128 / kOutBytes;          // columns of one 128-byte staged row
@@ -194,7 +289,7 @@ __device__ __forceinline__ void epilogue_drain(const CUtensorMap *map, int32_t r
             __syncwarp();
             if (lane == 0) release();
         }
-        stage_store_chunk<OUT>(map, rows_lim, cols_lim, stage_base, cc, row0, col0 + c * kChunkCols, lane, v0, v1);
+        stage_store_chunk<OUT>(map, rows_lim, cols_lim, stage_base, cc, row0, col0 + c * kChunkCols, lane, v0, v1, e);
     }
 }
 
@@ -238,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             ptx::mbar_init(tempty_bar(b), kEpiWarps);
         }
         ptx::mbar_init(drain_bar, 1);
+        for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(drain_bar + 8u * (1 + w), 1);   // C_in loads
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -362,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
         const int q = warp & 3;                          // TMEM lane quarter = tile rows 32q..32q+31
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
+        EpiCtx ectx{&p, drain_bar + 8u * (1 + ew), 0u, wc};
         uint32_t local = 0, cc = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             const uint32_t buf = local & 1u;
@@ -377,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             const uint32_t t_acc = tmem_base + lane_base + buf * BN;
             const uint32_t release_bar = tempty_bar(buf);
             epilogue_drain<BN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
-                                    [&] { ptx::mbar_arrive(release_bar); });
+                                    [&] { ptx::mbar_arrive(release_bar); }, ectx);
         }
         if (lane == 0) ptx::bulk_wait_group_all();
         __syncwarp();

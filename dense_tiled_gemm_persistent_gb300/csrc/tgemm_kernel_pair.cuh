@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);
         }
         ptx::mbar_init(drain_bar, 1);
+        for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(drain_bar + 8u * (1 + w), 1);   // C_in loads
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -268,6 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
         volatile int *last_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::flag_off);
+        EpiCtx ectx{&p, drain_bar + 8u * (1 + ew), 0u, wc};
+        EpiCtx raw{nullptr, 0u, 0u, wc};                 // stream-K partials: raw FP32
         uint32_t local = 0, cc = 0;
         PairWorkIter items(p, cluster_id, num_clusters);
         PairWork w;
@@ -291,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             const uint32_t release_bar = ptx::map_to_cta(tempty_bar(buf), 0);
             if (!w.partial) {
                 epilogue_drain<kPairBN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
-                                             [&] { ptx::mbar_arrive_cluster(release_bar); });
+                                             [&] { ptx::mbar_arrive_cluster(release_bar); }, ectx);
                 continue;
             }
             // ---- stream-K segment: FP32 partial tile into the workspace
             const int32_t prow = (int32_t)(w.slot * kPairBM) + 128 * (int32_t)rank + 32 * q;
             epilogue_drain<kPairBN, OUT_F32>(&p.tma_ws, INT32_MAX, kPairBN, t_acc, stage_base, cc, prow, 0, lane,
-                                             [&] { ptx::mbar_arrive_cluster(release_bar); });
+                                             [&] { ptx::mbar_arrive_cluster(release_bar); }, raw);
             if (lane == 0) {
                 ptx::bulk_wait_group_all();          // this warp's partial rows are written
                 ptx::fence_proxy_async_global();
@@ -354,18 +357,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
                     if (lane == 0) ptx::bulk_wait_group_read<1>();
                     __syncwarp();
+                    const bool fused = (p.epi & 1) != 0;
+                    const bool with_cin = fused && (p.epi & 2) && fetch_cin(ectx, sbuf, col0 + c * kCols, row0, lane);
+                    const int64_t col = (int64_t)col0 + c * kCols + col4 * 4;
 #pragma unroll
                     for (int i = 0; i < kPasses; ++i) {
                         const uint32_t r = (uint32_t)(i * kRowsPerPass + sub_row);
                         if constexpr (OUT == OUT_F32) {
-                            ptx::st_shared_v4(sbuf + r * 128 + (((uint32_t)col4 ^ (r & 7)) << 4), __float_as_uint(acc[i].x),
-                                              __float_as_uint(acc[i].y), __float_as_uint(acc[i].z),
-                                              __float_as_uint(acc[i].w));
+                            const uint32_t addr = sbuf + r * 128 + (((uint32_t)col4 ^ (r & 7)) << 4);
+                            if (fused) {
+                                float4 ci = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (with_cin) ci = ptx::ld_shared_v4(addr);
+                                acc[i].x = epi_value(p, acc[i].x, ci.x, col);
+                                acc[i].y = epi_value(p, acc[i].y, ci.y, col + 1);
+                                acc[i].z = epi_value(p, acc[i].z, ci.z, col + 2);
+                                acc[i].w = epi_value(p, acc[i].w, ci.w, col + 3);
+                            }
+                            ptx::st_shared_v4(addr, __float_as_uint(acc[i].x), __float_as_uint(acc[i].y),
+                                              __float_as_uint(acc[i].z), __float_as_uint(acc[i].w));
                         } else {
+                            const uint32_t addr = sbuf + r * 128 + ((((uint32_t)col4 >> 1) ^ (r & 7)) << 4) + (col4 & 1) * 8;
+                            if (fused) {
+                                float2 c0 = make_float2(0.f, 0.f), c1 = make_float2(0.f, 0.f);
+                                if (with_cin) {
+                                    uint32_t q0, q1;
+                                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(q0), "=r"(q1) : "r"(addr) : "memory");
+                                    c0 = unpack_out(q0, OUT);
+                                    c1 = unpack_out(q1, OUT);
+                                }
+                                acc[i].x = epi_value(p, acc[i].x, c0.x, col);
+                                acc[i].y = epi_value(p, acc[i].y, c0.y, col + 1);
+                                acc[i].z = epi_value(p, acc[i].z, c1.x, col + 2);
+                                acc[i].w = epi_value(p, acc[i].w, c1.y, col + 3);
+                            }
                             const uint32_t a0 = pack_out(acc[i].x, acc[i].y, OUT);
                             const uint32_t a1 = pack_out(acc[i].z, acc[i].w, OUT);
-                            const uint32_t off = r * 128 + ((((uint32_t)col4 >> 1) ^ (r & 7)) << 4) + (col4 & 1) * 8;
-                            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(sbuf + off), "r"(a0), "r"(a1) : "memory");
+                            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a0), "r"(a1) : "memory");
                         }
                     }
                     ptx::fence_proxy_async_smem();

@@ -56,6 +56,24 @@ __device__ __forceinline__ void store_out(void *c, int64_t idx, float v)
     }
 }
 
+// C[m][n] = v with the fused epilogue (when enabled): C_in read with a
+// plain load, bias by output column n.
+template <int OUT>
+__device__ __forceinline__ void store_out_epi(const GemmParams &p, int m, int64_t n, float v)
+{
+    if (p.epi & 1) {
+        float cin = 0.f;
+        if (p.epi & 2) {
+            const int64_t ci = (int64_t)m * p.ldc_in + n;
+            if constexpr (OUT == OUT_F32) cin = static_cast<const float *>(p.cin_ptr)[ci];
+            else if constexpr (OUT == OUT_F16) cin = __half2float(static_cast<const __half *>(p.cin_ptr)[ci]);
+            else cin = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.cin_ptr)[ci]);
+        }
+        v = epi_value(p, v, cin, n);
+    }
+    store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v);
+}
+
 template <int NPAD, int OUT, bool W_MN>
 __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_constant__ GemmParams p)
 {
@@ -209,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
                 if (n < p.N)
 #pragma unroll
                     for (int m = 0; m < NPAD; ++m)
-                        if (m < M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v[m]);
+                        if (m < M) store_out_epi<OUT>(p, m, n, v[m]);
             } else {
                 // Partial of this split, [split][nt][row][NPAD]: each thread
                 // owns one weight row and writes its NPAD sums contiguously.
@@ -264,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
                     if (n < p.N)
 #pragma unroll
                         for (int m = 0; m < NPAD; ++m)
-                            if (m < M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, acc[m]);
+                            if (m < M) store_out_epi<OUT>(p, m, n, acc[m]);
                     if (warp == 2 && lane == 0) p.counters[nt] = 0u;   // every split of this tile has arrived
                 }
             }

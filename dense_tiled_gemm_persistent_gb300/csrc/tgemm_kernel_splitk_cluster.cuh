@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_splitk_cluster_kernel(const 
         if (n < p.N)
 #pragma unroll
             for (int m = 0; m < NPAD; ++m)
-                if (m < p.M) store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v[m]);
+                if (m < p.M) store_out_epi<OUT>(p, m, n, v[m]);
     }
 
     ptx::tc_fence_before_sync();

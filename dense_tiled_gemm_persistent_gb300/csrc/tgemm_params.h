@@ -23,6 +23,7 @@ enum WaitSite : uint32_t {
     SITE_DRAIN_MMA = 6,
     SITE_DEBUG = 7,
     SITE_SPLITK_COUNTER = 8,
+    SITE_EPI_CIN = 9,
 };
 
 constexpr uint32_t kFaultTimeout = 7u;
@@ -34,6 +35,7 @@ struct alignas(128) GemmParams {
     CUtensorMap tma_b;      // B: NK dims {K, N} box {64, bn}; KN dims {N, K} box {64, 64}
     CUtensorMap tma_c;      // C: dims {N, M}, box {128 bytes of columns, 32}, 128-byte swizzle
     CUtensorMap tma_ws;     // stream-K partial tiles (FP32): dims {256, slots * 256}, box {32, 32}
+    CUtensorMap tma_cin;    // fused epilogue C_in (output type): same geometry as tma_c
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_tiles, num_kb;
     int32_t group_m;
@@ -51,6 +53,15 @@ struct alignas(128) GemmParams {
     int32_t dp_tiles;       // tiles [0, dp_tiles) are processed whole
     int32_t sk_tiles;       // tiles [dp_tiles, dp_tiles + sk_tiles) are spread over
     int32_t sk_units;       // the first sk_units pairs, evenly by k-block
+    // fused epilogue D = act(alpha * acc + beta * C_in + bias[column]) before
+    // the cast; epi = 0 keeps the plain cast
+    float alpha, beta;
+    const void *bias;       // N entries or null
+    int32_t bias_dtype;     // 0 F16, 1 BF16, 2 F32
+    int32_t act;            // 0 none, 1 ReLU, 2 GELU (tanh form)
+    int32_t epi;            // bit 0: fused epilogue on; bit 1: read C_in (beta != 0)
+    const void *cin_ptr;    // C_in for the kernels that store with plain stores
+    int64_t ldc_in;
 };
 
 using LaunchFn = cudaError_t (*)(const GemmParams &, int grid, cudaStream_t);

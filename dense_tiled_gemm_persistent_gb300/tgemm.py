@@ -22,7 +22,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 # Every symbol include/tgemm.h declares.
 EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
-           "tgemm_debug_wait_timeout", "tgemm_run_noalloc")
+           "tgemm_debug_wait_timeout", "tgemm_run_noalloc", "tgemm_run_ex")
+
+ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 
 
 class TgemmError(RuntimeError):
@@ -37,6 +39,13 @@ class Config(ctypes.Structure):
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class Epilogue(ctypes.Structure):
+    """D = act(alpha * (A*B) + beta * C_in + bias), FP32 before the cast."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("c_in", ctypes.c_void_p),
+                ("ldc_in", ctypes.c_int64), ("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int),
+                ("act", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -72,6 +81,8 @@ def load(path: str = LIB_PATH):
         lib.tgemm_tile_coord.argtypes = [_i64, _i64, _i, _i, _i, _i64, ctypes.POINTER(_i64),
                                          ctypes.POINTER(_i64)]
         lib.tgemm_tile_coord.restype = _i
+        lib.tgemm_run_ex.argtypes = run_args + [ctypes.POINTER(Epilogue), ctypes.POINTER(Config)]
+        lib.tgemm_run_ex.restype = _i
         lib.tgemm_run_noalloc.argtypes = run_args
         lib.tgemm_run_noalloc.restype = _i
         lib.tgemm_debug_wait_timeout.argtypes = [ctypes.c_uint32, _p]
@@ -84,6 +95,13 @@ def load(path: str = LIB_PATH):
 
 def tgemm_run(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None) -> int:
     return load().tgemm_run(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream)
+
+
+def tgemm_run_ex(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None, ep=None,
+                 cfg=None) -> int:
+    """tgemm_run with a fused epilogue (Epilogue or None) and an optional Config."""
+    return load().tgemm_run_ex(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream,
+                               None if ep is None else ctypes.byref(ep), None if cfg is None else ctypes.byref(cfg))
 
 
 def tgemm_run_noalloc(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None) -> int:

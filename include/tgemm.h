@@ -82,6 +82,41 @@ tgemm_status tgemm_run(int64_t M, int64_t N, int64_t K,
                        void *C, int64_t ldc,
                        tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream);
 
+/*
+ * Fused epilogue: D = act(alpha * (A * B) + beta * C_in + bias), evaluated
+ * in FP32 on the accumulator and cast once to out_dtype.  The Croqtile
+ * tutorial counts epilogue fusion among cuBLAS's advantages (its comparison
+ * with cuBLAS); this is the usual affine-plus-activation form.
+ *   alpha    scale of the product (1 = none)
+ *   beta     scale of C_in; 0 = C_in is not read
+ *   c_in     M x N matrix of type out_dtype, row pitch ldc_in (elements); may be
+ *            C itself (in-place accumulate); 16-byte aligned like C
+ *   bias     N values of type bias_dtype added to every row, or NULL
+ *   act      TGEMM_ACT_NONE, TGEMM_ACT_RELU (max(x, 0)) or TGEMM_ACT_GELU_TANH
+ *            (0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))))
+ */
+typedef enum { TGEMM_ACT_NONE = 0, TGEMM_ACT_RELU = 1, TGEMM_ACT_GELU_TANH = 2 } tgemm_activation;
+
+typedef struct {
+    float alpha;
+    float beta;
+    const void *c_in;
+    int64_t ldc_in;
+    const void *bias;
+    tgemm_dtype bias_dtype;
+    tgemm_activation act;
+} tgemm_epilogue;
+
+/* tgemm_run with a fused epilogue (ep may be NULL: plain C = A * B) and an
+ * optional explicit configuration (cfg NULL: the library's choice).  With
+ * K = 0 the product is the empty sum and D = act(beta * C_in + bias). */
+tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K,
+                          const void *A, int64_t lda,
+                          const void *B, int64_t ldb, tgemm_b_layout b_layout,
+                          void *C, int64_t ldc,
+                          tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
+                          const tgemm_epilogue *ep, const tgemm_config *cfg);
+
 /* The configuration tgemm_run would use for this problem (no device work,
  * but it reads the current device's SM count and compute capability). */
 tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
