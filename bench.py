@@ -241,6 +241,8 @@ def main():
     ap.add_argument("--config", default="auto", choices=["auto", "pair", "pairsk", "1cta256", "1cta128", "workspace"],
                     help="tile shape: the library's pick, or a forced one (tuning)")
     ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
+    ap.add_argument("--epilogue", default="none", choices=["none", "bias_gelu", "residual"],
+                    help="fused epilogue (timing of a widened row; the headline line uses none)")
     ap.add_argument("--split-k", type=int, default=0, help="split count override for the swap-AB path (tuning)")
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
                     help="replay the timed launches from a CUDA graph (auto: problems under 1e11 FLOP)")
@@ -302,10 +304,25 @@ def main():
                               group_m=args.group_m or picked.group_m, split_k=sk, swap_ab=0, grid=0)
         picked = forced
 
+    ep = None
+    if args.epilogue != "none":
+        g_ep = torch.Generator().manual_seed(11)
+        bias_t = torch.randn(wl.N, generator=g_ep).to(gen.TORCH_DTYPE[wl.out_dtype]).to(dev)
+        cin_t = torch.randn(wl.M, wl.N, generator=g_ep).to(gen.TORCH_DTYPE[wl.out_dtype]).to(dev)
+        if args.epilogue == "bias_gelu":
+            ep = tgemm.Epilogue(alpha=1.0, beta=0.0, c_in=None, ldc_in=wl.N, bias=bias_t.data_ptr(),
+                                bias_dtype=wl.out_dtype, act=tgemm.ACT_GELU_TANH)
+        else:   # residual: D = A*B + C_in
+            ep = tgemm.Epilogue(alpha=1.0, beta=1.0, c_in=cin_t.data_ptr(), ldc_in=wl.N, bias=None,
+                                bias_dtype=wl.out_dtype, act=tgemm.ACT_NONE)
+
     def step(c_ptr=None, a_ptr=None, b_ptr=None, stream_handle=None):
         args_ = (wl.M, wl.N, wl.K, a_ptr or A.data_ptr(), lda, b_ptr or B.data_ptr(), ldb,
                  wl.b_layout, c_ptr or C.data_ptr(), ldc, wl.in_dtype, wl.out_dtype, stream_handle or sh)
-        rc = tgemm.tgemm_run(*args_) if forced is None else tgemm.tgemm_run_config(*args_, forced)
+        if ep is not None:
+            rc = tgemm.tgemm_run_ex(*args_, ep, forced)
+        else:
+            rc = tgemm.tgemm_run(*args_) if forced is None else tgemm.tgemm_run_config(*args_, forced)
         if rc != 0:
             raise RuntimeError("tgemm_run: " + tgemm.status_string(rc))
 
@@ -449,7 +466,8 @@ def main():
             "vs_baseline": value / PUBLISHED_TFLOPS if wl.name == WORKLOAD else None,
             "dtype": gen.DTYPE_NAME[wl.in_dtype], "data": "synthetic",
             "config": dict(config_dict(wl, world), kernel=picked.as_dict(),
-                           launch="cuda_graph" if graph is not None else "stream"), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                           launch="cuda_graph" if graph is not None else "stream", epilogue=args.epilogue),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": args.steps,
             "kernel_ms": {"mean": avg_launch},
         }

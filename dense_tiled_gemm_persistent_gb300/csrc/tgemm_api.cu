@@ -575,6 +575,7 @@ tgemm_status epilogue_params(const tgemm_epilogue *ep, int64_t M, int64_t N, int
         return TGEMM_ERR_INVALID_ARG;
     if (ep->bias && ep->bias_dtype != TGEMM_F16 && ep->bias_dtype != TGEMM_BF16 && ep->bias_dtype != TGEMM_F32)
         return TGEMM_ERR_INVALID_ARG;
+    if (ep->bias && ((uintptr_t)ep->bias % 16) != 0) return TGEMM_ERR_MISALIGNED;   // read in 16-byte runs
     p->alpha = ep->alpha;
     p->beta = ep->beta;
     p->bias = ep->bias;

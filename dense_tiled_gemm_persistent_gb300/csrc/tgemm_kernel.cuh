@@ -132,28 +132,6 @@ __device__ __forceinline__ uint32_t pack_out(float lo, float hi, int out)
 // epilogue fusion the Croqtile tutorial credits cuBLAS with (its comparison
 // with cuBLAS), in the usual affine-plus-activation form.  GELU uses its tanh
 // form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
-__device__ __forceinline__ float load_bias(const void *b, int dt, int64_t j)
-{
-    if (dt == OUT_F32) return __ldg(static_cast<const float *>(b) + j);
-    if (dt == OUT_F16) return __half2float(__ldg(static_cast<const __half *>(b) + j));
-    return __bfloat162float(__ldg(static_cast<const __nv_bfloat16 *>(b) + j));
-}
-
-__device__ __forceinline__ float act_apply(float x, int act)
-{
-    if (act == 1) return fmaxf(x, 0.f);
-    if (act == 2) return 0.5f * x * (1.f + tanhf(0.7978845608f * (x + 0.044715f * x * x * x)));
-    return x;
-}
-
-__device__ __forceinline__ float epi_value(const GemmParams &p, float acc, float cin, int64_t col)
-{
-    float r = p.alpha * acc;
-    if (p.epi & 2) r = fmaf(p.beta, cin, r);
-    if (p.bias && col < p.N) r += load_bias(p.bias, p.bias_dtype, col);
-    return act_apply(r, p.act);
-}
-
 // Unpack two 16-bit output-type values (low, high) to floats.
 __device__ __forceinline__ float2 unpack_out(uint32_t u, int out)
 {
@@ -165,6 +143,73 @@ __device__ __forceinline__ float2 unpack_out(uint32_t u, int out)
     __nv_bfloat162 h;
     memcpy(&h, &u, 4);
     return __bfloat1622float2(h);
+}
+
+__device__ __forceinline__ float load_bias(const void *b, int dt, int64_t j)
+{
+    if (dt == OUT_F32) return __ldg(static_cast<const float *>(b) + j);
+    if (dt == OUT_F16) return __half2float(__ldg(static_cast<const __half *>(b) + j));
+    return __bfloat162float(__ldg(static_cast<const __nv_bfloat16 *>(b) + j));
+}
+
+// GELU's tanh form rewritten with 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)):
+// x / (1 + exp(-2u)), u = sqrt(2/pi) (x + 0.044715 x^3).  exp overflows to
+// +inf for very negative x, which gives the limit 0.
+__device__ __forceinline__ float act_apply(float x, int act)
+{
+    if (act == 1) return fmaxf(x, 0.f);
+    if (act == 2) {
+        const float u = 0.7978845608f * fmaf(0.044715f * x * x, x, x);
+        return __fdividef(x, 1.f + __expf(-2.f * u));
+    }
+    return x;
+}
+
+__device__ __forceinline__ float epi_combine(const GemmParams &p, float acc, float cin, float bias)
+{
+    float r = p.alpha * acc;
+    if (p.epi & 2) r = fmaf(p.beta, cin, r);
+    return act_apply(r + bias, p.act);
+}
+
+__device__ __forceinline__ float epi_value(const GemmParams &p, float acc, float cin, int64_t col)
+{
+    const float b = (p.bias && col < p.N) ? load_bias(p.bias, p.bias_dtype, col) : 0.f;
+    return epi_combine(p, acc, cin, b);
+}
+
+// Bias values of columns [col, col + n) (n = 4 or 8), zero past N or without
+// a bias; one or two 16-byte loads when the run lies inside the vector.
+template <int n>
+__device__ __forceinline__ void load_bias_run(const GemmParams &p, int64_t col, float (&out)[n])
+{
+    if (!p.bias) {
+#pragma unroll
+        for (int t = 0; t < n; ++t) out[t] = 0.f;
+        return;
+    }
+    if (col + n <= p.N) {
+        if (p.bias_dtype == OUT_F32) {
+            const float4 *b = reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias) + col);
+#pragma unroll
+            for (int h = 0; h < n / 4; ++h) {
+                const float4 v = __ldg(b + h);
+                out[4 * h] = v.x, out[4 * h + 1] = v.y, out[4 * h + 2] = v.z, out[4 * h + 3] = v.w;
+            }
+        } else if constexpr (n == 8) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias) + col));
+            const float2 a = unpack_out(v.x, p.bias_dtype), b = unpack_out(v.y, p.bias_dtype);
+            const float2 c = unpack_out(v.z, p.bias_dtype), d = unpack_out(v.w, p.bias_dtype);
+            out[0] = a.x, out[1] = a.y, out[2] = b.x, out[3] = b.y, out[4] = c.x, out[5] = c.y, out[6] = d.x, out[7] = d.y;
+        } else {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.bias) + col));
+            const float2 a = unpack_out(v.x, p.bias_dtype), b = unpack_out(v.y, p.bias_dtype);
+            out[0] = a.x, out[1] = a.y, out[2] = b.x, out[3] = b.y;
+        }
+        return;
+    }
+#pragma unroll
+    for (int t = 0; t < n; ++t) out[t] = col + t < p.N ? load_bias(p.bias, p.bias_dtype, col + t) : 0.f;
 }
 
 __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr)
@@ -224,9 +269,11 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
                     c[0] = __uint_as_float(q.x), c[1] = __uint_as_float(q.y);
                     c[2] = __uint_as_float(q.z), c[3] = __uint_as_float(q.w);
                 }
+                float bv[4];
+                load_bias_run<4>(*e.p, (int64_t)x + 4 * j, bv);
 #pragma unroll
                 for (int t = 0; t < 4; ++t)
-                    v0[4 * j + t] = __float_as_uint(epi_value(*e.p, __uint_as_float(v0[4 * j + t]), c[t], x + 4 * j + t));
+                    v0[4 * j + t] = __float_as_uint(epi_combine(*e.p, __uint_as_float(v0[4 * j + t]), c[t], bv[t]));
             }
             w0 = v0[4 * j + 0];
             w1 = v0[4 * j + 1];
@@ -243,9 +290,11 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
                     const float2 c2 = unpack_out(q.z, OUT), c3 = unpack_out(q.w, OUT);
                     c[0] = c0.x, c[1] = c0.y, c[2] = c1.x, c[3] = c1.y, c[4] = c2.x, c[5] = c2.y, c[6] = c3.x, c[7] = c3.y;
                 }
+                float bv[8];
+                load_bias_run<8>(*e.p, (int64_t)x + 8 * j, bv);
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
-                    src[t] = __float_as_uint(epi_value(*e.p, __uint_as_float(src[t]), c[t], x + 8 * j + t));
+                    src[t] = __float_as_uint(epi_combine(*e.p, __uint_as_float(src[t]), c[t], bv[t]));
             }
             w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
             w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);

@@ -91,7 +91,8 @@ tgemm_status tgemm_run(int64_t M, int64_t N, int64_t K,
  *   beta     scale of C_in; 0 = C_in is not read
  *   c_in     M x N matrix of type out_dtype, row pitch ldc_in (elements); may be
  *            C itself (in-place accumulate); 16-byte aligned like C
- *   bias     N values of type bias_dtype added to every row, or NULL
+ *   bias     N values of type bias_dtype added to every row, or NULL; 16-byte
+ *            aligned
  *   act      TGEMM_ACT_NONE, TGEMM_ACT_RELU (max(x, 0)) or TGEMM_ACT_GELU_TANH
  *            (0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))))
  */
