@@ -361,32 +361,37 @@ CUtensorMapDataType map_dtype(int dt)
 // 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
 // `ld` elements between rows; boxes of box_inner x box_outer, 128-byte swizzle,
 // zero fill outside the tensor.
-bool encode_2d_uncached(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-                        uint32_t box_inner, uint32_t box_outer)
+// Row-major tensor of `outer` rows of `inner` elements, `ld` elements apart;
+// rank 3 adds `batch` copies `bstride` elements apart (the outermost
+// coordinate).  Boxes of box_inner x box_outer (x 1), 128-byte swizzle, zero
+// fill outside the tensor.
+bool encode_map_uncached(CUtensorMap *map, int dt, const void *ptr, int rank, uint64_t inner, uint64_t outer,
+                         uint64_t ld, uint64_t batch, uint64_t bstride, uint32_t box_inner, uint32_t box_outer)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {ld * elem_size(dt)};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, map_dtype(dt), 2, const_cast<void *>(ptr), dims, strides, box, estr,
+    const size_t e = elem_size(dt);
+    const cuuint64_t dims[3] = {inner, outer, batch};
+    const cuuint64_t strides[2] = {ld * e, bstride * e};
+    const cuuint32_t box[3] = {box_inner, box_outer, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, map_dtype(dt), (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // A small direct-mapped cache of encoded tensor maps: a descriptor depends
-// only on (address, type, extents, row pitch, box), so repeated calls on the
-// same buffers skip the driver's encoder.
+// only on (address, type, rank, extents, pitches, box), so repeated calls on
+// the same buffers skip the driver's encoder.
 struct MapKey {
     const void *ptr;
-    int dt;
-    uint64_t inner, outer, ld;
+    int dt, rank;
+    uint64_t inner, outer, ld, batch, bstride;
     uint32_t box_inner, box_outer;
     bool operator==(const MapKey &o) const
     {
-        return ptr == o.ptr && dt == o.dt && inner == o.inner && outer == o.outer && ld == o.ld &&
-               box_inner == o.box_inner && box_outer == o.box_outer;
+        return ptr == o.ptr && dt == o.dt && rank == o.rank && inner == o.inner && outer == o.outer && ld == o.ld &&
+               batch == o.batch && bstride == o.bstride && box_inner == o.box_inner && box_outer == o.box_outer;
     }
 };
 struct MapSlot {
@@ -398,16 +403,18 @@ constexpr int kMapSlots = 256;
 std::mutex g_map_mu;
 MapSlot g_maps[kMapSlots];
 
-// 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
-// `ld` elements between rows; boxes of box_inner x box_outer, 128-byte swizzle,
-// zero fill outside the tensor.
-bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-               uint32_t box_inner, uint32_t box_outer)
+bool encode_map(CUtensorMap *map, int dt, const void *ptr, int rank, uint64_t inner, uint64_t outer, uint64_t ld,
+                uint64_t batch, uint64_t bstride, uint32_t box_inner, uint32_t box_outer)
 {
-    const MapKey key{ptr, dt, inner, outer, ld, box_inner, box_outer};
+    if (rank == 2) {
+        batch = 1;
+        bstride = 0;
+    }
+    const MapKey key{ptr, dt, rank, inner, outer, ld, batch, bstride, box_inner, box_outer};
     uint64_t h = (uint64_t)(uintptr_t)ptr * 0x9E3779B97F4A7C15ull;
-    h ^= (inner * 31 + outer) * 0xC2B2AE3D27D4EB4Full;
+    h ^= (inner * 31 + outer + (uint64_t)rank * 7) * 0xC2B2AE3D27D4EB4Full;
     h ^= (ld + ((uint64_t)box_inner << 20) + ((uint64_t)box_outer << 40) + (uint64_t)dt) * 0x165667B19E3779F9ull;
+    h ^= (batch * 131 + bstride) * 0x27D4EB2F165667C5ull;
     MapSlot &slot = g_maps[(h >> 32) % kMapSlots];
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
@@ -416,13 +423,36 @@ bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64
             return true;
         }
     }
-    if (!encode_2d_uncached(map, dt, ptr, inner, outer, ld, box_inner, box_outer)) return false;
+    if (!encode_map_uncached(map, dt, ptr, rank, inner, outer, ld, batch, bstride, box_inner, box_outer)) return false;
     std::lock_guard<std::mutex> lk(g_map_mu);
     slot.valid = true;
     slot.key = key;
     slot.map = *map;
     return true;
 }
+
+bool encode_2d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer)
+{
+    return encode_map(map, dt, ptr, 2, inner, outer, ld, 1, 0, box_inner, box_outer);
+}
+
+// The 3-D map of one operand of the tile kernels: `batch` copies `bstride`
+// elements apart, or one copy shared by every batch (bstride = 0).
+bool encode_3d(CUtensorMap *map, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint64_t batch, uint64_t bstride, uint32_t box_inner, uint32_t box_outer)
+{
+    if (bstride == 0) {
+        batch = 1;
+        bstride = ld * outer;   // any legal pitch: the single copy is never stepped over
+    }
+    return encode_map(map, dt, ptr, 3, inner, outer, ld, batch, bstride, box_inner, box_outer);
+}
+
+// Batch description of a call (count 1: not batched).  Strides in elements.
+struct Batch {
+    int64_t count = 1, sa = 0, sb = 0, sc = 0;
+};
 
 tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_dtype, int b_layout,
                           const KernelVariant **v)
@@ -536,8 +566,8 @@ tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *str
     cudaGetDevice(&devno);
     tgemm_status st = split_workspace(devno, stream_ptr, part, &p->counters, &p->partials);
     if (st != TGEMM_OK) return st;
-    if (!encode_2d(&p->tma_ws, TGEMM_F32, p->partials, (uint64_t)kPairBN, (uint64_t)(slots * kPairBM),
-                   (uint64_t)kPairBN, 32, 32))
+    if (!encode_3d(&p->tma_ws, TGEMM_F32, p->partials, (uint64_t)kPairBN, (uint64_t)(slots * kPairBM),
+                   (uint64_t)kPairBN, 1, 0, 32, 32))
         return TGEMM_ERR_CUDA;
     p->dp_tiles = (int32_t)dp;
     p->sk_tiles = (int32_t)sk_tiles;
@@ -565,7 +595,8 @@ __global__ void epilogue_only_kernel(const __grid_constant__ GemmParams p)
 }
 
 // Epilogue arguments: host checks and the kernel parameter fields.
-tgemm_status epilogue_params(const tgemm_epilogue *ep, int64_t M, int64_t N, int out_dtype, GemmParams *p)
+tgemm_status epilogue_params(const tgemm_epilogue *ep, int64_t M, int64_t N, int out_dtype, GemmParams *p,
+                             const Batch &bt = Batch())
 {
     p->alpha = 1.f;
     p->beta = 0.f;
@@ -590,9 +621,10 @@ tgemm_status epilogue_params(const tgemm_epilogue *ep, int64_t M, int64_t N, int
         p->epi |= 2;
         p->cin_ptr = ep->c_in;
         p->ldc_in = ep->ldc_in;
+        // C_in steps through the batches like C (stride_c)
         if (M > 0 && N > 0 &&
-            !encode_2d(&p->tma_cin, out_dtype, ep->c_in, (uint64_t)N, (uint64_t)M, (uint64_t)ep->ldc_in,
-                       (uint32_t)(128 / eo), 32))
+            !encode_3d(&p->tma_cin, out_dtype, ep->c_in, (uint64_t)N, (uint64_t)M, (uint64_t)ep->ldc_in,
+                       (uint64_t)bt.count, (uint64_t)(bt.count > 1 ? bt.sc : 0), (uint32_t)(128 / eo), 32))
             return TGEMM_ERR_CUDA;
     }
     return TGEMM_OK;
@@ -653,7 +685,7 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
 tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                       int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
                       void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags,
-                      const tgemm_epilogue *ep = nullptr)
+                      const tgemm_epilogue *ep = nullptr, const Batch &bt = Batch())
 {
     bool noop = false;
     tgemm_status st = validate(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, &noop);
@@ -664,8 +696,9 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         cfg = *forced;
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
         if (st != TGEMM_OK) return st;
+        if (bt.count > 1 && cfg.swap_ab) return TGEMM_ERR_UNSUPPORTED;   // the skinny kernels are not batched
     }
-    if (noop) return TGEMM_OK;
+    if (noop || bt.count == 0) return TGEMM_OK;
     DeviceState *dev = nullptr;
     st = device_state(&dev);
     if (st != TGEMM_OK) return st;
@@ -678,33 +711,43 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         tgemm_status est = epilogue_params(ep, 0, N, out_dtype, &probe);
         if (est != TGEMM_OK) return est;
         if (K == 0 && probe.epi) {
-            // The empty sum under the epilogue: D = act(beta * C_in + bias).
-            GemmParams q;
-            std::memset(&q, 0, sizeof q);
-            epilogue_params(ep, 0, N, out_dtype, &q);
-            q.M = (int32_t)M;
-            q.N = (int32_t)N;
-            q.c_ptr = C;
-            q.ldc = ldc;
-            const int64_t total = M * N;
-            const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * (int64_t)dev->sm_count);
-            if (out_dtype == TGEMM_F32) epilogue_only_kernel<OUT_F32><<<blocks, 256, 0, stream>>>(q);
-            else if (out_dtype == TGEMM_F16) epilogue_only_kernel<OUT_F16><<<blocks, 256, 0, stream>>>(q);
-            else epilogue_only_kernel<OUT_BF16><<<blocks, 256, 0, stream>>>(q);
-            if (cudaGetLastError() != cudaSuccess) return TGEMM_ERR_CUDA;
+            // The empty sum under the epilogue: D = act(beta * C_in + bias), per batch.
+            for (int64_t b = 0; b < bt.count; ++b) {
+                GemmParams q;
+                std::memset(&q, 0, sizeof q);
+                epilogue_params(ep, 0, N, out_dtype, &q);
+                q.M = (int32_t)M;
+                q.N = (int32_t)N;
+                q.c_ptr = static_cast<char *>(C) + (size_t)(b * bt.sc) * eo;
+                q.ldc = ldc;
+                if (q.epi & 2) q.cin_ptr = static_cast<const char *>(q.cin_ptr) + (size_t)(b * bt.sc) * eo;
+                const int64_t total = M * N;
+                const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * (int64_t)dev->sm_count);
+                if (out_dtype == TGEMM_F32) epilogue_only_kernel<OUT_F32><<<blocks, 256, 0, stream>>>(q);
+                else if (out_dtype == TGEMM_F16) epilogue_only_kernel<OUT_F16><<<blocks, 256, 0, stream>>>(q);
+                else epilogue_only_kernel<OUT_BF16><<<blocks, 256, 0, stream>>>(q);
+                if (cudaGetLastError() != cudaSuccess) return TGEMM_ERR_CUDA;
+            }
             return TGEMM_OK;
         }
     }
     if (K == 0) {
         // The empty sum: C = 0 (all-zero bits are +0 in every output type).
-        if (cudaMemset2DAsync(C, (size_t)ldc * eo, 0, (size_t)N * eo, (size_t)M, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return TGEMM_ERR_CUDA;
-        }
+        for (int64_t b = 0; b < bt.count; ++b)
+            if (cudaMemset2DAsync(static_cast<char *>(C) + (size_t)(b * bt.sc) * eo, (size_t)ldc * eo, 0,
+                                  (size_t)N * eo, (size_t)M, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return TGEMM_ERR_CUDA;
+            }
         return TGEMM_OK;
     }
     if (!forced) {
         choose_config(M, N, K, b_layout, dev->sm_count, &cfg);
+        if (bt.count > 1 && cfg.swap_ab) {
+            // the skinny kernels are not batched: the best tile kernel instead
+            choose_config_model(65, N, K, dev->sm_count, &cfg);
+        }
+        if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
         if (st != TGEMM_OK) return st;
     }
@@ -719,27 +762,35 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
 
     GemmParams p;
     std::memset(&p, 0, sizeof p);
-    bool ok = encode_2d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kBK, kBM);
+    const uint64_t nb = (uint64_t)bt.count;
+    const uint64_t sa = bt.count > 1 ? (uint64_t)bt.sa : 0, sb = bt.count > 1 ? (uint64_t)bt.sb : 0;
+    const uint64_t sc = bt.count > 1 ? (uint64_t)bt.sc : 0;
+    bool ok = encode_3d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, nb, sa, kBK, kBM);
     if (b_mn)
-        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, kBK);
+        ok = ok && encode_3d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, sb, 64, kBK);
     else
-        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kBK, b_box_rows);
-    ok = ok && encode_2d(&p.tma_c, out_dtype, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc,
+        ok = ok && encode_3d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, sb, kBK,
+                             b_box_rows);
+    ok = ok && encode_3d(&p.tma_c, out_dtype, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc, nb, sc,
                          (uint32_t)(128 / eo), 32);
     if (!ok) return TGEMM_ERR_CUDA;
+    if (grid.count() * bt.count >= ((int64_t)1 << 31)) return TGEMM_ERR_UNSUPPORTED;
     p.M = (int32_t)M;
     p.N = (int32_t)N;
     p.K = (int32_t)K;
     p.tiles_m = (int32_t)grid.tiles_m;
     p.tiles_n = (int32_t)grid.tiles_n;
-    p.num_tiles = (int32_t)grid.count();
+    p.tiles_per_batch = (int32_t)grid.count();
+    p.a_batched = sa != 0;
+    p.b_batched = sb != 0;
+    p.num_tiles = (int32_t)(grid.count() * bt.count);
     p.num_kb = (int32_t)ceil_div(K, kBK);
     p.group_m = cfg.group_m;
     p.idesc = make_idesc(in_dtype == TGEMM_BF16, b_mn, cfg.bm, cfg.bn);
     p.debug_flags = debug_flags;
     p.status = dev->status;
     p.timeout_ns = wait_timeout_ns();
-    st = epilogue_params(ep, M, N, out_dtype, &p);
+    st = epilogue_params(ep, M, N, out_dtype, &p, bt);
     if (st != TGEMM_OK) return st;
 
     int g;
@@ -798,6 +849,33 @@ TGEMM_EXPORT tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K, const vo
                                        const tgemm_epilogue *ep, const tgemm_config *cfg)
 {
     return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0, ep);
+}
+
+TGEMM_EXPORT tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void *A,
+                                                    int64_t lda, int64_t stride_a, const void *B, int64_t ldb,
+                                                    int64_t stride_b, tgemm_b_layout b_layout, void *C, int64_t ldc,
+                                                    int64_t stride_c, tgemm_dtype in_dtype, tgemm_dtype out_dtype,
+                                                    void *stream, const tgemm_epilogue *ep, const tgemm_config *cfg)
+{
+    if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0) return TGEMM_ERR_INVALID_ARG;
+    if (batch > 1 && M > 0 && N > 0) {
+        // Batches may share A or B (stride 0) but must not overlap otherwise;
+        // outputs never overlap.  Strides keep rows 16-byte aligned.
+        const int64_t b_rows = b_layout == TGEMM_B_KN ? K : N;
+        if ((stride_a != 0 && stride_a < M * lda) || (stride_b != 0 && stride_b < b_rows * ldb) ||
+            stride_c < M * ldc)
+            return TGEMM_ERR_INVALID_ARG;
+        const size_t ei = in_dtype == TGEMM_F32 ? 4 : 2, eo = out_dtype == TGEMM_F32 ? 4 : 2;
+        if (((uint64_t)stride_a * ei) % 16 || ((uint64_t)stride_b * ei) % 16 || ((uint64_t)stride_c * eo) % 16)
+            return TGEMM_ERR_MISALIGNED;
+        if (batch >= ((int64_t)1 << 31)) return TGEMM_ERR_UNSUPPORTED;
+    }
+    Batch bt;
+    bt.count = batch;
+    bt.sa = stride_a;
+    bt.sb = stride_b;
+    bt.sc = stride_c;
+    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0, ep, bt);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,

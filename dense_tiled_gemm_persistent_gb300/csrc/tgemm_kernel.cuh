@@ -226,7 +226,16 @@ struct EpiCtx {
     uint32_t cin_bar;       // this warp's mbarrier for C_in loads
     uint32_t cin_phase;     // loads issued so far (parity)
     WaitCtx wc;
+    int32_t z = 0;          // batch coordinate of the current tile
 };
+
+// Tile number -> (batch, tile row, tile column): batches are consecutive runs
+// of tiles_per_batch tile numbers, each walked in grouped order.
+__device__ __forceinline__ void batched_tile(const GemmParams &p, int tile, int &b, int64_t &tr, int64_t &tc)
+{
+    b = tile / p.tiles_per_batch;
+    grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile - b * p.tiles_per_batch, tr, tc);
+}
 
 // Fetch the C_in block (x, row0) of this warp into the staging block `sbuf`
 // and wait for it.  Returns false if the wait timed out.
@@ -234,7 +243,7 @@ __device__ __forceinline__ bool fetch_cin(EpiCtx &e, uint32_t sbuf, int32_t x, i
 {
     if (lane == 0) {
         ptx::mbar_arrive_expect_tx(e.cin_bar, kStageCBytes);
-        ptx::tma_load_2d(sbuf, &e.p->tma_cin, e.cin_bar, x, row0);
+        ptx::tma_load_3d(sbuf, &e.p->tma_cin, e.cin_bar, x, row0, e.z);
     }
     const bool ok = wait_bounded(e.cin_bar, e.cin_phase & 1u, e.wc, SITE_EPI_CIN);
     ++e.cin_phase;
@@ -306,7 +315,7 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        if (x < cols_lim && row0 < rows_lim) ptx::tma_store_2d(map, sbuf, x, row0);
+        if (x < cols_lim && row0 < rows_lim) ptx::tma_store_3d(map, sbuf, x, row0, e.z);
         ptx::bulk_commit_group();
     }
     ++cc;
@@ -413,9 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             bool first = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int64_t tr, tc;
-                grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+                int bz;
+                batched_tile(p, tile, bz, tr, tc);
                 const int32_t m0 = (int32_t)tr * kBM;
                 const int32_t n0 = (int32_t)tc * BN;
+                const int32_t za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
                         ok = false;
@@ -427,14 +438,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         const uint32_t fb = full_bar(s);
                         ptx::mbar_arrive_expect_tx(fb, kStageBytes);
                         const int32_t k0 = kb * kBK;
-                        ptx::tma_load_2d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0);
+                        ptx::tma_load_3d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
                         if (B_MN) {
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
-                                ptx::tma_load_2d(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
-                                                 n0 + 64 * j, k0);
+                                ptx::tma_load_3d(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
+                                                 n0 + 64 * j, k0, zb);
                         } else {
-                            ptx::tma_load_2d(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0);
+                            ptx::tma_load_3d(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0, zb);
                         }
                         issued_mask |= 1u << s;
                         issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
@@ -517,7 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             ptx::tc_fence_after_sync();
 
             int64_t tr, tc;
-            grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile, tr, tc);
+            int bz;
+            batched_tile(p, tile, bz, tr, tc);
+            ectx.z = bz;
             const int32_t row0 = (int32_t)tr * kBM + 32 * q;
             const int32_t col0 = (int32_t)tc * BN;
             const uint32_t t_acc = tmem_base + lane_base + buf * BN;

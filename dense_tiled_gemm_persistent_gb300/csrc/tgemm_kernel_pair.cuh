@@ -173,9 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             PairWork w;
             while (ok && items.next(w)) {
                 int64_t tr, tc;
-                grouped_tile(p.tiles_m, p.tiles_n, p.group_m, w.tile, tr, tc);
+                int bz;
+                batched_tile(p, w.tile, bz, tr, tc);
                 const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank;
                 const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
+                const int32_t za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
                 for (int kb = w.k0; kb < w.k1; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
                         ok = false;
@@ -184,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     const uint32_t fb = ptx::map_to_cta(full_bar(s), 0);   // the leader's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);
                     const int32_t k0 = kb * kBK;
-                    ptx::tma_load_2d_pair(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0);
+                    ptx::tma_load_3d_pair(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
                     if (B_MN) {
 #pragma unroll
                         for (int j = 0; j < kHalfN / 64; ++j)
-                            ptx::tma_load_2d_pair(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
-                                                  n0 + 64 * j, k0);
+                            ptx::tma_load_3d_pair(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
+                                                  n0 + 64 * j, k0, zb);
                     } else {
-                        ptx::tma_load_2d_pair(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0);
+                        ptx::tma_load_3d_pair(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0, zb);
                     }
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
@@ -287,7 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             ptx::tc_fence_after_sync();
 
             int64_t tr, tc;
-            grouped_tile(p.tiles_m, p.tiles_n, p.group_m, w.tile, tr, tc);
+            int bz;
+            batched_tile(p, w.tile, bz, tr, tc);
+            ectx.z = bz;
             const int32_t row0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 32 * q;
             const int32_t col0 = (int32_t)tc * kPairBN;
             const uint32_t t_acc = tmem_base + lane_base + buf * kPairBN;
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     __syncwarp();
                     if (lane == 0) {
                         const int32_t x = col0 + c * kCols;
-                        if (x < p.N && row0 < p.M) ptx::tma_store_2d(&p.tma_c, sbuf, x, row0);
+                        if (x < p.N && row0 < p.M) ptx::tma_store_3d(&p.tma_c, sbuf, x, row0, bz);
                         ptx::bulk_commit_group();
                     }
                     ++cc;

@@ -30,14 +30,19 @@ constexpr uint32_t kFaultTimeout = 7u;
 
 // Everything one persistent GEMM launch needs.  The three tensor maps must
 // stay 128-byte aligned (CUtensorMap) inside the parameter space.
+// The tile kernels (one CTA, CTA pair) address every operand with 3-D tensor
+// maps whose outermost coordinate is the batch (extent 1 when not batched, or
+// when the operand is shared by all batches); the skinny kernels use 2-D maps.
 struct alignas(128) GemmParams {
-    CUtensorMap tma_a;      // A: dims {K, M}, box {64, 128}, 128-byte swizzle
-    CUtensorMap tma_b;      // B: NK dims {K, N} box {64, bn}; KN dims {N, K} box {64, 64}
-    CUtensorMap tma_c;      // C: dims {N, M}, box {128 bytes of columns, 32}, 128-byte swizzle
-    CUtensorMap tma_ws;     // stream-K partial tiles (FP32): dims {256, slots * 256}, box {32, 32}
+    CUtensorMap tma_a;      // A: dims {K, M, batch}, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tma_b;      // B: NK dims {K, N, batch} box {64, bn, 1}; KN dims {N, K, batch} box {64, 64, 1}
+    CUtensorMap tma_c;      // C: dims {N, M, batch}, box {128 bytes of columns, 32, 1}, 128-byte swizzle
+    CUtensorMap tma_ws;     // stream-K partial tiles (FP32): dims {256, slots * 256, 1}, box {32, 32, 1}
     CUtensorMap tma_cin;    // fused epilogue C_in (output type): same geometry as tma_c
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_tiles, num_kb;
+    int32_t tiles_per_batch;   // tiles_m * tiles_n; tile t is batch t / tiles_per_batch
+    int32_t a_batched, b_batched;   // 0: the operand is shared by every batch (z = 0)
     int32_t group_m;
     uint32_t idesc;         // tcgen05 instruction descriptor (kind::f16)
     uint32_t debug_flags;   // bit 0: the producer skips its first load (timeout test)

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 # Every symbol include/tgemm.h declares.
 EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
-           "tgemm_debug_wait_timeout", "tgemm_run_noalloc", "tgemm_run_ex")
+           "tgemm_debug_wait_timeout", "tgemm_run_noalloc", "tgemm_run_ex", "tgemm_run_strided_batched")
 
 ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 
@@ -83,6 +83,10 @@ def load(path: str = LIB_PATH):
         lib.tgemm_tile_coord.restype = _i
         lib.tgemm_run_ex.argtypes = run_args + [ctypes.POINTER(Epilogue), ctypes.POINTER(Config)]
         lib.tgemm_run_ex.restype = _i
+        lib.tgemm_run_strided_batched.argtypes = [_i64, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64, _i64, _i, _p,
+                                                  _i64, _i64, _i, _i, _p, ctypes.POINTER(Epilogue),
+                                                  ctypes.POINTER(Config)]
+        lib.tgemm_run_strided_batched.restype = _i
         lib.tgemm_run_noalloc.argtypes = run_args
         lib.tgemm_run_noalloc.restype = _i
         lib.tgemm_debug_wait_timeout.argtypes = [ctypes.c_uint32, _p]
@@ -102,6 +106,14 @@ def tgemm_run_ex(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype,
     """tgemm_run with a fused epilogue (Epilogue or None) and an optional Config."""
     return load().tgemm_run_ex(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream,
                                None if ep is None else ctypes.byref(ep), None if cfg is None else ctypes.byref(cfg))
+
+
+def tgemm_run_strided_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, b_layout, C, ldc, stride_c,
+                              in_dtype, out_dtype, stream=None, ep=None, cfg=None) -> int:
+    return load().tgemm_run_strided_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, b_layout, C, ldc,
+                                            stride_c, in_dtype, out_dtype, stream,
+                                            None if ep is None else ctypes.byref(ep),
+                                            None if cfg is None else ctypes.byref(cfg))
 
 
 def tgemm_run_noalloc(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream=None) -> int:

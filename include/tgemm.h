@@ -118,6 +118,24 @@ tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K,
                           tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
                           const tgemm_epilogue *ep, const tgemm_config *cfg);
 
+/*
+ * `batch` independent products C_b = A_b * B_b (b = 0 .. batch-1), the batched
+ * form of the CUDA Programming Guide 13.4.2 (unofficial Chinese translation),
+ * section 2.4.9.1 ("matmul and mma support 3-D batched multiplication"):
+ * A_b at A + b*stride_a, B_b at B + b*stride_b, C_b at C + b*stride_c
+ * (strides in elements).  A stride of 0 shares that operand across every
+ * batch; otherwise strides must not make batches overlap (stride_a >= M*lda,
+ * stride_b >= rows*ldb, stride_c >= M*ldc) and must keep 16-byte alignment.
+ * With an epilogue, C_in steps like C.  All batches run in one launch of the
+ * tile kernels (the skinny-M kernels are not batched).  batch = 0 is a no-op.
+ */
+tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                       const void *A, int64_t lda, int64_t stride_a,
+                                       const void *B, int64_t ldb, int64_t stride_b, tgemm_b_layout b_layout,
+                                       void *C, int64_t ldc, int64_t stride_c,
+                                       tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
+                                       const tgemm_epilogue *ep, const tgemm_config *cfg);
+
 /* The configuration tgemm_run would use for this problem (no device work,
  * but it reads the current device's SM count and compute capability). */
 tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
