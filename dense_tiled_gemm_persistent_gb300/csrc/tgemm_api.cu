@@ -264,7 +264,7 @@ int cluster_splits_limit(int npad) { return npad == 16 ? ClusterSplitPlan<16>::m
 int cluster_stages(int npad) { return npad == 16 ? ClusterSplitPlan<16>::stages
                                     : npad == 32 ? ClusterSplitPlan<32>::stages : ClusterSplitPlan<64>::stages; }
 
-void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg);
+void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch = 1);
 
 // The configuration tgemm_run uses: the measured table where it covers the
 // shape and its entry is legal for it, the wave cost model otherwise.
@@ -289,7 +289,7 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, 
     choose_config_model(M, N, K, sm_count, cfg);
 }
 
-void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg)
+void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch)
 {
     if (M <= 64) {
         const int npad = skinny_npad(M);
@@ -332,7 +332,7 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         const int bm = c.cluster == 2 ? kPairBM : kBM;
         const TileGrid g(M, N, bm, c.bn);
         const int units = c.cluster == 2 ? sm_count / 2 : sm_count;
-        const double cost = (double)ceil_div(g.count(), units) * c.per_tile;
+        const double cost = (double)ceil_div(g.count() * batch, units) * c.per_tile;
         if (!pick || cost < best) {
             pick = &c;
             best = cost;
@@ -743,11 +743,13 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     }
     if (!forced) {
         choose_config(M, N, K, b_layout, dev->sm_count, &cfg);
-        if (bt.count > 1 && cfg.swap_ab) {
-            // the skinny kernels are not batched: the best tile kernel instead
-            choose_config_model(65, N, K, dev->sm_count, &cfg);
+        if (bt.count > 1) {
+            // The table was measured on single problems and the skinny kernels
+            // are not batched: the wave model over the tiles of all batches.
+            choose_config_model(M > 64 ? M : 65, N, K, dev->sm_count, &cfg, bt.count);
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
+        cfg.grid = 0;   // sized below from the tiles of all batches
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
         if (st != TGEMM_OK) return st;
     }
