@@ -18,6 +18,8 @@ from .oracle import (  # noqa: F401
     F16,
     BF16,
     F32,
+    E4M3,
+    E5M2,
     B_KN,
     B_NK,
 )

@@ -19,7 +19,7 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 B_KN, B_NK = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -71,11 +71,17 @@ def _load():
 
 
 def _u16(x) -> np.ndarray:
-    """A 16-bit pattern array: accepts numpy uint16/int16 or a torch tensor."""
-    if hasattr(x, "detach"):  # torch tensor (fp16/bf16): reinterpret its bits
+    """An input pattern array: numpy uint16/int16/uint8, or a torch tensor
+    (FP16/BF16 -> 16-bit patterns, FP8 -> 8-bit patterns)."""
+    if hasattr(x, "detach"):  # torch tensor: reinterpret its bits
         import torch
-        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+        t = x.detach().cpu().contiguous()
+        if t.element_size() == 1:
+            return np.ascontiguousarray(t.view(torch.uint8).numpy())
+        x = t.view(torch.int16).numpy()
     x = np.ascontiguousarray(x)
+    if x.dtype == np.uint8:
+        return x
     if x.dtype != np.uint16:
         x = x.view(np.uint16)
     return x

@@ -22,7 +22,8 @@
  *
  * Layouts: A is row-major M x K with leading dimension lda (A[i*lda + k]).
  *   B is either K x N row-major (layout KN: B[k*ldb + j]) or stored N x K
- *   row-major (layout NK: B[j*ldb + k]).  Elements are 16-bit patterns.
+ *   row-major (layout NK: B[j*ldb + k]).  Elements are 16-bit patterns
+ *   (FP16, BF16) or 8-bit patterns (FP8 E4M3, E5M2).
  *
  * Pins (tests/test_oracle_pins.py): exact rational brute force on tiny
  * shapes, identity and permutation matrices, integer inputs with an exact
@@ -35,7 +36,7 @@
 #include <string.h>
 #include <pthread.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
 enum { ORC_B_KN = 0, ORC_B_NK = 1 };
 
 /* ---- input decoding (IEEE binary16 and bfloat16 bit patterns) ---------- */
@@ -72,8 +73,38 @@ static double decode_bf16(uint16_t b)
     return sign ? -v : v;
 }
 
-static double g_table[2][65536];
-static int g_table_ready[2];
+/* FP8 E4M3 (the "fn" variant: no infinities): 1 sign, 4 exponent bits (bias
+ * 7), 3 fraction bits; S.1111.111 is NaN, the largest finite value 448. */
+static double decode_e4m3(uint8_t b)
+{
+    int sign = (b >> 7) & 1, expo = (b >> 3) & 0xf, frac = b & 7;
+    double v;
+    if (expo == 15 && frac == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);                  /* subnormal: frac/8 * 2^-6 */
+    else
+        v = ldexp((double)(frac | 8), expo - 10);     /* 1.frac * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* FP8 E5M2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits, IEEE-style
+ * infinities and NaNs. */
+static double decode_e5m2(uint8_t b)
+{
+    int sign = (b >> 7) & 1, expo = (b >> 2) & 0x1f, frac = b & 3;
+    double v;
+    if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else if (expo == 0)
+        v = ldexp((double)frac, -16);                 /* subnormal: frac/4 * 2^-14 */
+    else
+        v = ldexp((double)(frac | 4), expo - 17);     /* 1.frac * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+static double g_table[5][65536];
+static int g_table_ready[5];
 static pthread_mutex_t g_table_lock = PTHREAD_MUTEX_INITIALIZER;
 
 static const double *decode_table(int dtype)
@@ -81,7 +112,10 @@ static const double *decode_table(int dtype)
     pthread_mutex_lock(&g_table_lock);
     if (!g_table_ready[dtype]) {
         for (uint32_t u = 0; u < 65536; ++u)
-            g_table[dtype][u] = dtype == ORC_F16 ? decode_f16((uint16_t)u) : decode_bf16((uint16_t)u);
+            g_table[dtype][u] = dtype == ORC_F16    ? decode_f16((uint16_t)u)
+                                : dtype == ORC_BF16 ? decode_bf16((uint16_t)u)
+                                : dtype == ORC_E4M3 ? decode_e4m3((uint8_t)u)
+                                                    : decode_e5m2((uint8_t)u);
         g_table_ready[dtype] = 1;
     }
     pthread_mutex_unlock(&g_table_lock);
@@ -92,6 +126,8 @@ double oracle_decode(uint32_t bits, int dtype)
 {
     if (dtype == ORC_F16) return decode_f16((uint16_t)bits);
     if (dtype == ORC_BF16) return decode_bf16((uint16_t)bits);
+    if (dtype == ORC_E4M3) return decode_e4m3((uint8_t)bits);
+    if (dtype == ORC_E5M2) return decode_e5m2((uint8_t)bits);
     if (dtype == ORC_F32) {
         float f;
         uint32_t u = bits;
@@ -105,25 +141,32 @@ double oracle_decode(uint32_t bits, int dtype)
 
 typedef struct {
     int64_t M, N, K;
-    const uint16_t *A; int64_t lda;
-    const uint16_t *B; int64_t ldb; int b_layout;
+    const void *A; int64_t lda;
+    const void *B; int64_t ldb; int b_layout;
     const double *tab;
+    int esz;                                        /* bytes per input element: 2, or 1 for FP8 */
 } problem_t;
+
+/* Bit pattern of element `idx` of an input array. */
+static uint32_t pattern(const problem_t *p, const void *base, int64_t idx)
+{
+    return p->esz == 1 ? ((const uint8_t *)base)[idx] : ((const uint16_t *)base)[idx];
+}
 
 static void dot(const problem_t *p, int64_t i, int64_t j, double *c, double *bound)
 {
     double s = 0.0, r = 0.0;
-    const uint16_t *arow = p->A + i * p->lda;
+    const int64_t arow = i * p->lda;
     if (p->b_layout == ORC_B_NK) {
-        const uint16_t *bcol = p->B + j * p->ldb;   /* column j of B is row j of the N x K store */
+        const int64_t bcol = j * p->ldb;            /* column j of B is row j of the N x K store */
         for (int64_t k = 0; k < p->K; ++k) {
-            double a = p->tab[arow[k]], b = p->tab[bcol[k]];
+            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, bcol + k)];
             s += a * b;
             r += fabs(a) * fabs(b);
         }
     } else {
         for (int64_t k = 0; k < p->K; ++k) {
-            double a = p->tab[arow[k]], b = p->tab[p->B[k * p->ldb + j]];
+            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, k * p->ldb + j)];
             s += a * b;
             r += fabs(a) * fabs(b);
         }
@@ -189,7 +232,7 @@ static int run_split(void *(*fn)(void *), work_t proto, int64_t first, int64_t l
 static int check_problem(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int b_layout, int in_dtype)
 {
     if (M < 0 || N < 0 || K < 0) return -1;
-    if (in_dtype != ORC_F16 && in_dtype != ORC_BF16) return -1;
+    if (in_dtype != ORC_F16 && in_dtype != ORC_BF16 && in_dtype != ORC_E4M3 && in_dtype != ORC_E5M2) return -1;
     if (b_layout != ORC_B_KN && b_layout != ORC_B_NK) return -1;
     if (lda < K) return -1;
     if (b_layout == ORC_B_KN ? ldb < N : ldb < K) return -1;
@@ -202,14 +245,15 @@ static int check_problem(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
  * same for Bound, which may be NULL.  Returns 0 on success, -1 on a bad argument.
  */
 int oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
-                     const uint16_t *A, int64_t lda,
-                     const uint16_t *B, int64_t ldb, int b_layout, int in_dtype,
+                     const void *A, int64_t lda,
+                     const void *B, int64_t ldb, int b_layout, int in_dtype,
                      int64_t row_begin, int64_t row_end,
                      double *C, int64_t ldc, double *Bound, int64_t ldbound, int threads)
 {
     if (check_problem(M, N, K, lda, ldb, b_layout, in_dtype)) return -1;
     if (row_begin < 0 || row_end > M || row_begin > row_end) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, decode_table(in_dtype)};
+    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, decode_table(in_dtype),
+                   (in_dtype == ORC_E4M3 || in_dtype == ORC_E5M2) ? 1 : 2};
     work_t proto;
     memset(&proto, 0, sizeof proto);
     proto.p = &p; proto.row0 = row_begin; proto.C = C; proto.ldc = ldc; proto.Bound = Bound; proto.ldbound = ldbound;
@@ -218,8 +262,8 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
 
 /* The full product: rows [0, M). */
 int oracle_gemm(int64_t M, int64_t N, int64_t K,
-                const uint16_t *A, int64_t lda,
-                const uint16_t *B, int64_t ldb, int b_layout, int in_dtype,
+                const void *A, int64_t lda,
+                const void *B, int64_t ldb, int b_layout, int in_dtype,
                 double *C, int64_t ldc, double *Bound, int64_t ldbound, int threads)
 {
     return oracle_gemm_rows(M, N, K, A, lda, B, ldb, b_layout, in_dtype, 0, M,
@@ -232,15 +276,16 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
  * the full product would take too long.
  */
 int oracle_gemm_elements(int64_t M, int64_t N, int64_t K,
-                         const uint16_t *A, int64_t lda,
-                         const uint16_t *B, int64_t ldb, int b_layout, int in_dtype,
+                         const void *A, int64_t lda,
+                         const void *B, int64_t ldb, int b_layout, int in_dtype,
                          int64_t count, const int64_t *ii, const int64_t *jj,
                          double *out, double *out_bound, int threads)
 {
     if (check_problem(M, N, K, lda, ldb, b_layout, in_dtype)) return -1;
     for (int64_t t = 0; t < count; ++t)
         if (ii[t] < 0 || ii[t] >= M || jj[t] < 0 || jj[t] >= N) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, decode_table(in_dtype)};
+    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, decode_table(in_dtype),
+                   (in_dtype == ORC_E4M3 || in_dtype == ORC_E5M2) ? 1 : 2};
     work_t proto;
     memset(&proto, 0, sizeof proto);
     proto.p = &p; proto.ii = ii; proto.jj = jj; proto.out = out; proto.out_bound = out_bound;

@@ -33,6 +33,9 @@ MUTANTS = {
     "gelu_constant": ("0.044715 * x * x * x", "0.047715 * x * x * x"),
     "bias_row_index": ("x += bias[j];", "x += bias[i % cols];"),
     "beta_dropped": ("if (cin) x += beta * cin[i * ldcin + j];", "if (cin) x += cin[i * ldcin + j];"),
+    "e4m3_bias": ("(double)(frac | 8), expo - 10)", "(double)(frac | 8), expo - 9)"),
+    "e5m2_subnormal": ("ldexp((double)frac, -16);", "ldexp((double)frac, -15);"),
+    "fp8_read_as_16bit": ("return p->esz == 1 ?", "return p->esz == 3 ?"),
 }
 
 

@@ -343,3 +343,47 @@ def test_epilogue_gelu_tanh_odd_part_and_torch(orc):
     assert np.allclose(g, ref, rtol=1e-14, atol=1e-14)
     # far from zero it is the identity or zero
     assert abs(g[-1] - 8.0) < 1e-12 and abs(g[0]) < 1e-12
+
+
+# --- FP8 inputs ----------------------------------------------------------------
+
+E4M3, E5M2 = 3, 4
+
+
+@pytest.mark.parametrize("dtype,tdt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+def test_decode_fp8_all_patterns_match_torch(orc, dtype, tdt):
+    bits = np.arange(256, dtype=np.uint32)
+    got = orc.decode(bits, dtype)
+    ref = torch.from_numpy(bits.astype(np.uint8)).view(tdt).double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+@pytest.mark.parametrize("dtype,tdt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_fp8_brute_force_rational(orc, dtype, tdt, layout):
+    """FP8 products have at most 8 significant bits and a bounded exponent
+    range, so small double sums are exact: equal to the rational result."""
+    rng = np.random.default_rng(300 + dtype + layout)
+    for _ in range(5):
+        M, N, K = (int(v) for v in rng.integers(1, 7, 3))
+        a = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(tdt)
+        b = torch.from_numpy(rng.standard_normal((K, N) if layout == KN else (N, K)).astype(np.float32)).to(tdt)
+        C, R = orc.gemm(a, b, M, N, K, K, b.shape[1], layout, dtype)
+        av, bv = a.double().numpy(), b.double().numpy()
+        for i in range(M):
+            for j in range(N):
+                s = sum(Fraction(float(av[i, k])) * Fraction(float(bv[k, j] if layout == KN else bv[j, k]))
+                        for k in range(K))
+                assert Fraction(C[i, j]) == s
+
+
+def test_fp8_integers_exact(orc):
+    M, N, K = 20, 24, 40
+    g = torch.Generator().manual_seed(5)
+    a = torch.randint(-2, 3, (M, K), generator=g).float().to(torch.float8_e4m3fn)
+    b = torch.randint(-2, 3, (N, K), generator=g).float().to(torch.float8_e5m2)
+    # same-type operands only on the GPU; the oracle itself decodes either
+    C, _ = orc.gemm(a, b.float().to(torch.float8_e4m3fn), M, N, K, K, K, NK, E4M3)
+    assert np.array_equal(C, a.double().numpy() @ b.double().numpy().T)
