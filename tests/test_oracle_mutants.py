@@ -16,15 +16,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "tgemm_oracle.c")
 
 MUTANTS = {
-    "dropped_last_term_nk": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[bcol[k]];",
-                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[bcol[k]];"),
-    "dropped_last_term_kn": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[p->B[k * p->ldb + j]];",
-                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[arow[k]], b = p->tab[p->B[k * p->ldb + j]];"),
+    "dropped_last_term_nk": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, bcol + k)];",
+                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, bcol + k)];"),
+    "dropped_last_term_kn": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, k * p->ldb + j)];",
+                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, k * p->ldb + j)];"),
     "wrong_sign": ("            s += a * b;\n            r += fabs(a) * fabs(b);\n        }\n    } else {",
                    "            s -= a * b;\n            r += fabs(a) * fabs(b);\n        }\n    } else {"),
-    "transposed_b_kn": ("p->B[k * p->ldb + j]", "p->B[j * p->ldb + k]"),
-    "wrong_row_nk": ("p->B + j * p->ldb", "p->B + i * p->ldb"),
-    "ignores_lda": ("p->A + i * p->lda", "p->A + i * p->K"),
+    "transposed_b_kn": ("pattern(p, p->B, k * p->ldb + j)", "pattern(p, p->B, j * p->ldb + k)"),
+    "wrong_row_nk": ("const int64_t bcol = j * p->ldb;", "const int64_t bcol = i * p->ldb;"),
+    "ignores_lda": ("const int64_t arow = i * p->lda;", "const int64_t arow = i * p->K;"),
     "f16_bias_off_by_one": ("expo - 25); /* 1.frac", "expo - 24); /* 1.frac"),
     "bf16_fraction_width": ("(frac | 0x80), expo - 134)", "(frac | 0x80), expo - 133)"),
     "ties_away_from_zero": ("double r = nearbyint(a / q) * q;", "double r = round(a / q) * q;"),
