@@ -397,10 +397,14 @@ def main():
     avg_launch = local_ms / args.steps
 
     peaks = measured_peaks()
+    # FP8 runs at twice the dense 16-bit tensor rate (4.5 vs 2.25 PFLOP/s nominal)
+    rate = 2.0 if gen.DTYPE_SIZE[wl.in_dtype] == 1 else 1.0
     if peaks and peaks.get("bf16_tflops"):
-        peak_t, src_t = float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate equals bf16)"
+        peak_t, src_t = rate * float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate equals bf16)"
+        if rate != 1.0:
+            src_t = "measured cuBLAS bf16 burst x 2 (nominal FP8/BF16 dense ratio)"
     else:
-        peak_t, src_t = FALLBACK_TENSOR_TFLOPS, "fallback"
+        peak_t, src_t = rate * FALLBACK_TENSOR_TFLOPS, "fallback" + (" x 2 (FP8)" if rate != 1.0 else "")
     if peaks and peaks.get("hbm_gbs"):
         peak_h, src_h = float(peaks["hbm_gbs"]), "measured (copy)"
     else:
@@ -412,7 +416,7 @@ def main():
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t, "peak_source": src_t}
         if peaks and peaks.get("bf16_tflops_sustained"):
-            roofline["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+            roofline["frac_of_sustained"] = achieved / (rate * float(peaks["bf16_tflops_sustained"]))
     else:
         achieved = wl.algorithmic_bytes / (avg_launch * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_h, "unit": "GB/s",

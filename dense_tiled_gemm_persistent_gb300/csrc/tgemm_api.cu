@@ -82,7 +82,10 @@ uint64_t wait_timeout_ns()
     return ns;
 }
 
-size_t elem_size(int dt) { return dt == TGEMM_F32 ? 4 : 2; }
+size_t elem_size(int dt) { return dt == TGEMM_F32 ? 4 : (dt == TGEMM_E4M3 || dt == TGEMM_E5M2) ? 1 : 2; }
+bool is_f8(int dt) { return dt == TGEMM_E4M3 || dt == TGEMM_E5M2; }
+// K elements in one 128-byte k-block row
+int kblock_elems(int in_dtype) { return is_f8(in_dtype) ? 128 : kBK; }
 
 // Current device's state; allocates the status word on first use.
 tgemm_status device_state(DeviceState **out)
@@ -130,11 +133,12 @@ tgemm_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
 {
     *noop = false;
     if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
-    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16 && in_dtype != TGEMM_F32)
+    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16 && in_dtype != TGEMM_F32 && !is_f8(in_dtype))
         return TGEMM_ERR_INVALID_ARG;
     if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
         return TGEMM_ERR_INVALID_ARG;
     if (in_dtype == TGEMM_F32) return TGEMM_ERR_UNSUPPORTED;   // FP32 operands are not provided
+    if (is_f8(in_dtype) && b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;   // FP8: K-major B only
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
     // Tensor coordinates are signed 32-bit.
     const int64_t kMax = (int64_t)1 << 31;
@@ -156,7 +160,7 @@ tgemm_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     return TGEMM_OK;
 }
 
-const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int cluster)
+const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int cluster, int f8 = 0)
 {
     const KernelVariant *tab = nullptr;
     int n = 0;
@@ -167,7 +171,8 @@ const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int clu
     default: return nullptr;
     }
     for (int i = 0; i < n; ++i)
-        if (tab[i].bn == bn && tab[i].stages == stages && tab[i].b_mn == b_mn && tab[i].cluster == cluster)
+        if (tab[i].bn == bn && tab[i].stages == stages && tab[i].b_mn == b_mn && tab[i].cluster == cluster &&
+            tab[i].f8 == f8)
             return &tab[i];
     return nullptr;
 }
@@ -354,6 +359,8 @@ CUtensorMapDataType map_dtype(int dt)
     switch (dt) {
     case TGEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case TGEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case TGEMM_E4M3:
+    case TGEMM_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // the copy engine only moves bytes
     default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     }
 }
@@ -455,9 +462,18 @@ struct Batch {
 };
 
 tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_dtype, int b_layout,
-                          const KernelVariant **v)
+                          const KernelVariant **v, int in_dtype = TGEMM_F16)
 {
     if (c.bk != kBK || c.grid < 0 || c.group_m < 1) return TGEMM_ERR_UNSUPPORTED;
+    if (is_f8(in_dtype)) {
+        // FP8: the tile kernels, K-major B (bk names the 128-byte k-block)
+        if (c.swap_ab != 0 || b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
+        if (!(c.split_k == 1 || (c.split_k == 0 && c.cluster_m == 2))) return TGEMM_ERR_UNSUPPORTED;
+        if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
+            return TGEMM_ERR_UNSUPPORTED;
+        *v = find_variant(c.bn, c.stages, out_dtype, 0, c.cluster_m, 1);
+        return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+    }
     const int b_mn = b_layout == TGEMM_B_KN ? 1 : 0;
     if (c.swap_ab == 1) {
         // swap-AB, split-K through a global workspace: bm weight rows per
@@ -694,7 +710,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     const KernelVariant *var = nullptr;
     if (forced) {
         cfg = *forced;
-        st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
+        st = legal_config(cfg, M, K, out_dtype, b_layout, &var, in_dtype);
         if (st != TGEMM_OK) return st;
         if (bt.count > 1 && cfg.swap_ab) return TGEMM_ERR_UNSUPPORTED;   // the skinny kernels are not batched
     }
@@ -748,9 +764,13 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
             // are not batched: the wave model over the tiles of all batches.
             choose_config_model(M > 64 ? M : 65, N, K, dev->sm_count, &cfg, bt.count);
         }
+        if (is_f8(in_dtype) && cfg.swap_ab) {
+            // the skinny kernels take 16-bit operands: the tile kernels for FP8
+            choose_config_model(65, N, K, dev->sm_count, &cfg, bt.count);
+        }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
         cfg.grid = 0;   // sized below from the tiles of all batches
-        st = legal_config(cfg, M, K, out_dtype, b_layout, &var);
+        st = legal_config(cfg, M, K, out_dtype, b_layout, &var, in_dtype);
         if (st != TGEMM_OK) return st;
     }
     if (cfg.swap_ab)
@@ -767,11 +787,12 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     const uint64_t nb = (uint64_t)bt.count;
     const uint64_t sa = bt.count > 1 ? (uint64_t)bt.sa : 0, sb = bt.count > 1 ? (uint64_t)bt.sb : 0;
     const uint64_t sc = bt.count > 1 ? (uint64_t)bt.sc : 0;
-    bool ok = encode_3d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, nb, sa, kBK, kBM);
+    const uint32_t kbe = (uint32_t)kblock_elems(in_dtype);   // K elements per 128-byte k-block row
+    bool ok = encode_3d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, nb, sa, kbe, kBM);
     if (b_mn)
         ok = ok && encode_3d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, sb, 64, kBK);
     else
-        ok = ok && encode_3d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, sb, kBK,
+        ok = ok && encode_3d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, sb, kbe,
                              b_box_rows);
     ok = ok && encode_3d(&p.tma_c, out_dtype, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc, nb, sc,
                          (uint32_t)(128 / eo), 32);
@@ -786,9 +807,10 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     p.a_batched = sa != 0;
     p.b_batched = sb != 0;
     p.num_tiles = (int32_t)(grid.count() * bt.count);
-    p.num_kb = (int32_t)ceil_div(K, kBK);
+    p.num_kb = (int32_t)ceil_div(K, kbe);
     p.group_m = cfg.group_m;
-    p.idesc = make_idesc(in_dtype == TGEMM_BF16, b_mn, cfg.bm, cfg.bn);
+    // kind::f16: type codes 0 F16 / 1 BF16; kind::f8f6f4: 0 E4M3 / 1 E5M2
+    p.idesc = make_idesc(in_dtype == TGEMM_BF16 || in_dtype == TGEMM_E5M2, b_mn, cfg.bm, cfg.bn);
     p.debug_flags = debug_flags;
     p.status = dev->status;
     p.timeout_ns = wait_timeout_ns();
@@ -867,7 +889,7 @@ TGEMM_EXPORT tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, in
         if ((stride_a != 0 && stride_a < M * lda) || (stride_b != 0 && stride_b < b_rows * ldb) ||
             stride_c < M * ldc)
             return TGEMM_ERR_INVALID_ARG;
-        const size_t ei = in_dtype == TGEMM_F32 ? 4 : 2, eo = out_dtype == TGEMM_F32 ? 4 : 2;
+        const size_t ei = elem_size(in_dtype), eo = elem_size(out_dtype);
         if (((uint64_t)stride_a * ei) % 16 || ((uint64_t)stride_b * ei) % 16 || ((uint64_t)stride_c * eo) % 16)
             return TGEMM_ERR_MISALIGNED;
         if (batch >= ((int64_t)1 << 31)) return TGEMM_ERR_UNSUPPORTED;
@@ -886,7 +908,8 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
 {
     if (!out_cfg) return TGEMM_ERR_INVALID_ARG;
     if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
-    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16) return TGEMM_ERR_UNSUPPORTED;
+    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16 && !is_f8(in_dtype)) return TGEMM_ERR_UNSUPPORTED;
+    if (is_f8(in_dtype) && b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
     if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
         return TGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
@@ -894,6 +917,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     tgemm_status st = device_state(&dev);
     if (st != TGEMM_OK) return st;
     choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, dev->sm_count, out_cfg);
+    if (is_f8(in_dtype) && out_cfg->swap_ab) choose_config_model(65, N, K, dev->sm_count, out_cfg);
     return TGEMM_OK;
 }
 

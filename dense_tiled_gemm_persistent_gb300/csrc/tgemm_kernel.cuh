@@ -47,6 +47,10 @@ namespace tgemm {
 constexpr int kBM = 128;           // rows of one CTA tile = TMEM lanes
 constexpr int kBK = 64;            // K depth of one stage: 64 x 2 bytes = one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
+// FP8 operands keep the byte geometry: a 128-byte row holds 128 elements and
+// one kind::f8f6f4 MMA covers K = 32 (32 bytes), so every shared-memory
+// offset is the same and only the element count of a k-block doubles.
+template <bool F8> struct KBlock { static constexpr int elems = F8 ? 128 : 64; };
 constexpr int kThreads = 192;      // 6 warps
 constexpr int kEpiWarps = 4;
 constexpr uint32_t kStageCBytes = 32 * 128;   // one staged 32-row x 128-byte block of C
@@ -351,9 +355,10 @@ __device__ __forceinline__ void epilogue_drain(const CUtensorMap *map, int32_t r
     }
 }
 
-template <int BN, int STAGES, int OUT, bool B_MN>
+template <int BN, int STAGES, int OUT, bool B_MN, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p)
 {
+    static_assert(!(F8 && B_MN), "FP8 operands are K-major only");
     using Plan = SmemPlan<BN, STAGES>;
     constexpr uint32_t kStageBytes = Plan::a_stage + Plan::b_stage;
     constexpr uint32_t kTmemCols = TmemCols<BN>::value;
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                     if (!skip) {
                         const uint32_t fb = full_bar(s);
                         ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                        const int32_t k0 = kb * kBK;
+                        const int32_t k0 = kb * KBlock<F8>::elems;
                         ptx::tma_load_3d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
                         if (B_MN) {
 #pragma unroll
@@ -493,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
                         const uint64_t bd = B_MN ? desc_at(kDescMNMajor, b_addr + k * (kUmmaK * 128))
                                                  : desc_at(kDescKMajor, b_addr + k * (kUmmaK * 2));
-                        ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        if constexpr (F8) ptx::mma_f8_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        else ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(empty_bar(s));       // stage reusable once these MMAs finish
                     if (++s == STAGES) {
@@ -550,10 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     }
 }
 
-template <int BN, int STAGES, int OUT, bool B_MN>
+template <int BN, int STAGES, int OUT, bool B_MN, bool F8 = false>
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = gemm_persistent_kernel<BN, STAGES, OUT, B_MN>;
+    auto kern = gemm_persistent_kernel<BN, STAGES, OUT, B_MN, F8>;
     constexpr uint32_t smem = SmemPlan<BN, STAGES>::alloc_bytes;
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
@@ -568,5 +574,7 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
 
 #define TGEMM_VARIANT(BN, ST, OUT, BMN) \
     {BN, ST, OUT, BMN, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, (BMN) != 0>, 1, nullptr}
+#define TGEMM_VARIANT_F8(BN, ST, OUT) \
+    {BN, ST, OUT, 0, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, false, true>, 1, nullptr, 1}
 
 }  // namespace tgemm

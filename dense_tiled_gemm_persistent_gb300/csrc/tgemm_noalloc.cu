@@ -160,7 +160,8 @@ TGEMM_EXPORT tgemm_status tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, con
     // ---- host checks, before any CUDA call -------------------------------
     if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
     if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16) {
-        return in_dtype == TGEMM_F32 ? TGEMM_ERR_UNSUPPORTED : TGEMM_ERR_INVALID_ARG;
+        return (in_dtype == TGEMM_F32 || in_dtype == TGEMM_E4M3 || in_dtype == TGEMM_E5M2) ? TGEMM_ERR_UNSUPPORTED
+                                                                                           : TGEMM_ERR_INVALID_ARG;
     }
     if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32) return TGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;

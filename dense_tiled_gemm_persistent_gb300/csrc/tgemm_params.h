@@ -81,6 +81,7 @@ struct KernelVariant {
     LaunchFn launch;
     int cluster;
     OccupancyFn max_active;
+    int f8 = 0;            // 1: FP8 operands (kind::f8f6f4), 128 elements per k-block
 };
 
 // Defined in the kernel translation units (one per output type).

@@ -10,7 +10,8 @@ Recipe (the pages give seeds and distributions but no generator):
     orientation (K x N for layout KN, N x K for layout NK), both in float32;
   * uniform(a, b) is ``a + (b - a) * torch.rand``; normal(mu, sigma) is
     ``mu + sigma * torch.randn``; ints(lo, hi) is ``torch.randint(lo, hi + 1)``;
-  * the float32 draws are rounded to FP16/BF16 with ``Tensor.to`` (RNE);
+  * the float32 draws are rounded to FP16/BF16/FP8 with ``Tensor.to`` (RNE;
+    FP8 draws are kept inside the FP8 type's finite range by the caller);
   * a leading dimension larger than the row length pads each row; the pad
     holds ``pad_value`` (NaN by default for the poison tests), never data.
 """
@@ -21,12 +22,13 @@ from typing import Optional, Tuple
 
 import torch
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 B_KN, B_NK = 0, 1
 
-TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}
-DTYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32"}
-DTYPE_SIZE = {F16: 2, BF16: 2, F32: 4}
+TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32,
+               E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+DTYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32", E4M3: "e4m3", E5M2: "e5m2"}
+DTYPE_SIZE = {F16: 2, BF16: 2, F32: 4, E4M3: 1, E5M2: 1}
 
 
 @dataclass(frozen=True)
@@ -126,7 +128,8 @@ class Workload:
         return self.M * self.K * e_in + self.K * self.N * e_in + self.M * self.N * e_out
 
 
-# The five problem families the benchmark configuration lists, by shape.
+# The five problem families the benchmark configuration lists, by shape, and
+# the FP8 form of the square one.
 WORKLOADS = {
     w.name: w for w in [
         Workload("gemm_256x256x256_f16_kn_f32", 256, 256, 256, F16, F32, B_KN,
@@ -143,5 +146,7 @@ WORKLOADS = {
                  normal(0, 1), normal(0, 0.02), 4),
         Workload("proj_16x4096x4096_bf16_nk_bf16", 16, 4096, 4096, BF16, BF16, B_NK,
                  normal(0, 1), normal(0, 0.02), 4),
+        Workload("gemm_8192x8192x8192_e4m3_nk_bf16", 8192, 8192, 8192, E4M3, BF16, B_NK,
+                 normal(0, 1), normal(0, 1), 5),
     ]
 }

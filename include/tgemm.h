@@ -41,7 +41,11 @@ extern "C" {
 
 typedef enum { TGEMM_B_KN = 0, TGEMM_B_NK = 1 } tgemm_b_layout;
 
-typedef enum { TGEMM_F16 = 0, TGEMM_BF16 = 1, TGEMM_F32 = 2 } tgemm_dtype;
+/* Element types.  FP8 (E4M3 "fn" variant with no infinities, E5M2) is an
+ * input type only: both operands the same FP8 type, B stored N x K, FP32
+ * accumulation, FP16/BF16/FP32 output (scale factors go in the epilogue's
+ * alpha). */
+typedef enum { TGEMM_F16 = 0, TGEMM_BF16 = 1, TGEMM_F32 = 2, TGEMM_E4M3 = 3, TGEMM_E5M2 = 4 } tgemm_dtype;
 
 typedef enum {
     TGEMM_OK = 0,
