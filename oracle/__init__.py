@@ -20,6 +20,7 @@ from .oracle import (  # noqa: F401
     F32,
     E4M3,
     E5M2,
+    TF32,
     B_KN,
     B_NK,
 )

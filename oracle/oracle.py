@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY: imported by tests/, the package smoke entry and the
 benchmark's CPU-baseline leg, never by the product path.  It shares no code
 with the CUDA library.
 
-Inputs are 16-bit patterns (numpy uint16 arrays, or anything convertible);
-outputs are float64 numpy arrays.  Each wrapper states the passage it follows
+Inputs are bit patterns: numpy uint16 (FP16/BF16), uint8 (FP8) or uint32
+(FP32 storage read as TF32) arrays, or torch tensors of those dtypes; outputs
+are float64 numpy arrays.  Each wrapper states the passage it follows
 in the C file's header: the defining sum C[i][j] = sum_k A[i][k] B[k][j] from
 "Writing high-performance matrix multiplication with NVIDIA CUDA Tile"
 (juejin.cn, "What is matrix multiplication?").
@@ -19,7 +20,7 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+F16, BF16, F32, E4M3, E5M2, TF32 = 0, 1, 2, 3, 4, 5
 B_KN, B_NK = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -71,17 +72,22 @@ def _load():
 
 
 def _u16(x) -> np.ndarray:
-    """An input pattern array: numpy uint16/int16/uint8, or a torch tensor
-    (FP16/BF16 -> 16-bit patterns, FP8 -> 8-bit patterns)."""
+    """An input pattern array: numpy uint16/int16/uint8/uint32/float32, or a
+    torch tensor (FP16/BF16 -> 16-bit patterns, FP8 -> 8-bit patterns, FP32
+    -> 32-bit patterns)."""
     if hasattr(x, "detach"):  # torch tensor: reinterpret its bits
         import torch
         t = x.detach().cpu().contiguous()
         if t.element_size() == 1:
             return np.ascontiguousarray(t.view(torch.uint8).numpy())
+        if t.element_size() == 4:
+            return np.ascontiguousarray(t.view(torch.int32).numpy().view(np.uint32))
         x = t.view(torch.int16).numpy()
     x = np.ascontiguousarray(x)
-    if x.dtype == np.uint8:
+    if x.dtype in (np.uint8, np.uint32):
         return x
+    if x.dtype in (np.float32, np.int32):
+        return x.view(np.uint32)
     if x.dtype != np.uint16:
         x = x.view(np.uint16)
     return x
@@ -174,7 +180,8 @@ def epilogue(C, alpha=1.0, beta=0.0, cin=None, bias=None, act=ACT_NONE) -> np.nd
 
 
 def decode(bits, dtype) -> np.ndarray:
-    """Value of 16-bit (F16/BF16) or 32-bit (F32) patterns as float64."""
+    """Value of 16-bit (F16/BF16), 8-bit (E4M3/E5M2) or 32-bit (F32, or TF32:
+    the FP32 pattern with its low 13 fraction bits dropped) patterns as float64."""
     lib = _load()
     b = np.ascontiguousarray(bits, dtype=np.uint32)
     out = np.zeros(b.shape, dtype=np.float64)

@@ -23,7 +23,16 @@
  * Layouts: A is row-major M x K with leading dimension lda (A[i*lda + k]).
  *   B is either K x N row-major (layout KN: B[k*ldb + j]) or stored N x K
  *   row-major (layout NK: B[j*ldb + k]).  Elements are 16-bit patterns
- *   (FP16, BF16) or 8-bit patterns (FP8 E4M3, E5M2).
+ *   (FP16, BF16), 8-bit patterns (FP8 E4M3, E5M2) or 32-bit FP32 patterns
+ *   taken as TF32.
+ *
+ * FP32 operands (the pages pick a separate, smaller tile for them in
+ * "Writing high-performance matrix multiplication with NVIDIA CUDA Tile",
+ * section "Launching the kernel from the host", and say no more about how
+ * they are multiplied) are read as TF32: sign, 8-bit exponent and the top 10
+ * fraction bits, the low 13 fraction bits dropped (truncation toward zero),
+ * which is how the tensor core reads 32-bit containers.  Every product of
+ * two TF32 values is exact in double (at most 22 significant bits).
  *
  * Pins (tests/test_oracle_pins.py): exact rational brute force on tiny
  * shapes, identity and permutation matrices, integer inputs with an exact
@@ -36,7 +45,7 @@
 #include <string.h>
 #include <pthread.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_TF32 = 5 };
 enum { ORC_B_KN = 0, ORC_B_NK = 1 };
 
 /* ---- input decoding (IEEE binary16 and bfloat16 bit patterns) ---------- */
@@ -103,6 +112,18 @@ static double decode_e5m2(uint8_t b)
     return sign ? -v : v;
 }
 
+/* TF32 from an FP32 pattern: keep sign, exponent and the top 10 fraction
+ * bits.  Clearing bits only ever moves a finite value toward zero; zeros,
+ * subnormals and infinities keep their class (a NaN whose payload sits only
+ * in the dropped bits would read as an infinity). */
+static double decode_tf32(uint32_t u)
+{
+    uint32_t t = u & 0xffffe000u;
+    float f;
+    memcpy(&f, &t, sizeof f);
+    return (double)f;
+}
+
 static double g_table[5][65536];
 static int g_table_ready[5];
 static pthread_mutex_t g_table_lock = PTHREAD_MUTEX_INITIALIZER;
@@ -134,6 +155,7 @@ double oracle_decode(uint32_t bits, int dtype)
         memcpy(&f, &u, sizeof f);
         return (double)f;
     }
+    if (dtype == ORC_TF32) return decode_tf32(bits);
     return NAN;
 }
 
@@ -143,14 +165,15 @@ typedef struct {
     int64_t M, N, K;
     const void *A; int64_t lda;
     const void *B; int64_t ldb; int b_layout;
-    const double *tab;
-    int esz;                                        /* bytes per input element: 2, or 1 for FP8 */
+    const double *tab;                              /* decode table of 8/16-bit patterns (NULL for TF32) */
+    int esz;                                        /* bytes per input element: 2, 1 for FP8, 4 for TF32 */
 } problem_t;
 
-/* Bit pattern of element `idx` of an input array. */
-static uint32_t pattern(const problem_t *p, const void *base, int64_t idx)
+/* Value of element `idx` of an input array. */
+static double elem(const problem_t *p, const void *base, int64_t idx)
 {
-    return p->esz == 1 ? ((const uint8_t *)base)[idx] : ((const uint16_t *)base)[idx];
+    if (p->esz == 4) return decode_tf32(((const uint32_t *)base)[idx]);
+    return p->tab[p->esz == 1 ? ((const uint8_t *)base)[idx] : ((const uint16_t *)base)[idx]];
 }
 
 static void dot(const problem_t *p, int64_t i, int64_t j, double *c, double *bound)
@@ -160,13 +183,13 @@ static void dot(const problem_t *p, int64_t i, int64_t j, double *c, double *bou
     if (p->b_layout == ORC_B_NK) {
         const int64_t bcol = j * p->ldb;            /* column j of B is row j of the N x K store */
         for (int64_t k = 0; k < p->K; ++k) {
-            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, bcol + k)];
+            double a = elem(p, p->A, arow + k), b = elem(p, p->B, bcol + k);
             s += a * b;
             r += fabs(a) * fabs(b);
         }
     } else {
         for (int64_t k = 0; k < p->K; ++k) {
-            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, k * p->ldb + j)];
+            double a = elem(p, p->A, arow + k), b = elem(p, p->B, k * p->ldb + j);
             s += a * b;
             r += fabs(a) * fabs(b);
         }
@@ -229,10 +252,17 @@ static int run_split(void *(*fn)(void *), work_t proto, int64_t first, int64_t l
     return 0;
 }
 
+static int in_esz(int in_dtype)
+{
+    return in_dtype == ORC_TF32 ? 4 : (in_dtype == ORC_E4M3 || in_dtype == ORC_E5M2) ? 1 : 2;
+}
+
 static int check_problem(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int b_layout, int in_dtype)
 {
     if (M < 0 || N < 0 || K < 0) return -1;
-    if (in_dtype != ORC_F16 && in_dtype != ORC_BF16 && in_dtype != ORC_E4M3 && in_dtype != ORC_E5M2) return -1;
+    if (in_dtype != ORC_F16 && in_dtype != ORC_BF16 && in_dtype != ORC_E4M3 && in_dtype != ORC_E5M2 &&
+        in_dtype != ORC_TF32)
+        return -1;
     if (b_layout != ORC_B_KN && b_layout != ORC_B_NK) return -1;
     if (lda < K) return -1;
     if (b_layout == ORC_B_KN ? ldb < N : ldb < K) return -1;
@@ -252,8 +282,8 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
 {
     if (check_problem(M, N, K, lda, ldb, b_layout, in_dtype)) return -1;
     if (row_begin < 0 || row_end > M || row_begin > row_end) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, decode_table(in_dtype),
-                   (in_dtype == ORC_E4M3 || in_dtype == ORC_E5M2) ? 1 : 2};
+    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, in_dtype == ORC_TF32 ? NULL : decode_table(in_dtype),
+                   in_esz(in_dtype)};
     work_t proto;
     memset(&proto, 0, sizeof proto);
     proto.p = &p; proto.row0 = row_begin; proto.C = C; proto.ldc = ldc; proto.Bound = Bound; proto.ldbound = ldbound;
@@ -284,8 +314,8 @@ int oracle_gemm_elements(int64_t M, int64_t N, int64_t K,
     if (check_problem(M, N, K, lda, ldb, b_layout, in_dtype)) return -1;
     for (int64_t t = 0; t < count; ++t)
         if (ii[t] < 0 || ii[t] >= M || jj[t] < 0 || jj[t] >= N) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, decode_table(in_dtype),
-                   (in_dtype == ORC_E4M3 || in_dtype == ORC_E5M2) ? 1 : 2};
+    problem_t p = {M, N, K, A, lda, B, ldb, b_layout, in_dtype == ORC_TF32 ? NULL : decode_table(in_dtype),
+                   in_esz(in_dtype)};
     work_t proto;
     memset(&proto, 0, sizeof proto);
     proto.p = &p; proto.ii = ii; proto.jj = jj; proto.out = out; proto.out_bound = out_bound;

@@ -16,13 +16,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "tgemm_oracle.c")
 
 MUTANTS = {
-    "dropped_last_term_nk": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, bcol + k)];",
-                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, bcol + k)];"),
-    "dropped_last_term_kn": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, k * p->ldb + j)];",
-                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = p->tab[pattern(p, p->A, arow + k)], b = p->tab[pattern(p, p->B, k * p->ldb + j)];"),
+    "dropped_last_term_nk": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = elem(p, p->A, arow + k), b = elem(p, p->B, bcol + k);",
+                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = elem(p, p->A, arow + k), b = elem(p, p->B, bcol + k);"),
+    "dropped_last_term_kn": ("for (int64_t k = 0; k < p->K; ++k) {\n            double a = elem(p, p->A, arow + k), b = elem(p, p->B, k * p->ldb + j);",
+                             "for (int64_t k = 0; k < p->K - 1; ++k) {\n            double a = elem(p, p->A, arow + k), b = elem(p, p->B, k * p->ldb + j);"),
     "wrong_sign": ("            s += a * b;\n            r += fabs(a) * fabs(b);\n        }\n    } else {",
                    "            s -= a * b;\n            r += fabs(a) * fabs(b);\n        }\n    } else {"),
-    "transposed_b_kn": ("pattern(p, p->B, k * p->ldb + j)", "pattern(p, p->B, j * p->ldb + k)"),
+    "transposed_b_kn": ("elem(p, p->B, k * p->ldb + j)", "elem(p, p->B, j * p->ldb + k)"),
     "wrong_row_nk": ("const int64_t bcol = j * p->ldb;", "const int64_t bcol = i * p->ldb;"),
     "ignores_lda": ("const int64_t arow = i * p->lda;", "const int64_t arow = i * p->K;"),
     "f16_bias_off_by_one": ("expo - 25); /* 1.frac", "expo - 24); /* 1.frac"),
@@ -35,7 +35,10 @@ MUTANTS = {
     "beta_dropped": ("if (cin) x += beta * cin[i * ldcin + j];", "if (cin) x += cin[i * ldcin + j];"),
     "e4m3_bias": ("(double)(frac | 8), expo - 10)", "(double)(frac | 8), expo - 9)"),
     "e5m2_subnormal": ("ldexp((double)frac, -16);", "ldexp((double)frac, -15);"),
-    "fp8_read_as_16bit": ("return p->esz == 1 ?", "return p->esz == 3 ?"),
+    "fp8_read_as_16bit": ("p->tab[p->esz == 1 ?", "p->tab[p->esz == 3 ?"),
+    "tf32_keeps_low_bits": ("uint32_t t = u & 0xffffe000u;", "uint32_t t = u;"),
+    "tf32_nine_fraction_bits": ("uint32_t t = u & 0xffffe000u;", "uint32_t t = u & 0xffffc000u;"),
+    "tf32_read_as_16bit": ("if (p->esz == 4) return", "if (p->esz == 5) return"),
 }
 
 

@@ -387,3 +387,103 @@ def test_fp8_integers_exact(orc):
     # same-type operands only on the GPU; the oracle itself decodes either
     C, _ = orc.gemm(a, b.float().to(torch.float8_e4m3fn), M, N, K, K, K, NK, E4M3)
     assert np.array_equal(C, a.double().numpy() @ b.double().numpy().T)
+
+
+# --- FP32 operands read as TF32 --------------------------------------------------
+#
+# TF32 keeps the FP32 sign, the 8-bit exponent and the top 10 of the 23
+# fraction bits.  The pins below restate that format with Python's struct
+# module (an FP32 pattern with its low 13 bits cleared) and with closed-form
+# values, never through the oracle's own decoder.
+
+TF32 = 5
+
+
+def tf32_exact(bits: int) -> Fraction:
+    return Fraction(struct.unpack("<f", struct.pack("<I", bits & 0xFFFFE000))[0])
+
+
+def f32_bits(x: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", x))[0]
+
+
+def test_tf32_decode_closed_forms(orc):
+    cases = {
+        f32_bits(1.0 + 3 * 2.0 ** -12): 1.0,                    # 0.75 of a TF32 step: dropped, not rounded up
+        f32_bits(-(1.0 + 3 * 2.0 ** -12)): -1.0,                # toward zero for negatives too
+        f32_bits(1.0 + 2.0 ** -10): 1.0 + 2.0 ** -10,           # one TF32 step is kept
+        f32_bits(1.0 + 2.0 ** -10 + 2.0 ** -11): 1.0 + 2.0 ** -10,
+        f32_bits(3.0): 3.0,
+        0x7F7FFFFF: (2.0 - 2.0 ** -10) * 2.0 ** 127,            # largest FP32 -> largest TF32
+        0x00000001: 0.0,                                         # smallest subnormal drops out
+        0x00002000: 2.0 ** -136,                                 # lowest kept subnormal bit
+        0x80000000: -0.0,
+        0x7F800000: math.inf,
+    }
+    bits = np.array(list(cases), dtype=np.uint32)
+    got = orc.decode(bits, TF32)
+    for b, g in zip(bits.tolist(), got.tolist()):
+        assert g == cases[b] and math.copysign(1, g) == math.copysign(1, cases[b]), hex(b)
+
+
+def test_tf32_decode_matches_struct_on_random_patterns(orc):
+    rng = np.random.default_rng(17)
+    bits = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]            # finite patterns
+    got = orc.decode(bits, TF32)
+    ref = np.array([float(tf32_exact(int(b))) for b in bits.tolist()])
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("layout", [KN, NK])
+def test_tf32_brute_force_rational(orc, layout):
+    """Random FP32 patterns in a bounded exponent range: every product of
+    two TF32 values has at most 22 significant bits, so the oracle is within
+    K * 2^-53 * bound of the exact rational sum of truncated values."""
+    rng = np.random.default_rng(400 + layout)
+    for _ in range(6):
+        M, N, K = (int(v) for v in rng.integers(1, 8, 3))
+        def pats(shape):
+            x = rng.standard_normal(shape).astype(np.float32) * np.float32(3.0)
+            return x.view(np.uint32)
+        A = pats((M, K))
+        B = pats((K, N) if layout == KN else (N, K))
+        ldb = N if layout == KN else K
+        C, R = orc.gemm(A, B, M, N, K, K, ldb, layout, TF32)
+        for i in range(M):
+            for j in range(N):
+                s, r = Fraction(0), Fraction(0)
+                for k in range(K):
+                    x = tf32_exact(int(A[i, k]))
+                    y = tf32_exact(int(B[k, j] if layout == KN else B[j, k]))
+                    s += x * y
+                    r += abs(x) * abs(y)
+                assert abs(Fraction(C[i, j]) - s) <= Fraction(K) * Fraction(2) ** -53 * r
+                assert R[i, j] == float(r)
+
+
+def test_tf32_equals_f16_on_values_both_hold_exactly(orc):
+    """FP16 values have 10 fraction bits, so in FP32 storage they are TF32
+    values already: the TF32 product equals the FP16 one exactly."""
+    M, N, K = 33, 21, 70
+    g = torch.Generator().manual_seed(8)
+    a16 = (torch.rand(M, K, generator=g) * 4 - 2).half()
+    b16 = (torch.rand(N, K, generator=g) * 4 - 2).half()
+    C16, R16 = orc.gemm(a16, b16, M, N, K, K, K, NK, F16)
+    C32, R32 = orc.gemm(a16.float(), b16.float(), M, N, K, K, K, NK, TF32)
+    assert np.array_equal(C16, C32) and np.array_equal(R16, R32)
+
+
+def test_tf32_integers_exact_and_low_bits_ignored(orc):
+    M, N, K = 16, 12, 50
+    g = torch.Generator().manual_seed(9)
+    a = torch.randint(-3, 4, (M, K), generator=g).float()
+    b = torch.randint(-3, 4, (K, N), generator=g).float()
+    want = a.double().numpy() @ b.double().numpy()
+    C, _ = orc.gemm(a, b, M, N, K, K, N, KN, TF32)
+    assert np.array_equal(C, want)
+    # setting any of the 13 dropped bits of every element leaves C unchanged
+    noise = torch.randint(0, 1 << 13, (M, K), generator=g, dtype=torch.int32)
+    a_noisy = (a.view(torch.int32) | torch.where(a != 0, noise, torch.zeros_like(noise))).view(torch.float32)
+    C2, _ = orc.gemm(a_noisy, b, M, N, K, K, N, KN, TF32)
+    assert np.array_equal(C2, want)
