@@ -158,17 +158,26 @@ def workload(name=WORKLOAD):
     return gen.WORKLOADS[name]
 
 
+def oracle_input(in_dtype: int) -> int:
+    """The oracle's code for an input type: FP32 operands are multiplied as
+    TF32, which the oracle names separately; the other codes coincide."""
+    import oracle
+    from dense_tiled_gemm_persistent_gb300 import inputs as gen
+    return oracle.TF32 if in_dtype == gen.F32 else in_dtype
+
+
 def cpu_oracle_sample(wl, a, b, budget_s: float, threads: int):
     """Time the oracle on rows [0, r) of C, r a multiple of the thread count
     chosen to fill about budget_s seconds; returns (TFLOPS, seconds, rows)."""
     import oracle
     lda, ldb = a.shape[1], b.shape[1]
+    dt_in = oracle_input(wl.in_dtype)
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, oracle.B_NK, oracle.F16, 0, threads, False, threads)
+    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, wl.b_layout, dt_in, 0, threads, False, threads)
     t_wave = time.perf_counter() - t0                     # one row per thread
     rows = min(wl.M, max(1, int(budget_s / max(t_wave, 1e-9))) * threads)
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, oracle.B_NK, oracle.F16, 0, rows, False, threads)
+    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, wl.b_layout, dt_in, 0, rows, False, threads)
     dt = time.perf_counter() - t0
     return tflops(rows, wl.N, wl.K, dt * 1e3), dt, rows
 
@@ -177,16 +186,17 @@ def run_reference(args, rank, world):
     """The reference arm: the CPU oracle as it stands, rank 0 only."""
     if rank != 0:
         return
-    wl = workload()
+    wl = workload(getattr(args, "workload", WORKLOAD))
     a, b = wl.operands()
     threads = os.cpu_count() or 1
+    dt_in = oracle_input(wl.in_dtype)
     total_budget = 120.0
     per_step = max(0.05, min(20.0, total_budget / max(args.steps + args.warmup, 1)))
     import oracle
     oracle.build()
     # rows per step: calibrate on one row per thread
     t0 = time.perf_counter()
-    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], oracle.B_NK, oracle.F16, 0,
+    oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], wl.b_layout, dt_in, 0,
                      threads, False, threads)
     t_wave = time.perf_counter() - t0
     rows = max(1, min(wl.M, int(per_step / max(t_wave, 1e-9)) * threads))
@@ -197,7 +207,7 @@ def run_reference(args, rank, world):
     for step in range(args.warmup + args.steps):
         r0 = (step * rows) % max(wl.M - rows + 1, 1)
         t0 = time.perf_counter()
-        oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], oracle.B_NK, oracle.F16, r0,
+        oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], wl.b_layout, dt_in, r0,
                          r0 + rows, False, threads)
         if step >= args.warmup:
             times.append(time.perf_counter() - t0)
@@ -397,14 +407,15 @@ def main():
     avg_launch = local_ms / args.steps
 
     peaks = measured_peaks()
-    # FP8 runs at twice the dense 16-bit tensor rate (4.5 vs 2.25 PFLOP/s nominal)
-    rate = 2.0 if gen.DTYPE_SIZE[wl.in_dtype] == 1 else 1.0
+    # nominal dense rates relative to FP16/BF16 (2.25 PFLOP/s): FP8 4.5, TF32 1.1
+    rate = {1: 2.0, 2: 1.0, 4: 1.1 / 2.25}[gen.DTYPE_SIZE[wl.in_dtype]]
     if peaks and peaks.get("bf16_tflops"):
         peak_t, src_t = rate * float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate equals bf16)"
         if rate != 1.0:
-            src_t = "measured cuBLAS bf16 burst x 2 (nominal FP8/BF16 dense ratio)"
+            src_t = "measured cuBLAS bf16 burst x %.3g (nominal %s/BF16 dense ratio)" % (
+                rate, "FP8" if rate > 1 else "TF32")
     else:
-        peak_t, src_t = rate * FALLBACK_TENSOR_TFLOPS, "fallback" + (" x 2 (FP8)" if rate != 1.0 else "")
+        peak_t, src_t = rate * FALLBACK_TENSOR_TFLOPS, "fallback" + (" x %.3g" % rate if rate != 1.0 else "")
     if peaks and peaks.get("hbm_gbs"):
         peak_h, src_h = float(peaks["hbm_gbs"]), "measured (copy)"
     else:

@@ -84,8 +84,17 @@ uint64_t wait_timeout_ns()
 
 size_t elem_size(int dt) { return dt == TGEMM_F32 ? 4 : (dt == TGEMM_E4M3 || dt == TGEMM_E5M2) ? 1 : 2; }
 bool is_f8(int dt) { return dt == TGEMM_E4M3 || dt == TGEMM_E5M2; }
+// Operands that only the tile kernels take (K-major B): FP8, and FP32 read as TF32.
+bool tile_only(int dt) { return is_f8(dt) || dt == TGEMM_F32; }
+int mma_kind(int in_dtype) { return is_f8(in_dtype) ? KIND_F8 : in_dtype == TGEMM_F32 ? KIND_TF32 : KIND_F16; }
 // K elements in one 128-byte k-block row
-int kblock_elems(int in_dtype) { return is_f8(in_dtype) ? 128 : kBK; }
+int kblock_elems(int in_dtype) { return (int)(128 / elem_size(in_dtype)); }
+// Instruction-descriptor operand type: kind::f16 0 F16 / 1 BF16, kind::f8f6f4
+// 0 E4M3 / 1 E5M2, kind::tf32 2.
+uint32_t mma_type(int in_dtype)
+{
+    return in_dtype == TGEMM_F32 ? 2u : (in_dtype == TGEMM_BF16 || in_dtype == TGEMM_E5M2) ? 1u : 0u;
+}
 
 // Current device's state; allocates the status word on first use.
 tgemm_status device_state(DeviceState **out)
@@ -137,8 +146,7 @@ tgemm_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         return TGEMM_ERR_INVALID_ARG;
     if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
         return TGEMM_ERR_INVALID_ARG;
-    if (in_dtype == TGEMM_F32) return TGEMM_ERR_UNSUPPORTED;   // FP32 operands are not provided
-    if (is_f8(in_dtype) && b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;   // FP8: K-major B only
+    if (tile_only(in_dtype) && b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;   // FP8/TF32: K-major B only
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
     // Tensor coordinates are signed 32-bit.
     const int64_t kMax = (int64_t)1 << 31;
@@ -160,7 +168,7 @@ tgemm_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     return TGEMM_OK;
 }
 
-const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int cluster, int f8 = 0)
+const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int cluster, int kind = KIND_F16)
 {
     const KernelVariant *tab = nullptr;
     int n = 0;
@@ -172,7 +180,7 @@ const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int clu
     }
     for (int i = 0; i < n; ++i)
         if (tab[i].bn == bn && tab[i].stages == stages && tab[i].b_mn == b_mn && tab[i].cluster == cluster &&
-            tab[i].f8 == f8)
+            tab[i].kind == kind)
             return &tab[i];
     return nullptr;
 }
@@ -465,13 +473,13 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
                           const KernelVariant **v, int in_dtype = TGEMM_F16)
 {
     if (c.bk != kBK || c.grid < 0 || c.group_m < 1) return TGEMM_ERR_UNSUPPORTED;
-    if (is_f8(in_dtype)) {
-        // FP8: the tile kernels, K-major B (bk names the 128-byte k-block)
+    if (tile_only(in_dtype)) {
+        // FP8 / TF32: the tile kernels, K-major B (bk names the 128-byte k-block)
         if (c.swap_ab != 0 || b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
         if (!(c.split_k == 1 || (c.split_k == 0 && c.cluster_m == 2))) return TGEMM_ERR_UNSUPPORTED;
         if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
             return TGEMM_ERR_UNSUPPORTED;
-        *v = find_variant(c.bn, c.stages, out_dtype, 0, c.cluster_m, 1);
+        *v = find_variant(c.bn, c.stages, out_dtype, 0, c.cluster_m, mma_kind(in_dtype));
         return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
     }
     const int b_mn = b_layout == TGEMM_B_KN ? 1 : 0;
@@ -764,8 +772,8 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
             // are not batched: the wave model over the tiles of all batches.
             choose_config_model(M > 64 ? M : 65, N, K, dev->sm_count, &cfg, bt.count);
         }
-        if (is_f8(in_dtype) && cfg.swap_ab) {
-            // the skinny kernels take 16-bit operands: the tile kernels for FP8
+        if (tile_only(in_dtype) && cfg.swap_ab) {
+            // the skinny kernels take 16-bit operands: the tile kernels for FP8 and TF32
             choose_config_model(65, N, K, dev->sm_count, &cfg, bt.count);
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
@@ -810,7 +818,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     p.num_kb = (int32_t)ceil_div(K, kbe);
     p.group_m = cfg.group_m;
     // kind::f16: type codes 0 F16 / 1 BF16; kind::f8f6f4: 0 E4M3 / 1 E5M2
-    p.idesc = make_idesc(in_dtype == TGEMM_BF16 || in_dtype == TGEMM_E5M2, b_mn, cfg.bm, cfg.bn);
+    p.idesc = make_idesc(mma_type(in_dtype), b_mn, cfg.bm, cfg.bn);
     p.debug_flags = debug_flags;
     p.status = dev->status;
     p.timeout_ns = wait_timeout_ns();
@@ -908,8 +916,8 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
 {
     if (!out_cfg) return TGEMM_ERR_INVALID_ARG;
     if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
-    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16 && !is_f8(in_dtype)) return TGEMM_ERR_UNSUPPORTED;
-    if (is_f8(in_dtype) && b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
+    if (in_dtype != TGEMM_F16 && in_dtype != TGEMM_BF16 && !tile_only(in_dtype)) return TGEMM_ERR_INVALID_ARG;
+    if (tile_only(in_dtype) && b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
     if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
         return TGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
@@ -917,7 +925,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     tgemm_status st = device_state(&dev);
     if (st != TGEMM_OK) return st;
     choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, dev->sm_count, out_cfg);
-    if (is_f8(in_dtype) && out_cfg->swap_ab) choose_config_model(65, N, K, dev->sm_count, out_cfg);
+    if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(65, N, K, dev->sm_count, out_cfg);
     return TGEMM_OK;
 }
 

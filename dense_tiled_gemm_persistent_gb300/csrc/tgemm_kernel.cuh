@@ -47,10 +47,28 @@ namespace tgemm {
 constexpr int kBM = 128;           // rows of one CTA tile = TMEM lanes
 constexpr int kBK = 64;            // K depth of one stage: 64 x 2 bytes = one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
-// FP8 operands keep the byte geometry: a 128-byte row holds 128 elements and
-// one kind::f8f6f4 MMA covers K = 32 (32 bytes), so every shared-memory
-// offset is the same and only the element count of a k-block doubles.
-template <bool F8> struct KBlock { static constexpr int elems = F8 ? 128 : 64; };
+// Operand kinds.  FP8 and TF32 operands keep the 16-bit byte geometry: a
+// 128-byte row holds 128 FP8 or 32 FP32 elements and one MMA covers 32 bytes
+// of K (K = 32 for kind::f8f6f4, 8 for kind::tf32), so every shared-memory
+// offset is the same and only the element count of a k-block changes.
+enum { KIND_F16 = 0, KIND_F8 = 1, KIND_TF32 = 2 };
+template <int KIND> struct KBlock { static constexpr int elems = KIND == KIND_F8 ? 128 : KIND == KIND_TF32 ? 32 : 64; };
+
+// One MMA of the operand kind, issued by the CTA (PAIR false) or by the
+// leader of a CTA pair (PAIR true).
+template <int KIND, bool PAIR>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
+{
+    if constexpr (PAIR) {
+        if constexpr (KIND == KIND_F8) ptx::mma_f8_ss_pair(d_tmem, ad, bd, idesc, acc);
+        else if constexpr (KIND == KIND_TF32) ptx::mma_tf32_ss_pair(d_tmem, ad, bd, idesc, acc);
+        else ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, acc);
+    } else {
+        if constexpr (KIND == KIND_F8) ptx::mma_f8_ss(d_tmem, ad, bd, idesc, acc);
+        else if constexpr (KIND == KIND_TF32) ptx::mma_tf32_ss(d_tmem, ad, bd, idesc, acc);
+        else ptx::mma_f16_ss(d_tmem, ad, bd, idesc, acc);
+    }
+}
 constexpr int kThreads = 192;      // 6 warps
 constexpr int kEpiWarps = 4;
 constexpr uint32_t kStageCBytes = 32 * 128;   // one staged 32-row x 128-byte block of C
@@ -83,12 +101,14 @@ constexpr uint64_t kDescMNMajor = desc_sw128(kBK * 128, 1024);
 
 // ---- instruction descriptor (kind::f16) -------------------------------------
 //
-// Bits 4-5 D type (1 = F32), 7-9 A type and 10-12 B type (0 = F16, 1 = BF16),
-// 15 A major and 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16, bool b_mn_major, int m, int n,
+// Bits 4-5 D type (1 = F32), 7-9 A type and 10-12 B type (kind::f16: 0 F16,
+// 1 BF16; kind::f8f6f4: 0 E4M3, 1 E5M2; kind::tf32: 2 TF32), 15 A major and
+// 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.  The same layout
+// serves the three kinds.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_type, bool b_mn_major, int m, int n,
                                                   bool a_mn_major = false)
 {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+    return (1u << 4) | ((ab_type & 7u) << 7) | ((ab_type & 7u) << 10) |
            ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
 }
@@ -355,10 +375,10 @@ __device__ __forceinline__ void epilogue_drain(const CUtensorMap *map, int32_t r
     }
 }
 
-template <int BN, int STAGES, int OUT, bool B_MN, bool F8 = false>
+template <int BN, int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
 __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p)
 {
-    static_assert(!(F8 && B_MN), "FP8 operands are K-major only");
+    static_assert(KIND == KIND_F16 || !B_MN, "FP8 and TF32 operands are K-major only");
     using Plan = SmemPlan<BN, STAGES>;
     constexpr uint32_t kStageBytes = Plan::a_stage + Plan::b_stage;
     constexpr uint32_t kTmemCols = TmemCols<BN>::value;
@@ -442,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                     if (!skip) {
                         const uint32_t fb = full_bar(s);
                         ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                        const int32_t k0 = kb * KBlock<F8>::elems;
+                        const int32_t k0 = kb * KBlock<KIND>::elems;
                         ptx::tma_load_3d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
                         if (B_MN) {
 #pragma unroll
@@ -498,8 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
                         const uint64_t bd = B_MN ? desc_at(kDescMNMajor, b_addr + k * (kUmmaK * 128))
                                                  : desc_at(kDescKMajor, b_addr + k * (kUmmaK * 2));
-                        if constexpr (F8) ptx::mma_f8_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
-                        else ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_issue<KIND, false>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(empty_bar(s));       // stage reusable once these MMAs finish
                     if (++s == STAGES) {
@@ -556,10 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     }
 }
 
-template <int BN, int STAGES, int OUT, bool B_MN, bool F8 = false>
+template <int BN, int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = gemm_persistent_kernel<BN, STAGES, OUT, B_MN, F8>;
+    auto kern = gemm_persistent_kernel<BN, STAGES, OUT, B_MN, KIND>;
     constexpr uint32_t smem = SmemPlan<BN, STAGES>::alloc_bytes;
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
@@ -574,7 +593,7 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
 
 #define TGEMM_VARIANT(BN, ST, OUT, BMN) \
     {BN, ST, OUT, BMN, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, (BMN) != 0>, 1, nullptr}
-#define TGEMM_VARIANT_F8(BN, ST, OUT) \
-    {BN, ST, OUT, 0, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, false, true>, 1, nullptr, 1}
+#define TGEMM_VARIANT_KIND(BN, ST, OUT, KIND) \
+    {BN, ST, OUT, 0, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, false, KIND>, 1, nullptr, KIND}
 
 }  // namespace tgemm

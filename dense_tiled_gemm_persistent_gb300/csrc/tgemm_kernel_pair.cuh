@@ -95,10 +95,10 @@ struct PairWorkIter {
     }
 };
 
-template <int STAGES, int OUT, bool B_MN, bool F8 = false>
+template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
 __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p)
 {
-    static_assert(!(F8 && B_MN), "FP8 operands are K-major only");
+    static_assert(KIND == KIND_F16 || !B_MN, "FP8 and TF32 operands are K-major only");
     constexpr int kHalfN = kPairBN / 2;
     using Plan = SmemPlan<kHalfN, STAGES>;                 // A 16 KiB + B 16 KiB per stage
     constexpr uint32_t kPairStageBytes = 2 * (Plan::a_stage + Plan::b_stage);
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     }
                     const uint32_t fb = ptx::map_to_cta(full_bar(s), 0);   // the leader's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);
-                    const int32_t k0 = kb * KBlock<F8>::elems;
+                    const int32_t k0 = kb * KBlock<KIND>::elems;
                     ptx::tma_load_3d_pair(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
                     if (B_MN) {
 #pragma unroll
@@ -247,8 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
                         const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
                         const uint64_t bd = desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
-                        if constexpr (F8) ptx::mma_f8_ss_pair(d_tmem, ad, bd, p.idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
-                        else ptx::mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
+                        mma_issue<KIND, true>(d_tmem, ad, bd, p.idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(empty_bar(s), 0x3);   // stage s free in both CTAs
                     if (++s == STAGES) {
@@ -433,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
     }
 }
 
-template <int STAGES, int OUT, bool B_MN, bool F8 = false>
+template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
 cudaError_t launch_gemm_pair(const GemmParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = gemm_pair_kernel<STAGES, OUT, B_MN, F8>;
+    auto kern = gemm_pair_kernel<STAGES, OUT, B_MN, KIND>;
     constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
@@ -457,10 +456,10 @@ cudaError_t launch_gemm_pair(const GemmParams &p, int grid, cudaStream_t stream)
 }
 
 // Number of CTA pairs of this kernel that can be resident at once.
-template <int STAGES, int OUT, bool B_MN, bool F8 = false>
+template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
 int max_active_pairs()
 {
-    auto kern = gemm_pair_kernel<STAGES, OUT, B_MN, F8>;
+    auto kern = gemm_pair_kernel<STAGES, OUT, B_MN, KIND>;
     constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 0;
@@ -486,8 +485,8 @@ int max_active_pairs()
 #define TGEMM_PAIR_VARIANT(ST, OUT, BMN)                                                              \
     {256, ST, OUT, BMN, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_pair<ST, OUT, (BMN) != 0>, \
      2, &max_active_pairs<ST, OUT, (BMN) != 0>}
-#define TGEMM_PAIR_VARIANT_F8(ST, OUT)                                                                    \
-    {256, ST, OUT, 0, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_pair<ST, OUT, false, true>, 2, \
-     &max_active_pairs<ST, OUT, false, true>, 1}
+#define TGEMM_PAIR_VARIANT_KIND(ST, OUT, KIND)                                                            \
+    {256, ST, OUT, 0, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_pair<ST, OUT, false, KIND>, 2, \
+     &max_active_pairs<ST, OUT, false, KIND>, KIND}
 
 }  // namespace tgemm

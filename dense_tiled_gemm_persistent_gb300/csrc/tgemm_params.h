@@ -81,7 +81,7 @@ struct KernelVariant {
     LaunchFn launch;
     int cluster;
     OccupancyFn max_active;
-    int f8 = 0;            // 1: FP8 operands (kind::f8f6f4), 128 elements per k-block
+    int kind = 0;          // operand kind: 0 FP16/BF16 (kind::f16), 1 FP8 (kind::f8f6f4), 2 TF32 (kind::tf32)
 };
 
 // Defined in the kernel translation units (one per output type).

@@ -129,7 +129,7 @@ class Workload:
 
 
 # The five problem families the benchmark configuration lists, by shape, and
-# the FP8 form of the square one.
+# the FP8 and FP32 (multiplied as TF32) forms of the square one.
 WORKLOADS = {
     w.name: w for w in [
         Workload("gemm_256x256x256_f16_kn_f32", 256, 256, 256, F16, F32, B_KN,
@@ -148,5 +148,7 @@ WORKLOADS = {
                  normal(0, 1), normal(0, 0.02), 4),
         Workload("gemm_8192x8192x8192_e4m3_nk_bf16", 8192, 8192, 8192, E4M3, BF16, B_NK,
                  normal(0, 1), normal(0, 1), 5),
+        Workload("gemm_8192x8192x8192_tf32_nk_f32", 8192, 8192, 8192, F32, F32, B_NK,
+                 uniform(-0.5, 0.5), uniform(-0.5, 0.5), 6),
     ]
 }

@@ -12,7 +12,7 @@ import ctypes
 import os
 import threading
 
-F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4   # FP8 codes: inputs only, B stored N x K
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4   # FP8 inputs only; FP8/FP32 inputs: B stored N x K
 B_KN, B_NK = 0, 1
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_OOM, ERR_TIMEOUT = range(8)
@@ -183,10 +183,10 @@ def _stream_handle(stream):
 def matmul(A, B, b_layout: int = B_NK, out_dtype=None, C=None, stream=None, config: Config = None):
     """C = A @ B on the GPU through tgemm_run (or tgemm_run_config).
 
-    A: (M, K) row-major CUDA tensor, FP16, BF16 or FP8 (float8_e4m3fn,
-    float8_e5m2).  B: (K, N) for B_KN or (N, K) for B_NK, same dtype (FP8:
-    B_NK only).  C: optional (M, N) output (allocated with torch.empty when
-    omitted, dtype out_dtype, else A.dtype for 16-bit inputs and BF16 for FP8).
+    A: (M, K) row-major CUDA tensor, FP16, BF16, FP8 (float8_e4m3fn,
+    float8_e5m2) or FP32 (multiplied as TF32).  B: (K, N) for B_KN or (N, K)
+    for B_NK, same dtype (FP8 and FP32: B_NK only).  C: optional (M, N) output (allocated with torch.empty when
+    omitted, dtype out_dtype, else BF16 for FP8 inputs and A.dtype otherwise).
     """
     import torch
     if not (A.is_cuda and B.is_cuda):
@@ -199,7 +199,7 @@ def matmul(A, B, b_layout: int = B_NK, out_dtype=None, C=None, stream=None, conf
     if kb != K:
         raise ValueError("inner dimensions differ")
     if C is None:
-        default = A.dtype if A.element_size() == 2 else torch.bfloat16
+        default = torch.bfloat16 if A.element_size() == 1 else A.dtype
         C = torch.empty((M, N), dtype=out_dtype or default, device=A.device)
     args = (M, N, K, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), b_layout, C.data_ptr(), _ld(C),
             _dtype_code(A.dtype), _dtype_code(C.dtype), _stream_handle(stream))

@@ -44,7 +44,12 @@ typedef enum { TGEMM_B_KN = 0, TGEMM_B_NK = 1 } tgemm_b_layout;
 /* Element types.  FP8 (E4M3 "fn" variant with no infinities, E5M2) is an
  * input type only: both operands the same FP8 type, B stored N x K, FP32
  * accumulation, FP16/BF16/FP32 output (scale factors go in the epilogue's
- * alpha). */
+ * alpha).  TGEMM_F32 as in_dtype means FP32 operands multiplied on the
+ * tensor cores as TF32: each element's low 13 fraction bits are dropped
+ * (truncation toward zero, as the tensor core reads 32-bit containers), the
+ * products are summed in FP32; B stored N x K.  The cuTile tutorial gives
+ * FP32 operands their own tile shape ("Launching the kernel from the host")
+ * without saying how they are multiplied. */
 typedef enum { TGEMM_F16 = 0, TGEMM_BF16 = 1, TGEMM_F32 = 2, TGEMM_E4M3 = 3, TGEMM_E5M2 = 4 } tgemm_dtype;
 
 typedef enum {
@@ -75,8 +80,10 @@ typedef struct {
 } tgemm_config;
 
 /*
- * C = A * B.  in_dtype (TGEMM_F16 or TGEMM_BF16) is the type of both A and
- * B; out_dtype is TGEMM_F16, TGEMM_BF16 or TGEMM_F32.  M, N or K may be 0:
+ * C = A * B.  in_dtype (TGEMM_F16, TGEMM_BF16, TGEMM_E4M3, TGEMM_E5M2 or
+ * TGEMM_F32, see tgemm_dtype) is the type of both A and B; out_dtype is
+ * TGEMM_F16, TGEMM_BF16 or TGEMM_F32.  FP8 and FP32 operands need B stored
+ * N x K (TGEMM_B_NK), else TGEMM_ERR_UNSUPPORTED.  M, N or K may be 0:
  * M = 0 or N = 0 is a no-op; K = 0 writes zeros (the empty sum).
  * Returns TGEMM_OK once the work is enqueued on `stream`.
  */

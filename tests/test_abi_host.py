@@ -78,7 +78,9 @@ FAKE = 1 << 20   # a 16-byte aligned non-null address, never dereferenced by hos
     (dict(layout=7), tgemm.ERR_INVALID_ARG),
     (dict(ind=5), tgemm.ERR_INVALID_ARG),
     (dict(out=9), tgemm.ERR_INVALID_ARG),
-    (dict(ind=tgemm.F32), tgemm.ERR_UNSUPPORTED),     # FP32 operands are not provided
+    (dict(ind=tgemm.F32, layout=tgemm.B_KN, ldb=96), tgemm.ERR_UNSUPPORTED),    # TF32 operands: B N x K only
+    (dict(ind=tgemm.E4M3, layout=tgemm.B_KN, ldb=96), tgemm.ERR_UNSUPPORTED),   # FP8 operands: B N x K only
+    (dict(ind=tgemm.E5M2, lda=72), tgemm.ERR_MISALIGNED),                       # 72-byte FP8 rows
     (dict(M=1 << 31), tgemm.ERR_UNSUPPORTED),
 ])
 def test_host_argument_checks(lib, case, expect):

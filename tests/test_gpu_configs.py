@@ -40,7 +40,12 @@ def run_default(wl, a, b):
 FULL = ["gemm_256x256x256_f16_kn_f32", "proj_16x4096x4096_bf16_nk_bf16"]
 SAMPLED = ["gemm_4000x3000x5000_bf16_nk_bf16", "gemm_4096x4096x4096_f16_kn_f16",
            "gemm_8192x8192x8192_f16_nk_f16", "proj_16384x14336x4096_bf16_nk_bf16",
-           "gemm_8192x8192x8192_e4m3_nk_bf16"]
+           "gemm_8192x8192x8192_e4m3_nk_bf16", "gemm_8192x8192x8192_tf32_nk_f32"]
+
+
+def orc_in(wl):
+    """The oracle's input code: FP32 operands are multiplied as TF32."""
+    return oracle.TF32 if wl.in_dtype == gen.F32 else wl.in_dtype
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -68,7 +73,7 @@ def test_config_sampled(name):
     ii, jj = sampled_points(wl.M, wl.N, seed=wl.seed)
     got = C[torch.from_numpy(ii).to("cuda:0"), torch.from_numpy(jj).to("cuda:0")].double().cpu().numpy()
     ref, bound = oracle.gemm_elements(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], wl.b_layout,
-                                      wl.in_dtype, ii, jj)
+                                      orc_in(wl), ii, jj)
     assert len(ii) >= 4096
     assert_close(got, ref, bound, wl.out_dtype, name)
     # every boundary row/column of the sample is fully present
