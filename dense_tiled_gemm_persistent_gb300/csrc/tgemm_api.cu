@@ -570,11 +570,24 @@ tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *str
     p->sk_units = 0;
     const int64_t full = T / P, rem = T % P;
     if (rem == 0) return TGEMM_OK;
-    const int64_t dp = full >= 1 ? (full - 1) * P : 0;
-    const int64_t sk_tiles = T - dp;
+    int64_t dp, sk_tiles, units;
+    if (full >= 1 && 2 * rem <= P) {
+        // The leftover wave is at most half full: keep every full wave whole
+        // and cut each leftover tile into s = P / rem equal k-ranges, one per
+        // pair, so the tail takes 1/s of a tile's time.
+        dp = full * P;
+        sk_tiles = rem;
+        units = (P / rem) * rem;
+        if (KB / (P / rem) < kMinSkIters) units = (KB / kMinSkIters) * rem;
+        if (units > P) units = P;
+    } else {
+        // Share the last full wave and the leftover tiles among all pairs.
+        dp = full >= 1 ? (full - 1) * P : 0;
+        sk_tiles = T - dp;
+        units = sk_tiles * KB / kMinSkIters;
+        if (units > P) units = P;
+    }
     const int64_t total = sk_tiles * KB;
-    int64_t units = total / kMinSkIters;
-    if (units > P) units = P;
     if (units <= sk_tiles && full == 0) return TGEMM_OK;   // no more pairs than tiles to share with
     if (units < 2) return TGEMM_OK;
     if (2 * sk_tiles * 4 > (int64_t)kCounterBytes) return TGEMM_OK;

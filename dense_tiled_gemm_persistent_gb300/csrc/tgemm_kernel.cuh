@@ -505,23 +505,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                for (int kb = 0; kb < p.num_kb;) {
+                    // Two k-blocks in adjacent stages per pass (one fence, one
+                    // loop overhead for both): the lone issuing thread's
+                    // per-k-block overhead would otherwise idle the tensor pipe.
+                    const int n = (kb + 1 < p.num_kb && s + 1 < STAGES) ? 2 : 1;
+                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL) ||
+                        (n == 2 && !wait_bounded(full_bar(s + 1), ph, wc, SITE_MMA_FULL))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t a_addr = sA + s * Plan::a_stage;
-                    const uint32_t b_addr = sB + s * Plan::b_stage;
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
-                        const uint64_t bd = B_MN ? desc_at(kDescMNMajor, b_addr + k * (kUmmaK * 128))
-                                                 : desc_at(kDescKMajor, b_addr + k * (kUmmaK * 2));
-                        mma_issue<KIND, false>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < n) {
+                            const uint32_t a_addr = sA + (s + h) * Plan::a_stage;
+                            const uint32_t b_addr = sB + (s + h) * Plan::b_stage;
+#pragma unroll
+                            for (int k = 0; k < kBK / kUmmaK; ++k) {
+                                const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
+                                const uint64_t bd = B_MN ? desc_at(kDescMNMajor, b_addr + k * (kUmmaK * 128))
+                                                         : desc_at(kDescKMajor, b_addr + k * (kUmmaK * 2));
+                                mma_issue<KIND, false>(d_tmem, ad, bd, p.idesc, ((kb + h) | k) != 0 ? 1u : 0u);
+                            }
+                            ptx::mma_commit(empty_bar(s + h));   // stage reusable once these MMAs finish
+                        }
                     }
-                    ptx::mma_commit(empty_bar(s));       // stage reusable once these MMAs finish
-                    if (++s == STAGES) {
+                    kb += n;
+                    s += n;
+                    if (s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }

@@ -235,22 +235,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * kPairBN;
-                for (int kb = w.k0; kb < w.k1; ++kb) {
-                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                for (int kb = w.k0; kb < w.k1;) {
+                    // Two k-blocks in adjacent stages per pass (one fence, one
+                    // loop overhead for both): the lone issuing thread's
+                    // per-k-block overhead would otherwise idle the tensor pipe.
+                    const int n = (kb + 1 < w.k1 && s + 1 < STAGES) ? 2 : 1;
+                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL) ||
+                        (n == 2 && !wait_bounded(full_bar(s + 1), ph, wc, SITE_MMA_FULL))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t a_addr = sA + s * Plan::a_stage;
-                    const uint32_t b_addr = sB + s * Plan::b_stage;
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
-                        const uint64_t bd = desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
-                        mma_issue<KIND, true>(d_tmem, ad, bd, p.idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < n) {
+                            const uint32_t a_addr = sA + (s + h) * Plan::a_stage;
+                            const uint32_t b_addr = sB + (s + h) * Plan::b_stage;
+#pragma unroll
+                            for (int k = 0; k < kBK / kUmmaK; ++k) {
+                                const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
+                                const uint64_t bd =
+                                    desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
+                                mma_issue<KIND, true>(d_tmem, ad, bd, p.idesc, (kb + h > w.k0 || k > 0) ? 1u : 0u);
+                            }
+                            ptx::mma_commit_pair(empty_bar(s + h), 0x3);   // the stage is free in both CTAs
+                        }
                     }
-                    ptx::mma_commit_pair(empty_bar(s), 0x3);   // stage s free in both CTAs
-                    if (++s == STAGES) {
+                    kb += n;
+                    s += n;
+                    if (s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
