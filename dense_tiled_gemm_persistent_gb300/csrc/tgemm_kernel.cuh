@@ -560,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             const uint32_t buf = local & 1u;
             const uint32_t bph = (local >> 1) & 1u;
-            if (!warp_wait_idle(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL, lane)) break;
+            const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
+            if (!__all_sync(0xffffffffu, got)) break;
             ptx::tc_fence_after_sync();
 
             int64_t tr, tc;

@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         for (; items.next(w); ++local) {
             const uint32_t buf = local & 1u;
             const uint32_t bph = (local >> 1) & 1u;
-            const bool got = warp_wait_idle(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL, lane);
+            const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
             // The four epilogue warps decide together (the stream-K hand-off
             // below synchronises them, so none may leave alone).
             if (!ptx::named_barrier_and(2, kEpiWarps * 32, got)) {

@@ -61,22 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// try_wait with a suspend-time hint: a thread whose phase is not complete
-// sleeps until it completes or about hint_ns nanoseconds pass, instead of
-// returning at once (for waits that are long and not latency critical).
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return done != 0;
-}
-
 // ---- TMA -------------------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tensormap(const void *map)

@@ -58,33 +58,4 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     return wait_slow(bar, parity, w, site, honour_abort);
 }
 
-// The epilogue's wait for a finished accumulator lasts a whole tile's
-// mainloop.  One lane waits here with suspend-time hints (the warp waits in
-// __syncwarp meanwhile), so 128 epilogue threads do not spin on the barrier
-// for tens of microseconds, which costs issue slots and power on a
-// power-capped part.  A completed phase still wakes the thread at once.
-static __device__ __noinline__ bool wait_idle_slow(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site)
-{
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (uint32_t poll = 1;; ++poll) {
-        if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if ((poll & 7u) == 0) {
-            if (*w.abort_flag) return false;
-            if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
-                record_fault(w, site);
-                return false;
-            }
-        }
-    }
-}
-
-// Called by all 32 lanes of a warp; returns the same answer in each.
-__device__ __forceinline__ bool warp_wait_idle(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site,
-                                               int lane)
-{
-    int got = 1;
-    if (lane == 0 && !ptx::mbar_try_wait(bar, parity)) got = wait_idle_slow(bar, parity, w, site) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, got, 0) != 0;
-}
-
 }  // namespace tgemm
