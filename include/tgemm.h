@@ -211,9 +211,11 @@ tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream);
  * that loads the library, until the process exits) and never calls
  * cudaMalloc, cudaFree or any allocating routine.
  *
- * Same arguments and result as tgemm_run (C = A * B, same layouts, dtypes
- * and alignment rules), computed by the same swap-AB split-K kernel, with
- * these limits:
+ * Same arguments and result as tgemm_run (C = A * B, same layouts and
+ * alignment rules), computed by the same swap-AB split-K kernel, with these
+ * limits:
+ *   - in_dtype TGEMM_F16 or TGEMM_BF16 (FP8 and FP32 operands return
+ *     TGEMM_ERR_UNSUPPORTED);
  *   - 0 <= M <= 64 and N <= 524288 (4096 column tiles of 128); larger sizes
  *     return TGEMM_ERR_UNSUPPORTED before anything is launched;
  *   - every call shares the one array, so calls whose work overlaps on the
