@@ -506,15 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * BN;
                 for (int kb = 0; kb < p.num_kb;) {
-                    // Two k-blocks in adjacent stages per pass (one fence, one
-                    // loop overhead for both): the lone issuing thread's
-                    // per-k-block overhead would otherwise idle the tensor pipe.
-                    const int n = (kb + 1 < p.num_kb && s + 1 < STAGES) ? 2 : 1;
-                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL) ||
-                        (n == 2 && !wait_bounded(full_bar(s + 1), ph, wc, SITE_MMA_FULL))) {
+                    // Two k-blocks in adjacent stages per pass when the second
+                    // one's data is already in (one fence, one loop overhead for
+                    // both): the lone issuing thread's per-k-block overhead would
+                    // otherwise idle the tensor pipe.  The second stage is only
+                    // tested, never waited for, so a tile's first MMAs are not
+                    // held back while the ring fills.
+                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
+                    const int n =
+                        (kb + 1 < p.num_kb && s + 1 < STAGES && ptx::mbar_test_wait(full_bar(s + 1), ph)) ? 2 : 1;
                     ptx::tc_fence_after_sync();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
