@@ -35,9 +35,9 @@ FALLBACK_TENSOR_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
 GRAPH_FLOPS = 1e11
-KERNEL_SOURCES = ["tgemm_kernel.cuh", "tgemm_kernel_pair.cuh", "tgemm_kernel_skinny.cuh",
-                  "tgemm_kernel_splitk_cluster.cuh", "tgemm_ptx.cuh", "tgemm_wait.cuh", "tgemm_sched.h",
-                  "tgemm_params.h"]
+KERNEL_SOURCES = ["tgemm_kernel.cuh", "tgemm_kernel_pair.cuh", "tgemm_kernel_quad.cuh",
+                  "tgemm_kernel_skinny.cuh", "tgemm_kernel_splitk_cluster.cuh", "tgemm_ptx.cuh", "tgemm_wait.cuh",
+                  "tgemm_sched.h", "tgemm_params.h"]
 
 
 def tflops(M: int, N: int, K: int, ms: float) -> float:

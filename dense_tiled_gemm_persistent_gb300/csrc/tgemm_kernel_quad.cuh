@@ -1,0 +1,329 @@
+// Persistent GEMM on clusters of two CTA pairs ("quads"): one 256 x 512
+// output block per cluster of four CTAs, pair q (ranks 2q, 2q + 1) computing
+// the 256 x 256 tile in columns [n0 + 256 q, n0 + 256 q + 256).
+//
+// Both pairs need the same 256 rows of A, so each A half-tile is fetched once
+// for the two pairs: CTA 2q + r (r = rank in its pair) loads rows
+// [m0 + 128 r + 64 q, + 64) of the k-block and multicasts them to CTAs r and
+// r + 2, which each receive the full 128 rows of their half from the two
+// loads.  B is loaded by each CTA for itself, as in the pair kernel.  Per CTA
+// and k-block that is 24 KiB of TMA requests instead of 32 KiB: a quarter
+// less L2 -> SM traffic and TMA request rate for the same tensor work, which
+// matters where rows of A and B are not 128-byte aligned (every box row then
+// straddles two cache lines) and for the energy of a power-capped GEMM.
+// Multicast stays inside one GPU's memory.
+//
+// Synchronisation (per stage s, per accumulator buffer b):
+//   full[s]       in each pair leader; armed with the pair's 64 KiB, completed by
+//                 the pair's B loads and by the A loads of both pairs (a
+//                 multicast load signals each destination's pair leader);
+//   empty[s]      in all four CTAs, count 2: both pair leaders' MMA commits
+//                 arrive on every CTA, since a stage is refilled only when
+//                 neither pair still reads it (its A rows come from both);
+//   tmem_full[b]  in both CTAs of a pair; that pair's leader commits;
+//   tmem_empty[b] in each pair leader; the pair's eight epilogue warps arrive.
+// Every wait is bounded (tgemm_wait.cuh); a timeout raises the abort flag in
+// all four CTAs, which then wind down as the pair kernel does.  Whole tiles
+// only (no stream-K tail); when the tile columns are odd the second pair of
+// the last block column computes a tile past N (its B reads zeros, its
+// stores are skipped) so that it still feeds its partner's A.
+#pragma once
+
+#include "tgemm_kernel_pair.cuh"
+
+namespace tgemm {
+
+constexpr int kQuadBN = 2 * kPairBN;    // columns of a quad block
+
+template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
+__global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_constant__ GemmParams p)
+{
+    static_assert(KIND == KIND_F16 || !B_MN, "FP8 and TF32 operands are K-major only");
+    constexpr int kHalfN = kPairBN / 2;
+    using Plan = SmemPlan<kHalfN, STAGES>;                 // A 16 KiB + B 16 KiB per stage
+    constexpr uint32_t kPairStageBytes = 2 * (Plan::a_stage + Plan::b_stage);
+    constexpr uint32_t kAHalfBytes = Plan::a_stage / 2;     // 64 rows of A
+    constexpr uint32_t kTmemCols = 512;
+    static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base + Plan::a_off;
+    const uint32_t sB = base + Plan::b_off;
+    const uint32_t sC = base + Plan::c_off;
+    const uint32_t bar = base + Plan::bar_off;
+    auto full_bar = [&](int s) { return bar + 8u * s; };
+    auto empty_bar = [&](int s) { return bar + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar + 8u * (2 * STAGES + 4);
+    const uint32_t slot = base + Plan::slot_off;
+    const uint32_t abort_addr = base + Plan::abort_off;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t crank = ptx::cluster_ctarank();          // 0..3
+    const uint32_t q = crank >> 1;                          // pair of the quad
+    const uint32_t rank = crank & 1u;                       // rank in the pair
+    const uint32_t pair_leader = 2u * q;
+    const bool leader = rank == 0;
+    const uint16_t pair_mask = (uint16_t)(0x3u << (2u * q));
+    const uint16_t a_mask = (uint16_t)((1u << rank) | (1u << (rank + 2u)));   // this A half's two holders
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 2);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(drain_bar + 8u * (1 + w), 1);   // C_in loads
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&p.tma_a);
+        ptx::prefetch_tensormap(&p.tma_b);
+        ptx::prefetch_tensormap(&p.tma_c);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(slot, kTmemCols);
+        ptx::tmem_relinquish_pair();
+        ptx::tc_fence_before_sync();
+    }
+    __syncthreads();
+    ptx::cluster_sync();          // all four CTAs' barriers initialised, both pairs' TMEM allocated
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
+
+    WaitCtx wc{p.status, abort_flag, p.timeout_ns};
+    wc.peer_mask = 0xFu & ~(1u << crank);
+    wc.abort_local = abort_addr;
+    const int cluster_id = blockIdx.x >> 2;
+    const int num_clusters = gridDim.x >> 2;
+    bool aborted = false;
+
+    // Block number -> (batch, block row, this pair's tile column).
+    auto block_coord = [&](int blk, int &bz, int64_t &tr, int64_t &tc) {
+        int64_t tcq;
+        bz = blk / p.tiles_per_batch;
+        grouped_tile(p.tiles_m, p.tiles_n, p.group_m, blk - bz * p.tiles_per_batch, tr, tcq);
+        tc = 2 * tcq + q;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int blk = cluster_id; ok && blk < p.num_tiles; blk += num_clusters) {
+                int64_t tr, tc;
+                int bz;
+                block_coord(blk, bz, tr, tc);
+                const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 64 * (int32_t)q;
+                const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
+                const int32_t za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ptx::map_to_cta(full_bar(s), pair_leader);
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);
+                    const int32_t k0 = kb * KBlock<KIND>::elems;
+                    ptx::tma_load_3d_pair_mc(sA + s * Plan::a_stage + q * kAHalfBytes, &p.tma_a, fb, k0, m0, za,
+                                             a_mask);
+                    if (B_MN) {
+#pragma unroll
+                        for (int j = 0; j < kHalfN / 64; ++j)
+                            ptx::tma_load_3d_pair(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
+                                                  n0 + 64 * j, k0, zb);
+                    } else {
+                        ptx::tma_load_3d_pair(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0, zb);
+                    }
+                    issued_mask |= 1u << s;
+                    issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                aborted = true;
+                if (leader)
+                    for (int t = 0; t < STAGES; ++t)
+                        if (issued_mask & (1u << t))
+                            wait_bounded(full_bar(t), (issued_parity >> t) & 1u, wc, SITE_DRAIN_LOADS, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA (pair leaders)
+        if (lane == 0 && leader) {
+            const uint64_t kDescB = B_MN ? kDescMNMajor : kDescKMajor;
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t local = 0;
+            bool ok = true;
+            for (int blk = cluster_id; ok && blk < p.num_tiles; blk += num_clusters, ++local) {
+                const uint32_t buf = local & 1u;
+                const uint32_t bph = (local >> 1) & 1u;
+                if (!wait_bounded(tempty_bar(buf), bph ^ 1u, wc, SITE_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * kPairBN;
+                for (int kb = 0; kb < p.num_kb;) {
+                    // two k-blocks per pass when the second stage is already full
+                    if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    const int n =
+                        (kb + 1 < p.num_kb && s + 1 < STAGES && ptx::mbar_test_wait(full_bar(s + 1), ph)) ? 2 : 1;
+                    ptx::tc_fence_after_sync();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < n) {
+                            const uint32_t a_addr = sA + (s + h) * Plan::a_stage;
+                            const uint32_t b_addr = sB + (s + h) * Plan::b_stage;
+#pragma unroll
+                            for (int k = 0; k < kBK / kUmmaK; ++k) {
+                                const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
+                                const uint64_t bd =
+                                    desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
+                                mma_issue<KIND, true>(d_tmem, ad, bd, p.idesc, (kb + h > 0 || k > 0) ? 1u : 0u);
+                            }
+                            ptx::mma_commit_pair(empty_bar(s + h), 0xF);   // the stage is free for this pair, in all four CTAs
+                        }
+                    }
+                    kb += n;
+                    s += n;
+                    if (s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(tfull_bar(buf), pair_mask);    // this pair's accumulator is ready
+            }
+            if (!ok) {
+                aborted = true;
+                ptx::mma_commit_pair(drain_bar, (uint16_t)(1u << crank));
+                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;
+        const int qw = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
+        const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
+        EpiCtx ectx{&p, drain_bar + 8u * (1 + ew), 0u, wc};
+        uint32_t local = 0, cc = 0;
+        for (int blk = cluster_id; blk < p.num_tiles; blk += num_clusters, ++local) {
+            const uint32_t buf = local & 1u;
+            const uint32_t bph = (local >> 1) & 1u;
+            const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
+            if (!__all_sync(0xffffffffu, got)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            int64_t tr, tc;
+            int bz;
+            block_coord(blk, bz, tr, tc);
+            ectx.z = bz;
+            const int32_t row0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 32 * qw;
+            const int32_t col0 = (int32_t)tc * kPairBN;
+            const uint32_t t_acc = tmem_base + lane_base + buf * kPairBN;
+            const uint32_t release_bar = ptx::map_to_cta(tempty_bar(buf), pair_leader);
+            epilogue_drain<kPairBN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
+                                         [&] { ptx::mbar_arrive_cluster(release_bar); }, ectx);
+        }
+        if (lane == 0) ptx::bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    if (aborted || *abort_flag) {
+        // copies issued by any CTA of the quad may land in this one: let them settle
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::cluster_sync();          // no CTA frees TMEM or exits while another still works
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
+cudaError_t launch_gemm_quad(const GemmParams &p, int grid, cudaStream_t stream)
+{
+    auto kern = gemm_quad_kernel<STAGES, OUT, B_MN, KIND>;
+    constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
+    static std::atomic<unsigned long long> smem_set{0};
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 4;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Number of quads (clusters of four) of this kernel that can be resident at once.
+template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
+int max_active_quads()
+{
+    auto kern = gemm_quad_kernel<STAGES, OUT, B_MN, KIND>;
+    constexpr uint32_t smem = SmemPlan<kPairBN / 2, STAGES>::alloc_bytes;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 4;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// Variant table entry: cluster 4 = quad.
+#define TGEMM_QUAD_VARIANT(ST, OUT, BMN)                                                              \
+    {256, ST, OUT, BMN, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_quad<ST, OUT, (BMN) != 0>, \
+     4, &max_active_quads<ST, OUT, (BMN) != 0>}
+
+}  // namespace tgemm

@@ -364,6 +364,20 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *map, 
         : "memory");
 }
 
+// Pair-mode TMA load multicast to the CTAs of `cta_mask` (same shared-memory
+// offset in each); every destination's completion is signalled on the
+// mbarrier at the same offset in the leader (even rank) of that
+// destination's CTA pair.  bar_cluster is this CTA's pair leader's barrier.
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void *map, uint32_t bar_cluster, int32_t x,
+                                                    int32_t y, int32_t z, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)

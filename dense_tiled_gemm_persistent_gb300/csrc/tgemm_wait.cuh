@@ -22,6 +22,8 @@ struct WaitCtx {
     volatile int *abort_flag;    // in shared memory, one per CTA
     uint64_t timeout_ns;
     uint32_t peer_abort = 0;     // shared::cluster address of the pair partner's flag (0: none)
+    uint32_t peer_mask = 0;      // or: cluster ranks whose flag (at abort_local) is raised too
+    uint32_t abort_local = 0;    // shared::cta address of the flag, for peer_mask
 };
 
 __device__ __forceinline__ void record_fault(const WaitCtx &w, uint32_t site)
@@ -30,6 +32,11 @@ __device__ __forceinline__ void record_fault(const WaitCtx &w, uint32_t site)
     *w.abort_flag = 1;
     if (w.peer_abort)   // the partner CTA of a pair winds down too
         asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(w.peer_abort), "r"(1) : "memory");
+    for (uint32_t r = 0; r < 8; ++r)   // every CTA of a larger cluster that shares this one's copies
+        if ((w.peer_mask >> r) & 1u) {
+            const uint32_t a = ptx::map_to_cta(w.abort_local, r);
+            asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+        }
     if (w.status) atomicCAS(w.status, 0u, code);
 }
 

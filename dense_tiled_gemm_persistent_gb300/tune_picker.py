@@ -42,8 +42,8 @@ SKINNY_K = [10, 12, 13]
 L2 = 129 * 1000 * 1000
 
 
-def candidates(tg, M):
-    """(kind, Config) pairs valid for M rows of A."""
+def candidates(tg, M, N=0):
+    """(kind, Config) pairs valid for M rows of A (and N columns of B)."""
     C = tg.Config
     out = []
     if M <= 64:
@@ -60,6 +60,14 @@ def candidates(tg, M):
     out.append(("pair256", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=1, swap_ab=0, grid=0)))
     out.append(("pair256sk", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=0, swap_ab=0,
                                grid=0)))
+    if M >= 256 and N >= 512:
+        # two pairs sharing A (cluster of four): a quarter fewer operand loads per CTA
+        out.append(("quad256", C(bm=256, bn=256, bk=64, stages=6, cluster_m=4, group_m=8, split_k=1, swap_ab=0,
+                                 grid=0)))
+    if M >= 4096 and N >= 4096:
+        # wider raster bands: more A reuse in L2 per wave on the largest shapes
+        out.append(("pair256g16", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=16, split_k=1, swap_ab=0,
+                                    grid=0)))
     out.append(("cta256", C(bm=128, bn=256, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
     out.append(("cta128", C(bm=128, bn=128, bk=64, stages=6, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
     return out
@@ -145,7 +153,7 @@ def main():
             Cc = torch.empty(M, N, device=dev, dtype=torch.float16)
             copies.append((A, B, Cc))
         best = None
-        for kind, cfg in candidates(tg, M):
+        for kind, cfg in candidates(tg, M, N):
             us = time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters)
             if us is None:
                 continue

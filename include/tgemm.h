@@ -73,7 +73,10 @@ typedef enum {
  * N, with the K loop split over split_k CTAs whose partial sums are added
  * through a global FP32 workspace (swap_ab = 1) or inside a thread-block
  * cluster of split_k CTAs (swap_ab = 2, cluster_m = split_k); grid is the
- * number of CTAs launched (0 = the library's choice).
+ * number of CTAs launched (0 = the library's choice).  Tile kernels:
+ * cluster_m = 1 (bm 128, bn 128 or 256), 2 (a CTA pair, 256 x 256; split_k =
+ * 0 adds a stream-K tail) or 4 (two CTA pairs on neighbouring 256 x 256
+ * tiles sharing their A rows, 16-bit operands, whole tiles).
  */
 typedef struct {
     int bm, bn, bk, stages, cluster_m, group_m, split_k, swap_ab, grid;

@@ -38,6 +38,7 @@ CONFIGS = {
     "cta128": C(bn=128, stages=6),
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
+    "quad": C(bm=256, stages=6, cluster_m=4),
     "skinny_cluster": C(bn=16, stages=12, cluster_m=3, group_m=1, split_k=3, swap_ab=2),
     "skinny_workspace": C(bn=16, stages=4, group_m=1, split_k=5, swap_ab=1),
 }

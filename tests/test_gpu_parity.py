@@ -28,16 +28,18 @@ def gpu():
     ensure_built()
 
 
-def cfg(bn, stages=None, group_m=8, grid=0, pair=False):
-    if pair:
-        return tgemm.Config(bm=256, bn=256, bk=64, stages=stages or 6, cluster_m=2, group_m=group_m,
+def cfg(bn, stages=None, group_m=8, grid=0, pair=False, quad=False):
+    if pair or quad:
+        return tgemm.Config(bm=256, bn=256, bk=64, stages=stages or 6, cluster_m=4 if quad else 2, group_m=group_m,
                             split_k=1, swap_ab=0, grid=grid)
     return tgemm.Config(bm=128, bn=bn, bk=64, stages=stages or (4 if bn == 256 else 6), cluster_m=1,
                         group_m=group_m, split_k=1, swap_ab=0, grid=grid)
 
 
-# every compiled tile shape: 128 x 256 and 128 x 128 on one CTA, 256 x 256 on a CTA pair
-SHAPE_CFGS = [("1cta_128x256", dict(bn=256)), ("1cta_128x128", dict(bn=128)), ("pair_256x256", dict(bn=256, pair=True))]
+# every compiled tile shape: 128 x 256 and 128 x 128 on one CTA, 256 x 256 on a CTA pair, and two
+# 256 x 256 pairs sharing A in a cluster of four
+SHAPE_CFGS = [("1cta_128x256", dict(bn=256)), ("1cta_128x128", dict(bn=128)), ("pair_256x256", dict(bn=256, pair=True)),
+              ("quad_256x512", dict(bn=256, quad=True))]
 
 
 # ---- one tile, exact integers: descriptor and layout sanity ------------------
@@ -45,7 +47,7 @@ SHAPE_CFGS = [("1cta_128x256", dict(bn=256)), ("1cta_128x128", dict(bn=128)), ("
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("name,kw", SHAPE_CFGS, ids=[n for n, _ in SHAPE_CFGS])
 def test_one_tile_integers_exact(layout, name, kw):
-    M, N, K = (256 if kw.get("pair") else 128), kw["bn"], 64
+    M, N, K = (256 if kw.get("pair") or kw.get("quad") else 128), kw["bn"], 64
     a, b = operands(M, N, K, gen.F16, layout, gen.ints(-2, 2), seed=1)
     check_full(a, b, M, N, K, layout, gen.F16, gen.F32, exact=True, config=cfg(**kw),
                what="one tile %s %s" % (LNAME[layout], name))
@@ -112,6 +114,19 @@ def test_k_tails(K):
 
 
 # ---- the persistent loop: many tiles per CTA -----------------------------------
+
+@pytest.mark.parametrize("grid", [4, 8, 0])
+@pytest.mark.parametrize("group_m", [1, 3, 8])
+def test_quad_persistent_block_loop(grid, group_m):
+    """Quads walk several 256 x 512 blocks each (odd tile columns: the last
+    block's second pair computes past N and stores nothing)."""
+    M, N, K = 1100, 1300, 700
+    for layout in LAYOUTS:
+        a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=61 + group_m)
+        check_full(a, b, M, N, K, layout, gen.BF16, gen.F32, exact=True,
+                   config=cfg(256, quad=True, group_m=group_m, grid=grid),
+                   what="quad grid=%d group_m=%d %s" % (grid, group_m, LNAME[layout]))
+
 
 @pytest.mark.parametrize("grid", [2, 6, 0])
 @pytest.mark.parametrize("group_m", [1, 3, 8, 16])
@@ -185,6 +200,15 @@ def test_runs_on_a_side_stream():
     C = run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F16, stream=s)
     ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.F16)
     assert np.array_equal(bits(C[:M, :N], gen.F16), oracle.round_bits(ref, gen.F16))
+
+
+def test_misaligned_rows_pick_the_quad_kernel():
+    # K = 5000 BF16 rows are 10000 bytes: not a multiple of 128
+    rc, c = tgemm.tgemm_query_config(4000, 3000, 5000, gen.B_NK, gen.BF16, gen.BF16)
+    assert rc == 0 and (c.cluster_m, c.bm, c.bn, c.split_k) == (4, 256, 256, 1)
+    # FP8 operands keep the pair kernel (the quad is built for 16-bit operands)
+    rc, c = tgemm.tgemm_query_config(4000, 3000, 5008, gen.B_NK, gen.E4M3, gen.BF16)
+    assert rc == 0 and c.cluster_m != 4
 
 
 def test_query_config_matches_what_runs():
