@@ -39,7 +39,9 @@ def test_every_row_is_a_legal_configuration():
             if e["swap_ab"] == 2:
                 assert e["cluster_m"] == e["split_k"] and e["stages"] == {16: 12, 32: 10, 64: 9}[e["bn"]]
         else:
-            assert (e["cluster_m"], e["bm"]) in ((1, 128), (2, 256))
+            assert (e["cluster_m"], e["bm"]) in ((1, 128), (2, 256), (4, 256))   # 4: two pairs sharing A
+            if e["cluster_m"] == 4:
+                assert e["bn"] == 256 and e["split_k"] == 1
             assert e["split_k"] == 1 or (e["split_k"] == 0 and e["cluster_m"] == 2)   # 0: stream-K tail
 
 
