@@ -436,6 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
 
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
     const int num_tiles = p.num_tiles;
+    ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
+    ptx::launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -598,11 +600,16 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see ptx::grid_dependency_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
+    ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
+    ptx::launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -305,11 +307,16 @@ cudaError_t launch_gemm_skinny(const GemmParams &p, int grid, cudaStream_t strea
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see ptx::grid_dependency_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

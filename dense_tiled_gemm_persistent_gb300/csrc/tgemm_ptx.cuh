@@ -75,6 +75,23 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+//
+// Kernels are launched with programmatic stream serialisation: the next
+// kernel in the stream may start (barrier set-up, TMEM allocation, tensor-map
+// prefetch) while this one drains.  Every kernel waits here for the grids it
+// depends on to complete, with their memory visible, before its first global
+// access, and then lets its own dependents be scheduled.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA -------------------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tensormap(const void *map)
