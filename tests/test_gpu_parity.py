@@ -373,3 +373,44 @@ def test_stream_k_is_deterministic_across_calls():
     a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.normal(0, 1), seed=59)
     outs = [run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, config=sk_cfg()) for _ in range(3)]
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# ---- back-to-back dependent launches ------------------------------------------
+
+@pytest.mark.parametrize("kinds", [("pair", "pair", "pair"), ("pair", "cta128", "quad"), ("quad", "auto", "cta256")])
+def test_chained_products_see_each_others_results(kinds):
+    """C1 = A B, C2 = C1 D, C3 = C2 E launched back to back on one stream with
+    no synchronisation in between: each launch may start early (programmatic
+    dependent launch) and must still read the previous product complete.
+    Small integers keep every intermediate exact in FP16, so C3 is compared bit
+    for bit with the oracle's chain."""
+    M, K1, N1, N2, N3 = 256, 16, 128, 512, 256
+    g = torch.Generator().manual_seed(77)
+    A = torch.randint(-1, 2, (M, K1), generator=g).half()
+    B = torch.randint(-1, 2, (N1, K1), generator=g).half()       # N x K
+    D = torch.randint(-1, 2, (N2, N1), generator=g).half()
+    E = torch.randint(-1, 2, (N3, N2), generator=g).half()
+    configs = {
+        "pair": cfg(256, pair=True), "quad": cfg(256, quad=True), "cta128": cfg(128), "cta256": cfg(256),
+        "auto": None,
+    }
+    dev = "cuda:0"
+    Ad, Bd, Dd, Ed = A.to(dev), B.to(dev), D.to(dev), E.to(dev)
+    C1 = torch.empty(M, N1, dtype=torch.float16, device=dev)
+    C2 = torch.empty(M, N2, dtype=torch.float16, device=dev)
+    C3 = torch.empty(M, N3, dtype=torch.float32, device=dev)
+    steps = [(Ad, Bd, C1, K1, N1, gen.F16), (C1, Dd, C2, N1, N2, gen.F16), (C2, Ed, C3, N2, N3, gen.F32)]
+    for (x, w, c, k, n, out), kind in zip(steps, kinds):
+        args = (M, n, k, x.data_ptr(), k, w.data_ptr(), k, gen.B_NK, c.data_ptr(), n, gen.F16, out, None)
+        conf = configs[kind]
+        rc = tgemm.tgemm_run(*args) if conf is None else tgemm.tgemm_run_config(*args, conf)
+        assert rc == tgemm.OK, tgemm.status_string(rc)
+    assert tgemm.tgemm_check() == tgemm.OK
+    # the oracle's chain, each intermediate rounded to FP16 as the GPU stores it
+    r1, _ = oracle.gemm(A, B, M, N1, K1, K1, K1, gen.B_NK, gen.F16)
+    c1 = torch.from_numpy(oracle.round_bits(r1, gen.F16).astype(np.uint16).view(np.int16)).view(torch.float16)
+    r2, _ = oracle.gemm(c1, D, M, N2, N1, N1, N1, gen.B_NK, gen.F16)
+    c2 = torch.from_numpy(oracle.round_bits(r2, gen.F16).astype(np.uint16).view(np.int16)).view(torch.float16)
+    r3, _ = oracle.gemm(c2, E, M, N3, N2, N2, N2, gen.B_NK, gen.F16)
+    assert np.abs(r2).max() <= 2048                                 # every intermediate exact in FP16
+    assert np.array_equal(bits(C3.cpu(), gen.F32), oracle.round_bits(r3, gen.F32))
