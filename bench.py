@@ -435,34 +435,60 @@ def main():
     roofline.update({"traffic": recorded_traffic(wl.name), "algorithmic_bytes": wl.algorithmic_bytes,
                      "flops_per_launch": wl.flops, "arithmetic_intensity": ai})
 
-    # end to end through the C ABI with host buffers: H2D of A and B from
-    # pinned memory, the GEMM, D2H of C into pinned memory, every step
+    # End to end through the C ABI with host buffers: every step copies its A
+    # and B in from pinned host memory, runs the GEMM and copies its C out to
+    # pinned host memory.  Steps are pipelined over three streams with two
+    # device buffer sets: the H2D copy of step i+1 and the D2H copy of step i-1
+    # overlap the GEMM of step i (events order each buffer's reuse).
     e2e = None
     if not args.no_e2e:
         ha = a_cpu.pin_memory()
         hb = b_cpu.pin_memory()
-        hc = torch.empty((wl.M, wl.N), dtype=gen.TORCH_DTYPE[wl.out_dtype]).pin_memory()
-        A2, B2 = torch.empty_like(A), torch.empty_like(B)
-        C2 = torch.empty_like(C)
-        for _ in range(2):
-            A2.copy_(ha, non_blocking=True)
-            B2.copy_(hb, non_blocking=True)
-            step(C2.data_ptr(), A2.data_ptr(), B2.data_ptr())
-            hc.copy_(C2, non_blocking=True)
+        hcs = [torch.empty((wl.M, wl.N), dtype=gen.TORCH_DTYPE[wl.out_dtype]).pin_memory() for _ in range(2)]
+        bufs = [(torch.empty_like(A), torch.empty_like(B), torch.empty_like(C)) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_comp = stream
+        comp_h = ctypes.c_void_p(s_comp.cuda_stream)
+        in_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+        for ev in comp_done + out_done:
+            ev.record(s_comp)
+
+        def e2e_step(i):
+            bi = i % 2
+            A2, B2, C2 = bufs[bi]
+            s_in.wait_event(comp_done[bi])          # the GEMM two steps back is done reading A2, B2
+            with torch.cuda.stream(s_in):
+                A2.copy_(ha, non_blocking=True)
+                B2.copy_(hb, non_blocking=True)
+            in_done[bi].record(s_in)
+            s_comp.wait_event(in_done[bi])
+            s_comp.wait_event(out_done[bi])         # C2 from two steps back is on the host
+            step(C2.data_ptr(), A2.data_ptr(), B2.data_ptr(), comp_h)
+            comp_done[bi].record(s_comp)
+            s_out.wait_event(comp_done[bi])
+            with torch.cuda.stream(s_out):
+                hcs[bi].copy_(C2, non_blocking=True)
+            out_done[bi].record(s_out)
+
+        for i in range(4):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            A2.copy_(ha, non_blocking=True)
-            B2.copy_(hb, non_blocking=True)
-            step(C2.data_ptr(), A2.data_ptr(), B2.data_ptr())
-            hc.copy_(C2, non_blocking=True)
-        e1.record(stream)
+        e0.record(s_comp)
+        s_in.wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        s_comp.wait_event(out_done[(args.e2e_steps - 1) % 2])
+        s_comp.wait_event(out_done[args.e2e_steps % 2])
+        e1.record(s_comp)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
         e2e = {"value": tflops(wl.M, wl.N, wl.K, e2e_ms) * world, "unit": "TFLOPS",
-               "h2d_bytes_per_step": a_cpu.numel() * 2 + b_cpu.numel() * 2,
-               "d2h_bytes_per_step": hc.numel() * hc.element_size(), "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size() + b_cpu.numel() * b_cpu.element_size(),
+               "d2h_bytes_per_step": hcs[0].numel() * hcs[0].element_size(), "ms_per_step": e2e_ms,
+               "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the GEMM of step i (two buffer sets)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
