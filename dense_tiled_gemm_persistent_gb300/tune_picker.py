@@ -4,7 +4,8 @@ picker table the library compiles in.
 For each grid point (M, N, K, B layout) the script times each candidate
 configuration through tgemm_run_config on the current GPU (FP16 in, FP16
 out, back-to-back launches over enough rotating operand copies to exceed L2),
-keeps the fastest, and writes
+twice (forward and reverse candidate order, best of the two), keeps the
+fastest, and writes
 
   * picker_table.csv              every measurement (committed, for review);
   * csrc/tgemm_picker_table.inc   the winner per grid point, as a C array.
@@ -73,7 +74,7 @@ def candidates(tg, M, N=0):
     return out
 
 
-def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters):
+def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustained=False):
     """Microseconds per launch, replaying `iters` launches from a CUDA graph
     (so the host's per-call cost does not hide the kernel's own time)."""
     n = len(copies)
@@ -99,14 +100,28 @@ def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters):
                 return None
     graph.replay()
     torch.cuda.synchronize()
+    # Long launches are timed in the GPU's steady, power-capped state (a
+    # quarter second of warm-up replays, then a quarter second timed): a
+    # burst from a cool GPU runs at higher clocks and favours configurations
+    # that move more data.
+    replays = 1
+    if sustained:
+        t0 = time.time()
+        n = 0
+        while time.time() - t0 < 0.25:
+            graph.replay()
+            torch.cuda.synchronize()
+            n += 1
+        replays = n                          # as many again, timed: about a quarter second
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    graph.replay()
+    for _ in range(replays):
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     if tg.tgemm_check(ctypes.c_void_p(stream.cuda_stream)) != 0:
         return None
-    return e0.elapsed_time(e1) / iters * 1000.0   # microseconds
+    return e0.elapsed_time(e1) / (iters * replays) * 1000.0   # microseconds
 
 
 def main():
@@ -153,10 +168,21 @@ def main():
             Cc = torch.empty(M, N, device=dev, dtype=torch.float16)
             copies.append((A, B, Cc))
         best = None
-        for kind, cfg in candidates(tg, M, N):
-            us = time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters)
-            if us is None:
+        # Two passes, the second in reverse order, each candidate keeping its
+        # better time: the GPU warms up (and its power-capped clock drops)
+        # through a point's candidates, which otherwise favours whichever is
+        # timed first.
+        cands = candidates(tg, M, N)
+        times = {}
+        for order in (cands, cands[::-1]):
+            for kind, cfg in order:
+                us = time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustained=flops >= 2e11)
+                if us is not None and (kind not in times or us < times[kind]):
+                    times[kind] = us
+        for kind, cfg in cands:
+            if kind not in times:
                 continue
+            us = times[kind]
             rows.append(dict(em=em, en=en, ek=ek, layout=layout, kind=kind, us=round(us, 3),
                              tflops=round(flops / us / 1e6, 1)))
             if best is None or us < best[0]:
