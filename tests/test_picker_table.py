@@ -57,5 +57,8 @@ def test_table_rows_are_the_fastest_measurement_of_their_point():
 
 
 def test_large_square_problems_pick_the_cta_pair():
+    # 256 x 256 tiles on CTA pairs: whole tiles, stream-K tail, wider raster
+    # bands, or two pairs sharing A
     big = [e for e in rows() if e["em"] >= 13 and e["en"] >= 13 and e["ek"] >= 12]
-    assert big and all(e["kind"] in ("pair256", "pair256sk") for e in big)
+    assert big and all(e["kind"] in ("pair256", "pair256sk", "pair256g16", "quad256") for e in big)
+    assert all(e["bm"] == 256 and e["bn"] == 256 and e["cluster_m"] in (2, 4) for e in big)
