@@ -477,7 +477,8 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
         // FP8 / TF32: the tile kernels, K-major B (bk names the 128-byte k-block)
         if (c.swap_ab != 0 || b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
         if (!(c.split_k == 1 || (c.split_k == 0 && c.cluster_m == 2))) return TGEMM_ERR_UNSUPPORTED;
-        if (!((c.cluster_m == 1 && c.bm == kBM) || (c.cluster_m == 2 && c.bm == kPairBM && c.bn == kPairBN)))
+        if (!((c.cluster_m == 1 && c.bm == kBM) ||
+              ((c.cluster_m == 2 || c.cluster_m == 4) && c.bm == kPairBM && c.bn == kPairBN)))
             return TGEMM_ERR_UNSUPPORTED;
         *v = find_variant(c.bn, c.stages, out_dtype, 0, c.cluster_m, mma_kind(in_dtype));
         return *v ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
@@ -729,11 +730,11 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
 // fewer requests, and measured 17-20 % faster than the pair kernel on such
 // shapes (110 -> 91 us on 4000 x 3000 x 5000); on aligned rows the pair
 // kernel's independent rings win.  So a pair choice (whole tiles or
-// stream-K) becomes a quad one for 16-bit operands with misaligned rows.
+// stream-K) becomes a quad one when rows are misaligned.
 void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, int64_t lda, int64_t ldb,
                                      int in_dtype)
 {
-    if (cfg->cluster_m != 2 || cfg->swap_ab != 0 || tile_only(in_dtype)) return;
+    if (cfg->cluster_m != 2 || cfg->swap_ab != 0) return;
     const int64_t e = (int64_t)elem_size(in_dtype);
     if ((lda * e) % 128 == 0 && (ldb * e) % 128 == 0) return;
     if (M < 256 || N < 512) return;

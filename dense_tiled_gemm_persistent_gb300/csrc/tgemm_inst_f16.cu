@@ -4,7 +4,7 @@
 // entries run 256 x 256 tiles on CTA pairs; the skinny entries are the
 // swap-AB split-K kernels for at most 64 rows of A (global-workspace and
 // in-cluster reductions), by padded row count; the quad entries run two pairs
-// that share A (clusters of four); the last six take FP8 and FP32-as-TF32
+// that share A (clusters of four); the last eight take FP8 and FP32-as-TF32
 // operands (B stored N x K).
 #include "tgemm_kernel_quad.cuh"
 #include "tgemm_kernel_skinny.cuh"
@@ -36,9 +36,11 @@ const KernelVariant kVariantsF16[] = {
     TGEMM_VARIANT_KIND(256, 4, OUT_F16, KIND_F8),
     TGEMM_VARIANT_KIND(128, 6, OUT_F16, KIND_F8),
     TGEMM_PAIR_VARIANT_KIND(6, OUT_F16, KIND_F8),
+    TGEMM_QUAD_VARIANT_KIND(6, OUT_F16, KIND_F8),
     TGEMM_VARIANT_KIND(256, 4, OUT_F16, KIND_TF32),
     TGEMM_VARIANT_KIND(128, 6, OUT_F16, KIND_TF32),
     TGEMM_PAIR_VARIANT_KIND(6, OUT_F16, KIND_TF32),
+    TGEMM_QUAD_VARIANT_KIND(6, OUT_F16, KIND_TF32),
 };
 const int kNumVariantsF16 = (int)(sizeof(kVariantsF16) / sizeof(kVariantsF16[0]));
 

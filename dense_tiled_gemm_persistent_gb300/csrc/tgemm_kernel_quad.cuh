@@ -325,9 +325,12 @@ int max_active_quads()
     return n;
 }
 
-// Variant table entry: cluster 4 = quad.
+// Variant table entries: cluster 4 = quad.
 #define TGEMM_QUAD_VARIANT(ST, OUT, BMN)                                                              \
     {256, ST, OUT, BMN, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_quad<ST, OUT, (BMN) != 0>, \
      4, &max_active_quads<ST, OUT, (BMN) != 0>}
+#define TGEMM_QUAD_VARIANT_KIND(ST, OUT, KIND)                                                            \
+    {256, ST, OUT, 0, SmemPlan<kPairBN / 2, ST>::alloc_bytes, &launch_gemm_quad<ST, OUT, false, KIND>, 4, \
+     &max_active_quads<ST, OUT, false, KIND>, KIND}
 
 }  // namespace tgemm

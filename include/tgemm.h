@@ -76,7 +76,7 @@ typedef enum {
  * number of CTAs launched (0 = the library's choice).  Tile kernels:
  * cluster_m = 1 (bm 128, bn 128 or 256), 2 (a CTA pair, 256 x 256; split_k =
  * 0 adds a stream-K tail) or 4 (two CTA pairs on neighbouring 256 x 256
- * tiles sharing their A rows, 16-bit operands, whole tiles).
+ * tiles sharing their A rows, whole tiles).
  */
 typedef struct {
     int bm, bn, bk, stages, cluster_m, group_m, split_k, swap_ab, grid;

@@ -45,6 +45,7 @@ CONFIGS = {
     "cta128": C(bn=128, stages=6),
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
+    "quad": C(bm=256, stages=6, cluster_m=4),
 }
 
 

@@ -206,8 +206,10 @@ def test_misaligned_rows_pick_the_quad_kernel():
     # K = 5000 BF16 rows are 10000 bytes: not a multiple of 128
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5000, gen.B_NK, gen.BF16, gen.BF16)
     assert rc == 0 and (c.cluster_m, c.bm, c.bn, c.split_k) == (4, 256, 256, 1)
-    # FP8 operands keep the pair kernel (the quad is built for 16-bit operands)
+    # FP8 rows of 5008 bytes (16-byte aligned, not 128) are misaligned too; 5120-byte rows are not
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5008, gen.B_NK, gen.E4M3, gen.BF16)
+    assert rc == 0 and c.cluster_m == 4
+    rc, c = tgemm.tgemm_query_config(4000, 3000, 5120, gen.B_NK, gen.E4M3, gen.BF16)
     assert rc == 0 and c.cluster_m != 4
 
 
