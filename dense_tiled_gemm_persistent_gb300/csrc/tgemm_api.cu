@@ -847,6 +847,8 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
                          (uint32_t)(128 / eo), 32);
     if (!ok) return TGEMM_ERR_CUDA;
     if (grid.count() * bt.count >= ((int64_t)1 << 31)) return TGEMM_ERR_UNSUPPORTED;
+    // the kernels map tiles with 32-bit arithmetic (grouped_tile32)
+    if ((int64_t)cfg.group_m * grid.tiles_n >= ((int64_t)1 << 31)) return TGEMM_ERR_UNSUPPORTED;
     p.M = (int32_t)M;
     p.N = (int32_t)N;
     p.K = (int32_t)K;
@@ -1066,7 +1068,15 @@ TGEMM_EXPORT tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn,
         return TGEMM_ERR_INVALID_ARG;
     const TileGrid g(M, N, bm, bn);
     if (bid < 0 || bid >= g.count()) return TGEMM_ERR_INVALID_ARG;
-    grouped_tile(g.tiles_m, g.tiles_n, group_m, bid, *bid_m, *bid_n);
+    if (g.count() * (int64_t)group_m < ((int64_t)1 << 31)) {
+        // the kernels' 32-bit form (every grid they run fits it)
+        int32_t r, c;
+        grouped_tile32((int32_t)g.tiles_m, (int32_t)g.tiles_n, group_m, (int32_t)bid, r, c);
+        *bid_m = r;
+        *bid_n = c;
+    } else {
+        grouped_tile(g.tiles_m, g.tiles_n, group_m, bid, *bid_m, *bid_n);
+    }
     return TGEMM_OK;
 }
 

@@ -258,7 +258,10 @@ struct EpiCtx {
 __device__ __forceinline__ void batched_tile(const GemmParams &p, int tile, int &b, int64_t &tr, int64_t &tc)
 {
     b = tile / p.tiles_per_batch;
-    grouped_tile(p.tiles_m, p.tiles_n, p.group_m, tile - b * p.tiles_per_batch, tr, tc);
+    int32_t r, c;
+    grouped_tile32(p.tiles_m, p.tiles_n, p.group_m, tile - b * p.tiles_per_batch, r, c);
+    tr = r;
+    tc = c;
 }
 
 // Fetch the C_in block (x, row0) of this warp into the staging block `sbuf`

@@ -114,10 +114,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
 
     // Block number -> (batch, block row, this pair's tile column).
     auto block_coord = [&](int blk, int &bz, int64_t &tr, int64_t &tc) {
-        int64_t tcq;
+        int32_t r, cq;
         bz = blk / p.tiles_per_batch;
-        grouped_tile(p.tiles_m, p.tiles_n, p.group_m, blk - bz * p.tiles_per_batch, tr, tcq);
-        tc = 2 * tcq + q;
+        grouped_tile32(p.tiles_m, p.tiles_n, p.group_m, blk - bz * p.tiles_per_batch, r, cq);
+        tr = r;
+        tc = 2 * (int64_t)cq + q;
     };
 
     if (warp == 0) {

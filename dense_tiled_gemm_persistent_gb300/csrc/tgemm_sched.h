@@ -52,6 +52,21 @@ TGEMM_HD void grouped_tile(int64_t tiles_m, int64_t tiles_n, int group_m, int64_
     tile_col = (bid - band * band_tiles) / rows;
 }
 
+// The same mapping in 32-bit arithmetic, for the kernels (tile counts are
+// kept below 2^31 by the host; 64-bit division is a long instruction
+// sequence on the GPU, run at every tile start by the producer and epilogue).
+TGEMM_HD void grouped_tile32(int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t bid, int32_t &tile_row,
+                             int32_t &tile_col)
+{
+    const int32_t band_tiles = group_m * tiles_n;
+    const int32_t band = bid / band_tiles;
+    const int32_t row0 = band * group_m;
+    int32_t rows = tiles_m - row0;
+    if (rows > group_m) rows = group_m;
+    tile_row = row0 + bid % rows;
+    tile_col = (bid - band * band_tiles) / rows;
+}
+
 // Stream-K split of the last tiles ("Stream-K" work decomposition: equal
 // shares of multiply-accumulate iterations instead of whole tiles).  The
 // sk_tiles tail tiles hold sk_tiles * kb k-block iterations, numbered tile by
