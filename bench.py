@@ -254,6 +254,8 @@ def main():
     ap.add_argument("--epilogue", default="none", choices=["none", "bias_gelu", "residual"],
                     help="fused epilogue (timing of a widened row; the headline line uses none)")
     ap.add_argument("--split-k", type=int, default=0, help="split count override for the swap-AB path (tuning)")
+    ap.add_argument("--stages", type=int, default=0,
+                    help="ring depth override for the swap-AB path (tuning; selects the in-cluster ring budget)")
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
                     help="replay the timed launches from a CUDA graph (auto: problems under 1e11 FLOP)")
     ap.add_argument("--workload", default=WORKLOAD,
@@ -300,10 +302,11 @@ def main():
         forced = tgemm.Config(bm=picked.bm, bn=picked.bn, bk=64, stages=4, cluster_m=1, group_m=1,
                               split_k=args.split_k or picked.split_k, swap_ab=1, grid=0)
         picked = forced
-    elif args.split_k and picked.swap_ab:
-        forced = tgemm.Config(bm=picked.bm, bn=picked.bn, bk=64, stages=picked.stages,
-                              cluster_m=args.split_k if picked.swap_ab == 2 else 1, group_m=1,
-                              split_k=args.split_k, swap_ab=picked.swap_ab, grid=0)
+    elif (args.split_k or args.stages) and picked.swap_ab:
+        sk = args.split_k or picked.split_k
+        forced = tgemm.Config(bm=picked.bm, bn=picked.bn, bk=64, stages=args.stages or picked.stages,
+                              cluster_m=sk if picked.swap_ab == 2 else 1, group_m=1,
+                              split_k=sk, swap_ab=picked.swap_ab, grid=0)
         picked = forced
     elif args.config != "auto" or args.group_m:
         shapes = {"pair": (256, 256, 6, 2, 1), "pairsk": (256, 256, 6, 2, 0), "1cta256": (128, 256, 4, 1, 1),

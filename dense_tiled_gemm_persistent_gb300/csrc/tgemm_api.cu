@@ -271,9 +271,20 @@ bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, t
     return false;
 }
 
-int cluster_splits_limit(int npad) { return npad == 16 ? ClusterSplitPlan<16>::max_splits
-                                           : npad == 32 ? ClusterSplitPlan<32>::max_splits
-                                                        : ClusterSplitPlan<64>::max_splits; }
+// Largest split count of the in-cluster kernel: the leader's ring receives
+// the other ranks' partials (the half-size ring, named by its stage count,
+// holds fewer).
+template <int NPAD>
+int cluster_splits_limit_of(int stages)
+{
+    return stages == ClusterSplitPlan<NPAD, 108>::stages ? ClusterSplitPlan<NPAD, 108>::max_splits
+                                                         : ClusterSplitPlan<NPAD>::max_splits;
+}
+int cluster_splits_limit(int npad, int stages = 0)
+{
+    return npad == 16 ? cluster_splits_limit_of<16>(stages)
+                      : npad == 32 ? cluster_splits_limit_of<32>(stages) : cluster_splits_limit_of<64>(stages);
+}
 int cluster_stages(int npad) { return npad == 16 ? ClusterSplitPlan<16>::stages
                                     : npad == 32 ? ClusterSplitPlan<32>::stages : ClusterSplitPlan<64>::stages; }
 
@@ -286,7 +297,7 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, 
     if (table_config(M, N, K, b_layout, sm_count, cfg)) {
         const int64_t kb = ceil_div(K, kBK);
         bool ok = cfg->split_k <= kb;
-        if (ok && cfg->swap_ab == 2) ok = cfg->split_k <= cluster_splits_limit(cfg->bn);
+        if (ok && cfg->swap_ab == 2) ok = cfg->split_k <= cluster_splits_limit(cfg->bn, cfg->stages);
         if (ok) {
             if (cfg->swap_ab)
                 cfg->grid = (int)(ceil_div(N, kSkinnyRows) * cfg->split_k);
@@ -310,9 +321,15 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         const int64_t kb = ceil_div(K, kBK);
         // In-cluster split-K: one CTA per SM, the splits of a tile reduce
         // through distributed shared memory.  Used unless the tiles are so few
-        // that the cluster limit leaves most SMs idle.
+        // that the cluster limit leaves most SMs idle.  For up to 16 rows the
+        // half-size ring (two CTAs per SM) measured faster across the tuning
+        // grid; its second slot per SM lets up to sm_count tiles split in two.
+        const bool half = npad == 16;
+        const int stages = half ? ClusterSplitPlan<16, 108>::stages : cluster_stages(npad);
+        const int limit = cluster_splits_limit(npad, stages);
         int64_t cs = sm_count / (tiles > 0 ? tiles : 1);
-        if (cs > cluster_splits_limit(npad)) cs = cluster_splits_limit(npad);
+        if (half && cs < 2 && tiles <= sm_count) cs = 2;
+        if (cs > limit) cs = limit;
         if (cs > kb) cs = kb;
         if (cs < 1) cs = 1;
         cfg->bm = kSkinnyRows;
@@ -320,7 +337,7 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         cfg->bk = kBK;
         cfg->group_m = 1;
         if (2 * tiles * cs >= sm_count || cs == kb) {
-            cfg->stages = cluster_stages(npad);
+            cfg->stages = stages;
             cfg->cluster_m = (int)cs;
             cfg->split_k = (int)cs;
             cfg->swap_ab = 2;

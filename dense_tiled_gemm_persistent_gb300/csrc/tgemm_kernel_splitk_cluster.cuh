@@ -21,6 +21,11 @@
 // No device memory besides A, B and C is touched, no atomics, no counters.
 // S is limited by the cluster size (8) and by the leader's ring holding
 // S-1 partials.
+//
+// RING_KB is the operand ring's budget.  216 KiB keeps one CTA per SM with
+// the most weight bytes in flight; 108 KiB lets two CTAs share an SM, so the
+// CTAs of the next launch can be resident (prologue done, waiting on
+// griddepcontrol.wait) while this one streams its weights.
 #pragma once
 
 #include "tgemm_kernel_skinny.cuh"
@@ -29,12 +34,14 @@ namespace tgemm {
 
 constexpr int kMaxClusterSplits = 8;
 
-template <int NPAD>
+template <int NPAD, int RING_KB = 216>
 struct ClusterSplitPlan {
     static constexpr uint32_t w_stage = kSkinnyRows * kBK * 2;
     static constexpr uint32_t x_stage = NPAD * kBK * 2;
     static constexpr uint32_t stage_bytes = w_stage + x_stage;
-    static constexpr int stages = (int)((216u * 1024u) / stage_bytes);     // 12, 11, 9 for NPAD 16, 32, 64
+    // 216 KiB: 12, 11, 9 stages for NPAD 16, 32, 64; 108 KiB: 6, 5, 4
+    static constexpr int stages = (int)((RING_KB * 1024u) / stage_bytes);
+    static constexpr int ctas_per_sm = RING_KB <= 108 ? 2 : 1;
     static constexpr uint32_t w_off = 0;
     static constexpr uint32_t x_off = w_off + stages * w_stage;
     static constexpr uint32_t bar_off = x_off + stages * x_stage;
@@ -49,13 +56,16 @@ struct ClusterSplitPlan {
     static constexpr int max_splits = max_splits_by_ring < kMaxClusterSplits ? max_splits_by_ring : kMaxClusterSplits;
 };
 
-template <int NPAD, int OUT, bool W_MN>
-__global__ void __launch_bounds__(kThreads, 1) gemm_splitk_cluster_kernel(const __grid_constant__ GemmParams p)
+template <int NPAD, int OUT, bool W_MN, int RING_KB>
+__global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::ctas_per_sm)
+    gemm_splitk_cluster_kernel(const __grid_constant__ GemmParams p)
 {
-    using Plan = ClusterSplitPlan<NPAD>;
+    using Plan = ClusterSplitPlan<NPAD, RING_KB>;
     constexpr int S = Plan::stages;
     constexpr uint32_t kTmemCols = NPAD < 32 ? 32 : NPAD;
     static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
+    static_assert(Plan::ctas_per_sm == 1 || Plan::alloc_bytes <= 232448 / 2 - 1024,
+                  "two CTAs of this plan must fit one SM");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -240,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_splitk_cluster_kernel(const 
     }
 }
 
-template <int NPAD, int OUT, bool W_MN>
+template <int NPAD, int OUT, bool W_MN, int RING_KB>
 cudaError_t launch_gemm_splitk_cluster(const GemmParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = gemm_splitk_cluster_kernel<NPAD, OUT, W_MN>;
-    constexpr uint32_t smem = ClusterSplitPlan<NPAD>::alloc_bytes;
+    auto kern = gemm_splitk_cluster_kernel<NPAD, OUT, W_MN, RING_KB>;
+    constexpr uint32_t smem = ClusterSplitPlan<NPAD, RING_KB>::alloc_bytes;
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
@@ -265,16 +275,19 @@ cudaError_t launch_gemm_splitk_cluster(const GemmParams &p, int grid, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int NPAD>
+template <int NPAD, int RING_KB>
 int cluster_max_splits()
 {
-    return ClusterSplitPlan<NPAD>::max_splits;
+    return ClusterSplitPlan<NPAD, RING_KB>::max_splits;
 }
 
-// stages carries the ring depth; cluster = 3 marks these entries; max_active
-// reports the largest split count the leader's ring can receive.
-#define TGEMM_CLUSTER_SPLIT_VARIANT(NPAD, OUT, BMN)                                                             \
-    {NPAD, ClusterSplitPlan<NPAD>::stages, OUT, BMN, ClusterSplitPlan<NPAD>::alloc_bytes,                      \
-     &launch_gemm_splitk_cluster<NPAD, OUT, (BMN) != 0>, 3, &cluster_max_splits<NPAD>}
+// stages carries the ring depth (it tells the two ring budgets apart);
+// cluster = 3 marks these entries; max_active reports the largest split count
+// the leader's ring can receive.
+#define TGEMM_CLUSTER_SPLIT_VARIANT_RING(NPAD, OUT, BMN, RING)                                                  \
+    {NPAD, ClusterSplitPlan<NPAD, RING>::stages, OUT, BMN, ClusterSplitPlan<NPAD, RING>::alloc_bytes,          \
+     &launch_gemm_splitk_cluster<NPAD, OUT, (BMN) != 0, RING>, 3, &cluster_max_splits<NPAD, RING>}
+#define TGEMM_CLUSTER_SPLIT_VARIANT(NPAD, OUT, BMN) TGEMM_CLUSTER_SPLIT_VARIANT_RING(NPAD, OUT, BMN, 216), \
+                                                    TGEMM_CLUSTER_SPLIT_VARIANT_RING(NPAD, OUT, BMN, 108)
 
 }  // namespace tgemm

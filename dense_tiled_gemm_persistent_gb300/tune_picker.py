@@ -55,6 +55,13 @@ def candidates(tg, M, N=0):
             if s <= mx:
                 out.append(("cluster%d" % s, C(bm=128, bn=npad, bk=64, stages=st, cluster_m=s, group_m=1,
                                              split_k=s, swap_ab=2, grid=0)))
+        # the half-size ring (two CTAs per SM): twice the resident clusters
+        st_h = {16: 6, 32: 5, 64: 4}[npad]
+        mx_h = {16: 8, 32: 7, 64: 4}[npad]
+        for s in (1, 2, 3, 4, 6, 8):
+            if s <= mx_h:
+                out.append(("cluster%dh" % s, C(bm=128, bn=npad, bk=64, stages=st_h, cluster_m=s, group_m=1,
+                                              split_k=s, swap_ab=2, grid=0)))
         for s in (4, 8, 16):
             out.append(("workspace%d" % s, C(bm=128, bn=npad, bk=64, stages=4, cluster_m=1, group_m=1,
                                              split_k=s, swap_ab=1, grid=0)))
@@ -127,6 +134,8 @@ def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustaine
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--quick", action="store_true", help="a few grid points only (smoke)")
+    ap.add_argument("--skinny-only", action="store_true",
+                    help="re-measure the M <= 64 band only and merge it into the existing table and CSV")
     ap.add_argument("--csv", default=CSV_PATH)
     ap.add_argument("--inc", default=INC_PATH)
     args = ap.parse_args()
@@ -151,6 +160,9 @@ def main():
                     points.append((em, en, ek, layout))
     if args.quick:
         points = points[::37]
+    all_points = list(points)
+    if args.skinny_only:
+        points = [pt for pt in points if pt[0] in SKINNY_M]
 
     rows, winners = [], []
     t0 = time.time()
@@ -194,6 +206,25 @@ def main():
                                                  best[0] if best else -1), flush=True)
     print("sweep took %.0f s" % (time.time() - t0))
 
+    lines = {}
+    for em, en, ek, layout, (us, kind, c) in winners:
+        lines[(em, en, ek, layout)] = "{%d, %d, %d, %d, {%d, %d, %d, %d, %d, %d, %d}, %.3ff},  // %s\n" % (
+            em, en, ek, layout, c.bm, c.bn, c.stages, c.cluster_m, c.group_m, c.split_k, c.swap_ab, us, kind)
+    if args.skinny_only:
+        # keep the other grid points' measurements and winners as they are
+        measured = set(points)
+        with open(args.csv, newline="") as f:
+            kept = [r for r in csv.DictReader(f)
+                    if (int(r["em"]), int(r["en"]), int(r["ek"]), int(r["layout"])) not in measured]
+        rows = kept + rows
+        with open(args.inc) as f:
+            for line in f:
+                if line.startswith("{"):
+                    key = tuple(int(x) for x in line[1:].split(",")[:4])
+                    if key not in measured:
+                        lines[key] = line
+        order = {pt: i for i, pt in enumerate(all_points)}
+        rows.sort(key=lambda r: order.get((int(r["em"]), int(r["en"]), int(r["ek"]), int(r["layout"])), -1))
     with open(args.csv, "w", newline="") as f:
         w = csv.DictWriter(f, fieldnames=["em", "en", "ek", "layout", "kind", "us", "tflops"])
         w.writeheader()
@@ -203,9 +234,9 @@ def main():
         f.write("// Generated by dense_tiled_gemm_persistent_gb300/tune_picker.py on %s.\n" % gpu)
         f.write("// log2 M, log2 N, log2 K, B layout (0 = KxN, 1 = NxK) -> fastest measured configuration\n")
         f.write("// {bm, bn, stages, cluster_m, group_m, split_k, swap_ab}, and its time in us.\n")
-        for em, en, ek, layout, (us, kind, c) in winners:
-            f.write("{%d, %d, %d, %d, {%d, %d, %d, %d, %d, %d, %d}, %.3ff},  // %s\n" % (
-                em, en, ek, layout, c.bm, c.bn, c.stages, c.cluster_m, c.group_m, c.split_k, c.swap_ab, us, kind))
+        for pt in all_points:
+            if pt in lines:
+                f.write(lines[pt])
     print("wrote", args.csv, "and", args.inc)
 
 

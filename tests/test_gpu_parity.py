@@ -266,11 +266,14 @@ def test_skinny_forced_splits_integers_exact(layout, splits):
 
 CLUSTER_STAGES = {16: 12, 32: 10, 64: 9}
 CLUSTER_MAX_SPLITS = {16: 8, 32: 8, 64: 7}
+# the half-size ring: two CTAs per SM
+HALF_STAGES = {16: 6, 32: 5, 64: 4}
+HALF_MAX_SPLITS = {16: 8, 32: 7, 64: 4}
 
 
-def cluster_cfg(npad, splits):
-    return tgemm.Config(bm=128, bn=npad, bk=64, stages=CLUSTER_STAGES[npad], cluster_m=splits, group_m=1,
-                        split_k=splits, swap_ab=2, grid=0)
+def cluster_cfg(npad, splits, half=False):
+    return tgemm.Config(bm=128, bn=npad, bk=64, stages=(HALF_STAGES if half else CLUSTER_STAGES)[npad],
+                        cluster_m=splits, group_m=1, split_k=splits, swap_ab=2, grid=0)
 
 
 @pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
@@ -285,12 +288,34 @@ def test_cluster_split_k_integers_exact(layout, npad):
                    what="cluster splits=%d npad=%d" % (splits, npad))
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("npad", [16, 32, 64])
+def test_cluster_split_k_half_ring_integers_exact(layout, npad):
+    """The half-size ring (two CTAs per SM, fewer stages, fewer partials the
+    leader can receive), every cluster size it allows."""
+    M, N, K = min(npad, 40), 700, 1600
+    a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=47 + npad)
+    for splits in range(1, HALF_MAX_SPLITS[npad] + 1):
+        check_full(a, b, M, N, K, layout, gen.BF16, gen.F32, exact=True, config=cluster_cfg(npad, splits, True),
+                   what="half ring splits=%d npad=%d" % (splits, npad))
+
+
+def test_cluster_split_k_half_ring_two_ctas_per_sm():
+    """More CTAs than SMs (128 tiles x 2 splits = 256), all resident two per
+    SM, and a ragged last tile; sampled against the oracle."""
+    M, N, K = 16, 16384 - 40, 4096
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=53, dist_b=gen.normal(0, 0.02))
+    for splits in (2, 3):
+        check_full(a, b, M, N, K, gen.B_NK, gen.BF16, gen.BF16, config=cluster_cfg(16, splits, True),
+                   what="half ring 16x16344x4096 splits=%d" % splits)
+
+
 def test_cluster_split_k_rejects_too_many_splits():
     x = torch.empty(1 << 16, dtype=torch.bfloat16, device="cuda:0")
     p = x.data_ptr()
-    for npad, too_many in ((16, 9), (64, 8)):
+    for npad, too_many, half in ((16, 9, False), (64, 8, False), (16, 9, True), (64, 5, True)):
         rc = tgemm.tgemm_run_config(16, 256, 1024, p, 1024, p, 1024, gen.B_NK, p, 256, gen.BF16, gen.BF16, None,
-                                    cluster_cfg(npad, too_many))
+                                    cluster_cfg(npad, too_many, half))
         assert rc == tgemm.ERR_UNSUPPORTED
 
 

@@ -37,7 +37,11 @@ def test_every_row_is_a_legal_configuration():
             M = 1 << e["em"]
             assert M <= 64 and e["bn"] >= M and e["bm"] == 128
             if e["swap_ab"] == 2:
-                assert e["cluster_m"] == e["split_k"] and e["stages"] == {16: 12, 32: 10, 64: 9}[e["bn"]]
+                # the full ring (one CTA per SM) or the half ring (two per SM)
+                assert e["cluster_m"] == e["split_k"]
+                assert e["stages"] in ({16: 12, 32: 10, 64: 9}[e["bn"]], {16: 6, 32: 5, 64: 4}[e["bn"]])
+                if e["stages"] == {16: 6, 32: 5, 64: 4}[e["bn"]]:
+                    assert e["split_k"] <= {16: 8, 32: 7, 64: 4}[e["bn"]]
         else:
             assert (e["cluster_m"], e["bm"]) in ((1, 128), (2, 256), (4, 256))   # 4: two pairs sharing A
             if e["cluster_m"] == 4:
