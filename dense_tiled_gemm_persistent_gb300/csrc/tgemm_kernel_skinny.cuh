@@ -59,7 +59,7 @@ __device__ __forceinline__ void store_out(void *c, int64_t idx, float v)
 // C[m][n] = v with the fused epilogue (when enabled): C_in read with a
 // plain load, bias by output column n.
 template <int OUT>
-__device__ __forceinline__ void store_out_epi(const GemmParams &p, int m, int64_t n, float v)
+__device__ __forceinline__ float epi_apply(const GemmParams &p, int m, int64_t n, float v)
 {
     if (p.epi & 1) {
         float cin = 0.f;
@@ -71,7 +71,13 @@ __device__ __forceinline__ void store_out_epi(const GemmParams &p, int m, int64_
         }
         v = epi_value(p, v, cin, n);
     }
-    store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, v);
+    return v;
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_out_epi(const GemmParams &p, int m, int64_t n, float v)
+{
+    store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, epi_apply<OUT>(p, m, n, v));
 }
 
 template <int NPAD, int OUT, bool W_MN>

@@ -12,11 +12,14 @@
 //   2. cluster barrier: every CTA of the cluster has finished its MMAs, so the
 //      leader's (rank 0) operand ring is free;
 //   3. ranks 1..S-1 store their partials into the leader's ring with
-//      st.shared::cluster;
+//      st.shared::cluster, 16-byte chunk c of weight row r at
+//      ((rank - 1) * NPAD/4 + c) * 128 + r, so that the 32 lanes of a warp
+//      touch 512 consecutive bytes (no bank conflicts on either side);
 //   4. cluster barrier: the partials are visible to the leader;
 //   5. the leader adds them to its own in rank order 0, 1, ..., S-1 (fixed,
-//      so results do not depend on timing), casts with round-to-nearest-even
-//      and writes C.
+//      so results do not depend on timing), casts with round-to-nearest-even,
+//      stages the 128-column slice of C in its ring (row-major) and writes it
+//      with 16-byte stores along the rows of C.
 //
 // No device memory besides A, B and C is touched, no atomics, no counters.
 // S is limited by the cluster size (8) and by the leader's ring holding
@@ -216,30 +219,60 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     const bool epi = warp >= 2;
     const int nl = 32 * (warp & 3) + lane;           // weight row inside the tile (epilogue warps)
     const bool failed = *abort_flag != 0;
+    constexpr uint32_t kChunkStride = kSkinnyRows * 16;   // bytes between chunk c and c + 1 of one partial
     if (epi && rank != 0 && have && !failed) {
-        const uint32_t dst = ptx::map_to_cta(sW + ((rank - 1) * kSkinnyRows + nl) * (NPAD * 4), 0);
+        const uint32_t dst = ptx::map_to_cta(sW + (rank - 1) * (NPAD / 4) * kChunkStride + nl * 16, 0);
 #pragma unroll
         for (int c = 0; c < NPAD / 4; ++c)
-            ptx::st_cluster_v4(dst + 16 * c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            ptx::st_cluster_v4(dst + c * kChunkStride, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     }
     ptx::cluster_sync();                              // partials visible in the leader
+    // `failed` is read after the cluster barrier and `have` is false only
+    // where a wait gave up (which raised the flag first), so all four
+    // epilogue warps of the leader take this branch together.
     if (epi && rank == 0 && have && !failed) {
         for (int r = 1; r < splits; ++r) {            // fixed order: rank 0 (own), 1, 2, ...
-            const uint32_t src = sW + ((r - 1) * kSkinnyRows + nl) * (NPAD * 4);
+            const uint32_t src = sW + (r - 1) * (NPAD / 4) * kChunkStride + nl * 16;
 #pragma unroll
             for (int c = 0; c < NPAD / 4; ++c) {
-                const float4 t = ptx::ld_shared_v4(src + 16 * c);
+                const float4 t = ptx::ld_shared_v4(src + c * kChunkStride);
                 v[4 * c] += t.x;
                 v[4 * c + 1] += t.y;
                 v[4 * c + 2] += t.z;
                 v[4 * c + 3] += t.w;
             }
         }
+        // The partials are in registers: the ring now stages C's slice,
+        // [m][128 columns] of the output type, at its start.
+        constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
+        constexpr int kPerChunk = 16 / kOutBytes;               // output elements per 16-byte store
+        constexpr int kChunksPerRow = kSkinnyRows / kPerChunk;
         const int64_t n = (int64_t)n0 + nl;
-        if (n < p.N)
+        const int rows = p.M < NPAD ? (int)p.M : NPAD;
+        ptx::named_barrier(1, 4 * 32);
+        uint8_t *stg = base_ptr + Plan::w_off;
 #pragma unroll
-            for (int m = 0; m < NPAD; ++m)
-                if (m < p.M) store_out_epi<OUT>(p, m, n, v[m]);
+        for (int m = 0; m < NPAD; ++m) {
+            const float x = (m < rows && n < p.N) ? epi_apply<OUT>(p, m, n, v[m]) : 0.f;
+            if constexpr (OUT == OUT_F32) reinterpret_cast<float *>(stg)[m * kSkinnyRows + nl] = x;
+            else if constexpr (OUT == OUT_F16) reinterpret_cast<__half *>(stg)[m * kSkinnyRows + nl] = __float2half_rn(x);
+            else reinterpret_cast<__nv_bfloat16 *>(stg)[m * kSkinnyRows + nl] = __float2bfloat16_rn(x);
+        }
+        ptx::named_barrier(1, 4 * 32);
+        for (int c = nl; c < rows * kChunksPerRow; c += kSkinnyRows) {
+            const int m = c / kChunksPerRow, j = c % kChunksPerRow;
+            const int64_t col = (int64_t)n0 + j * kPerChunk;
+            const uint4 q = *reinterpret_cast<const uint4 *>(stg + (m * kSkinnyRows + j * kPerChunk) * kOutBytes);
+            // C and ldc * element size are 16-byte aligned (checked by the host)
+            char *dst = static_cast<char *>(p.c_ptr) + ((int64_t)m * p.ldc + col) * kOutBytes;
+            if (col + kPerChunk <= p.N) {
+                *reinterpret_cast<uint4 *>(dst) = q;
+            } else {
+                const char *qb = reinterpret_cast<const char *>(&q);
+                for (int e = 0; e < kPerChunk && col + e < p.N; ++e)
+                    for (int b = 0; b < kOutBytes; ++b) dst[e * kOutBytes + b] = qb[e * kOutBytes + b];
+            }
+        }
     }
 
     ptx::tc_fence_before_sync();
