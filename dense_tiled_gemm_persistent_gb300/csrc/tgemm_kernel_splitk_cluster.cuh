@@ -6,21 +6,28 @@
 // form one cluster and add their partial sums through distributed shared
 // memory instead of a global workspace:
 //
-//   1. every CTA runs its K range through a STAGES-deep TMA ring (one CTA per
-//      SM, so the whole shared memory keeps weight bytes in flight) and reads
+//   1. every CTA runs its K range through a STAGES-deep TMA ring and reads
 //      its 128 x NPAD FP32 partial from tensor memory into registers;
-//   2. cluster barrier: every CTA of the cluster has finished its MMAs, so the
-//      leader's (rank 0) operand ring is free;
-//   3. ranks 1..S-1 store their partials into the leader's ring with
-//      st.shared::cluster, 16-byte chunk c of weight row r at
-//      ((rank - 1) * NPAD/4 + c) * 128 + r, so that the 32 lanes of a warp
-//      touch 512 consecutive bytes (no bank conflicts on either side);
-//   4. cluster barrier: the partials are visible to the leader;
+//   2. once the leader's (rank 0) MMAs are done reading its ring, its MMA
+//      thread arrives on a "ring free" mbarrier in each other rank;
+//   3. ranks 1..S-1 wait for that and send their partials into the leader's
+//      ring with st.async, each store counting its 16 bytes on the leader's
+//      "partials" mbarrier (which expects all (S-1) partials' bytes); chunk c
+//      of weight row r goes to ((rank - 1) * NPAD/4 + c) * 128 + r, so the 32
+//      lanes of a warp touch 512 consecutive bytes (no bank conflicts);
+//   4. the leader waits for the partials' bytes;
 //   5. the leader adds them to its own in rank order 0, 1, ..., S-1 (fixed,
 //      so results do not depend on timing), casts with round-to-nearest-even,
 //      stages the 128-column slice of C in its ring (row-major) and writes it
 //      with 16-byte stores along the rows of C.
 //
+// No CTA waits for the whole cluster on the way: a cluster barrier's
+// release/acquire costs about a microsecond here, two of them a tenth of a
+// 32 MiB projection.  The barrier halves at start and exit only order the
+// mbarrier set-up and keep every CTA's shared memory alive while others may
+// write into it.  After a fault the ranks still send their (meaningless)
+// partials, so the leader never waits for bytes that will not come; the
+// status word reports the fault.
 // No device memory besides A, B and C is touched, no atomics, no counters.
 // S is limited by the cluster size (8) and by the leader's ring holding
 // S-1 partials.
@@ -48,7 +55,7 @@ struct ClusterSplitPlan {
     static constexpr uint32_t w_off = 0;
     static constexpr uint32_t x_off = w_off + stages * w_stage;
     static constexpr uint32_t bar_off = x_off + stages * x_stage;
-    static constexpr uint32_t n_bars = 2 * stages + 2;                   // full, empty, tmem_full, drain
+    static constexpr uint32_t n_bars = 2 * stages + 4;   // full, empty, tmem_full, drain, ring free, partials
     static constexpr uint32_t slot_off = bar_off + 8 * n_bars;
     static constexpr uint32_t abort_off = slot_off + 4;
     static constexpr uint32_t bytes = abort_off + 4;
@@ -81,6 +88,8 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     auto empty_bar = [&](int s) { return bar + 8u * (S + s); };
     const uint32_t tfull_bar = bar + 8u * (2 * S);
     const uint32_t drain_bar = bar + 8u * (2 * S + 1);
+    const uint32_t free_bar = bar + 8u * (2 * S + 2);   // ranks 1..S-1: the leader's ring may be filled
+    const uint32_t part_bar = bar + 8u * (2 * S + 3);   // leader: the other ranks' partials have arrived
     const uint32_t slot = base + Plan::slot_off;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
 
@@ -100,6 +109,10 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         }
         ptx::mbar_init(tfull_bar, 1);
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(free_bar, 1);
+        ptx::mbar_init(part_bar, 1);
+        if (rank == 0 && splits > 1)
+            ptx::mbar_arrive_expect_tx(part_bar, (uint32_t)(splits - 1) * Plan::partial_bytes);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -113,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         ptx::tc_fence_before_sync();
     }
     __syncthreads();
+    ptx::cluster_arrive_relaxed();   // this CTA's barriers are initialised (waited on before any remote access)
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
@@ -120,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     ptx::launch_dependents();
 
     float v[NPAD];
+#pragma unroll
+    for (int m = 0; m < NPAD; ++m) v[m] = 0.f;
     bool have = false;
 
     if (warp == 0) {
@@ -213,24 +229,35 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         }
     }
 
-    // Every CTA of the cluster is past its mainloop; the leader's ring is free.
-    __syncthreads();
-    ptx::cluster_sync();
+    ptx::cluster_wait();   // every CTA's barriers are initialised
     const bool epi = warp >= 2;
     const int nl = 32 * (warp & 3) + lane;           // weight row inside the tile (epilogue warps)
-    const bool failed = *abort_flag != 0;
     constexpr uint32_t kChunkStride = kSkinnyRows * 16;   // bytes between chunk c and c + 1 of one partial
-    if (epi && rank != 0 && have && !failed) {
-        const uint32_t dst = ptx::map_to_cta(sW + (rank - 1) * (NPAD / 4) * kChunkStride + nl * 16, 0);
+    bool received = true;
+    if (splits > 1) {
+        if (rank == 0 && warp == 1 && lane == 0) {
+            // Every MMA of this CTA is complete (tfull or drain waited on
+            // above): the other ranks may fill the ring.  A relaxed arrive
+            // is enough: the hazard is write-after-read, the reads are done
+            // before the arrive is issued and no write is issued before a
+            // rank has seen it.
+            for (int r = 1; r < splits; ++r) ptx::mbar_arrive_remote_relaxed(ptx::map_to_cta(free_bar, (uint32_t)r));
+        }
+        if (epi && rank != 0) {
+            wait_bounded(free_bar, 0, wc, SITE_CLUSTER_EXCHANGE, false);
+            const uint32_t dst = ptx::map_to_cta(sW + (rank - 1) * (NPAD / 4) * kChunkStride + nl * 16, 0);
+            const uint32_t leader_bar = ptx::map_to_cta(part_bar, 0);
 #pragma unroll
-        for (int c = 0; c < NPAD / 4; ++c)
-            ptx::st_cluster_v4(dst + c * kChunkStride, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            for (int c = 0; c < NPAD / 4; ++c)
+                ptx::st_async_v4(dst + c * kChunkStride, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3],
+                                 leader_bar);
+        }
+        if (epi && rank == 0) received = wait_bounded(part_bar, 0, wc, SITE_CLUSTER_EXCHANGE, false);
     }
-    ptx::cluster_sync();                              // partials visible in the leader
-    // `failed` is read after the cluster barrier and `have` is false only
-    // where a wait gave up (which raised the flag first), so all four
-    // epilogue warps of the leader take this branch together.
-    if (epi && rank == 0 && have && !failed) {
+    // The leader's four epilogue warps decide together (a fault may be
+    // recorded by another warp while they read the flag).
+    const bool go = epi && rank == 0 && ptx::named_barrier_and(1, 4 * 32, have && received && *abort_flag == 0);
+    if (go) {
         for (int r = 1; r < splits; ++r) {            // fixed order: rank 0 (own), 1, 2, ...
             const uint32_t src = sW + (r - 1) * (NPAD / 4) * kChunkStride + nl * 16;
 #pragma unroll
@@ -275,6 +302,13 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         }
     }
 
+    // No CTA leaves while another may still write into its shared memory:
+    // the leader arrives once every partial has landed, the others once
+    // their stores are issued; the leader's MMA thread releases its remote
+    // arrives.
+    if (rank == 0 && warp == 1) ptx::cluster_arrive_release();
+    else ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait();
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {

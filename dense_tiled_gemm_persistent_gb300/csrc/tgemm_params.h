@@ -24,6 +24,7 @@ enum WaitSite : uint32_t {
     SITE_DEBUG = 7,
     SITE_SPLITK_COUNTER = 8,
     SITE_EPI_CIN = 9,
+    SITE_CLUSTER_EXCHANGE = 10,
 };
 
 constexpr uint32_t kFaultTimeout = 7u;

@@ -337,6 +337,41 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t cta)
 
 // 16-byte store into the shared memory of another CTA of the cluster
 // (a shared::cluster address from map_to_cta).
+// 16 bytes into another CTA's shared memory; completion counts 16
+// transaction bytes on that CTA's mbarrier `cluster_bar` (whose phase
+// completion makes the bytes visible to the threads waiting on it).
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
+// Arrive on another CTA's mbarrier with no memory ordering (a signal that an
+// asynchronous reader of this CTA's shared memory is done).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// The two halves of a cluster barrier, per thread (not warp-aligned).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d)
 {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
