@@ -56,6 +56,21 @@ __device__ __forceinline__ void store_out(void *c, int64_t idx, float v)
     }
 }
 
+// One output element into shared memory (shared-window address), rounded
+// to nearest even for 16-bit outputs.
+template <int OUT>
+__device__ __forceinline__ void st_shared_out(uint32_t addr, float v)
+{
+    if constexpr (OUT == OUT_F32) {
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+    } else {
+        unsigned short h;
+        if constexpr (OUT == OUT_F16) h = __half_as_ushort(__float2half_rn(v));
+        else h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(h) : "memory");
+    }
+}
+
 // C[m][n] = v with the fused epilogue (when enabled): C_in read with a
 // plain load, bias by output column n.
 template <int OUT>
@@ -78,6 +93,25 @@ template <int OUT>
 __device__ __forceinline__ void store_out_epi(const GemmParams &p, int m, int64_t n, float v)
 {
     store_out<OUT>(p.c_ptr, (int64_t)m * p.ldc + n, epi_apply<OUT>(p, m, n, v));
+}
+
+// Rows 0 .. rows-1 of column n of C from registers: the fused epilogue
+// first, then the stores, with the pointer and pitch held in registers.
+// (Interleaving stores with parameter reads made the compiler re-read the
+// parameters per element: about 70 ns per row.)
+template <int OUT, int NPAD>
+__device__ __forceinline__ void store_column(const GemmParams &p, int rows, int64_t n, float (&v)[NPAD])
+{
+    if (p.epi & 1) {
+#pragma unroll
+        for (int m = 0; m < NPAD; ++m)
+            if (m < rows) v[m] = epi_apply<OUT>(p, m, n, v[m]);
+    }
+    void *const c = p.c_ptr;
+    const int64_t ldc = p.ldc;
+#pragma unroll
+    for (int m = 0; m < NPAD; ++m)
+        if (m < rows) store_out<OUT>(c, (int64_t)m * ldc + n, v[m]);
 }
 
 template <int NPAD, int OUT, bool W_MN>
@@ -232,10 +266,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
                 for (int j = 0; j < 16; ++j) v[16 * c + j] = __uint_as_float(r[j]);
             }
             if (p.splits == 1) {
-                if (n < p.N)
-#pragma unroll
-                    for (int m = 0; m < NPAD; ++m)
-                        if (m < M) store_out_epi<OUT>(p, m, n, v[m]);
+                if (n < p.N) store_column<OUT, NPAD>(p, M, n, v);
             } else {
                 // Partial of this split, [split][nt][row][NPAD]: each thread
                 // owns one weight row and writes its NPAD sums contiguously.
@@ -287,10 +318,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
                             acc[4 * c + 2] += t.z;
                             acc[4 * c + 3] += t.w;
                         }
-                    if (n < p.N)
-#pragma unroll
-                        for (int m = 0; m < NPAD; ++m)
-                            if (m < M) store_out_epi<OUT>(p, m, n, acc[m]);
+                    if (n < p.N) store_column<OUT, NPAD>(p, M, n, acc);
                     if (warp == 2 && lane == 0) p.counters[nt] = 0u;   // every split of this tile has arrived
                 }
             }

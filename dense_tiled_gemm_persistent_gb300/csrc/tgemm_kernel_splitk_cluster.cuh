@@ -276,27 +276,33 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         constexpr int kChunksPerRow = kSkinnyRows / kPerChunk;
         const int64_t n = (int64_t)n0 + nl;
         const int rows = p.M < NPAD ? (int)p.M : NPAD;
-        ptx::named_barrier(1, 4 * 32);
-        uint8_t *stg = base_ptr + Plan::w_off;
+        // The fused epilogue first, all in registers: stores between the
+        // parameter reads made the compiler re-read them per element (the
+        // staging loop then took 1.1 us for 16 rows, 5 us for 64).
+        if ((p.epi & 1) && n < p.N) {
 #pragma unroll
-        for (int m = 0; m < NPAD; ++m) {
-            const float x = (m < rows && n < p.N) ? epi_apply<OUT>(p, m, n, v[m]) : 0.f;
-            if constexpr (OUT == OUT_F32) reinterpret_cast<float *>(stg)[m * kSkinnyRows + nl] = x;
-            else if constexpr (OUT == OUT_F16) reinterpret_cast<__half *>(stg)[m * kSkinnyRows + nl] = __float2half_rn(x);
-            else reinterpret_cast<__nv_bfloat16 *>(stg)[m * kSkinnyRows + nl] = __float2bfloat16_rn(x);
+            for (int m = 0; m < NPAD; ++m)
+                if (m < rows) v[m] = epi_apply<OUT>(p, m, n, v[m]);
         }
         ptx::named_barrier(1, 4 * 32);
+        const uint8_t *stg = base_ptr + Plan::w_off;
+        const uint32_t stg_row = sW + nl * kOutBytes;   // shared address of element (0, nl)
+#pragma unroll
+        for (int m = 0; m < NPAD; ++m) st_shared_out<OUT>(stg_row + m * kSkinnyRows * kOutBytes, v[m]);
+        ptx::named_barrier(1, 4 * 32);
+        char *const c_base = static_cast<char *>(p.c_ptr);
+        const int64_t ldc = p.ldc, N = p.N;
         for (int c = nl; c < rows * kChunksPerRow; c += kSkinnyRows) {
             const int m = c / kChunksPerRow, j = c % kChunksPerRow;
             const int64_t col = (int64_t)n0 + j * kPerChunk;
             const uint4 q = *reinterpret_cast<const uint4 *>(stg + (m * kSkinnyRows + j * kPerChunk) * kOutBytes);
             // C and ldc * element size are 16-byte aligned (checked by the host)
-            char *dst = static_cast<char *>(p.c_ptr) + ((int64_t)m * p.ldc + col) * kOutBytes;
-            if (col + kPerChunk <= p.N) {
+            char *dst = c_base + ((int64_t)m * ldc + col) * kOutBytes;
+            if (col + kPerChunk <= N) {
                 *reinterpret_cast<uint4 *>(dst) = q;
             } else {
                 const char *qb = reinterpret_cast<const char *>(&q);
-                for (int e = 0; e < kPerChunk && col + e < p.N; ++e)
+                for (int e = 0; e < kPerChunk && col + e < N; ++e)
                     for (int b = 0; b < kOutBytes; ++b) dst[e * kOutBytes + b] = qb[e * kOutBytes + b];
             }
         }
