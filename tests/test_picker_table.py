@@ -50,14 +50,15 @@ def test_every_row_is_a_legal_configuration():
 
 
 def test_table_rows_are_the_fastest_measurement_of_their_point():
-    best = {}
+    times = {}
     for m in csv.DictReader(open(CSV)):
         key = (int(m["em"]), int(m["en"]), int(m["ek"]), int(m["layout"]))
-        if key not in best or float(m["us"]) < best[key][0]:
-            best[key] = (float(m["us"]), m["kind"])
+        times.setdefault(key, {})[m["kind"]] = float(m["us"])
     for e in rows():
-        us, kind = best[(e["em"], e["en"], e["ek"], e["layout"])]
-        assert kind == e["kind"] and us == pytest.approx(e["us"], abs=1e-3)
+        t = times[(e["em"], e["en"], e["ek"], e["layout"])]
+        # the CSV rounds to 1 ns, so two kinds may tie there
+        assert e["kind"] in t and t[e["kind"]] == pytest.approx(min(t.values()), abs=1e-3)
+        assert e["us"] == pytest.approx(t[e["kind"]], abs=1e-3)
 
 
 def test_large_square_problems_pick_the_cta_pair():
