@@ -189,14 +189,34 @@ __device__ __forceinline__ float act_apply(float x, int act)
     return x;
 }
 
-__device__ __forceinline__ float epi_combine(const GemmParams &p, float acc, float cin, float bias)
+// The epilogue's scalars in registers.  Loops that interleave shared-memory
+// stores (asm with a memory clobber) with reads of the launch parameters made
+// the compiler re-read the parameters per element; the per-chunk loops take
+// this copy instead.  Member names match GemmParams, so the helpers below
+// accept either.
+struct EpiScalars {
+    const void *bias;
+    int32_t N;
+    int32_t bias_dtype;
+    float alpha, beta;
+    int32_t act;
+    int32_t epi;
+    __device__ __forceinline__ static EpiScalars of(const GemmParams &p)
+    {
+        return EpiScalars{p.bias, p.N, p.bias_dtype, p.alpha, p.beta, p.act, p.epi};
+    }
+};
+
+template <class P>
+__device__ __forceinline__ float epi_combine(const P &p, float acc, float cin, float bias)
 {
     float r = p.alpha * acc;
     if (p.epi & 2) r = fmaf(p.beta, cin, r);
     return act_apply(r + bias, p.act);
 }
 
-__device__ __forceinline__ float epi_value(const GemmParams &p, float acc, float cin, int64_t col)
+template <class P>
+__device__ __forceinline__ float epi_value(const P &p, float acc, float cin, int64_t col)
 {
     const float b = (p.bias && col < p.N) ? load_bias(p.bias, p.bias_dtype, col) : 0.f;
     return epi_combine(p, acc, cin, b);
@@ -204,8 +224,8 @@ __device__ __forceinline__ float epi_value(const GemmParams &p, float acc, float
 
 // Bias values of columns [col, col + n) (n = 4 or 8), zero past N or without
 // a bias; one or two 16-byte loads when the run lies inside the vector.
-template <int n>
-__device__ __forceinline__ void load_bias_run(const GemmParams &p, int64_t col, float (&out)[n])
+template <int n, class P>
+__device__ __forceinline__ void load_bias_run(const P &p, int64_t col, float (&out)[n])
 {
     if (!p.bias) {
 #pragma unroll
@@ -293,6 +313,7 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
     const uint32_t row_addr = sbuf + lane * 128;
     const bool fused = e.p != nullptr && (e.p->epi & 1);
     const bool with_cin = fused && (e.p->epi & 2) && fetch_cin(e, sbuf, x, row0, lane);
+    const EpiScalars es = fused ? EpiScalars::of(*e.p) : EpiScalars{};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint32_t addr = row_addr + ((uint32_t)(j ^ (lane & 7)) << 4);   // 128-byte swizzle
@@ -306,10 +327,10 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
                     c[2] = __uint_as_float(q.z), c[3] = __uint_as_float(q.w);
                 }
                 float bv[4];
-                load_bias_run<4>(*e.p, (int64_t)x + 4 * j, bv);
+                load_bias_run<4>(es, (int64_t)x + 4 * j, bv);
 #pragma unroll
                 for (int t = 0; t < 4; ++t)
-                    v0[4 * j + t] = __float_as_uint(epi_combine(*e.p, __uint_as_float(v0[4 * j + t]), c[t], bv[t]));
+                    v0[4 * j + t] = __float_as_uint(epi_combine(es, __uint_as_float(v0[4 * j + t]), c[t], bv[t]));
             }
             w0 = v0[4 * j + 0];
             w1 = v0[4 * j + 1];
@@ -327,10 +348,10 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap *map, int32_
                     c[0] = c0.x, c[1] = c0.y, c[2] = c1.x, c[3] = c1.y, c[4] = c2.x, c[5] = c2.y, c[6] = c3.x, c[7] = c3.y;
                 }
                 float bv[8];
-                load_bias_run<8>(*e.p, (int64_t)x + 8 * j, bv);
+                load_bias_run<8>(es, (int64_t)x + 8 * j, bv);
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
-                    src[t] = __float_as_uint(epi_combine(*e.p, __uint_as_float(src[t]), c[t], bv[t]));
+                    src[t] = __float_as_uint(epi_combine(es, __uint_as_float(src[t]), c[t], bv[t]));
             }
             w0 = pack_out(__uint_as_float(src[0]), __uint_as_float(src[1]), OUT);
             w1 = pack_out(__uint_as_float(src[2]), __uint_as_float(src[3]), OUT);

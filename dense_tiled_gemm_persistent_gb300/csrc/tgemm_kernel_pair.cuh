@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     const bool fused = (p.epi & 1) != 0;
                     const bool with_cin = fused && (p.epi & 2) && fetch_cin(ectx, sbuf, col0 + c * kCols, row0, lane);
                     const int64_t col = (int64_t)col0 + c * kCols + col4 * 4;
+                    const EpiScalars es = EpiScalars::of(p);
 #pragma unroll
                     for (int i = 0; i < kPasses; ++i) {
                         const uint32_t r = (uint32_t)(i * kRowsPerPass + sub_row);
@@ -391,10 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                             if (fused) {
                                 float4 ci = make_float4(0.f, 0.f, 0.f, 0.f);
                                 if (with_cin) ci = ptx::ld_shared_v4(addr);
-                                acc[i].x = epi_value(p, acc[i].x, ci.x, col);
-                                acc[i].y = epi_value(p, acc[i].y, ci.y, col + 1);
-                                acc[i].z = epi_value(p, acc[i].z, ci.z, col + 2);
-                                acc[i].w = epi_value(p, acc[i].w, ci.w, col + 3);
+                                acc[i].x = epi_value(es, acc[i].x, ci.x, col);
+                                acc[i].y = epi_value(es, acc[i].y, ci.y, col + 1);
+                                acc[i].z = epi_value(es, acc[i].z, ci.z, col + 2);
+                                acc[i].w = epi_value(es, acc[i].w, ci.w, col + 3);
                             }
                             ptx::st_shared_v4(addr, __float_as_uint(acc[i].x), __float_as_uint(acc[i].y),
                                               __float_as_uint(acc[i].z), __float_as_uint(acc[i].w));
@@ -408,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                                     c0 = unpack_out(q0, OUT);
                                     c1 = unpack_out(q1, OUT);
                                 }
-                                acc[i].x = epi_value(p, acc[i].x, c0.x, col);
-                                acc[i].y = epi_value(p, acc[i].y, c0.y, col + 1);
-                                acc[i].z = epi_value(p, acc[i].z, c1.x, col + 2);
-                                acc[i].w = epi_value(p, acc[i].w, c1.y, col + 3);
+                                acc[i].x = epi_value(es, acc[i].x, c0.x, col);
+                                acc[i].y = epi_value(es, acc[i].y, c0.y, col + 1);
+                                acc[i].z = epi_value(es, acc[i].z, c1.x, col + 2);
+                                acc[i].w = epi_value(es, acc[i].w, c1.y, col + 3);
                             }
                             const uint32_t a0 = pack_out(acc[i].x, acc[i].y, OUT);
                             const uint32_t a1 = pack_out(acc[i].z, acc[i].w, OUT);
