@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&p.tma_a);
         ptx::prefetch_tensormap(&p.tma_b);
+        prefetch_weights_l2<W_MN>(&p.tma_b, n0, kb0, kb1);
     }
     if (warp == 1) {
         ptx::tmem_alloc(slot, kTmemCols);

@@ -99,6 +99,16 @@ __device__ __forceinline__ void prefetch_tensormap(const void *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// Bring the box at (x, y) of a 2-D tensor map into L2, without a shared
+// memory destination or a completion signal.  Only a hint: L2 is the point
+// of coherence for device memory, so a prefetch issued before an earlier
+// kernel's writes are visible cannot make a later load read stale data.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled load global -> shared; completion is signalled on `bar` as
 // transaction bytes.  x is the innermost (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t bar, int32_t x,
