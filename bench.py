@@ -248,7 +248,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--config", default="auto", choices=["auto", "pair", "pairsk", "1cta256", "1cta128", "workspace"],
+    ap.add_argument("--config", default="auto",
+                    choices=["auto", "pair", "pairsk", "quad", "quadsk", "1cta256", "1cta128", "workspace"],
                     help="tile shape: the library's pick, or a forced one (tuning)")
     ap.add_argument("--group-m", type=int, default=0, help="GROUP_SIZE_M override (0: library default)")
     ap.add_argument("--epilogue", default="none", choices=["none", "bias_gelu", "residual"],
@@ -309,7 +310,8 @@ def main():
                               split_k=sk, swap_ab=picked.swap_ab, grid=0)
         picked = forced
     elif args.config != "auto" or args.group_m:
-        shapes = {"pair": (256, 256, 6, 2, 1), "pairsk": (256, 256, 6, 2, 0), "1cta256": (128, 256, 4, 1, 1),
+        shapes = {"pair": (256, 256, 6, 2, 1), "pairsk": (256, 256, 6, 2, 0), "quad": (256, 256, 6, 4, 1),
+                  "quadsk": (256, 256, 6, 4, 0), "1cta256": (128, 256, 4, 1, 1),
                   "1cta128": (128, 128, 6, 1, 1)}
         bm, bn, st, cl, sk = shapes[args.config] if args.config != "auto" else (
             picked.bm, picked.bn, picked.stages, picked.cluster_m, picked.split_k)

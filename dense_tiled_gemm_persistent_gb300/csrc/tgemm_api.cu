@@ -493,7 +493,8 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
     if (tile_only(in_dtype)) {
         // FP8 / TF32: the tile kernels, K-major B (bk names the 128-byte k-block)
         if (c.swap_ab != 0 || b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
-        if (!(c.split_k == 1 || (c.split_k == 0 && c.cluster_m == 2))) return TGEMM_ERR_UNSUPPORTED;
+        if (!(c.split_k == 1 || (c.split_k == 0 && (c.cluster_m == 2 || c.cluster_m == 4))))
+            return TGEMM_ERR_UNSUPPORTED;
         if (!((c.cluster_m == 1 && c.bm == kBM) ||
               ((c.cluster_m == 2 || c.cluster_m == 4) && c.bm == kPairBM && c.bn == kPairBN)))
             return TGEMM_ERR_UNSUPPORTED;
@@ -520,9 +521,10 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
         return TGEMM_OK;
     }
     if (c.swap_ab != 0) return TGEMM_ERR_UNSUPPORTED;
-    // split_k = 0 asks the pair kernel for a stream-K tail; cluster_m = 4 is
-    // two pairs sharing A (256 x 256 per pair, whole tiles only)
-    if (!(c.split_k == 1 || (c.split_k == 0 && c.cluster_m == 2))) return TGEMM_ERR_UNSUPPORTED;
+    // split_k = 0 asks the pair or quad kernel for a stream-K tail; cluster_m
+    // = 4 is two pairs sharing A (256 x 256 per pair)
+    if (!(c.split_k == 1 || (c.split_k == 0 && (c.cluster_m == 2 || c.cluster_m == 4))))
+        return TGEMM_ERR_UNSUPPORTED;
     if (!((c.cluster_m == 1 && c.bm == kBM) || ((c.cluster_m == 2 || c.cluster_m == 4) && c.bm == kPairBM &&
                                                 c.bn == kPairBN)))
         return TGEMM_ERR_UNSUPPORTED;
@@ -575,14 +577,19 @@ int resident_pairs(DeviceState *dev, const KernelVariant *v)
     return n;
 }
 
-// Stream-K tail for the pair kernel: when the tiles leave the last wave of
-// pairs partly idle, the last one or two waves' tiles are shared out by
-// k-block iterations (at least kMinSkIters per pair, at most kMaxSegments
-// tiles touched per pair).  Fills p.dp_tiles/sk_tiles/sk_units, the FP32
-// partial-tile workspace and its tensor map; sk_units = 0 keeps whole tiles.
+// Stream-K tail for the pair and quad kernels: when the work items (pair
+// tiles, or the quad's 256 x 512 blocks of tiles_per_item = 2 tiles) leave
+// the last wave partly idle, the last one or two waves' items are shared out
+// by k-block iterations (at least kMinSkIters per unit, at most kMaxSegments
+// items touched per unit).  Fills p.dp_tiles/sk_tiles/sk_units, the FP32
+// partial-tile workspace and its tensor map; sk_units = 0 keeps whole items.
+// The quad shares only a leftover wave that is at most half full: sharing a
+// full wave as well measured 3-5 % slower than whole blocks on 4000 x 3000 x
+// 5000 and 4096 x 3072 x 5000 (96 blocks on 36 quads), where the FP32
+// partials of 60 shared blocks cost more than the idle third of a wave.
 constexpr int64_t kMinSkIters = 8;
 
-tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *stream_ptr)
+tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *stream_ptr, int tiles_per_item = 1)
 {
     (void)dev;
     const int64_t T = p->num_tiles, KB = p->num_kb, P = pairs;
@@ -603,6 +610,7 @@ tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *str
         if (units > P) units = P;
     } else {
         // Share the last full wave and the leftover tiles among all pairs.
+        if (tiles_per_item > 1 && full >= 1) return TGEMM_OK;
         dp = full >= 1 ? (full - 1) * P : 0;
         sk_tiles = T - dp;
         units = sk_tiles * KB / kMinSkIters;
@@ -611,14 +619,14 @@ tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *str
     const int64_t total = sk_tiles * KB;
     if (units <= sk_tiles && full == 0) return TGEMM_OK;   // no more pairs than tiles to share with
     if (units < 2) return TGEMM_OK;
-    if (2 * sk_tiles * 4 > (int64_t)kCounterBytes) return TGEMM_OK;
+    if (2 * tiles_per_item * sk_tiles * 4 > (int64_t)kCounterBytes) return TGEMM_OK;
     const StreamK sk{sk_tiles, units, KB};
     for (int64_t u = 0; u < units; ++u) {
         if (sk.bound(u + 1) <= sk.bound(u)) return TGEMM_OK;                 // empty share
         const int64_t segs = (sk.bound(u + 1) - 1) / KB - sk.bound(u) / KB + 1;
         if (segs > kMaxSegments) return TGEMM_OK;
     }
-    const int64_t slots = units * kMaxSegments;
+    const int64_t slots = units * kMaxSegments * tiles_per_item;    // one partial tile per slot
     const size_t part = (size_t)slots * kPairBM * kPairBN * sizeof(float);
     int devno = 0;
     cudaGetDevice(&devno);
@@ -749,14 +757,16 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
 // kernel's independent rings win.  So a pair choice (whole tiles or
 // stream-K) becomes a quad one when rows are misaligned.
 void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, int64_t lda, int64_t ldb,
-                                     int in_dtype)
+                                     int in_dtype, bool batched = false)
 {
     if (cfg->cluster_m != 2 || cfg->swap_ab != 0) return;
     const int64_t e = (int64_t)elem_size(in_dtype);
     if ((lda * e) % 128 == 0 && (ldb * e) % 128 == 0) return;
     if (M < 256 || N < 512) return;
     cfg->cluster_m = 4;
-    cfg->split_k = 1;
+    // stream-K where a leftover wave is at most half full (plan_stream_k
+    // keeps whole blocks otherwise): 2000 x 3000 x 5000 53.9 -> 44.0 us
+    cfg->split_k = batched ? 1 : 0;
     cfg->group_m = 8;
 }
 
@@ -831,7 +841,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
             choose_config_model(65, N, K, dev->sm_count, &cfg, bt.count);
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
-        prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype);
+        prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, bt.count > 1);
         cfg.grid = 0;   // sized below from the tiles of all batches
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var, in_dtype);
         if (st != TGEMM_OK) return st;
@@ -903,13 +913,20 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
             if (p.sk_units > 0 && p.dp_tiles == 0) g = 2 * p.sk_units;   // only the sharing pairs have work
         }
     } else if (quad) {
-        // grid counts CTAs: four per quad, at most one quad per block
+        // grid counts CTAs: four per quad, at most one quad per block with
+        // whole blocks
         int quads = cfg.grid > 0 ? cfg.grid / 4 : dev->sm_count / 4;
         const int resident = resident_pairs(dev, var);       // resident quads for this variant
         if (quads > resident) quads = resident;
-        if (quads > p.num_tiles) quads = p.num_tiles;
+        if (cfg.split_k != 0 && quads > p.num_tiles) quads = p.num_tiles;
         if (quads < 1) quads = 1;
         g = 4 * quads;
+        if (cfg.split_k == 0) {
+            tgemm_status st2 = plan_stream_k(&p, quads, dev, stream_ptr, 2);
+            if (st2 != TGEMM_OK) return st2;
+            if (p.sk_units == 0 && quads > p.num_tiles) g = 4 * p.num_tiles;
+            if (p.sk_units > 0 && p.dp_tiles == 0) g = 4 * p.sk_units;   // only the sharing quads have work
+        }
     } else {
         g = cfg.grid > 0 ? cfg.grid : dev->sm_count;
         if (g > p.num_tiles) g = p.num_tiles;

@@ -23,10 +23,16 @@
 //   tmem_full[b]  in both CTAs of a pair; that pair's leader commits;
 //   tmem_empty[b] in each pair leader; the pair's eight epilogue warps arrive.
 // Every wait is bounded (tgemm_wait.cuh); a timeout raises the abort flag in
-// all four CTAs, which then wind down as the pair kernel does.  Whole tiles
-// only (no stream-K tail); when the tile columns are odd the second pair of
-// the last block column computes a tile past N (its B reads zeros, its
-// stores are skipped) so that it still feeds its partner's A.
+// all four CTAs, which then wind down as the pair kernel does.  When the
+// tile columns are odd the second pair of the last block column computes a
+// tile past N (its B reads zeros, its stores are skipped) so that it still
+// feeds its partner's A.
+//
+// Stream-K tail (sk_units > 0), as in the pair kernel but with 256 x 512
+// blocks as the shared items: both pairs of a quad run the same k-range of
+// the same block (they share its A rows), each writes the FP32 partial of
+// its own tile, and per tile half the last arriving CTA adds the partials
+// in k order (quad_stream_k_segment).
 #pragma once
 
 #include "tgemm_kernel_pair.cuh"
@@ -34,6 +40,140 @@
 namespace tgemm {
 
 constexpr int kQuadBN = 2 * kPairBN;    // columns of a quad block
+constexpr int kQuadTiles = 2;          // pair tiles per quad block
+
+// A stream-K segment of the quad kernel, in the four epilogue warps of one
+// CTA: the CTA's FP32 partial of its 128-row half of tile jt of a 256 x 512
+// block goes to a workspace slot (TMA stores), the tile half's arrival
+// counter is bumped, and the CTA that brings the last segment adds all of
+// them in k order (unit u0, u0 + 1, ...: fixed, so results do not depend on
+// timing), applies the fused epilogue, casts, stores C and resets the
+// counter.  Slot s of a unit holds tile jt at workspace rows (2 s + jt) * 256;
+// the counter of tile jt's half `rank` is (2 t_sk + jt) * 2 + rank.  The pair
+// kernel does the same step inline for one tile per item; calling a shared
+// function from it changed its code generation (228 instead of 226
+// registers) and made whole-tile launches 1-1.5 % slower on 8192^3, 4096^3
+// and 4096 x 3072 x 5000 (same GB300, alternating builds), so the two copies
+// stay separate.
+template <int OUT>
+__device__ __forceinline__ void quad_stream_k_segment(const GemmParams &p, const PairWork &w, int jt, uint32_t rank,
+                                                      int q, int ew, int lane, int32_t row0, int32_t col0, int bz,
+                                                      uint32_t t_acc, uint32_t stage_base, uint32_t &cc,
+                                                      uint32_t release_bar, volatile int *last_flag, EpiCtx &ectx,
+                                                      EpiCtx &raw)
+{
+    const int64_t counter = (w.t_sk * kQuadTiles + jt) * 2 + rank;
+    const int32_t prow = (int32_t)((w.slot * kQuadTiles + jt) * kPairBM) + 128 * (int32_t)rank + 32 * q;
+    epilogue_drain<kPairBN, OUT_F32>(&p.tma_ws, INT32_MAX, kPairBN, t_acc, stage_base, cc, prow, 0, lane,
+                                     [&] { ptx::mbar_arrive_cluster(release_bar); }, raw);
+    if (lane == 0) {
+        ptx::bulk_wait_group_all();          // this warp's partial rows are written
+        ptx::fence_proxy_async_global();
+    }
+    __syncwarp();
+    __threadfence();
+    const StreamK sk{p.sk_tiles, p.sk_units, p.num_kb};
+    const int64_t first = w.t_sk * p.num_kb, stop = first + p.num_kb;
+    const int64_t u0 = sk.unit_of(first);
+    ptx::named_barrier(1, kEpiWarps * 32);
+    if (ew == 0 && lane == 0) {
+        uint32_t segs = 0;
+        for (int64_t u = u0; u < sk.sk_units && sk.bound(u) < stop; ++u) ++segs;
+        const uint32_t prev = atomicAdd(&p.counters[counter], 1u);
+        *last_flag = (prev + 1 == segs) ? 1 : 0;
+    }
+    ptx::named_barrier(1, kEpiWarps * 32);
+    if (*last_flag) {
+        // Every segment of this tile half is in: add them in k order.
+        __threadfence();
+        // Column-parallel over this warp's 32 rows: per store chunk (32
+        // FP32 or 64 16-bit columns) each lane owns 4 columns of a row,
+        // so every load of the warp reads whole row segments.  The sums
+        // go straight into the warp's swizzled staging block, which a
+        // TMA store then writes to C.
+        constexpr int kCols = OUT == OUT_F32 ? 32 : 64;
+        constexpr int kLanesPerRow = kCols / 4;
+        constexpr int kRowsPerPass = 32 / kLanesPerRow;
+        constexpr int kPasses = 32 / kRowsPerPass;
+        const int sub_row = lane / kLanesPerRow, col4 = lane % kLanesPerRow;
+        int64_t u_end = u0;
+        while (u_end < sk.sk_units && sk.bound(u_end) < stop) ++u_end;
+        const int64_t warp_row = 128 * (int64_t)rank + 32 * q;       // first row of this warp in the tile
+#pragma unroll 1
+        for (int c = 0; c < kPairBN / kCols; ++c) {
+            float4 acc[kPasses];
+#pragma unroll
+            for (int i = 0; i < kPasses; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int64_t u = u0; u < u_end; ++u) {                    // k order: unit u0, u0 + 1, ...
+                const int64_t prow_u = (sk.slot(u, w.t_sk) * kQuadTiles + jt) * kPairBM + warp_row + sub_row;
+                const float4 *src = reinterpret_cast<const float4 *>(p.partials + (prow_u * kPairBN + c * kCols) +
+                                                                     col4 * 4);
+                float4 t[kPasses];
+#pragma unroll
+                for (int i = 0; i < kPasses; ++i) t[i] = __ldcg(src + (int64_t)i * kRowsPerPass * (kPairBN / 4));
+#pragma unroll
+                for (int i = 0; i < kPasses; ++i) {
+                    acc[i].x += t[i].x;
+                    acc[i].y += t[i].y;
+                    acc[i].z += t[i].z;
+                    acc[i].w += t[i].w;
+                }
+            }
+            const uint32_t sbuf = stage_base + (cc & 1u) * kStageCBytes;
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+            const bool fused = (p.epi & 1) != 0;
+            const bool with_cin = fused && (p.epi & 2) && fetch_cin(ectx, sbuf, col0 + c * kCols, row0, lane);
+            const int64_t col = (int64_t)col0 + c * kCols + col4 * 4;
+            const EpiScalars es = EpiScalars::of(p);
+#pragma unroll
+            for (int i = 0; i < kPasses; ++i) {
+                const uint32_t r = (uint32_t)(i * kRowsPerPass + sub_row);
+                if constexpr (OUT == OUT_F32) {
+                    const uint32_t addr = sbuf + r * 128 + (((uint32_t)col4 ^ (r & 7)) << 4);
+                    if (fused) {
+                        float4 ci = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (with_cin) ci = ptx::ld_shared_v4(addr);
+                        acc[i].x = epi_value(es, acc[i].x, ci.x, col);
+                        acc[i].y = epi_value(es, acc[i].y, ci.y, col + 1);
+                        acc[i].z = epi_value(es, acc[i].z, ci.z, col + 2);
+                        acc[i].w = epi_value(es, acc[i].w, ci.w, col + 3);
+                    }
+                    ptx::st_shared_v4(addr, __float_as_uint(acc[i].x), __float_as_uint(acc[i].y),
+                                      __float_as_uint(acc[i].z), __float_as_uint(acc[i].w));
+                } else {
+                    const uint32_t addr = sbuf + r * 128 + ((((uint32_t)col4 >> 1) ^ (r & 7)) << 4) + (col4 & 1) * 8;
+                    if (fused) {
+                        float2 c0 = make_float2(0.f, 0.f), c1 = make_float2(0.f, 0.f);
+                        if (with_cin) {
+                            uint32_t q0, q1;
+                            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(q0), "=r"(q1) : "r"(addr) : "memory");
+                            c0 = unpack_out(q0, OUT);
+                            c1 = unpack_out(q1, OUT);
+                        }
+                        acc[i].x = epi_value(es, acc[i].x, c0.x, col);
+                        acc[i].y = epi_value(es, acc[i].y, c0.y, col + 1);
+                        acc[i].z = epi_value(es, acc[i].z, c1.x, col + 2);
+                        acc[i].w = epi_value(es, acc[i].w, c1.y, col + 3);
+                    }
+                    const uint32_t a0 = pack_out(acc[i].x, acc[i].y, OUT);
+                    const uint32_t a1 = pack_out(acc[i].z, acc[i].w, OUT);
+                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a0), "r"(a1) : "memory");
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int32_t x = col0 + c * kCols;
+                if (x < p.N && row0 < p.M) ptx::tma_store_3d(&p.tma_c, sbuf, x, row0, bz);
+                ptx::bulk_commit_group();
+            }
+            ++cc;
+        }
+        if (ew == 0 && lane == 0) p.counters[counter] = 0u;   // ready for the next call
+    }
+}
+
 
 template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
 __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_constant__ GemmParams p)
@@ -128,14 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int blk = cluster_id; ok && blk < p.num_tiles; blk += num_clusters) {
+            PairWorkIter items(p, cluster_id, num_clusters);
+            PairWork w;
+            while (ok && items.next(w)) {
                 int64_t tr, tc;
                 int bz;
-                block_coord(blk, bz, tr, tc);
+                block_coord(w.tile, bz, tr, tc);
                 const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 64 * (int32_t)q;
                 const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
                 const int32_t za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = w.k0; kb < w.k1; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
@@ -178,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
             uint32_t ph = 0;
             uint32_t local = 0;
             bool ok = true;
-            for (int blk = cluster_id; ok && blk < p.num_tiles; blk += num_clusters, ++local) {
+            PairWorkIter items(p, cluster_id, num_clusters);
+            PairWork w;
+            for (; ok && items.next(w); ++local) {
                 const uint32_t buf = local & 1u;
                 const uint32_t bph = (local >> 1) & 1u;
                 if (!wait_bounded(tempty_bar(buf), bph ^ 1u, wc, SITE_MMA_TMEM_EMPTY)) {
@@ -187,14 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * kPairBN;
-                for (int kb = 0; kb < p.num_kb;) {
+                for (int kb = w.k0; kb < w.k1;) {
                     // two k-blocks per pass when the second stage is already full
                     if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     const int n =
-                        (kb + 1 < p.num_kb && s + 1 < STAGES && ptx::mbar_test_wait(full_bar(s + 1), ph)) ? 2 : 1;
+                        (kb + 1 < w.k1 && s + 1 < STAGES && ptx::mbar_test_wait(full_bar(s + 1), ph)) ? 2 : 1;
                     ptx::tc_fence_after_sync();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -206,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
                                 const uint64_t ad = desc_at(kDescKMajor, a_addr + k * (kUmmaK * 2));
                                 const uint64_t bd =
                                     desc_at(kDescB, b_addr + (B_MN ? k * (kUmmaK * 128) : k * (kUmmaK * 2)));
-                                mma_issue<KIND, true>(d_tmem, ad, bd, p.idesc, (kb + h > 0 || k > 0) ? 1u : 0u);
+                                mma_issue<KIND, true>(d_tmem, ad, bd, p.idesc, (kb + h > w.k0 || k > 0) ? 1u : 0u);
                             }
                             ptx::mma_commit_pair(empty_bar(s + h), 0xF);   // the stage is free for this pair, in all four CTAs
                         }
@@ -234,27 +378,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
         const int qw = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
         const uint32_t stage_base = sC + ew * 2 * kStageCBytes;
+        volatile int *last_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::flag_off);
         EpiCtx ectx{&p, drain_bar + 8u * (1 + ew), 0u, wc};
+        EpiCtx raw{nullptr, 0u, 0u, wc};                 // stream-K partials: raw FP32
         uint32_t local = 0, cc = 0;
-        for (int blk = cluster_id; blk < p.num_tiles; blk += num_clusters, ++local) {
+        PairWorkIter items(p, cluster_id, num_clusters);
+        PairWork w;
+        for (; items.next(w); ++local) {
             const uint32_t buf = local & 1u;
             const uint32_t bph = (local >> 1) & 1u;
             const bool got = wait_bounded(tfull_bar(buf), bph, wc, SITE_EPI_TMEM_FULL);
-            if (!__all_sync(0xffffffffu, got)) {
+            // The four epilogue warps decide together (the stream-K hand-off
+            // synchronises them, so none may leave alone).
+            if (!ptx::named_barrier_and(2, kEpiWarps * 32, got)) {
                 aborted = true;
                 break;
             }
             ptx::tc_fence_after_sync();
             int64_t tr, tc;
             int bz;
-            block_coord(blk, bz, tr, tc);
+            block_coord(w.tile, bz, tr, tc);
             ectx.z = bz;
             const int32_t row0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 32 * qw;
             const int32_t col0 = (int32_t)tc * kPairBN;
             const uint32_t t_acc = tmem_base + lane_base + buf * kPairBN;
             const uint32_t release_bar = ptx::map_to_cta(tempty_bar(buf), pair_leader);
-            epilogue_drain<kPairBN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
-                                         [&] { ptx::mbar_arrive_cluster(release_bar); }, ectx);
+            if (!w.partial) {
+                epilogue_drain<kPairBN, OUT>(&p.tma_c, p.M, p.N, t_acc, stage_base, cc, row0, col0, lane,
+                                             [&] { ptx::mbar_arrive_cluster(release_bar); }, ectx);
+                continue;
+            }
+            // stream-K segment of this pair's tile (tile q of the block)
+            quad_stream_k_segment<OUT>(p, w, (int)q, rank, qw, ew, lane, row0, col0, bz, t_acc, stage_base, cc,
+                                     release_bar, last_flag, ectx, raw);
         }
         if (lane == 0) ptx::bulk_wait_group_all();
         __syncwarp();

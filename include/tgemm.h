@@ -74,9 +74,11 @@ typedef enum {
  * through a global FP32 workspace (swap_ab = 1) or inside a thread-block
  * cluster of split_k CTAs (swap_ab = 2, cluster_m = split_k); grid is the
  * number of CTAs launched (0 = the library's choice).  Tile kernels:
- * cluster_m = 1 (bm 128, bn 128 or 256), 2 (a CTA pair, 256 x 256; split_k =
- * 0 adds a stream-K tail) or 4 (two CTA pairs on neighbouring 256 x 256
- * tiles sharing their A rows, whole tiles).
+ * cluster_m = 1 (bm 128, bn 128 or 256), 2 (a CTA pair, 256 x 256) or 4
+ * (two CTA pairs on neighbouring 256 x 256 tiles sharing their A rows); for
+ * cluster_m = 2 and 4, split_k = 0 adds a stream-K tail (the last waves'
+ * tiles, or the quad's 256 x 512 blocks, shared out by k-range and summed
+ * in a fixed order).
  */
 typedef struct {
     int bm, bn, bk, stages, cluster_m, group_m, split_k, swap_ab, grid;

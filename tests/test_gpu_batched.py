@@ -35,6 +35,7 @@ CONFIGS = {
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
     "quad": C(bm=256, stages=6, cluster_m=4),
+    "quad_streamk": C(bm=256, stages=6, cluster_m=4, split_k=0),
 }
 
 

@@ -39,6 +39,7 @@ CONFIGS = {
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
     "quad": C(bm=256, stages=6, cluster_m=4),
+    "quad_streamk": C(bm=256, stages=6, cluster_m=4, split_k=0),
     "skinny_cluster": C(bn=16, stages=12, cluster_m=3, group_m=1, split_k=3, swap_ab=2),
     "skinny_workspace": C(bn=16, stages=4, group_m=1, split_k=5, swap_ab=1),
 }
@@ -102,7 +103,7 @@ def test_epilogue_output_and_bias_types(cfg_name, out_dtype, bias_dtype):
     run_case(cfg_name, "all", out_dtype=out_dtype, bias_dtype=bias_dtype, layout=gen.B_KN)
 
 
-@pytest.mark.parametrize("cfg_name", ["cta128", "pair_streamk", "skinny_workspace"])
+@pytest.mark.parametrize("cfg_name", ["cta128", "pair_streamk", "quad_streamk", "skinny_workspace"])
 def test_epilogue_in_place_accumulate(cfg_name):
     """C_in may be C itself: D = alpha*A*B + beta*C_old."""
     run_case(cfg_name, "beta", inplace=True)

@@ -46,6 +46,7 @@ CONFIGS = {
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
     "quad": C(bm=256, stages=6, cluster_m=4),
+    "quad_streamk": C(bm=256, stages=6, cluster_m=4, split_k=0),
 }
 
 
@@ -100,6 +101,21 @@ def test_fp8_random_matches_oracle(name, fp8, out_dtype):
     assert_close(out[:M, :N].double().numpy(), ref, bound, out_dtype, "%s %s" % (name, fp8))
 
 
+@pytest.mark.parametrize("name", ["pair_streamk", "quad_streamk"])
+@pytest.mark.parametrize("fp8", sorted(FP8))
+def test_fp8_stream_k_integers_bit_exact(name, fp8):
+    # 1100 x 1300 with K = 3000 (24 k-blocks of 128 FP8 elements): enough
+    # k-blocks that the tail is shared out by k-range on both kernels.
+    dt = FP8[fp8]
+    M, N, K = 1100, 1300, 3000
+    a, b = fp8_operands(M, N, K, dt, gen.ints(-3, 3), seed=15)
+    out = run(a, b, M, N, K, dt, gen.F32, CONFIGS[name])
+    ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, dt)
+    got = bits(out[:M, :N], gen.F32)
+    want = oracle.round_bits(ref, gen.F32)
+    assert np.array_equal(got, want), "%d bit mismatches" % (got != want).sum()
+
+
 @pytest.mark.parametrize("fp8", sorted(FP8))
 @pytest.mark.parametrize("M,N,K", [(1, 1, 16), (16, 4096, 4096), (64, 300, 2000), (129, 257, 4112),
                                    (1024, 1024, 16384)])
@@ -130,7 +146,7 @@ def test_fp8_scaled_epilogue_bias_gelu():
     alpha = 0.0625
     ep = tgemm.Epilogue(alpha=alpha, beta=0.0, c_in=None, ldc_in=0, bias=bias_d.data_ptr(), bias_dtype=gen.F32,
                         act=tgemm.ACT_GELU_TANH)
-    for name in ("cta256", "pair", "pair_streamk"):
+    for name in ("cta256", "pair", "pair_streamk", "quad_streamk"):
         out = run(a, b, M, N, K, dt, gen.BF16, CONFIGS[name], ep=ep)
         ref, bound = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, dt)
         want = oracle.epilogue(ref, alpha=alpha, bias=bias.double().numpy(), act=oracle.ACT_GELU_TANH)

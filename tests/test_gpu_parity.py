@@ -205,7 +205,7 @@ def test_runs_on_a_side_stream():
 def test_misaligned_rows_pick_the_quad_kernel():
     # K = 5000 BF16 rows are 10000 bytes: not a multiple of 128
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5000, gen.B_NK, gen.BF16, gen.BF16)
-    assert rc == 0 and (c.cluster_m, c.bm, c.bn, c.split_k) == (4, 256, 256, 1)
+    assert rc == 0 and (c.cluster_m, c.bm, c.bn, c.split_k) == (4, 256, 256, 0)
     # FP8 rows of 5008 bytes (16-byte aligned, not 128) are misaligned too; 5120-byte rows are not
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5008, gen.B_NK, gen.E4M3, gen.BF16)
     assert rc == 0 and c.cluster_m == 4
@@ -399,6 +399,48 @@ def test_stream_k_is_deterministic_across_calls():
     M, N, K = 640, 1280, 6000
     a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.normal(0, 1), seed=59)
     outs = [run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, config=sk_cfg()) for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# ---- stream-K tail of the quad kernel ---------------------------------------------
+
+def qsk_cfg(quads=0, group_m=8):
+    return tgemm.Config(bm=256, bn=256, bk=64, stages=6, cluster_m=4, group_m=group_m, split_k=0, swap_ab=0,
+                        grid=4 * quads)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+@pytest.mark.parametrize("n", [1300, 1100], ids=["even_cols", "odd_cols"])
+@pytest.mark.parametrize("quads", [2, 3, 4, 6, 7, 0])
+def test_quad_stream_k_integers_exact(layout, n, quads):
+    """1100 x N blocks of 256 x 512 (5 x 3 = 15) over 2, 3, 4, 6, 7 or all
+    resident quads.  Where the leftover wave is at most half full (2, 6, 7
+    quads) its blocks are shared out by k-block; with more quads than blocks
+    all of them are; 3 quads leave no leftover and 4 a more than half full
+    one, which stay whole blocks.  Both pairs of a quad run the same k-range,
+    and each tile half is summed from its partials.  N = 1100 has odd tile
+    columns: the last block's second tile lies past N and stores nothing."""
+    M, N, K = 1100, n, 1500
+    a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=83)
+    check_full(a, b, M, N, K, layout, gen.BF16, gen.F32, exact=True, config=qsk_cfg(quads),
+               what="quad stream-K quads=%d N=%d %s" % (quads, N, LNAME[layout]))
+
+
+@pytest.mark.parametrize("shape", [(256, 512, 8192), (300, 520, 4000), (1000, 1500, 2500), (2304, 1280, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out_dtype", [gen.F32, gen.BF16], ids=["o32", "obf16"])
+def test_quad_stream_k_random_values(shape, out_dtype):
+    """Random values, including rows that are not 128-byte multiples
+    (K = 2500 BF16: 5000-byte rows), which is where the quad is chosen."""
+    M, N, K = shape
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=89)
+    check_full(a, b, M, N, K, gen.B_NK, gen.BF16, out_dtype, config=qsk_cfg(), what="quad stream-K %s" % (shape,))
+
+
+def test_quad_stream_k_is_deterministic_across_calls():
+    M, N, K = 640, 1280, 6000
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.normal(0, 1), seed=97)
+    outs = [run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, config=qsk_cfg()) for _ in range(3)]
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 

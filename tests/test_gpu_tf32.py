@@ -44,6 +44,7 @@ CONFIGS = {
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
     "quad": C(bm=256, stages=6, cluster_m=4),
+    "quad_streamk": C(bm=256, stages=6, cluster_m=4, split_k=0),
 }
 
 
@@ -133,7 +134,7 @@ def test_tf32_epilogue_residual():
     cin_d = cin.to(DEV)
     ep = tgemm.Epilogue(alpha=0.5, beta=1.0, c_in=cin_d.data_ptr(), ldc_in=ldc, bias=None, bias_dtype=gen.F32,
                         act=tgemm.ACT_NONE)
-    for name in ("cta256", "pair", "pair_streamk"):
+    for name in ("cta256", "pair", "pair_streamk", "quad_streamk"):
         out = run(a, b, M, N, K, gen.F32, CONFIGS[name], ep=ep)
         acc, bound = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, TF32)
         c64 = cin[:, :N].double().numpy()
