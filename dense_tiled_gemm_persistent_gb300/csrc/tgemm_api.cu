@@ -1114,6 +1114,30 @@ TGEMM_EXPORT tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn,
     return TGEMM_OK;
 }
 
+namespace tgemm {
+// tgemm_debug.cu
+cudaError_t launch_tile_order_probe(int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t count, int32_t *rows,
+                                    int32_t *cols, cudaStream_t st);
+}  // namespace tgemm
+
+TGEMM_EXPORT tgemm_status tgemm_debug_tile_order(int64_t M, int64_t N, int bm, int bn, int group_m, int32_t *rows,
+                                                 int32_t *cols, void *stream)
+{
+    if (M <= 0 || N <= 0 || bm <= 0 || bn <= 0 || group_m <= 0 || !rows || !cols) return TGEMM_ERR_INVALID_ARG;
+    const TileGrid g(M, N, bm, bn);
+    // the kernels' 32-bit form: the host keeps every grid they run below this
+    if (g.count() * (int64_t)group_m >= ((int64_t)1 << 31)) return TGEMM_ERR_UNSUPPORTED;
+    DeviceState *dev = nullptr;
+    tgemm_status st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    if (launch_tile_order_probe((int32_t)g.tiles_m, (int32_t)g.tiles_n, group_m, (int32_t)g.count(), rows, cols,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
 TGEMM_EXPORT tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream)
 {
     DeviceState *dev = nullptr;

@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 # Every symbol include/tgemm.h declares.
 EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
-           "tgemm_debug_wait_timeout", "tgemm_run_noalloc", "tgemm_run_ex", "tgemm_run_strided_batched")
+           "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_run_noalloc", "tgemm_run_ex",
+           "tgemm_run_strided_batched")
 
 ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH):
         lib.tgemm_run_noalloc.restype = _i
         lib.tgemm_debug_wait_timeout.argtypes = [ctypes.c_uint32, _p]
         lib.tgemm_debug_wait_timeout.restype = _i
+        lib.tgemm_debug_tile_order.argtypes = [_i64, _i64, _i, _i, _i, _p, _p, _p]
+        lib.tgemm_debug_tile_order.restype = _i
         _lib = lib
         return lib
 
@@ -158,6 +161,12 @@ def tgemm_tile_coord(M, N, bm, bn, group_m, bid):
 
 def tgemm_debug_wait_timeout(timeout_us: int, stream=None) -> int:
     return load().tgemm_debug_wait_timeout(timeout_us, stream)
+
+
+def tgemm_debug_tile_order(M, N, bm, bn, group_m, rows, cols, stream=None) -> int:
+    """The scheduler's tile order computed on the GPU into two int32 device
+    arrays (pointers) of ceil(M/bm) * ceil(N/bn) elements."""
+    return load().tgemm_debug_tile_order(M, N, bm, bn, group_m, rows, cols, stream)
 
 
 # ---- torch convenience ------------------------------------------------------

@@ -194,6 +194,23 @@ tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn, int group_m,
                               int64_t *bid_m, int64_t *bid_n);
 
 /*
+ * Diagnostic: the tile order of the persistent scheduler as the GPU computes
+ * it.  For every tile number bid of the ceil(M/bm) x ceil(N/bn) grid, one
+ * launch writes the tile row to rows[bid] and the tile column to cols[bid],
+ * using the device copy of the mapping the GEMM kernels run (the
+ * swizzle_2d_from_bid order of "Writing high-performance matrix
+ * multiplication with NVIDIA CUDA Tile", section "Performance optimisation:
+ * Swizzle"), so that tests can check it against tgemm_tile_coord.
+ *   rows, cols  caller-owned device arrays of at least ceil(M/bm) * ceil(N/bn)
+ *               int32 elements
+ * Asynchronous on `stream`.  Returns TGEMM_ERR_INVALID_ARG for non-positive
+ * sizes or NULL arrays, TGEMM_ERR_UNSUPPORTED when tiles * group_m reaches
+ * 2^31 (beyond the 32-bit form the kernels use).
+ */
+tgemm_status tgemm_debug_tile_order(int64_t M, int64_t N, int bm, int bn, int group_m, int32_t *rows, int32_t *cols,
+                                    void *stream);
+
+/*
  * Diagnostic: launch one block that waits on a pipeline barrier nobody
  * signals, with a wait limit of `timeout_us` microseconds.  The kernel gives
  * up, records TGEMM_ERR_TIMEOUT's fault code in the status word and returns;

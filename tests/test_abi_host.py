@@ -105,6 +105,14 @@ def test_run_config_rejects_unknown_configuration(lib):
     assert rc == tgemm.ERR_UNSUPPORTED
 
 
+def test_tile_order_probe_checks_arguments_on_the_host(lib):
+    # rejected before any device query: no GPU needed
+    assert tgemm.tgemm_debug_tile_order(0, 10, 128, 128, 8, FAKE, FAKE) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_tile_order(10, 10, 128, 0, 8, FAKE, FAKE) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_tile_order(10, 10, 128, 128, 8, None, FAKE) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_tile_order(1 << 20, 1 << 20, 1, 1, 8, FAKE, FAKE) == tgemm.ERR_UNSUPPORTED
+
+
 # ---- tile space and grouped order ---------------------------------------------
 
 def coords(M, N, bm, bn, g):

@@ -222,6 +222,37 @@ def test_query_config_matches_what_runs():
     assert c.grid <= torch.cuda.get_device_properties(0).multi_processor_count
 
 
+@pytest.mark.parametrize("group_m", [1, 2, 3, 4, 8, 16])
+def test_device_tile_order_equals_host(group_m):
+    """The kernels' tile order, computed on the GPU, equals the host mapping
+    (tgemm_tile_coord) and is a bijection onto the tile grid, for grids up
+    to 64 x 64 tiles including short last bands."""
+    sizes = [1, 2, 3, 5, 7, 8, 13, 16, 31, 64]
+    for tm in sizes:
+        for tn in sizes:
+            M, N = 128 * tm - 5, 256 * tn - 7
+            n = tm * tn
+            rows = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+            cols = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+            assert tgemm.tgemm_debug_tile_order(M, N, 128, 256, group_m, rows.data_ptr(), cols.data_ptr()) == 0
+            assert tgemm.tgemm_check() == 0
+            r, c = rows.cpu().numpy(), cols.cpu().numpy()
+            host = [tgemm.tgemm_tile_coord(M, N, 128, 256, group_m, bid) for bid in range(n)]
+            assert all(h[0] == 0 for h in host)
+            assert np.array_equal(r, [h[1] for h in host]) and np.array_equal(c, [h[2] for h in host]), \
+                "grid %dx%d group %d" % (tm, tn, group_m)
+            assert len(set(zip(r.tolist(), c.tolist()))) == n
+
+
+def test_device_tile_order_rejects_bad_arguments():
+    x = torch.empty(4, dtype=torch.int32, device="cuda")
+    assert tgemm.tgemm_debug_tile_order(0, 10, 128, 128, 8, x.data_ptr(), x.data_ptr()) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_tile_order(10, 10, 128, 128, 0, x.data_ptr(), x.data_ptr()) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_tile_order(10, 10, 128, 128, 8, None, x.data_ptr()) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_tile_order(1 << 20, 1 << 20, 1, 1, 8, x.data_ptr(), x.data_ptr()) == \
+        tgemm.ERR_UNSUPPORTED
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """A wait on a barrier nothing signals gives up after ~1 ms; the host sees
     TGEMM_ERR_TIMEOUT and the next GEMM still runs correctly."""
