@@ -69,9 +69,12 @@ def candidates(tg, M, N=0):
     out.append(("pair256sk", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=0, swap_ab=0,
                                grid=0)))
     if M >= 256 and N >= 512:
-        # two pairs sharing A (cluster of four): a quarter fewer operand loads per CTA
+        # two pairs sharing A (cluster of four): a quarter fewer operand loads per CTA;
+        # with a stream-K tail when the leftover wave of blocks is at most half full
         out.append(("quad256", C(bm=256, bn=256, bk=64, stages=6, cluster_m=4, group_m=8, split_k=1, swap_ab=0,
                                  grid=0)))
+        out.append(("quad256sk", C(bm=256, bn=256, bk=64, stages=6, cluster_m=4, group_m=8, split_k=0, swap_ab=0,
+                                   grid=0)))
     if M >= 4096 and N >= 4096:
         # wider raster bands: more A reuse in L2 per wave on the largest shapes
         out.append(("pair256g16", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=16, split_k=1, swap_ab=0,

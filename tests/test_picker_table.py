@@ -45,8 +45,8 @@ def test_every_row_is_a_legal_configuration():
         else:
             assert (e["cluster_m"], e["bm"]) in ((1, 128), (2, 256), (4, 256))   # 4: two pairs sharing A
             if e["cluster_m"] == 4:
-                assert e["bn"] == 256 and e["split_k"] == 1
-            assert e["split_k"] == 1 or (e["split_k"] == 0 and e["cluster_m"] == 2)   # 0: stream-K tail
+                assert e["bn"] == 256
+            assert e["split_k"] == 1 or (e["split_k"] == 0 and e["cluster_m"] in (2, 4))   # 0: stream-K tail
 
 
 def test_table_rows_are_the_fastest_measurement_of_their_point():
@@ -65,5 +65,5 @@ def test_large_square_problems_pick_the_cta_pair():
     # 256 x 256 tiles on CTA pairs: whole tiles, stream-K tail, wider raster
     # bands, or two pairs sharing A
     big = [e for e in rows() if e["em"] >= 13 and e["en"] >= 13 and e["ek"] >= 12]
-    assert big and all(e["kind"] in ("pair256", "pair256sk", "pair256g16", "quad256") for e in big)
+    assert big and all(e["kind"] in ("pair256", "pair256sk", "pair256g16", "quad256", "quad256sk") for e in big)
     assert all(e["bm"] == 256 and e["bn"] == 256 and e["cluster_m"] in (2, 4) for e in big)
