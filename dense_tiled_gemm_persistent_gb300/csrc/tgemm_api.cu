@@ -290,6 +290,15 @@ int cluster_stages(int npad) { return npad == 16 ? ClusterSplitPlan<16>::stages
 
 void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch = 1);
 
+// CTAs of a quad launch (four per quad): one quad per 256 x 512 block with
+// whole blocks, every quad with a stream-K tail; resident limits apply later.
+int quad_grid(int64_t M, int64_t N, int split_k, int sm_count)
+{
+    const int64_t blocks = ceil_div(M, kPairBM) * ceil_div(ceil_div(N, kPairBN), 2);
+    const int64_t quads = split_k == 0 ? sm_count / 4 : std::min<int64_t>(blocks, sm_count / 4);
+    return (int)(4 * std::max<int64_t>(quads, 1));
+}
+
 // The configuration tgemm_run uses: the measured table where it covers the
 // shape and its entry is legal for it, the wave cost model otherwise.
 void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, tgemm_config *cfg)
@@ -305,6 +314,8 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, 
                 cfg->grid = cfg->split_k == 0 ? 2 * (sm_count / 2)
                                               : (int)(2 * std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(),
                                                                             sm_count / 2));
+            else if (cfg->cluster_m == 4)
+                cfg->grid = quad_grid(M, N, cfg->split_k, sm_count);
             else
                 cfg->grid = (int)std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(), sm_count);
             return;
@@ -757,7 +768,7 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
 // kernel's independent rings win.  So a pair choice (whole tiles or
 // stream-K) becomes a quad one when rows are misaligned.
 void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, int64_t lda, int64_t ldb,
-                                     int in_dtype, bool batched = false)
+                                     int in_dtype, int sm_count, bool batched = false)
 {
     if (cfg->cluster_m != 2 || cfg->swap_ab != 0) return;
     const int64_t e = (int64_t)elem_size(in_dtype);
@@ -768,6 +779,7 @@ void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, in
     // keeps whole blocks otherwise): 2000 x 3000 x 5000 53.9 -> 44.0 us
     cfg->split_k = batched ? 1 : 0;
     cfg->group_m = 8;
+    cfg->grid = quad_grid(M, N, cfg->split_k, sm_count);
 }
 
 tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -841,7 +853,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
             choose_config_model(65, N, K, dev->sm_count, &cfg, bt.count);
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
-        prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, bt.count > 1);
+        prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, dev->sm_count, bt.count > 1);
         cfg.grid = 0;   // sized below from the tiles of all batches
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var, in_dtype);
         if (st != TGEMM_OK) return st;
@@ -1012,7 +1024,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, dev->sm_count, out_cfg);
     if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(65, N, K, dev->sm_count, out_cfg);
     // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
-    prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype);
+    prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
     return TGEMM_OK;
 }
 

@@ -206,11 +206,26 @@ def test_misaligned_rows_pick_the_quad_kernel():
     # K = 5000 BF16 rows are 10000 bytes: not a multiple of 128
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5000, gen.B_NK, gen.BF16, gen.BF16)
     assert rc == 0 and (c.cluster_m, c.bm, c.bn, c.split_k) == (4, 256, 256, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert c.grid == 4 * (sms // 4)          # stream-K tail: every quad
     # FP8 rows of 5008 bytes (16-byte aligned, not 128) are misaligned too; 5120-byte rows are not
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5008, gen.B_NK, gen.E4M3, gen.BF16)
     assert rc == 0 and c.cluster_m == 4
     rc, c = tgemm.tgemm_query_config(4000, 3000, 5120, gen.B_NK, gen.E4M3, gen.BF16)
     assert rc == 0 and c.cluster_m != 4
+
+
+def test_query_config_grid_is_the_launch_grid_for_quads():
+    """A configuration returned by tgemm_query_config and passed back to
+    tgemm_run_config launches what tgemm_run launches: for the quad, one
+    cluster of four per 256 x 512 block (whole blocks)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for M, N, K in [(256, 14336, 4096), (192, 14336, 4096), (256, 16384, 4096)]:
+        rc, c = tgemm.tgemm_query_config(M, N, K, gen.B_NK, gen.F16, gen.F16)
+        assert rc == 0
+        if c.cluster_m == 4 and c.split_k == 1:
+            blocks = -(-M // 256) * -(-(-(-N // 256)) // 2)
+            assert c.grid == 4 * min(blocks, sms // 4), (M, N, K, c.grid)
 
 
 def test_query_config_matches_what_runs():
