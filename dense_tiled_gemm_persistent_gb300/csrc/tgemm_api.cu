@@ -600,15 +600,16 @@ int resident_pairs(DeviceState *dev, const KernelVariant *v)
 // partials of 60 shared blocks cost more than the idle third of a wave.
 constexpr int64_t kMinSkIters = 8;
 
-tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *stream_ptr, int tiles_per_item = 1)
+// The split itself, without allocation: T items of KB k-blocks over P units.
+// Returns false to keep whole items; otherwise dp whole items come first and
+// the sk_items after them are shared by `units` units in equal shares of
+// k-block iterations.  tgemm_stream_k_plan exposes it to host tests.
+bool stream_k_split(int64_t T, int64_t KB, int64_t P, int tiles_per_item, int64_t *dp_out, int64_t *sk_out,
+                    int64_t *units_out)
 {
-    (void)dev;
-    const int64_t T = p->num_tiles, KB = p->num_kb, P = pairs;
-    p->dp_tiles = (int32_t)T;
-    p->sk_tiles = 0;
-    p->sk_units = 0;
+    if (T <= 0 || KB <= 0 || P <= 0) return false;
     const int64_t full = T / P, rem = T % P;
-    if (rem == 0) return TGEMM_OK;
+    if (rem == 0) return false;
     int64_t dp, sk_tiles, units;
     if (full >= 1 && 2 * rem <= P) {
         // The leftover wave is at most half full: keep every full wave whole
@@ -621,22 +622,38 @@ tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *str
         if (units > P) units = P;
     } else {
         // Share the last full wave and the leftover tiles among all pairs.
-        if (tiles_per_item > 1 && full >= 1) return TGEMM_OK;
+        if (tiles_per_item > 1 && full >= 1) return false;
         dp = full >= 1 ? (full - 1) * P : 0;
         sk_tiles = T - dp;
         units = sk_tiles * KB / kMinSkIters;
         if (units > P) units = P;
     }
-    const int64_t total = sk_tiles * KB;
-    if (units <= sk_tiles && full == 0) return TGEMM_OK;   // no more pairs than tiles to share with
-    if (units < 2) return TGEMM_OK;
-    if (2 * tiles_per_item * sk_tiles * 4 > (int64_t)kCounterBytes) return TGEMM_OK;
+    if (units <= sk_tiles && full == 0) return false;   // no more pairs than tiles to share with
+    if (units < 2) return false;
+    // never a longer critical path than whole items (shallow K: shares held
+    // at kMinSkIters iterations can exceed one item's k-blocks)
+    if ((dp / P) * KB + ceil_div(sk_tiles * KB, units) > ceil_div(T, P) * KB) return false;
+    if (2 * tiles_per_item * sk_tiles * 4 > (int64_t)kCounterBytes) return false;
     const StreamK sk{sk_tiles, units, KB};
     for (int64_t u = 0; u < units; ++u) {
-        if (sk.bound(u + 1) <= sk.bound(u)) return TGEMM_OK;                 // empty share
+        if (sk.bound(u + 1) <= sk.bound(u)) return false;                 // empty share
         const int64_t segs = (sk.bound(u + 1) - 1) / KB - sk.bound(u) / KB + 1;
-        if (segs > kMaxSegments) return TGEMM_OK;
+        if (segs > kMaxSegments) return false;
     }
+    *dp_out = dp;
+    *sk_out = sk_tiles;
+    *units_out = units;
+    return true;
+}
+
+tgemm_status plan_stream_k(GemmParams *p, int pairs, DeviceState *dev, void *stream_ptr, int tiles_per_item = 1)
+{
+    (void)dev;
+    p->dp_tiles = p->num_tiles;
+    p->sk_tiles = 0;
+    p->sk_units = 0;
+    int64_t dp, sk_tiles, units;
+    if (!stream_k_split(p->num_tiles, p->num_kb, pairs, tiles_per_item, &dp, &sk_tiles, &units)) return TGEMM_OK;
     const int64_t slots = units * kMaxSegments * tiles_per_item;    // one partial tile per slot
     const size_t part = (size_t)slots * kPairBM * kPairBN * sizeof(float);
     int devno = 0;
@@ -1131,6 +1148,24 @@ namespace tgemm {
 cudaError_t launch_tile_order_probe(int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t count, int32_t *rows,
                                     int32_t *cols, cudaStream_t st);
 }  // namespace tgemm
+
+TGEMM_EXPORT tgemm_status tgemm_stream_k_plan(int64_t items, int64_t k_blocks, int units, int tiles_per_item,
+                                              int64_t *dp_items, int64_t *sk_items, int64_t *sk_units)
+{
+    if (items < 0 || k_blocks < 1 || units < 1 || (tiles_per_item != 1 && tiles_per_item != 2) || !dp_items ||
+        !sk_items || !sk_units)
+        return TGEMM_ERR_INVALID_ARG;
+    int64_t dp = items, sk = 0, u = 0;
+    if (!stream_k_split(items, k_blocks, units, tiles_per_item, &dp, &sk, &u)) {
+        dp = items;
+        sk = 0;
+        u = 0;
+    }
+    *dp_items = dp;
+    *sk_items = sk;
+    *sk_units = u;
+    return TGEMM_OK;
+}
 
 TGEMM_EXPORT tgemm_status tgemm_debug_tile_order(int64_t M, int64_t N, int bm, int bn, int group_m, int32_t *rows,
                                                  int32_t *cols, void *stream)

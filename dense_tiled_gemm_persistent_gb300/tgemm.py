@@ -22,8 +22,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 # Every symbol include/tgemm.h declares.
 EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
-           "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_run_noalloc", "tgemm_run_ex",
-           "tgemm_run_strided_batched")
+           "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_stream_k_plan", "tgemm_run_noalloc",
+           "tgemm_run_ex", "tgemm_run_strided_batched")
 
 ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 
@@ -94,6 +94,9 @@ def load(path: str = LIB_PATH):
         lib.tgemm_debug_wait_timeout.restype = _i
         lib.tgemm_debug_tile_order.argtypes = [_i64, _i64, _i, _i, _i, _p, _p, _p]
         lib.tgemm_debug_tile_order.restype = _i
+        lib.tgemm_stream_k_plan.argtypes = [_i64, _i64, _i, _i, ctypes.POINTER(_i64), ctypes.POINTER(_i64),
+                                            ctypes.POINTER(_i64)]
+        lib.tgemm_stream_k_plan.restype = _i
         _lib = lib
         return lib
 
@@ -157,6 +160,14 @@ def tgemm_tile_coord(M, N, bm, bn, group_m, bid):
     r, c = _i64(), _i64()
     rc = load().tgemm_tile_coord(M, N, bm, bn, group_m, bid, ctypes.byref(r), ctypes.byref(c))
     return rc, r.value, c.value
+
+
+def tgemm_stream_k_plan(items, k_blocks, units, tiles_per_item=1):
+    """(status, whole items, shared items, sharing units) of a stream-K launch."""
+    dp, sk, u = _i64(), _i64(), _i64()
+    rc = load().tgemm_stream_k_plan(items, k_blocks, units, tiles_per_item, ctypes.byref(dp), ctypes.byref(sk),
+                                    ctypes.byref(u))
+    return rc, dp.value, sk.value, u.value
 
 
 def tgemm_debug_wait_timeout(timeout_us: int, stream=None) -> int:

@@ -194,6 +194,22 @@ tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn, int group_m,
                               int64_t *bid_m, int64_t *bid_n);
 
 /*
+ * The stream-K plan of a pair (tiles_per_item = 1) or quad (2: its 256 x 512
+ * blocks) launch, exposed for host-side tests; no device is touched.  `items`
+ * work items of `k_blocks` k-blocks each run on `units` resident CTA pairs or
+ * quads.  On return the first *dp_items items are dealt out whole and the
+ * *sk_items after them are shared by *sk_units units, unit u taking k-block
+ * iterations [u * I / U, (u + 1) * I / U) of the I = sk_items * k_blocks
+ * shared ones, U = *sk_units (floor division).  *sk_units = 0 (with
+ * *dp_items = items) keeps every item whole.  Sharing splits work by
+ * iterations instead of tiles, a choice of this library: the pages deal
+ * whole tiles to blocks.  Returns TGEMM_ERR_INVALID_ARG for items < 0,
+ * k_blocks < 1, units < 1, tiles_per_item not 1 or 2, or NULL outputs.
+ */
+tgemm_status tgemm_stream_k_plan(int64_t items, int64_t k_blocks, int units, int tiles_per_item,
+                                 int64_t *dp_items, int64_t *sk_items, int64_t *sk_units);
+
+/*
  * Diagnostic: the tile order of the persistent scheduler as the GPU computes
  * it.  For every tile number bid of the ceil(M/bm) x ceil(N/bn) grid, one
  * launch writes the tile row to rows[bid] and the tile column to cols[bid],
