@@ -113,6 +113,68 @@ def test_tile_order_probe_checks_arguments_on_the_host(lib):
     assert tgemm.tgemm_debug_tile_order(1 << 20, 1 << 20, 1, 1, 8, FAKE, FAKE) == tgemm.ERR_UNSUPPORTED
 
 
+def _cfg(bm=128, bn=256, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0):
+    return tgemm.Config(bm=bm, bn=bn, bk=bk, stages=stages, cluster_m=cluster_m, group_m=group_m, split_k=split_k,
+                        swap_ab=swap_ab, grid=grid)
+
+
+LEGAL = [
+    ("cta256", dict(), 256, tgemm.F16),
+    ("cta128", dict(bn=128, stages=6), 256, tgemm.F16),
+    ("pair", dict(bm=256, stages=6, cluster_m=2), 256, tgemm.F16),
+    ("pair_streamk", dict(bm=256, stages=6, cluster_m=2, split_k=0), 256, tgemm.F16),
+    ("quad", dict(bm=256, stages=6, cluster_m=4), 256, tgemm.F16),
+    ("quad_streamk", dict(bm=256, stages=6, cluster_m=4, split_k=0), 256, tgemm.F16),
+    ("fp8_quad_streamk", dict(bm=256, stages=6, cluster_m=4, split_k=0), 256, tgemm.E4M3),
+    ("tf32_pair", dict(bm=256, stages=6, cluster_m=2), 256, tgemm.F32),
+    ("skinny_workspace", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 16, tgemm.F16),
+    ("skinny_cluster", dict(bn=16, stages=12, cluster_m=3, group_m=1, split_k=3, swap_ab=2), 16, tgemm.F16),
+    ("skinny_cluster_half_ring", dict(bn=16, stages=6, cluster_m=8, group_m=1, split_k=8, swap_ab=2), 16,
+     tgemm.F16),
+    ("skinny_cluster_64", dict(bn=64, stages=9, cluster_m=7, group_m=1, split_k=7, swap_ab=2), 64, tgemm.BF16),
+]
+
+ILLEGAL = [
+    ("bk_32", dict(bk=32), 256, tgemm.F16),
+    ("group_0", dict(group_m=0), 256, tgemm.F16),
+    ("negative_grid", dict(grid=-1), 256, tgemm.F16),
+    ("cta_split_2", dict(split_k=2), 256, tgemm.F16),
+    ("cta_streamk", dict(split_k=0), 256, tgemm.F16),                      # stream-K: pair and quad only
+    ("cta_stages_5", dict(stages=5), 256, tgemm.F16),                      # no such ring depth compiled
+    ("cluster_3_tiles", dict(bm=256, stages=6, cluster_m=3), 256, tgemm.F16),
+    ("pair_bn_128", dict(bm=256, bn=128, stages=6, cluster_m=2), 256, tgemm.F16),
+    ("workspace_stages", dict(bn=16, stages=6, group_m=1, split_k=5, swap_ab=1), 16, tgemm.F16),
+    ("workspace_bn_below_m", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 32, tgemm.F16),
+    ("cluster_mismatch", dict(bn=16, stages=12, cluster_m=2, group_m=1, split_k=3, swap_ab=2), 16, tgemm.F16),
+    ("cluster_9_splits", dict(bn=16, stages=12, cluster_m=9, group_m=1, split_k=9, swap_ab=2), 16, tgemm.F16),
+    ("half_ring_64_x5", dict(bn=64, stages=4, cluster_m=5, group_m=1, split_k=5, swap_ab=2), 64, tgemm.F16),
+    ("swap_3", dict(bn=16, group_m=1, split_k=5, swap_ab=3), 16, tgemm.F16),
+    ("fp8_swap", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 16, tgemm.E4M3),   # skinny kernels: 16-bit only
+    ("fp8_cta_split", dict(split_k=2), 256, tgemm.E4M3),
+]
+
+
+def _run_forced(cfg, M, ind):
+    # FAKE pointers: only ever run where no device answers, so that an
+    # accepted configuration stops at the device query instead of launching
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-path check with placeholder pointers; runs only without a GPU")
+    N, K = 512, 1024
+    return tgemm.tgemm_run_config(M, N, K, FAKE, K, FAKE, K, tgemm.B_NK, FAKE, N, ind, tgemm.BF16, None, cfg)
+
+
+@pytest.mark.parametrize("name,kw,M,ind", LEGAL, ids=[c[0] for c in LEGAL])
+def test_legal_configurations_pass_the_host_checks(lib, name, kw, M, ind):
+    # accepted: the call gets past every configuration check to the device query
+    assert _run_forced(_cfg(**kw), M, ind) in (tgemm.ERR_CUDA, tgemm.ERR_ARCH)
+
+
+@pytest.mark.parametrize("name,kw,M,ind", ILLEGAL, ids=[c[0] for c in ILLEGAL])
+def test_illegal_configurations_are_rejected_on_the_host(lib, name, kw, M, ind):
+    assert _run_forced(_cfg(**kw), M, ind) == tgemm.ERR_UNSUPPORTED
+
+
 # ---- tile space and grouped order ---------------------------------------------
 
 def coords(M, N, bm, bn, g):
