@@ -175,6 +175,33 @@ def test_illegal_configurations_are_rejected_on_the_host(lib, name, kw, M, ind):
     assert _run_forced(_cfg(**kw), M, ind) == tgemm.ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("case,expect", [
+    (dict(batch=-1), tgemm.ERR_INVALID_ARG),
+    (dict(sa=-64), tgemm.ERR_INVALID_ARG),
+    (dict(sa=100), tgemm.ERR_INVALID_ARG),          # A batches overlap (64 rows x 64 need 4096)
+    (dict(sb=1000), tgemm.ERR_INVALID_ARG),         # B batches overlap
+    (dict(sc=64), tgemm.ERR_INVALID_ARG),           # C batches overlap (C may not be shared)
+    (dict(sc=0), tgemm.ERR_INVALID_ARG),
+    (dict(sa=4100), tgemm.ERR_MISALIGNED),          # 8200 bytes: rows of later batches off 16 bytes
+    (dict(sc=4100), tgemm.ERR_MISALIGNED),
+    (dict(batch=1 << 31), tgemm.ERR_UNSUPPORTED),
+])
+def test_batched_argument_checks_on_the_host(lib, case, expect):
+    a = dict(batch=3, sa=4096, sb=0, sc=4096)
+    a.update(case)
+    rc = tgemm.tgemm_run_strided_batched(a["batch"], 64, 64, 64, FAKE, 64, a["sa"], FAKE, 64, a["sb"], tgemm.B_NK,
+                                         FAKE, 64, a["sc"], tgemm.BF16, tgemm.BF16, None, None, None)
+    assert rc == expect, tgemm.status_string(rc)
+
+
+def test_zero_batches_and_empty_products_need_no_device(lib):
+    args = (64, 64, 64, FAKE, 64, 4096, FAKE, 64, 0, tgemm.B_NK, FAKE, 64, 4096, tgemm.BF16, tgemm.BF16, None,
+            None, None)
+    assert tgemm.tgemm_run_strided_batched(0, *args) == tgemm.OK
+    assert tgemm.tgemm_run_strided_batched(3, 0, 64, 64, 0, 64, 0, 0, 64, 0, tgemm.B_NK, 0, 64, 0, tgemm.BF16,
+                                           tgemm.BF16, None, None, None) == tgemm.OK
+
+
 # ---- tile space and grouped order ---------------------------------------------
 
 def coords(M, N, bm, bn, g):
