@@ -52,6 +52,27 @@ def test_every_declared_symbol_is_exported(lib):
     assert exported == set(declared)
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/tgemm.h compiles as C99 on its own: plain pointers, sizes and
+    enums, no C++ or torch types in the boundary."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "tgemm.h"\n'
+                   "int main(void) {\n"
+                   "    tgemm_config c = {0};\n"
+                   "    tgemm_epilogue e = {1.0f, 0.0f, 0, 0, 0, TGEMM_F32, TGEMM_ACT_NONE};\n"
+                   "    (void)c; (void)e;\n"
+                   "    return tgemm_status_string(TGEMM_OK) == 0;\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I" + os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(lib):
     for code in range(8):
         s = tgemm.status_string(code)
