@@ -7,10 +7,19 @@ tutorial, "Performance at a glance").  A step is one tgemm_run call on the
 whole problem; the operands (128 MiB each) and C (128 MiB) together exceed
 the 129 MB L2, so back-to-back steps do not run from L2.
 
-Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
-plain FP64 triple loop) on a bounded sample of the same workload instead.
-Several GPUs under torchrun run independent replicas (no collective on the
-data path); value is the FLOPs of all ranks over the slowest rank's time.
+Prints one JSON line.  `--impl reference` times the CPU oracle (the plain
+FP64 triple loop) on a bounded sample of the same workload instead.  The
+library is single-GPU: with more than one GPU (`--gpus N`, or WORLD_SIZE > 1
+under torchrun) the GEMM arm prints a line saying so and does no work.  One
+of its kernels shares operand tiles between the CTAs of a cluster with TMA
+multicast, which is only allowed in code that runs on one GPU alone.
+
+Besides the timed K steps (whose mean is the headline value) the line
+carries the median and the best of K individually event-bracketed launches,
+SM clocks sampled through NVML every few milliseconds inside the timed
+region, a steady-state window of about a second after it (the GB300 settles
+at its power limit within a few hundred milliseconds of dense GEMMs), and,
+from the CPU-baseline leg, the oracle's check of sampled output elements.
 """
 from __future__ import annotations
 
@@ -30,7 +39,15 @@ sys.path.insert(0, ROOT)
 
 WORKLOAD = "gemm_8192x8192x8192_f16_nk_f16"
 METRIC = "GEMM TFLOPS (device-timed) and fraction of GB300 dense FP16/BF16 tensor peak"
-PUBLISHED_TFLOPS = 489.9      # Croqtile v4 on H800 PCIe, same shape and B layout (context, other GPU)
+# The pages' only figure for this shape: the Croqtile tutorial's tuned kernel,
+# 8192^3 FP16, B stored N x K, on an H800 PCIe with FP16 accumulation.  Another
+# GPU and another accumulator width: context, not a baseline.
+PAGE_CONTEXT = {"tflops": 489.9, "what": "Croqtile tutorial v4 kernel, 8192^3 FP16 N x K, H800 PCIe, "
+                                         "FP16 accumulation (another GPU and accumulator: context only)"}
+# Dense tensor FLOP per clock per SM of one tcgen05.mma issue stream, by
+# operand size in bytes (16-bit 8192; FP8 twice; TF32 half).
+FLOP_PER_CLK_SM = {2: 8192, 1: 16384, 4: 4096}
+STEADY_STATE_S = 1.0
 FALLBACK_TENSOR_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
@@ -45,19 +62,18 @@ def tflops(M: int, N: int, K: int, ms: float) -> float:
     return 2.0 * M * N * K / (ms * 1e-3) / 1e12
 
 
-def aggregate(total_ms_local: float, steps: int, flops_per_step: float, world: int, device="cpu"):
-    """Whole-job throughput of `world` replicas: every rank ran `steps` steps
-    of `flops_per_step`; the job's time is the slowest rank's.  Returns
-    (max_ms, ms_per_step, TFLOPS over all ranks)."""
-    total = float(total_ms_local)
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([total], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-    ms_per_step = total / steps
-    return total, ms_per_step, flops_per_step * world / (ms_per_step * 1e-3) / 1e12
+def launch_stats(ms_list):
+    """Median and best of per-launch times (milliseconds)."""
+    if not ms_list:
+        return None
+    return {"median": statistics.median(ms_list), "best": min(ms_list), "launches": len(ms_list)}
+
+
+def per_clock_efficiency(tflops_value: float, sms: int, flop_per_clk: int, sm_mhz):
+    """Achieved FLOP/s over what `sms` SMs issue at `sm_mhz` (None without a clock)."""
+    if not sm_mhz:
+        return None
+    return tflops_value * 1e12 / (sms * flop_per_clk * sm_mhz * 1e6)
 
 
 def kernel_digest() -> str:
@@ -94,61 +110,130 @@ def recorded_traffic(workload: str):
 
 # ---- clocks --------------------------------------------------------------------
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# Clock-event reason bits of NVML's public header (nvml.h).
+_REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+_NVML_CLOCK_SM = 1
 
 
 class ClockSampler:
-    def __init__(self, gpu_uuid=None):
-        self.proc = None
-        self.path = None
+    """Polls the GPU's SM clock, board power and clock-event reasons in a
+    background thread: through NVML (libnvidia-ml, every `period_s`) where
+    it loads, else through `nvidia-smi -lms 100`.  Samples carry host
+    timestamps (time.perf_counter), so a window can be cut out afterwards."""
+
+    def __init__(self, gpu_uuid=None, period_s=0.002):
         self.gpu_uuid = gpu_uuid
+        self.period_s = period_s
+        self.samples = []          # (t, sm_mhz, power_w, reasons frozenset)
+        self.max_mhz = None
+        self.source = None
+        self._stop = None
+        self._thread = None
+        self._proc = None
+        self._path = None
+
+    def _nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        rc = -1
+        if self.gpu_uuid:
+            rc = lib.nvmlDeviceGetHandleByUUID(self.gpu_uuid.encode(), ctypes.byref(h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(0), ctypes.byref(h))
+        if rc != 0:
+            return None
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, _NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return lib, h
 
     def start(self):
-        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
-        os.close(fd)
-        cmd = ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
-        if self.gpu_uuid:
-            cmd += ["-i", self.gpu_uuid]
-        try:
-            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+        import threading
+        nv = self._nvml()
+        if nv is not None:
+            import ctypes
+            lib, h = nv
+            self.source = "nvml every %g ms" % (self.period_s * 1e3)
+            self._stop = threading.Event()
+
+            def poll():
+                clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop.is_set():
+                    t = time.perf_counter()
+                    if lib.nvmlDeviceGetClockInfo(h, _NVML_CLOCK_SM, ctypes.byref(clk)) == 0:
+                        p = mw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else 0.0
+                        r = rs.value if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0 else 0
+                        self.samples.append((t, float(clk.value), p,
+                                             frozenset(n for n, bit in _REASON_BITS if r & bit)))
+                    time.sleep(self.period_s)
+
+            self._thread = threading.Thread(target=poll, daemon=True)
+            self._thread.start()
+        else:
+            fd, self._path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                   "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                   "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_uuid:
+                cmd += ["-i", self.gpu_uuid]
+            try:
+                self._t0 = time.perf_counter()
+                self._proc = subprocess.Popen(cmd, stdout=open(self._path, "w"), stderr=subprocess.DEVNULL)
+                self.source = "nvidia-smi every 100 ms (timestamps approximate)"
+            except OSError:
+                self._proc = None
+        time.sleep(0.05)
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.send_signal(signal.SIGTERM)
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        for ln in open(self.path).read().splitlines():
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self._proc is not None:
+            t1 = time.perf_counter()
+            self._proc.send_signal(signal.SIGTERM)
             try:
-                rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]), hw=f[5], hw_th=f[6],
-                                 sw_th=f[7], pcap=f[8]))
-            except ValueError:
-                continue
-        os.unlink(self.path)
-        if not rows:
-            return None
-        smax = max(r["max"] for r in rows)
-        loaded = [r for r in rows if r["power"] > 200] or rows
-        reasons = set()
-        for r in loaded:
-            for key, name in (("hw", "hw_slowdown"), ("hw_th", "hw_thermal_slowdown"),
-                              ("sw_th", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
-                if r[key].lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
-                "power_w_max": max(r["power"] for r in rows)}
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+            rows = []
+            for ln in open(self._path).read().splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                try:
+                    rows.append((float(f[0]), float(f[1]), float(f[2]),
+                                 frozenset(n for n, v in zip(("hw_slowdown", "hw_thermal_slowdown",
+                                                              "sw_thermal_slowdown", "sw_power_cap"), f[3:7])
+                                           if v.lower() == "active")))
+                except (ValueError, IndexError):
+                    continue
+            os.unlink(self._path)
+            # nvidia-smi prints no timestamps: spread its rows evenly
+            n = max(len(rows), 1)
+            self.samples = [(self._t0 + (t1 - self._t0) * (i + 0.5) / n, r[0], r[2], r[3])
+                            for i, r in enumerate(rows)]
+            self.max_mhz = max((r[1] for r in rows), default=None)
+
+    def window(self, t0: float, t1: float):
+        """Summary of the samples taken in [t0, t1] (host perf_counter seconds)."""
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        out = {"samples": len(inside), "source": self.source, "sm_max_mhz": self.max_mhz}
+        if len(inside) < 3:
+            out.update(sm_mhz=None, reasons=sorted(set().union(*[x[3] for x in inside])) if inside else [],
+                       note="fewer than 3 samples inside the window: no median")
+            return out
+        out.update(sm_mhz=statistics.median(x[1] for x in inside),
+                   sm_mhz_min=min(x[1] for x in inside),
+                   power_w_median=statistics.median(x[2] for x in inside),
+                   power_w_max=max(x[2] for x in inside),
+                   reasons=sorted(set().union(*[x[3] for x in inside])))
+        return out
 
 
 # ---- workload --------------------------------------------------------------------
@@ -180,6 +265,39 @@ def cpu_oracle_sample(wl, a, b, budget_s: float, threads: int):
     oracle.gemm_rows(a, b, wl.M, wl.N, wl.K, lda, ldb, wl.b_layout, dt_in, 0, rows, False, threads)
     dt = time.perf_counter() - t0
     return tflops(rows, wl.N, wl.K, dt * 1e3), dt, rows
+
+
+def sample_points(M: int, N: int, seed: int, n_random: int = 4096):
+    """Seeded random output positions plus the first and last row and column
+    and the rows/columns at multiples of 128 and 256 minus one and zero."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    ii, jj = [rng.integers(0, M, n_random)], [rng.integers(0, N, n_random)]
+    for r in sorted({0, 127, 128, 255, 256, M - 1} & set(range(M))):
+        ii.append(np.full(N, r))
+        jj.append(np.arange(N))
+    for c in sorted({0, 127, 128, 255, 256, N - 1} & set(range(N))):
+        ii.append(np.arange(M))
+        jj.append(np.full(M, c))
+    return np.concatenate(ii).astype(np.int64), np.concatenate(jj).astype(np.int64)
+
+
+def oracle_check(wl, a, b, c_gpu, threads: int):
+    """The oracle on sampled elements of the timed run's C: the worst error
+    as a fraction of the acceptance bound 1e-3 * sum|A||B| + ulp_out(C_ref)."""
+    import numpy as np
+    import oracle
+    ii, jj = sample_points(wl.M, wl.N, seed=wl.seed)
+    ref, bound = oracle.gemm_elements(a, b, wl.M, wl.N, wl.K, a.shape[1], b.shape[1], wl.b_layout,
+                                      oracle_input(wl.in_dtype), ii, jj, threads)
+    got = c_gpu[ii, jj].double().numpy()
+    tol = 1e-3 * bound + oracle.ulp(ref, wl.out_dtype)
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    return {"elements": int(len(ii)), "outside_bound": int(bad.sum()),
+            "max_err_over_tol": float(np.max(np.where(bad, np.inf, err / tol))),
+            "max_err_over_sum_abs": float(np.max(err / np.maximum(bound, 1e-300))),
+            "sample": "4096 seeded random elements plus rows and columns 0, 127, 128, 255, 256 and the last"}
 
 
 def run_reference(args, rank, world):
@@ -219,14 +337,15 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / max(len(times), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_dict(wl, world),
+        "data": "synthetic", "config": config_dict(wl),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": used, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def config_dict(wl, world):
+def config_dict(wl):
+    """The workload's description; the same dictionary on both arms."""
     from dense_tiled_gemm_persistent_gb300 import inputs as gen
     reps = -(-3 * L2_BYTES // wl.algorithmic_bytes) if wl.algorithmic_bytes < 3 * L2_BYTES else 1
     return {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
@@ -236,7 +355,15 @@ def config_dict(wl, world):
             "l2": ("back to back over %d copies of A, B, C (%.0f MB > 3 x 129 MB L2)"
                    % (reps, reps * wl.algorithmic_bytes / 1e6)) if reps > 1 else
                   ("operands+output %.0f MB > 129 MB L2, back to back" % (wl.algorithmic_bytes / 1e6)),
-            "parallelism": "replicas%d" % world if world > 1 else "single-gpu"}
+            "parallelism": "single-gpu"}
+
+
+def multi_gpu_line(args, world: int) -> dict:
+    """What the GEMM arm prints when asked for more than one GPU."""
+    return {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "unavailable": "single-GPU library: one of its kernels shares operand tiles within a cluster by "
+                           "TMA multicast, which may only run where one GPU alone is in use; no multi-GPU "
+                           "path is built"}
 
 
 def main():
@@ -247,6 +374,7 @@ def main():
     ap.add_argument("--impl", default="tgemm", choices=["tgemm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-steady-state", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--config", default="auto",
                     choices=["auto", "pair", "pairsk", "quad", "quadsk", "1cta256", "1cta128", "workspace"],
@@ -266,24 +394,24 @@ def main():
         args.warmup = 3
 
     rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-
+    world = max(int(os.environ.get("WORLD_SIZE", "1")), 1)
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    if world > 1 or args.gpus > 1:
+        if rank == 0:
+            print(json.dumps(multi_gpu_line(args, max(world, args.gpus))), flush=True)
+        return
+
+    import ctypes
 
     import torch
-    import torch.distributed as dist
     from dense_tiled_gemm_persistent_gb300 import build as libbuild
     from dense_tiled_gemm_persistent_gb300 import inputs as gen
     from dense_tiled_gemm_persistent_gb300 import tgemm
-    import ctypes
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     libbuild.build()
     tgemm.load()
 
@@ -294,6 +422,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
     lda, ldb, ldc = A.shape[1], B.shape[1], wl.N
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     rc, picked = tgemm.tgemm_query_config(wl.M, wl.N, wl.K, wl.b_layout, wl.in_dtype, wl.out_dtype)
     if rc != 0:
@@ -362,8 +491,6 @@ def main():
     if wl.algorithmic_bytes < 3 * L2_BYTES:
         reps = -(-3 * L2_BYTES // wl.algorithmic_bytes)
     copies = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(reps - 1)]
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize(dev)
     # Two events bracket the whole timed loop: the average launch duration is
     # the loop time over the launch count (an event after every launch would
@@ -371,26 +498,30 @@ def main():
     # replay the loop from a captured CUDA graph so that the host's per-call
     # cost does not starve the GPU; the graph holds the same launches.
     use_graph = args.graph == "on" or (args.graph == "auto" and wl.flops < GRAPH_FLOPS)
+    cap = torch.cuda.Stream(dev)
+    cap_h = ctypes.c_void_p(cap.cuda_stream)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(n):
+                a_, b_, c_ = copies[i % reps]
+                step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr(), cap_h)
+        return g
+
     graph = None
     if use_graph:
-        cap = torch.cuda.Stream(dev)
-        cap_h = ctypes.c_void_p(cap.cuda_stream)
         with torch.cuda.stream(cap):
             for i in range(reps):                      # per-stream set-up outside capture
                 a_, b_, c_ = copies[i]
                 step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr(), cap_h)
         torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            for i in range(args.steps):
-                a_, b_, c_ = copies[i % reps]
-                step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr(), cap_h)
+        graph = capture(args.steps)
         graph.replay()
         torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize(dev)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.perf_counter()
     e_start.record(stream)
     if graph is not None:
         graph.replay()
@@ -400,16 +531,92 @@ def main():
             step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
     e_end.record(stream)
     torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
+    t_host1 = time.perf_counter()
     rc = tgemm.tgemm_check(sh)
     if rc != 0:
         raise RuntimeError("timed region failed: " + tgemm.status_string(rc))
     total_ms = e_start.elapsed_time(e_end)
-    local_ms = total_ms
-    total_ms, ms_per_step, value = aggregate(local_ms, args.steps, wl.flops, world, dev)
-    avg_launch = local_ms / args.steps
+    ms_per_step = total_ms / args.steps
+    value = tflops(wl.M, wl.N, wl.K, ms_per_step)
+    avg_launch = ms_per_step
+    flop_clk = FLOP_PER_CLK_SM[gen.DTYPE_SIZE[wl.in_dtype]]
+    clocks = sampler.window(t_host0, t_host1)
+    clocks["window"] = "the timed region (%.1f ms of host time)" % ((t_host1 - t_host0) * 1e3)
+    # NVML's clock and power readings trail the hardware by tens of
+    # milliseconds (a 12 ms dense-GEMM burst reads as ~170 W on a board that
+    # draws 1.4 kW in it), so inside a region that short they show the state
+    # before it: they are reported, but no per-clock efficiency is derived
+    # from them.  The steady-state window below is long enough.
+    if (t_host1 - t_host0) < 0.25:
+        clocks["note"] = ("timed region shorter than NVML's update interval: its samples show the clock before "
+                          "the region; see steady_state for clocks under load")
+        clocks["per_clock_efficiency"] = None
+    else:
+        clocks["per_clock_efficiency"] = per_clock_efficiency(value, sms, flop_clk, clocks.get("sm_mhz"))
+
+    # Per-launch distribution: K more launches (graph mode: blocks of up to
+    # 10 replayed launches), each bracketed by its own pair of events.
+    per = []
+    if graph is not None:
+        blk = max(1, min(10, args.steps))
+        g_blk = capture(blk)
+        for _ in range(max(1, args.steps // blk)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g_blk.replay()
+            e1.record(stream)
+            e1.synchronize()
+            per.append(e0.elapsed_time(e1) / blk)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i, (e0, e1) in enumerate(evs):
+            a_, b_, c_ = copies[i % reps]
+            e0.record(stream)
+            step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per = [e0.elapsed_time(e1) for e0, e1 in evs]
+    kstats = launch_stats(per) or {}
+    kernel_ms = {"mean": avg_launch, "median": kstats.get("median"), "best": kstats.get("best"),
+                 "distribution": "%d %s, an event pair around each" % (
+                     len(per), "blocks of %d graph-replayed launches" % blk if graph is not None
+                     else "launches")}
+
+    # Steady state: about a second of back-to-back steps after the timed
+    # region, with the clocks sampled inside it.  The GPU reaches its power
+    # limit there; the timed K steps may still run at burst clocks.
+    steady = None
+    if not args.no_steady_state:
+        n_ss = max(args.steps, int(STEADY_STATE_S * 1e3 / max(avg_launch, 1e-4)))
+        if graph is not None:
+            n_rep = max(1, n_ss // args.steps)
+            n_ss = n_rep * args.steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        if graph is not None:
+            for _ in range(n_rep):
+                graph.replay()
+        else:
+            for i in range(n_ss):
+                a_, b_, c_ = copies[i % reps]
+                step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        ss_ms = e0.elapsed_time(e1) / n_ss
+        ss_val = tflops(wl.M, wl.N, wl.K, ss_ms)
+        # skip the first quarter: the clock falls from burst to its power-limited level
+        ss_clk = sampler.window(t0 + 0.25 * (t1 - t0), t1)
+        steady = {"steps": n_ss, "seconds": (t1 - t0), "ms_per_step": ss_ms, "value": ss_val, "unit": "TFLOPS",
+                  "clocks": ss_clk,
+                  "per_clock_efficiency": per_clock_efficiency(ss_val, sms, flop_clk, ss_clk.get("sm_mhz"))}
+    sampler.stop()
+    rc = tgemm.tgemm_check(sh)
+    if rc != 0:
+        raise RuntimeError("distribution/steady-state launches failed: " + tgemm.status_string(rc))
 
     peaks = measured_peaks()
     # nominal dense rates relative to FP16/BF16 (2.25 PFLOP/s): FP8 4.5, TF32 1.1
@@ -432,7 +639,10 @@ def main():
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t, "peak_source": src_t}
         if peaks and peaks.get("bf16_tflops_sustained"):
-            roofline["frac_of_sustained"] = achieved / (rate * float(peaks["bf16_tflops_sustained"]))
+            sus = rate * float(peaks["bf16_tflops_sustained"])
+            roofline["frac_of_sustained"] = achieved / sus
+            if steady is not None:
+                steady["frac_of_sustained"] = steady["value"] / sus
     else:
         achieved = wl.algorithmic_bytes / (avg_launch * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_h, "unit": "GB/s",
@@ -490,36 +700,43 @@ def main():
         e1.record(s_comp)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        e2e = {"value": tflops(wl.M, wl.N, wl.K, e2e_ms) * world, "unit": "TFLOPS",
+        e2e = {"value": tflops(wl.M, wl.N, wl.K, e2e_ms), "unit": "TFLOPS",
                "h2d_bytes_per_step": a_cpu.numel() * a_cpu.element_size() + b_cpu.numel() * b_cpu.element_size(),
                "d2h_bytes_per_step": hcs[0].numel() * hcs[0].element_size(), "ms_per_step": e2e_ms,
                "pipelined": "H2D of step i+1 and D2H of step i-1 overlap the GEMM of step i (two buffer sets)"}
+        rc = tgemm.tgemm_check(sh)
+        if rc != 0:
+            raise RuntimeError("end-to-end launches failed: " + tgemm.status_string(rc))
 
+    # CPU-baseline leg: the oracle timed on a row sample of the headline
+    # workload, and the oracle's check of sampled elements of the C that the
+    # timed launches wrote (any workload).
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
+    parity = None
+    if not args.no_cpu_baseline:
         import oracle
         oracle.build()
         threads = os.cpu_count() or 1
-        v, dt, rows = cpu_oracle_sample(wl, a_cpu, b_cpu, 15.0, threads)
-        cpu = {"value": v, "unit": "TFLOPS", "cores": min(threads, rows), "kind": "oracle",
-               "sample": "rows 0..%d of C (%d x %d outputs, K = %d), FP64 dot products, %.1f s" % (
-                   rows - 1, rows, wl.N, wl.K, dt)}
+        parity = oracle_check(wl, a_cpu, b_cpu, C.cpu(), threads)
+        if args.workload == WORKLOAD:
+            v, dt, rows = cpu_oracle_sample(wl, a_cpu, b_cpu, 15.0, threads)
+            cpu = {"value": v, "unit": "TFLOPS", "cores": min(threads, rows), "kind": "oracle",
+                   "sample": "rows 0..%d of C (%d x %d outputs, K = %d), FP64 dot products, %.1f s" % (
+                       rows - 1, rows, wl.N, wl.K, dt)}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": value / PUBLISHED_TFLOPS if wl.name == WORKLOAD else None,
-            "dtype": gen.DTYPE_NAME[wl.in_dtype], "data": "synthetic",
-            "config": dict(config_dict(wl, world), kernel=picked.as_dict(),
-                           launch="cuda_graph" if graph is not None else "stream", epilogue=args.epilogue),
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks, "gpu_launches": args.steps,
-            "kernel_ms": {"mean": avg_launch},
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": gen.DTYPE_NAME[wl.in_dtype], "data": "synthetic",
+        "config": config_dict(wl),
+        "kernel": dict(picked.as_dict(), launch="cuda_graph" if graph is not None else "stream",
+                       epilogue=args.epilogue),
+        "roofline": roofline, "cpu_baseline": cpu, "parity": parity, "e2e": e2e,
+        "clocks": clocks, "steady_state": steady, "gpu_launches": args.steps,
+        "kernel_ms": kernel_ms,
+        "page_context": dict(PAGE_CONTEXT, ratio=value / PAGE_CONTEXT["tflops"]) if wl.name == WORKLOAD else None,
+    }
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":
