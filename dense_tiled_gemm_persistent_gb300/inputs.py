@@ -152,3 +152,75 @@ WORKLOADS = {
                  uniform(-0.5, 0.5), uniform(-0.5, 0.5), 6),
     ]
 }
+
+
+# ---- operands on the output cast's edge cases ------------------------------
+
+CAST_EDGE_KINDS = ("f16_overflow", "f16_subnormal", "bf16_overflow")
+
+
+def cast_edge_operands(kind: str, M: int, N: int, K: int, b_layout: int, seed: int, scale: int = 1,
+                       lda: Optional[int] = None, ldb: Optional[int] = None,
+                       pad_value: float = float("nan")) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Seeded operands (K > 64) whose exact products sit on the edges of the
+    FP32 -> FP16/BF16 cast, with every partial sum exact in FP32 whatever the
+    summation order (all values are integer multiples of one power of two,
+    far below 2^24 units, and the terms of one output never change sign).
+
+    f16_overflow (FP16): A[i, k] = 1 and B[k, j] = +-1023 * scale for k < 64,
+        then 20 fixed k positions spread over the rest of K with A in {0, 1}
+        and B in {0, +-4 * scale}: scale * C[i, j] = +-(65472 + 4c) * scale,
+        c in 0..20 -- around FP16's largest finite value 65504, through the
+        tie at 65520 that rounds to infinity, and past it.  The sign
+        alternates by column.
+    f16_subnormal (FP16): A = 2^-12 * a, B = 2^-13 * b with a, b uniform
+        integers in -2..2: C = 2^-25 * n, mostly below FP16's smallest normal
+        2^-14, odd n falling half-way between two subnormals.
+    bf16_overflow (BF16): A[i, k] = 2^56 and B[k, j] = +-2^55 * 32640 for
+        k < 4 (the sum is BF16's largest finite value, 255 * 2^120), then 15
+        fixed k positions with A in {0, 2^58} and B in {0, +-2^58}:
+        C = +-(130560 + 32c) * 2^111, c in 0..15 -- the tie at
+        130816 * 2^111 rounds to infinity, and the largest sum stays below
+        FP32's largest finite value.
+    """
+    if K <= 64:
+        raise ValueError("cast-edge operands need K > 64")
+    g = torch.Generator("cpu").manual_seed(seed)
+    a = torch.zeros((M, K), dtype=torch.float64)
+    bl = torch.zeros((K, N), dtype=torch.float64)        # logical K x N
+    sign = torch.where(torch.arange(N) % 2 == 0, 1.0, -1.0).to(torch.float64)
+    if kind == "f16_overflow":
+        dt = torch.float16
+        a[:, :64] = 1.0
+        bl[:64, :] = 1023.0 * scale * sign
+        pos = 64 + (torch.arange(20) * (K - 64)) // 20
+        a[:, pos] = (torch.rand((M, 20), generator=g) < 0.75).to(torch.float64)
+        bl[pos, :] = (torch.rand((20, N), generator=g) < 0.75).to(torch.float64) * 4.0 * scale * sign
+    elif kind == "f16_subnormal":
+        dt = torch.float16
+        a = torch.randint(-2, 3, (M, K), generator=g).to(torch.float64) * 2.0 ** -12
+        bl = torch.randint(-2, 3, (K, N), generator=g).to(torch.float64) * 2.0 ** -13
+    elif kind == "bf16_overflow":
+        dt = torch.bfloat16
+        a[:, :4] = 2.0 ** 56
+        bl[:4, :] = 32640.0 * 2.0 ** 55 * sign
+        pos = 64 + (torch.arange(15) * (K - 64)) // 15
+        a[:, pos] = (torch.rand((M, 15), generator=g) < 0.75).to(torch.float64) * 2.0 ** 58
+        bl[pos, :] = (torch.rand((15, N), generator=g) < 0.75).to(torch.float64) * 2.0 ** 58 * sign
+    else:
+        raise ValueError("unknown cast-edge kind %r" % (kind,))
+    b = bl if b_layout == B_KN else bl.t().contiguous()
+    lda = K if lda is None else lda
+    ldb = b.shape[1] if ldb is None else ldb
+    ta, tb = a.to(dt), b.to(dt)
+    if not (torch.equal(ta.double(), a) and torch.equal(tb.double(), b)):
+        raise AssertionError("cast-edge values are not exact in the input type")
+    return _pad(ta, lda, pad_value), _pad(tb, ldb, pad_value)
+
+
+def cast_edge_in_dtype(kind: str) -> int:
+    return BF16 if kind == "bf16_overflow" else F16
+
+
+def cast_edge_out_dtype(kind: str) -> int:
+    return BF16 if kind == "bf16_overflow" else F16

@@ -8,6 +8,7 @@ byte count of the benchmark configuration it stands for.
 import math
 
 import numpy as np
+import pytest
 import torch
 
 from dense_tiled_gemm_persistent_gb300 import inputs as gen
@@ -104,3 +105,32 @@ def test_arithmetic_intensity_classes():
             assert 15 < ai < 16 and ai < ridge
         else:
             assert ai > ridge, name
+
+
+@pytest.mark.parametrize("kind", gen.CAST_EDGE_KINDS)
+@pytest.mark.parametrize("layout", [gen.B_NK, gen.B_KN])
+def test_cast_edge_operands_land_on_the_edges(orc, kind, layout):
+    """The cast-edge operands are exact in their input type, and the oracle's
+    exact sums round onto the edges they are named for."""
+    import numpy as np
+    M, N, K = 24, 40, 700
+    a, b = gen.cast_edge_operands(kind, M, N, K, layout, seed=1)
+    ind, outd = gen.cast_edge_in_dtype(kind), gen.cast_edge_out_dtype(kind)
+    assert a.dtype == gen.TORCH_DTYPE[ind] and b.dtype == gen.TORCH_DTYPE[ind]
+    ref, _ = orc.gemm(a, b, M, N, K, a.shape[1], b.shape[1], layout, ind)
+    v = orc.decode(orc.round_bits(ref, outd), outd)
+    if kind == "f16_overflow":
+        assert set(np.unique(np.abs(v))) <= {65472.0, 65504.0, np.inf}
+        assert np.isinf(v).any() and (np.abs(v) == 65504).any() and (np.abs(ref) == 65520).any()
+    elif kind == "bf16_overflow":
+        top = 255 * 2.0 ** 120
+        assert set(np.unique(np.abs(v))) <= {top, np.inf}
+        assert np.isinf(v).any() and (np.abs(v) == top).any()
+        assert np.abs(ref).max() < (2 - 2.0 ** -23) * 2.0 ** 127          # FP32 never overflows
+    else:
+        sub = (np.abs(v) < 2.0 ** -14) & (v != 0)
+        assert sub.mean() > 0.5
+        assert ((np.abs(ref) / 2.0 ** -25) % 2 == 1).any()               # half-way cases
+    # columns alternate in sign for the overflow kinds
+    if kind != "f16_subnormal":
+        assert (np.sign(ref[:, 0::2]) > 0).all() and (np.sign(ref[:, 1::2]) < 0).all()
