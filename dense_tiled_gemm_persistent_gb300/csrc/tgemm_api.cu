@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -724,6 +725,59 @@ tgemm_status epilogue_params(const tgemm_epilogue *ep, int64_t M, int64_t N, int
     return TGEMM_OK;
 }
 
+// What one call launched, for the TGEMM_LOG trace (filled by the launch
+// paths below, printed by run_impl's caller-facing wrapper).
+struct LaunchRecord {
+    const char *kernel = nullptr;   // nullptr: nothing launched
+    tgemm_config cfg{};
+    int grid = 0;                   // CTAs launched
+    int dp_tiles = 0, sk_units = 0; // stream-K split (0 units: whole tiles)
+};
+thread_local LaunchRecord t_rec;
+
+bool log_enabled()
+{
+    static const bool on = [] {
+        const char *s = std::getenv("TGEMM_LOG");
+        return s != nullptr && *s != '\0' && std::strcmp(s, "0") != 0;
+    }();
+    return on;
+}
+
+const char *dtype_name(int dt)
+{
+    switch (dt) {
+    case TGEMM_F16: return "f16";
+    case TGEMM_BF16: return "bf16";
+    case TGEMM_F32: return "f32";
+    case TGEMM_E4M3: return "e4m3";
+    case TGEMM_E5M2: return "e5m2";
+    }
+    return "?";
+}
+
+// One stderr line per call when TGEMM_LOG is set (and not "0"): the problem,
+// whether the configuration was the caller's or the library's choice, what
+// was launched with which configuration, and the call's status.
+void log_call(const char *entry, int64_t batch, int64_t M, int64_t N, int64_t K, int b_layout, int in_dtype,
+              int out_dtype, bool forced, bool epilogue, tgemm_status st)
+{
+    const LaunchRecord &r = t_rec;
+    char what[256];
+    if (r.kernel)
+        std::snprintf(what, sizeof what,
+                      "%s bm=%d bn=%d bk=%d stages=%d cluster_m=%d group_m=%d split_k=%d swap_ab=%d grid=%d "
+                      "dp_tiles=%d sk_units=%d",
+                      r.kernel, r.cfg.bm, r.cfg.bn, r.cfg.bk, r.cfg.stages, r.cfg.cluster_m, r.cfg.group_m,
+                      r.cfg.split_k, r.cfg.swap_ab, r.grid, r.dp_tiles, r.sk_units);
+    else
+        std::snprintf(what, sizeof what, "no kernel");
+    std::fprintf(stderr, "tgemm: %s batch=%lld M=%lld N=%lld K=%lld B=%s in=%s out=%s epilogue=%d config=%s -> %s; %s\n",
+                 entry, (long long)batch, (long long)M, (long long)N, (long long)K,
+                 b_layout == TGEMM_B_KN ? "KxN" : "NxK", dtype_name(in_dtype), dtype_name(out_dtype),
+                 epilogue ? 1 : 0, forced ? "caller" : "library", what, tgemm_status_string(st));
+}
+
 // C^T = B^T A^T on a swap-AB split-K kernel (M <= 64): the workspace
 // reduction (swap_ab = 1) or the in-cluster one (swap_ab = 2).
 tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -769,6 +823,10 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     }
     const int64_t grid = tiles_n * splits;
     if (grid > INT32_MAX) return TGEMM_ERR_UNSUPPORTED;
+    t_rec.kernel = cfg.swap_ab == 2 ? "skinny-cluster-splitk" : "skinny-workspace-splitk";
+    t_rec.cfg = cfg;
+    t_rec.cfg.split_k = splits;
+    t_rec.grid = (int)grid;
     if (var->launch(p, (int)grid, static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
@@ -799,10 +857,10 @@ void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, in
     cfg->grid = quad_grid(M, N, cfg->split_k, sm_count);
 }
 
-tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                       int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
                       void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags,
-                      const tgemm_epilogue *ep = nullptr, const Batch &bt = Batch())
+                      const tgemm_epilogue *ep, const Batch &bt)
 {
     bool noop = false;
     tgemm_status st = validate(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, &noop);
@@ -840,6 +898,8 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
                 if (q.epi & 2) q.cin_ptr = static_cast<const char *>(q.cin_ptr) + (size_t)(b * bt.sc) * eo;
                 const int64_t total = M * N;
                 const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * (int64_t)dev->sm_count);
+                t_rec.kernel = "epilogue-only";
+                t_rec.grid = blocks;
                 if (out_dtype == TGEMM_F32) epilogue_only_kernel<OUT_F32><<<blocks, 256, 0, stream>>>(q);
                 else if (out_dtype == TGEMM_F16) epilogue_only_kernel<OUT_F16><<<blocks, 256, 0, stream>>>(q);
                 else epilogue_only_kernel<OUT_BF16><<<blocks, 256, 0, stream>>>(q);
@@ -850,6 +910,7 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     }
     if (K == 0) {
         // The empty sum: C = 0 (all-zero bits are +0 in every output type).
+        t_rec.kernel = "memset";
         for (int64_t b = 0; b < bt.count; ++b)
             if (cudaMemset2DAsync(static_cast<char *>(C) + (size_t)(b * bt.sc) * eo, (size_t)ldc * eo, 0,
                                   (size_t)N * eo, (size_t)M, stream) != cudaSuccess) {
@@ -961,11 +1022,29 @@ tgemm_status run_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         if (g > p.num_tiles) g = p.num_tiles;
         if (g < 1) g = 1;
     }
+    t_rec.kernel = pair ? "pair" : quad ? "quad" : "tile";
+    t_rec.cfg = cfg;
+    t_rec.grid = g;
+    t_rec.dp_tiles = p.dp_tiles;
+    t_rec.sk_units = p.sk_units;
     if (var->launch(p, g, stream) != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
     }
     return TGEMM_OK;
+}
+
+tgemm_status run_impl(const char *entry, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
+                      void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags,
+                      const tgemm_epilogue *ep = nullptr, const Batch &bt = Batch())
+{
+    t_rec = LaunchRecord();
+    const tgemm_status st = run_body(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream_ptr,
+                                     forced, debug_flags, ep, bt);
+    if (log_enabled()) log_call(entry, bt.count, M, N, K, b_layout, in_dtype, out_dtype, forced != nullptr,
+                                ep != nullptr, st);
+    return st;
 }
 
 }  // namespace
@@ -977,7 +1056,8 @@ TGEMM_EXPORT tgemm_status tgemm_run(int64_t M, int64_t N, int64_t K, const void 
                                     const void *B, int64_t ldb, tgemm_b_layout b_layout, void *C,
                                     int64_t ldc, tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream)
 {
-    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, nullptr, 0);
+    return run_impl("tgemm_run", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, nullptr,
+                    0);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
@@ -986,7 +1066,8 @@ TGEMM_EXPORT tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K, cons
                                            void *stream, const tgemm_config *cfg)
 {
     if (!cfg) return TGEMM_ERR_INVALID_ARG;
-    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0);
+    return run_impl("tgemm_run_config", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg,
+                    0);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -994,7 +1075,8 @@ TGEMM_EXPORT tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K, const vo
                                        tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
                                        const tgemm_epilogue *ep, const tgemm_config *cfg)
 {
-    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0, ep);
+    return run_impl("tgemm_run_ex", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0,
+                    ep);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void *A,
@@ -1021,7 +1103,8 @@ TGEMM_EXPORT tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, in
     bt.sa = stride_a;
     bt.sb = stride_b;
     bt.sc = stride_c;
-    return run_impl(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0, ep, bt);
+    return run_impl("tgemm_run_strided_batched", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype,
+                    stream, cfg, 0, ep, bt);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
@@ -1062,26 +1145,35 @@ TGEMM_EXPORT tgemm_status tgemm_check(void *stream)
         std::lock_guard<std::mutex> lk(g_mu);
         status = g_dev[dev].status;
     }
-    if (!status) return TGEMM_OK;
-    uint32_t word = 0;
-    if (cudaMemcpy(&word, status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
-        cudaGetLastError();
-        return TGEMM_ERR_CUDA;
+    // The library's status word and the allocation-free path's (which lives
+    // in that path's built-in array); either may not exist yet.
+    uint32_t first = 0;
+    uint32_t *words[2] = {status, noalloc_status_word(dev)};
+    for (uint32_t *w : words) {
+        if (!w) continue;
+        uint32_t word = 0;
+        if (cudaMemcpy(&word, w, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        if (word == 0) continue;
+        if (first == 0) first = word;
+        if (cudaMemset(w, 0, sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
     }
-    if (word == 0) return TGEMM_OK;
-    g_last_fault.store(word);
+    if (first == 0) return TGEMM_OK;
+    g_last_fault.store(first);
     {
         // A kernel gave up part-way: split-K arrival counters may be left
-        // non-zero; clear them so the next call starts clean.
+        // non-zero; clear them so the next call starts clean.  (The
+        // allocation-free path clears its counters before every launch.)
         std::lock_guard<std::mutex> lk(g_mu);
         for (auto &kv : g_ws)
             if (kv.first.first == dev && kv.second.ptr) cudaMemset(kv.second.ptr, 0, kCounterBytes);
     }
-    if (cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) {
-        cudaGetLastError();
-        return TGEMM_ERR_CUDA;
-    }
-    return (word >> 28) == kFaultTimeout ? TGEMM_ERR_TIMEOUT : TGEMM_ERR_CUDA;
+    return (first >> 28) == kFaultTimeout ? TGEMM_ERR_TIMEOUT : TGEMM_ERR_CUDA;
 }
 
 TGEMM_EXPORT uint32_t tgemm_last_fault_code(void) { return g_last_fault.load(); }

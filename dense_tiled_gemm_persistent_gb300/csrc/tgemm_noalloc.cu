@@ -10,7 +10,8 @@
 //
 // The array (kScratchBytes, 4 MiB) is reserved on every GPU that loads the
 // library and stays reserved until the process exits.  Layout:
-//   [0, 256)                        reserved
+//   [0, 4)                          status word (0 = no fault; zero at load)
+//   [4, 256)                        unused
 //   [256, 256 + 16 KiB)             per-tile arrival counters (must start at 0)
 //   [256 + 16 KiB, kScratchBytes)   FP32 partial sums of the K splits
 // Every call uses the same array, so calls whose kernels overlap on the GPU
@@ -25,9 +26,9 @@
 // is current.  That first call should therefore not be made during CUDA
 // stream capture.
 //
-// Timeouts of the kernel's pipeline waits wind the kernel down as in the
-// other paths but are not recorded in tgemm_check's status word (which would
-// need an allocation); the kernel simply stops early.
+// A kernel that gives up on a pipeline wait winds down as in the other paths
+// and records the fault in the array's status word; tgemm_check reads and
+// clears it together with the library's own status word.
 #include "tgemm.h"
 
 #include <cuda.h>
@@ -148,9 +149,34 @@ const KernelVariant *na_variant(int npad, int out, int w_mn)
 }
 
 }  // namespace
+
+// The status word of the allocation-free path on device `dev`, or nullptr
+// before that path's first call there (tgemm_check reads it).
+uint32_t *noalloc_status_word(int dev)
+{
+    if (dev < 0 || dev >= kMaxDevs) return nullptr;
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    return static_cast<uint32_t *>(g_na_scratch[dev]);
+}
+
 }  // namespace tgemm
 
 using namespace tgemm;
+
+TGEMM_EXPORT tgemm_status tgemm_debug_noalloc_wait_timeout(uint32_t timeout_us, void *stream)
+{
+    if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return TGEMM_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    int sms = 0;
+    tgemm_status st = na_setup(&scratch, &sms);
+    if (st != TGEMM_OK) return st;
+    if (launch_wait_timeout_probe(static_cast<uint32_t *>(scratch), (uint64_t)timeout_us * 1000ull,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
 
 TGEMM_EXPORT tgemm_status tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                                             const void *B, int64_t ldb, tgemm_b_layout b_layout, void *C,
@@ -227,7 +253,7 @@ TGEMM_EXPORT tgemm_status tgemm_run_noalloc(int64_t M, int64_t N, int64_t K, con
     p.num_kb = (int32_t)num_kb;
     p.group_m = 1;
     p.idesc = make_idesc(in_dtype == TGEMM_BF16, false, kSkinnyRows, npad, w_mn);
-    p.status = nullptr;                      // no status word on this path
+    p.status = reinterpret_cast<uint32_t *>(base);   // the array's status word
     const char *env = std::getenv("TGEMM_WAIT_TIMEOUT_MS");
     long ms = env ? std::strtol(env, nullptr, 10) : 0;
     p.timeout_ns = (uint64_t)(ms > 0 ? ms : 2000) * 1000000ull;

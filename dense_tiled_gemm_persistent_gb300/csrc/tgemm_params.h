@@ -110,5 +110,8 @@ inline cudaError_t ensure_smem_limit(Kernel kern, unsigned smem, std::atomic<uns
 
 // The bounded-wait self test kernel launcher (tgemm_debug.cu).
 cudaError_t launch_wait_timeout_probe(uint32_t *status, uint64_t timeout_ns, cudaStream_t st);
+// tgemm_noalloc.cu: the allocation-free path's status word on a device
+// (nullptr before that path's first call there)
+uint32_t *noalloc_status_word(int dev);
 
 }  // namespace tgemm

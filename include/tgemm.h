@@ -153,13 +153,23 @@ tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, int64_t N, int6
                                        const tgemm_epilogue *ep, const tgemm_config *cfg);
 
 /* The configuration tgemm_run would use for this problem (no device work,
- * but it reads the current device's SM count and compute capability). */
+ * but it reads the current device's SM count and compute capability).  The
+ * pages leave tile sizes to the launcher ("Launching the kernel from the
+ * host" of the cuTile matrix multiplication tutorial picks them per dtype)
+ * and to measurement ("CUDA 13.1 new feature: the Tile programming model",
+ * section 7, autotuning over tile shapes); this returns the per-shape choice
+ * that the library's measured table or, off its grid, its wave model makes.
+ * With TGEMM_LOG set (not "0") every GEMM entry point prints the
+ * configuration it launched, one line per call on stderr. */
 tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
                                 tgemm_dtype in_dtype, tgemm_dtype out_dtype,
                                 tgemm_config *out_cfg);
 
-/* tgemm_run with an explicit configuration, for tuning and tests.  A
- * configuration the kernels do not provide returns TGEMM_ERR_UNSUPPORTED. */
+/* tgemm_run with an explicit configuration, for tuning and tests: the
+ * measurement side of the autotuning the pages describe (the Tile
+ * programming model overview, section 7, times candidate tile shapes; the
+ * cuTile tutorial's launcher fixes them by hand).  A configuration the
+ * kernels do not provide returns TGEMM_ERR_UNSUPPORTED. */
 tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K,
                               const void *A, int64_t lda,
                               const void *B, int64_t ldb, tgemm_b_layout b_layout,
@@ -169,17 +179,34 @@ tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K,
 
 /* Synchronise `stream`, then report the first failure since the last check:
  * a pending CUDA error (TGEMM_ERR_CUDA) or a kernel that timed out on a
- * pipeline wait (TGEMM_ERR_TIMEOUT; the status word is then cleared). */
+ * pipeline wait (TGEMM_ERR_TIMEOUT; the status word is then cleared).  Both
+ * the library's status word and the allocation-free entry point's are read.
+ * The Croqtile tutorial's summary warns that a hand-written warp-specialised
+ * pipeline can deadlock silently; every wait here is bounded instead, and
+ * this call is where a wait that gave up becomes visible to the caller. */
 tgemm_status tgemm_check(void *stream);
 
-/* The device status word's last recorded value for the current device
- * (0 = none), without clearing it; for diagnostics after tgemm_check. */
+/* The last non-zero status word tgemm_check read (0 = none): bits 28-31 the
+ * fault class (7 = timeout), bits 20-27 the wait site, bits 0-19 the CTA;
+ * for diagnostics after tgemm_check (the same silent-deadlock passage). */
 uint32_t tgemm_last_fault_code(void);
 
-/* A short English description of a status code (never NULL). */
+/* A short English description of a status code (never NULL).  The codes are
+ * the boundary's failure classes: argument checks from the CUDA Programming
+ * Guide 13.4.2 (unofficial Chinese translation), sections 2.4.12.1-2.4.12.2
+ * (non-overlapping __restrict__ arrays, 16-byte aligned rows), the GB300
+ * architecture check, CUDA errors, workspace allocation and the bounded-wait
+ * timeout. */
 const char *tgemm_status_string(tgemm_status s);
 
-/* Free every library-owned resource on every device it touched. */
+/* Free every library-owned resource on every device it touched: the status
+ * words, the split-K / stream-K workspaces and the tensor-descriptor cache.
+ * The pages' kernels own no memory beyond their operands (the cuTile
+ * tutorial's launcher allocates only C); this state exists because the
+ * persistent kernels here share tail tiles by k-range (the Croqtile
+ * tutorial's comparison with cuBLAS names persistent kernels as its edge),
+ * so this call has no counterpart on the pages.  The allocation-free entry
+ * point's built-in array is not freed: it lives as long as the library. */
 void tgemm_shutdown(void);
 
 /*
@@ -238,6 +265,17 @@ tgemm_status tgemm_debug_tile_order(int64_t M, int64_t N, int bm, int bn, int gr
 tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream);
 
 /*
+ * Diagnostic: the same bounded-wait self test (one block, one barrier nobody
+ * signals, `timeout_us` microseconds), recording into the status word kept in
+ * tgemm_run_noalloc's built-in array instead of the library's own.  It
+ * allocates nothing; tgemm_check(stream) must then report TGEMM_ERR_TIMEOUT.
+ * Like tgemm_run_noalloc, its first call on a device looks up the array's
+ * address, so make it outside CUDA stream capture.  Returns
+ * TGEMM_ERR_INVALID_ARG for timeout_us = 0 or above 10 s.
+ */
+tgemm_status tgemm_debug_noalloc_wait_timeout(uint32_t timeout_us, void *stream);
+
+/*
  * tgemm_run without any device allocation, for a skinny A (1..64 rows).
  *
  * The pages have no counterpart to this entry point; it exists for callers
@@ -261,8 +299,9 @@ tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream);
  *     other's results: order them;
  *   - the first call on each device looks up the array's device address
  *     (once); make that first call outside CUDA stream capture;
- *   - a pipeline-wait timeout stops the kernel early but is not reported by
- *     tgemm_check.
+ *   - a pipeline-wait timeout stops the kernel early and is recorded in a
+ *     status word kept in the same array: tgemm_check(stream) then returns
+ *     TGEMM_ERR_TIMEOUT (and clears it), as for the other entry points.
  */
 tgemm_status tgemm_run_noalloc(int64_t M, int64_t N, int64_t K,
                                const void *A, int64_t lda,

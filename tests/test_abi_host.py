@@ -297,3 +297,39 @@ def test_last_short_band_uses_the_tile_number(lib):
     tiles = coords(5, 2, 1, 1, 3)
     assert tiles[6] == (3, 0)
     assert tiles[7] == (4, 0)
+
+
+LOG_SCRIPT = r"""
+import sys
+sys.path.insert(0, %r)
+from dense_tiled_gemm_persistent_gb300 import tgemm
+F = 1 << 20
+tgemm.tgemm_run(-1, 96, 64, F, 64, F, 64, tgemm.B_NK, F, 96, tgemm.F16, tgemm.F16, None)
+tgemm.tgemm_run(0, 96, 64, 0, 64, 0, 64, tgemm.B_KN, 0, 96, tgemm.BF16, tgemm.F32, None)
+cfg = tgemm.Config(bm=128, bn=200, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)
+tgemm.tgemm_run_config(128, 96, 64, F, 64, F, 64, tgemm.B_NK, F, 96, tgemm.F16, tgemm.F16, None, cfg)
+"""
+
+
+@pytest.mark.parametrize("value,lines", [("1", 3), ("0", 0), (None, 0)])
+def test_log_prints_one_line_per_call(lib, value, lines):
+    """TGEMM_LOG (set, not "0") prints one stderr line per GEMM call: the
+    problem, whose configuration it was, what was launched and the status."""
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.pop("TGEMM_LOG", None)
+    if value is not None:
+        env["TGEMM_LOG"] = value
+    r = subprocess.run([sys.executable, "-c", LOG_SCRIPT % ROOT], env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    got = [ln for ln in r.stderr.splitlines() if ln.startswith("tgemm: ")]
+    assert len(got) == lines, r.stderr
+    if lines:
+        assert got[0].startswith("tgemm: tgemm_run batch=1 M=-1 N=96 K=64 B=NxK in=f16 out=f16 epilogue=0 "
+                                 "config=library -> no kernel; invalid argument")
+        assert got[1].startswith("tgemm: tgemm_run batch=1 M=0 N=96 K=64 B=KxN in=bf16 out=f32 epilogue=0 "
+                                 "config=library -> no kernel; ok")
+        assert "tgemm_run_config" in got[2] and "config=caller" in got[2] and got[2].endswith(
+            "unsupported dtype, size or configuration")

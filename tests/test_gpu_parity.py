@@ -529,3 +529,42 @@ def test_chained_products_see_each_others_results(kinds):
     r3, _ = oracle.gemm(c2, E, M, N3, N2, N2, N2, gen.B_NK, gen.F16)
     assert np.abs(r2).max() <= 2048                                 # every intermediate exact in FP16
     assert np.array_equal(bits(C3.cpu(), gen.F32), oracle.round_bits(r3, gen.F32))
+
+
+LOG_RUN = r"""
+import sys, torch
+sys.path.insert(0, %r)
+from dense_tiled_gemm_persistent_gb300 import tgemm
+for M, N, K in [(1024, 1024, 1024), (16, 4096, 4096), (4000, 3000, 5000)]:
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda:0")
+    B = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda:0")
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda:0")
+    assert tgemm.tgemm_run(M, N, K, A.data_ptr(), K, B.data_ptr(), K, tgemm.B_NK, C.data_ptr(), N, tgemm.BF16,
+                           tgemm.BF16, None) == 0
+    assert tgemm.tgemm_check() == 0
+    rc, c = tgemm.tgemm_query_config(M, N, K, tgemm.B_NK, tgemm.BF16, tgemm.BF16)
+    print("%%d %%d %%d %%d %%d %%d %%d %%d" %% (c.bm, c.bn, c.stages, c.cluster_m, c.group_m, c.split_k, c.swap_ab, c.grid))
+"""
+
+
+def test_log_line_shows_what_tgemm_query_config_returns():
+    """With TGEMM_LOG=1 every call prints the configuration it launched; for
+    the library's own choice that is tgemm_query_config's answer."""
+    import os
+    import re
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", LOG_RUN % root], env=dict(os.environ, TGEMM_LOG="1"),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    logged = [ln for ln in r.stderr.splitlines() if ln.startswith("tgemm: tgemm_run ")]
+    queried = r.stdout.split("\n")
+    assert len(logged) == 3
+    for ln, q in zip(logged, queried):
+        m = re.search(r"bm=(\d+) bn=(\d+) bk=64 stages=(\d+) cluster_m=(\d+) group_m=(\d+) split_k=(\d+) "
+                      r"swap_ab=(\d+) grid=(\d+)", ln)
+        assert m and ln.endswith("; ok") and "config=library" in ln, ln
+        got = [int(x) for x in m.groups()]
+        want = [int(x) for x in q.split()]
+        assert got[:7] == want[:7], (ln, q)
