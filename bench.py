@@ -520,6 +520,21 @@ def main():
         graph.replay()
         torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
+    # SM-clock probes (tgemm_debug_sm_clock: clock64 cycles over globaltimer
+    # time on one SM) just before and just after the timed region, outside
+    # its events, on the same stream.
+    probe_buf = torch.zeros(8, dtype=torch.int64, device=dev)
+
+    def probe(slot):
+        rc_ = tgemm.tgemm_debug_sm_clock(probe_buf.data_ptr() + 16 * slot, 20, sh)
+        if rc_ != 0:
+            raise RuntimeError("tgemm_debug_sm_clock: " + tgemm.status_string(rc_))
+
+    def probe_mhz(slot):
+        ns, cyc = probe_buf[2 * slot].item(), probe_buf[2 * slot + 1].item()
+        return cyc * 1e3 / ns if ns > 0 else None
+
+    probe(0)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_host0 = time.perf_counter()
     e_start.record(stream)
@@ -530,6 +545,7 @@ def main():
             a_, b_, c_ = copies[i % reps]
             step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
     e_end.record(stream)
+    probe(1)
     torch.cuda.synchronize(dev)
     t_host1 = time.perf_counter()
     rc = tgemm.tgemm_check(sh)
@@ -547,12 +563,19 @@ def main():
     # draws 1.4 kW in it), so inside a region that short they show the state
     # before it: they are reported, but no per-clock efficiency is derived
     # from them.  The steady-state window below is long enough.
+    mhz0, mhz1 = probe_mhz(0), probe_mhz(1)
+    clocks["sm_mhz_probe"] = {"before": mhz0, "after": mhz1,
+                              "how": "clock64 cycles over 20 us of globaltimer on one SM, just before and just "
+                                     "after the timed region"}
     if (t_host1 - t_host0) < 0.25:
-        clocks["note"] = ("timed region shorter than NVML's update interval: its samples show the clock before "
-                          "the region; see steady_state for clocks under load")
-        clocks["per_clock_efficiency"] = None
+        clocks["note"] = ("timed region shorter than NVML's update interval: its NVML samples show the clock "
+                          "before the region; the probes bracket it, and steady_state holds clocks under load")
+        mean_probe = (mhz0 + mhz1) / 2 if mhz0 and mhz1 else None
+        clocks["per_clock_efficiency"] = per_clock_efficiency(value, sms, flop_clk, mean_probe)
+        clocks["per_clock_basis"] = "mean of the two probes"
     else:
         clocks["per_clock_efficiency"] = per_clock_efficiency(value, sms, flop_clk, clocks.get("sm_mhz"))
+        clocks["per_clock_basis"] = "NVML median inside the region"
 
     # Per-launch distribution: K more launches (graph mode: blocks of up to
     # 10 replayed launches), each bracketed by its own pair of events.
@@ -604,12 +627,14 @@ def main():
                 a_, b_, c_ = copies[i % reps]
                 step(c_.data_ptr(), a_.data_ptr(), b_.data_ptr())
         e1.record(stream)
+        probe(2)
         torch.cuda.synchronize(dev)
         t1 = time.perf_counter()
         ss_ms = e0.elapsed_time(e1) / n_ss
         ss_val = tflops(wl.M, wl.N, wl.K, ss_ms)
         # skip the first quarter: the clock falls from burst to its power-limited level
         ss_clk = sampler.window(t0 + 0.25 * (t1 - t0), t1)
+        ss_clk["sm_mhz_probe_after"] = probe_mhz(2)
         steady = {"steps": n_ss, "seconds": (t1 - t0), "ms_per_step": ss_ms, "value": ss_val, "unit": "TFLOPS",
                   "clocks": ss_clk,
                   "per_clock_efficiency": per_clock_efficiency(ss_val, sms, flop_clk, ss_clk.get("sm_mhz"))}

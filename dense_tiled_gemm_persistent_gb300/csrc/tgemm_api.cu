@@ -223,15 +223,20 @@ int skinny_splits(int64_t N, int64_t K, int sm_count)
 // 128 x 256 one and keeps the tensor pipe less busy.  At most 64 rows of A
 // go to the swap-AB split-K path instead.
 // Measured winners per grid point (tune_picker.py); the last row is a sentinel.
+// Operand classes have rows of their own: 0 = FP16/BF16, 1 = FP8, 2 = FP32
+// read as TF32 (the last two measured with B stored N x K, the only layout
+// their kernels take, and more than 64 rows of A).
 struct PickRow {
-    int em, en, ek, layout;
+    int em, en, ek, layout, dclass;
     struct { int bm, bn, stages, cluster_m, group_m, split_k, swap_ab; } c;
     float us;
 };
 const PickRow kPickTable[] = {
 #include "tgemm_picker_table.inc"
-    {-1, -1, -1, -1, {0, 0, 0, 0, 0, 0, 0}, 0.f},
+    {-1, -1, -1, -1, -1, {0, 0, 0, 0, 0, 0, 0}, 0.f},
 };
+
+int pick_class(int in_dtype) { return is_f8(in_dtype) ? 1 : in_dtype == TGEMM_F32 ? 2 : 0; }
 
 int round_log2(int64_t x)
 {
@@ -244,12 +249,12 @@ int round_log2(int64_t x)
 
 // The measured winner at the grid point nearest (in log2) to this shape, if
 // the table has one; its tile shape and split are kept, sizes re-derived.
-bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, tgemm_config *cfg)
+bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, int sm_count, tgemm_config *cfg)
 {
     const int em = round_log2(M), en = round_log2(N), ek = round_log2(K);
     for (const PickRow &r : kPickTable) {
         if (r.em < 0) break;
-        if (r.em != em || r.en != en || r.ek != ek || r.layout != b_layout) continue;
+        if (r.em != em || r.en != en || r.ek != ek || r.layout != b_layout || r.dclass != dclass) continue;
         cfg->bm = r.c.bm;
         cfg->bn = r.c.bn;
         cfg->bk = kBK;
@@ -302,9 +307,9 @@ int quad_grid(int64_t M, int64_t N, int split_k, int sm_count)
 
 // The configuration tgemm_run uses: the measured table where it covers the
 // shape and its entry is legal for it, the wave cost model otherwise.
-void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int sm_count, tgemm_config *cfg)
+void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, int sm_count, tgemm_config *cfg)
 {
-    if (table_config(M, N, K, b_layout, sm_count, cfg)) {
+    if (table_config(M, N, K, b_layout, dclass, sm_count, cfg)) {
         const int64_t kb = ceil_div(K, kBK);
         bool ok = cfg->split_k <= kb;
         if (ok && cfg->swap_ab == 2) ok = cfg->split_k <= cluster_splits_limit(cfg->bn, cfg->stages);
@@ -812,6 +817,20 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     p.c_ptr = C;
     p.ldc = ldc;
     p.splits = splits;
+    if (cfg.swap_ab == 2) {
+        // Dependent-launch overlap of the in-cluster kernel: when the next
+        // launch's CTAs fit beside this one's (a grid of at most one CTA per
+        // SM) or each CTA streams a long slice (at least 12 k-blocks), start
+        // the next launch once every CTA has issued its last load and let it
+        // prefetch its whole weight slice; otherwise start it at once with a
+        // short prefetch.  Measured on one GB300, graph-replayed, best
+        // configuration per shape: 16x4096x4096 8.9 -> 8.2 us, 64x4096x4096
+        // 11.5 -> 11.0, 32x4096x8192 14.9 -> 14.4, 16x14336x4096 20.8 -> 19.9;
+        // 16x16384x1024 (256 CTAs of 8 k-blocks) stays early, 7.5 against 8.0.
+        const int64_t kb_per_cta = ceil_div(ceil_div(K, kBK), splits);
+        p.late_trigger = (kb_per_cta >= 12 || tiles_n * splits <= dev->sm_count) ? 1 : 0;
+        p.prefetch_kb = p.late_trigger ? (int32_t)kb_per_cta : kSkinnyPrefetchKb;
+    }
     tgemm_status est = epilogue_params(ep, M, N, out_dtype, &p);
     if (est != TGEMM_OK) return est;
     if (splits > 1 && cfg.swap_ab == 1) {
@@ -859,8 +878,8 @@ void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, in
 
 tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                       int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
-                      void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags,
-                      const tgemm_epilogue *ep, const Batch &bt)
+                      void *stream_ptr, const tgemm_config *forced, const tgemm_epilogue *ep,
+                      const Batch &bt)
 {
     bool noop = false;
     tgemm_status st = validate(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, &noop);
@@ -920,7 +939,7 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         return TGEMM_OK;
     }
     if (!forced) {
-        choose_config(M, N, K, b_layout, dev->sm_count, &cfg);
+        choose_config(M, N, K, b_layout, pick_class(in_dtype), dev->sm_count, &cfg);
         if (bt.count > 1) {
             // The table was measured on single problems and the skinny kernels
             // are not batched: the wave model over the tiles of all batches.
@@ -979,7 +998,6 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     p.group_m = cfg.group_m;
     // kind::f16: type codes 0 F16 / 1 BF16; kind::f8f6f4: 0 E4M3 / 1 E5M2
     p.idesc = make_idesc(mma_type(in_dtype), b_mn, cfg.bm, cfg.bn);
-    p.debug_flags = debug_flags;
     p.status = dev->status;
     p.timeout_ns = wait_timeout_ns();
     st = epilogue_params(ep, M, N, out_dtype, &p, bt);
@@ -1036,12 +1054,12 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
 
 tgemm_status run_impl(const char *entry, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                       const void *B, int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
-                      void *stream_ptr, const tgemm_config *forced, uint32_t debug_flags,
-                      const tgemm_epilogue *ep = nullptr, const Batch &bt = Batch())
+                      void *stream_ptr, const tgemm_config *forced, const tgemm_epilogue *ep = nullptr,
+                      const Batch &bt = Batch())
 {
     t_rec = LaunchRecord();
     const tgemm_status st = run_body(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream_ptr,
-                                     forced, debug_flags, ep, bt);
+                                     forced, ep, bt);
     if (log_enabled()) log_call(entry, bt.count, M, N, K, b_layout, in_dtype, out_dtype, forced != nullptr,
                                 ep != nullptr, st);
     return st;
@@ -1056,8 +1074,7 @@ TGEMM_EXPORT tgemm_status tgemm_run(int64_t M, int64_t N, int64_t K, const void 
                                     const void *B, int64_t ldb, tgemm_b_layout b_layout, void *C,
                                     int64_t ldc, tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream)
 {
-    return run_impl("tgemm_run", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, nullptr,
-                    0);
+    return run_impl("tgemm_run", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, nullptr);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
@@ -1066,8 +1083,7 @@ TGEMM_EXPORT tgemm_status tgemm_run_config(int64_t M, int64_t N, int64_t K, cons
                                            void *stream, const tgemm_config *cfg)
 {
     if (!cfg) return TGEMM_ERR_INVALID_ARG;
-    return run_impl("tgemm_run_config", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg,
-                    0);
+    return run_impl("tgemm_run_config", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -1075,7 +1091,7 @@ TGEMM_EXPORT tgemm_status tgemm_run_ex(int64_t M, int64_t N, int64_t K, const vo
                                        tgemm_dtype in_dtype, tgemm_dtype out_dtype, void *stream,
                                        const tgemm_epilogue *ep, const tgemm_config *cfg)
 {
-    return run_impl("tgemm_run_ex", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg, 0,
+    return run_impl("tgemm_run_ex", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype, stream, cfg,
                     ep);
 }
 
@@ -1104,7 +1120,7 @@ TGEMM_EXPORT tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, in
     bt.sb = stride_b;
     bt.sc = stride_c;
     return run_impl("tgemm_run_strided_batched", M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dtype,
-                    stream, cfg, 0, ep, bt);
+                    stream, cfg, ep, bt);
 }
 
 TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
@@ -1121,7 +1137,8 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     DeviceState *dev = nullptr;
     tgemm_status st = device_state(&dev);
     if (st != TGEMM_OK) return st;
-    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, dev->sm_count, out_cfg);
+    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, pick_class(in_dtype), dev->sm_count,
+                  out_cfg);
     if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(65, N, K, dev->sm_count, out_cfg);
     // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
     prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
@@ -1285,6 +1302,21 @@ TGEMM_EXPORT tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *st
     if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return TGEMM_ERR_INVALID_ARG;
     if (launch_wait_timeout_probe(dev->status, (uint64_t)timeout_us * 1000ull,
                                   static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
+TGEMM_EXPORT tgemm_status tgemm_debug_sm_clock(uint64_t *out, uint32_t duration_us, void *stream)
+{
+    if (!out || duration_us == 0 || duration_us > 100u * 1000u) return TGEMM_ERR_INVALID_ARG;
+    if (((uintptr_t)out % 8) != 0) return TGEMM_ERR_MISALIGNED;
+    DeviceState *dev = nullptr;
+    tgemm_status st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    if (launch_sm_clock_probe(out, (uint64_t)duration_us * 1000ull, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
     }

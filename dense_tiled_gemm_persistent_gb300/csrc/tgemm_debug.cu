@@ -7,6 +7,10 @@
 // Tile-order probe: every tile number of a grid mapped on the device by the
 // same grouped_tile32 the GEMM kernels use, so that tests can compare the
 // device's order with the host's.
+//
+// SM-clock probe: one thread counts %clock64 cycles over a stretch of
+// %globaltimer time, which gives the SM clock of the moment the probe runs
+// (for benchmark records; NVML's clock readings trail by tens of ms).
 #include "tgemm_params.h"
 #include "tgemm_ptx.cuh"
 #include "tgemm_sched.h"
@@ -48,6 +52,25 @@ __global__ void tile_order_probe_kernel(int32_t tiles_m, int32_t tiles_n, int32_
         rows[bid] = r;
         cols[bid] = c;
     }
+}
+
+__global__ void sm_clock_probe_kernel(uint64_t *out, uint64_t duration_ns)
+{
+    if (threadIdx.x != 0) return;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    const uint64_t c0 = clock64();
+    uint64_t t = t0;
+    // bounded twice: by the time asked for and by an iteration count far above it
+    for (uint32_t i = 0; i < (1u << 26) && t - t0 < duration_ns; ++i) t = ptx::globaltimer_ns();
+    const uint64_t c1 = clock64();
+    out[0] = t - t0;
+    out[1] = c1 - c0;
+}
+
+cudaError_t launch_sm_clock_probe(uint64_t *out, uint64_t duration_ns, cudaStream_t st)
+{
+    sm_clock_probe_kernel<<<1, 32, 0, st>>>(out, duration_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_tile_order_probe(int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t count, int32_t *rows,

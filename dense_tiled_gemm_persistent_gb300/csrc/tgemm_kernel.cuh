@@ -470,7 +470,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;   // latest load per stage, for wind-down
             bool ok = true;
-            bool first = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int64_t tr, tc;
                 int bz;
@@ -483,24 +482,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         ok = false;
                         break;
                     }
-                    const bool skip = first && (p.debug_flags & 1u);
-                    first = false;
-                    if (!skip) {
-                        const uint32_t fb = full_bar(s);
-                        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                        const int32_t k0 = kb * KBlock<KIND>::elems;
-                        ptx::tma_load_3d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
-                        if (B_MN) {
+                    const uint32_t fb = full_bar(s);
+                    ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                    const int32_t k0 = kb * KBlock<KIND>::elems;
+                    ptx::tma_load_3d(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
+                    if (B_MN) {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                ptx::tma_load_3d(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
-                                                 n0 + 64 * j, k0, zb);
-                        } else {
-                            ptx::tma_load_3d(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0, zb);
-                        }
-                        issued_mask |= 1u << s;
-                        issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                        for (int j = 0; j < BN / 64; ++j)
+                            ptx::tma_load_3d(sB + s * Plan::b_stage + j * (kBK * 128), &p.tma_b, fb,
+                                             n0 + 64 * j, k0, zb);
+                    } else {
+                        ptx::tma_load_3d(sB + s * Plan::b_stage, &p.tma_b, fb, k0, n0, zb);
                     }
+                    issued_mask |= 1u << s;
+                    issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;

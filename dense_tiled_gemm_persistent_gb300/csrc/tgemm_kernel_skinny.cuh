@@ -44,25 +44,27 @@ struct SkinnyPlan {
     static constexpr uint32_t alloc_bytes = bytes + 1024;
 };
 
-// L2 prefetch of the first k-blocks of this CTA's weight slice, issued by
-// the producer before griddepcontrol.wait.  A CTA of a dependent launch is
-// resident while the previous kernel still runs (the launch is triggered
-// early and the half-size ring leaves room for two CTAs per SM), so its
-// weights stream from HBM during the previous kernel's tail instead of after
-// it.  Weights are read-only inputs of the product; even if an earlier kernel
-// were still writing them, the prefetch only warms L2 and the TMA loads after
-// the wait read the current data.  Only the first kSkinnyPrefetchKb k-blocks
-// (16 KiB of weights each) are prefetched: that covers the ramp of the ring,
-// while a whole slice made the dependent launch compete with the running one
-// for the rest of its time.  Measured over the M <= 64 picker grid on a
-// GB300, best configuration per point, geometric mean: no prefetch +3.6 %,
-// 2 k-blocks +1.0 %, 8 +1.6 %, whole slices (at most 16) +2.4 % against 4.
+// L2 prefetch of the first `depth` k-blocks of this CTA's weight slice,
+// issued by the producer before griddepcontrol.wait.  A CTA of a dependent
+// launch is resident while the previous kernel still runs (the half-size ring
+// leaves room for two CTAs per SM), so its weights stream from HBM during the
+// previous kernel's tail instead of after it.  Weights are read-only inputs
+// of the product; even if an earlier kernel were still writing them, the
+// prefetch only warms L2 and the TMA loads after the wait read the current
+// data.  How deep to prefetch depends on when the dependent launch starts
+// (GemmParams::late_trigger): started at once, only the first
+// kSkinnyPrefetchKb k-blocks, since a whole slice would compete with the
+// running launch for all of its time (measured over the M <= 64 picker grid,
+// best configuration per point, geometric mean: no prefetch +3.6 %, 2
+// k-blocks +1.0 %, 8 +1.6 %, whole slices +2.4 % against 4); started once
+// the running launch has issued its last loads, the whole slice.
 constexpr int kSkinnyPrefetchKb = 4;
 
 template <bool W_MN>
-__device__ __forceinline__ void prefetch_weights_l2(const CUtensorMap *tma_b, int32_t n0, int kb0, int kb1)
+__device__ __forceinline__ void prefetch_weights_l2(const CUtensorMap *tma_b, int32_t n0, int kb0, int kb1,
+                                                    int depth)
 {
-    const int kbe = kb1 - kb0 > kSkinnyPrefetchKb ? kb0 + kSkinnyPrefetchKb : kb1;
+    const int kbe = kb1 - kb0 > depth ? kb0 + depth : kb1;
     for (int kb = kb0; kb < kbe; ++kb) {
         const int32_t k0 = kb * kBK;
         if (W_MN) {
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&p.tma_a);
         ptx::prefetch_tensormap(&p.tma_b);
-        prefetch_weights_l2<W_MN>(&p.tma_b, n0, kb0, kb1);
+        prefetch_weights_l2<W_MN>(&p.tma_b, n0, kb0, kb1, kSkinnyPrefetchKb);
     }
     if (warp == 1) {
         ptx::tmem_alloc(slot, kTmemCols);

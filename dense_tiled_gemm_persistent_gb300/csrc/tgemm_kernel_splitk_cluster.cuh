@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&p.tma_a);
         ptx::prefetch_tensormap(&p.tma_b);
-        prefetch_weights_l2<W_MN>(&p.tma_b, n0, kb0, kb1);
+        prefetch_weights_l2<W_MN>(&p.tma_b, n0, kb0, kb1, p.prefetch_kb);
     }
     if (warp == 1) {
         ptx::tmem_alloc(slot, kTmemCols);
@@ -132,7 +132,11 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
     ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
-    ptx::launch_dependents();
+    // The next launch on the stream may start its prologue (and weight
+    // prefetch) at once, or -- late_trigger -- once every CTA has issued its
+    // last load (the first call in a CTA counts; the later ones in the other
+    // roles are no-ops, kept so that every path reaches one).
+    if (!p.late_trigger) ptx::launch_dependents();
 
     float v[NPAD];
 #pragma unroll
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
                     ptx::tma_load_2d(sW + s * Plan::w_stage, &p.tma_b, fb, k0, n0);
                 }
                 ptx::tma_load_2d(sX + s * Plan::x_stage, &p.tma_a, fb, k0, 0);
+                if (p.late_trigger && kb + 1 == kb1) ptx::launch_dependents();
                 issued_mask |= 1u << s;
                 issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                 if (++s == S) {
@@ -168,12 +173,14 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
                     ph ^= 1u;
                 }
             }
+            if (p.late_trigger) ptx::launch_dependents();
             if (!ok)
                 for (int t = 0; t < S; ++t)
                     if (issued_mask & (1u << t))
                         wait_bounded(full_bar(t), (issued_parity >> t) & 1u, wc, SITE_DRAIN_LOADS, false);
         }
         __syncwarp();
+        if (p.late_trigger) ptx::launch_dependents();
     } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
@@ -212,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
             }
         }
         __syncwarp();
+        if (p.late_trigger) ptx::launch_dependents();
     } else {
         // -------------------------------------------------- epilogue: TMEM -> registers
         const int q = warp & 3;
@@ -228,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
             }
             have = true;
         }
+        if (p.late_trigger) ptx::launch_dependents();
     }
 
     ptx::cluster_wait();   // every CTA's barriers are initialised

@@ -46,7 +46,6 @@ struct alignas(128) GemmParams {
     int32_t a_batched, b_batched;   // 0: the operand is shared by every batch (z = 0)
     int32_t group_m;
     uint32_t idesc;         // tcgen05 instruction descriptor (kind::f16)
-    uint32_t debug_flags;   // bit 0: the producer skips its first load (timeout test)
     uint32_t *status;       // device status word (first fault wins)
     uint64_t timeout_ns;    // limit of every pipeline wait
     // swap-AB / split-K path only
@@ -55,6 +54,8 @@ struct alignas(128) GemmParams {
     float *partials;        // [splits][tiles_n][128 rows][npad] FP32 partial sums
     uint32_t *counters;     // [tiles_n] arrival counters, zero between calls
     int32_t splits;         // K is cut into `splits` runs of whole k-blocks
+    int32_t prefetch_kb;    // k-blocks of its weight slice a CTA prefetches into L2 before the dependency wait
+    int32_t late_trigger;   // 1: let the next launch start once this CTA has issued its last load (else at once)
     // stream-K tail of the CTA-pair kernel (sk_units = 0: whole tiles only)
     int32_t dp_tiles;       // tiles [0, dp_tiles) are processed whole
     int32_t sk_tiles;       // tiles [dp_tiles, dp_tiles + sk_tiles) are spread over
@@ -108,8 +109,9 @@ inline cudaError_t ensure_smem_limit(Kernel kern, unsigned smem, std::atomic<uns
     return e;
 }
 
-// The bounded-wait self test kernel launcher (tgemm_debug.cu).
+// The bounded-wait self test and SM-clock probe launchers (tgemm_debug.cu).
 cudaError_t launch_wait_timeout_probe(uint32_t *status, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_sm_clock_probe(uint64_t *out, uint64_t duration_ns, cudaStream_t st);
 // tgemm_noalloc.cu: the allocation-free path's status word on a device
 // (nullptr before that path's first call there)
 uint32_t *noalloc_status_word(int dev);

@@ -1,20 +1,26 @@
 """Measure every kernel configuration over a grid of shapes and write the
 picker table the library compiles in.
 
-For each grid point (M, N, K, B layout) the script times each candidate
-configuration through tgemm_run_config on the current GPU (FP16 in, FP16
-out, back-to-back launches over enough rotating operand copies to exceed L2),
+For each grid point (M, N, K, B layout, operand class) the script times each
+candidate configuration through tgemm_run_config on the current GPU
+(back-to-back launches over enough rotating operand copies to exceed L2),
 twice (forward and reverse candidate order, best of the two), keeps the
 fastest, and writes
 
   * picker_table.csv              every measurement (committed, for review);
   * csrc/tgemm_picker_table.inc   the winner per grid point, as a C array.
 
-Launches are timed from a replayed CUDA graph.  tgemm_run rounds log2 of
-each of M, N and K to the nearest grid exponent and
-uses the winner there; off the grid it falls back to its wave cost model.
+Operand classes: 0 = FP16/BF16 (measured FP16 in, FP16 out, both B
+layouts, the skinny band included), 1 = FP8 (E4M3 in, BF16 out) and 2 = FP32
+read as TF32 (FP32 in and out); the last two only with B stored N x K and
+more than 64 rows of A, which is all their kernels take.
 
-Usage (on the GPU machine):  python -m dense_tiled_gemm_persistent_gb300.tune_picker
+Launches are timed from a replayed CUDA graph.  tgemm_run rounds log2 of
+each of M, N and K to the nearest grid exponent and uses the winner of its
+operand class there; off the grid it falls back to its wave cost model.
+
+Usage (on the GPU machine):
+  python -m dense_tiled_gemm_persistent_gb300.tune_picker [--classes 0,1,2] [--skinny-only]
 """
 from __future__ import annotations
 
@@ -43,11 +49,15 @@ SKINNY_K = [10, 12, 13]
 L2 = 129 * 1000 * 1000
 
 
-def candidates(tg, M, N=0):
+# operand class -> (input type, output type) the class is measured with
+CLASS_TYPES = {0: (0, 0), 1: (3, 1), 2: (2, 2)}
+
+
+def candidates(tg, M, N=0, dclass=0):
     """(kind, Config) pairs valid for M rows of A (and N columns of B)."""
     C = tg.Config
     out = []
-    if M <= 64:
+    if M <= 64 and dclass == 0:
         npad = 16 if M <= 16 else (32 if M <= 32 else 64)
         st = {16: 12, 32: 10, 64: 9}[npad]
         mx = {16: 8, 32: 8, 64: 7}[npad]
@@ -84,7 +94,7 @@ def candidates(tg, M, N=0):
     return out
 
 
-def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustained=False):
+def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustained=False, types=(0, 0)):
     """Microseconds per launch, replaying `iters` launches from a CUDA graph
     (so the host's per-call cost does not hide the kernel's own time)."""
     n = len(copies)
@@ -94,7 +104,7 @@ def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustaine
     def run(i):
         A, B, C = copies[i % n]
         return tg.tgemm_run_config(M, N, K, A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1], layout,
-                                   C.data_ptr(), C.shape[1], 0, 0, sh, cfg)
+                                   C.data_ptr(), C.shape[1], types[0], types[1], sh, cfg)
 
     with torch.cuda.stream(cap):
         for i in range(3):
@@ -134,14 +144,35 @@ def time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustaine
     return e0.elapsed_time(e1) / (iters * replays) * 1000.0   # microseconds
 
 
+def read_rows(path):
+    """CSV rows with integer keys; rows written before the operand class
+    existed are class 0."""
+    with open(path, newline="") as f:
+        out = []
+        for r in csv.DictReader(f):
+            r = dict(r)
+            r["dclass"] = int(r.get("dclass") or 0)
+            for k in ("em", "en", "ek", "layout"):
+                r[k] = int(r[k])
+            out.append(r)
+        return out
+
+
+def point_key(r):
+    return (r["em"], r["en"], r["ek"], r["layout"], r["dclass"])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--quick", action="store_true", help="a few grid points only (smoke)")
     ap.add_argument("--skinny-only", action="store_true",
                     help="re-measure the M <= 64 band only and merge it into the existing table and CSV")
+    ap.add_argument("--classes", default="0,1,2",
+                    help="operand classes to measure (0 FP16/BF16, 1 FP8, 2 TF32); the others are kept")
     ap.add_argument("--csv", default=CSV_PATH)
     ap.add_argument("--inc", default=INC_PATH)
     args = ap.parse_args()
+    classes = [int(x) for x in args.classes.split(",") if x]
 
     import torch
     from dense_tiled_gemm_persistent_gb300 import build as lb
@@ -151,96 +182,108 @@ def main():
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
 
-    points = []
-    for layout in (tg.B_NK, tg.B_KN):
-        for em in BIG_M:
-            for en in BIG_N:
-                for ek in BIG_K:
-                    points.append((em, en, ek, layout))
-        for em in SKINNY_M:
-            for en in SKINNY_N:
-                for ek in SKINNY_K:
-                    points.append((em, en, ek, layout))
-    if args.quick:
-        points = points[::37]
-    all_points = list(points)
+    all_points = []
+    for dclass in (0, 1, 2):
+        for layout in ((tg.B_NK, tg.B_KN) if dclass == 0 else (tg.B_NK,)):
+            for em in BIG_M:
+                for en in BIG_N:
+                    for ek in BIG_K:
+                        all_points.append((em, en, ek, layout, dclass))
+            if dclass == 0:
+                for em in SKINNY_M:
+                    for en in SKINNY_N:
+                        for ek in SKINNY_K:
+                            all_points.append((em, en, ek, layout, dclass))
+    points = [pt for pt in all_points if pt[4] in classes]
     if args.skinny_only:
         points = [pt for pt in points if pt[0] in SKINNY_M]
+    if args.quick:
+        points = points[::37]
 
     rows, winners = [], []
     t0 = time.time()
-    for (em, en, ek, layout) in points:
+    for (em, en, ek, layout, dclass) in points:
         M, N, K = 1 << em, 1 << en, 1 << ek
-        bytes_ = 2 * (M * K + K * N + M * N)
+        tin, tout = CLASS_TYPES[dclass]
+        ein, eout = tg_size(tin), tg_size(tout)
+        bytes_ = ein * (M * K + K * N) + eout * M * N
         reps = max(1, -(-3 * L2 // bytes_))
         reps = min(reps, 64)
         flops = 2.0 * M * N * K
         iters = int(min(200, max(10, 2e13 / flops)))
         copies = []
+        tdt = {0: torch.float16, 1: torch.bfloat16, 2: torch.float32, 3: torch.float8_e4m3fn}
         for _ in range(reps):
-            A = torch.randn(M, K, device=dev).to(torch.float16)
-            B = torch.randn(*((N, K) if layout == tg.B_NK else (K, N)), device=dev).to(torch.float16)
-            Cc = torch.empty(M, N, device=dev, dtype=torch.float16)
+            A = torch.randn(M, K, device=dev).to(tdt[tin])
+            B = torch.randn(*((N, K) if layout == tg.B_NK else (K, N)), device=dev).to(tdt[tin])
+            Cc = torch.empty(M, N, device=dev, dtype=tdt[tout])
             copies.append((A, B, Cc))
         best = None
         # Two passes, the second in reverse order, each candidate keeping its
         # better time: the GPU warms up (and its power-capped clock drops)
         # through a point's candidates, which otherwise favours whichever is
         # timed first.
-        cands = candidates(tg, M, N)
+        cands = candidates(tg, M, N, dclass)
         times = {}
         for order in (cands, cands[::-1]):
             for kind, cfg in order:
-                us = time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustained=flops >= 2e11)
+                us = time_config(torch, tg, M, N, K, layout, cfg, copies, stream, iters, sustained=flops >= 2e11,
+                                 types=(tin, tout))
                 if us is not None and (kind not in times or us < times[kind]):
                     times[kind] = us
         for kind, cfg in cands:
             if kind not in times:
                 continue
             us = times[kind]
-            rows.append(dict(em=em, en=en, ek=ek, layout=layout, kind=kind, us=round(us, 3),
+            rows.append(dict(em=em, en=en, ek=ek, layout=layout, dclass=dclass, kind=kind, us=round(us, 3),
                              tflops=round(flops / us / 1e6, 1)))
             if best is None or us < best[0]:
                 best = (us, kind, cfg)
         del copies
         if best:
-            winners.append((em, en, ek, layout, best))
-        print("%5d %5d %5d %s -> %s %.2f us" % (M, N, K, "nk" if layout else "kn", best[1] if best else None,
-                                                 best[0] if best else -1), flush=True)
+            winners.append((em, en, ek, layout, dclass, best))
+        print("%5d %5d %5d %s class %d -> %s %.2f us" % (M, N, K, "nk" if layout else "kn", dclass,
+                                                          best[1] if best else None, best[0] if best else -1),
+              flush=True)
     print("sweep took %.0f s" % (time.time() - t0))
 
     lines = {}
-    for em, en, ek, layout, (us, kind, c) in winners:
-        lines[(em, en, ek, layout)] = "{%d, %d, %d, %d, {%d, %d, %d, %d, %d, %d, %d}, %.3ff},  // %s\n" % (
-            em, en, ek, layout, c.bm, c.bn, c.stages, c.cluster_m, c.group_m, c.split_k, c.swap_ab, us, kind)
-    if args.skinny_only:
-        # keep the other grid points' measurements and winners as they are
-        measured = set(points)
-        with open(args.csv, newline="") as f:
-            kept = [r for r in csv.DictReader(f)
-                    if (int(r["em"]), int(r["en"]), int(r["ek"]), int(r["layout"])) not in measured]
-        rows = kept + rows
+    for em, en, ek, layout, dclass, (us, kind, c) in winners:
+        lines[(em, en, ek, layout, dclass)] = "{%d, %d, %d, %d, %d, {%d, %d, %d, %d, %d, %d, %d}, %.3ff},  // %s\n" % (
+            em, en, ek, layout, dclass, c.bm, c.bn, c.stages, c.cluster_m, c.group_m, c.split_k, c.swap_ab, us,
+            kind)
+    # keep the measurements and winners of every grid point not measured now
+    measured = set(points)
+    if os.path.exists(args.csv):
+        rows = [r for r in read_rows(args.csv) if point_key(r) not in measured] + rows
+    if os.path.exists(args.inc):
         with open(args.inc) as f:
             for line in f:
                 if line.startswith("{"):
-                    key = tuple(int(x) for x in line[1:].split(",")[:4])
-                    if key not in measured:
+                    key = tuple(int(x) for x in line[1:].split(",")[:5])
+                    if key not in measured and key in set(all_points):
                         lines[key] = line
-        order = {pt: i for i, pt in enumerate(all_points)}
-        rows.sort(key=lambda r: order.get((int(r["em"]), int(r["en"]), int(r["ek"]), int(r["layout"])), -1))
+    order = {pt: i for i, pt in enumerate(all_points)}
+    rows.sort(key=lambda r: order.get(point_key(r), -1))
     with open(args.csv, "w", newline="") as f:
-        w = csv.DictWriter(f, fieldnames=["em", "en", "ek", "layout", "kind", "us", "tflops"])
+        w = csv.DictWriter(f, fieldnames=["em", "en", "ek", "layout", "dclass", "kind", "us", "tflops"])
         w.writeheader()
         w.writerows(rows)
     gpu = torch.cuda.get_device_name(dev)
     with open(args.inc, "w") as f:
         f.write("// Generated by dense_tiled_gemm_persistent_gb300/tune_picker.py on %s.\n" % gpu)
-        f.write("// log2 M, log2 N, log2 K, B layout (0 = KxN, 1 = NxK) -> fastest measured configuration\n")
-        f.write("// {bm, bn, stages, cluster_m, group_m, split_k, swap_ab}, and its time in us.\n")
+        f.write("// log2 M, log2 N, log2 K, B layout (0 = KxN, 1 = NxK), operand class (0 = FP16/BF16, 1 = FP8, "
+                "2 = TF32)\n")
+        f.write("// -> fastest measured configuration {bm, bn, stages, cluster_m, group_m, split_k, swap_ab}, "
+                "and its time in us.\n")
         for pt in all_points:
             if pt in lines:
                 f.write(lines[pt])
     print("wrote", args.csv, "and", args.inc)
+
+
+def tg_size(t):
+    return {0: 2, 1: 2, 2: 4, 3: 1}[t]
 
 
 if __name__ == "__main__":

@@ -276,6 +276,19 @@ tgemm_status tgemm_debug_wait_timeout(uint32_t timeout_us, void *stream);
 tgemm_status tgemm_debug_noalloc_wait_timeout(uint32_t timeout_us, void *stream);
 
 /*
+ * Diagnostic: the SM clock at the moment of the call's turn on `stream`.  One
+ * thread counts %clock64 cycles over `duration_us` microseconds of
+ * %globaltimer (1 .. 100000) and writes out[0] = the nanoseconds elapsed,
+ * out[1] = the cycles counted, so out[1] * 1000 / out[0] is the SM clock in
+ * MHz.  out is a caller-owned device array of two uint64_t, 8-byte aligned.
+ * Benchmarks place it just before and after a timed region: NVML's clock
+ * readings trail the hardware by tens of milliseconds.  The pages report
+ * throughput only; this exists so that a throughput can be set against the
+ * clock it ran at (per-clock tensor efficiency).
+ */
+tgemm_status tgemm_debug_sm_clock(uint64_t *out, uint32_t duration_us, void *stream);
+
+/*
  * tgemm_run without any device allocation, for a skinny A (1..64 rows).
  *
  * The pages have no counterpart to this entry point; it exists for callers

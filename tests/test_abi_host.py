@@ -333,3 +333,10 @@ def test_log_prints_one_line_per_call(lib, value, lines):
                                  "config=library -> no kernel; ok")
         assert "tgemm_run_config" in got[2] and "config=caller" in got[2] and got[2].endswith(
             "unsupported dtype, size or configuration")
+
+
+def test_sm_clock_probe_checks_arguments_on_the_host(lib):
+    assert tgemm.tgemm_debug_sm_clock(None, 20) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_sm_clock(FAKE, 0) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_sm_clock(FAKE, 100001) == tgemm.ERR_INVALID_ARG
+    assert tgemm.tgemm_debug_sm_clock(FAKE + 4, 20) == tgemm.ERR_MISALIGNED

@@ -568,3 +568,15 @@ def test_log_line_shows_what_tgemm_query_config_returns():
         got = [int(x) for x in m.groups()]
         want = [int(x) for x in q.split()]
         assert got[:7] == want[:7], (ln, q)
+
+
+def test_sm_clock_probe_reads_a_plausible_clock():
+    """tgemm_debug_sm_clock: cycles over at least the asked time, at a clock
+    between 300 MHz and the device's maximum (with 5 % slack)."""
+    out = torch.zeros(2, dtype=torch.int64, device="cuda:0")
+    assert tgemm.tgemm_debug_sm_clock(out.data_ptr(), 50) == 0
+    assert tgemm.tgemm_check() == 0
+    ns, cyc = out.tolist()
+    assert ns >= 50_000
+    mhz = cyc * 1e3 / ns
+    assert 300 <= mhz <= 2070 * 1.05, mhz

@@ -10,8 +10,8 @@ PKG = os.path.join(os.path.dirname(HERE), "dense_tiled_gemm_persistent_gb300")
 INC = os.path.join(PKG, "csrc", "tgemm_picker_table.inc")
 CSV = os.path.join(PKG, "picker_table.csv")
 
-ROW = re.compile(r"\{(-?\d+), (-?\d+), (-?\d+), (\d+), \{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}, "
-                 r"([0-9.]+)f\},\s*// (\w+)")
+ROW = re.compile(r"\{(-?\d+), (-?\d+), (-?\d+), (\d+), (\d+), \{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), "
+                 r"(\d+)\}, ([0-9.]+)f\},\s*// (\w+)")
 
 
 def rows():
@@ -19,9 +19,10 @@ def rows():
     for line in open(INC):
         m = ROW.match(line.strip())
         if m:
-            v = [int(x) for x in m.groups()[:11]]
-            out.append(dict(em=v[0], en=v[1], ek=v[2], layout=v[3], bm=v[4], bn=v[5], stages=v[6], cluster_m=v[7],
-                            group_m=v[8], split_k=v[9], swap_ab=v[10], us=float(m.group(12)), kind=m.group(13)))
+            v = [int(x) for x in m.groups()[:12]]
+            out.append(dict(em=v[0], en=v[1], ek=v[2], layout=v[3], dclass=v[4], bm=v[5], bn=v[6], stages=v[7],
+                            cluster_m=v[8], group_m=v[9], split_k=v[10], swap_ab=v[11], us=float(m.group(13)),
+                            kind=m.group(14)))
     return out
 
 
@@ -30,9 +31,13 @@ def test_every_row_is_a_legal_configuration():
     assert len(r) > 100
     seen = set()
     for e in r:
-        key = (e["em"], e["en"], e["ek"], e["layout"])
+        key = (e["em"], e["en"], e["ek"], e["layout"], e["dclass"])
         assert key not in seen, key
         seen.add(key)
+        assert e["dclass"] in (0, 1, 2)
+        if e["dclass"] != 0:
+            # FP8 and TF32 operands: tile kernels only, B stored N x K, more than 64 rows of A
+            assert e["swap_ab"] == 0 and e["layout"] == 1 and e["em"] > 6
         if e["swap_ab"]:
             M = 1 << e["em"]
             assert M <= 64 and e["bn"] >= M and e["bm"] == 128
@@ -52,10 +57,10 @@ def test_every_row_is_a_legal_configuration():
 def test_table_rows_are_the_fastest_measurement_of_their_point():
     times = {}
     for m in csv.DictReader(open(CSV)):
-        key = (int(m["em"]), int(m["en"]), int(m["ek"]), int(m["layout"]))
+        key = (int(m["em"]), int(m["en"]), int(m["ek"]), int(m["layout"]), int(m.get("dclass") or 0))
         times.setdefault(key, {})[m["kind"]] = float(m["us"])
     for e in rows():
-        t = times[(e["em"], e["en"], e["ek"], e["layout"])]
+        t = times[(e["em"], e["en"], e["ek"], e["layout"], e["dclass"])]
         # the CSV rounds to 1 ns, so two kinds may tie there
         assert e["kind"] in t and t[e["kind"]] == pytest.approx(min(t.values()), abs=1e-3)
         assert e["us"] == pytest.approx(t[e["kind"]], abs=1e-3)
@@ -64,6 +69,6 @@ def test_table_rows_are_the_fastest_measurement_of_their_point():
 def test_large_square_problems_pick_the_cta_pair():
     # 256 x 256 tiles on CTA pairs: whole tiles, stream-K tail, wider raster
     # bands, or two pairs sharing A
-    big = [e for e in rows() if e["em"] >= 13 and e["en"] >= 13 and e["ek"] >= 12]
+    big = [e for e in rows() if e["em"] >= 13 and e["en"] >= 13 and e["ek"] >= 12 and e["dclass"] == 0]
     assert big and all(e["kind"] in ("pair256", "pair256sk", "pair256g16", "quad256", "quad256sk") for e in big)
     assert all(e["bm"] == 256 and e["bn"] == 256 and e["cluster_m"] in (2, 4) for e in big)
