@@ -16,10 +16,11 @@ multicast, which is only allowed in code that runs on one GPU alone.
 
 Besides the timed K steps (whose mean is the headline value) the line
 carries the median and the best of K individually event-bracketed launches,
-SM clocks sampled through NVML every few milliseconds inside the timed
-region, a steady-state window of about a second after it (the GB300 settles
-at its power limit within a few hundred milliseconds of dense GEMMs), and,
-from the CPU-baseline leg, the oracle's check of sampled output elements.
+the SM clock the GEMM launches measured themselves (tgemm_debug_clock_record)
+beside NVML samples of the timed region and probes just before and after it,
+a steady-state window of about a second after it (the GB300 settles at its
+power limit within a few hundred milliseconds of dense GEMMs), and, from the
+CPU-baseline leg, the oracle's check of sampled output elements.
 """
 from __future__ import annotations
 
@@ -498,6 +499,22 @@ def main():
     # replay the loop from a captured CUDA graph so that the host's per-call
     # cost does not starve the GPU; the graph holds the same launches.
     use_graph = args.graph == "on" or (args.graph == "auto" and wl.flops < GRAPH_FLOPS)
+    # The kernels' own SM-clock record (tgemm_debug_clock_record): set before
+    # any graph is captured, so the captured launches carry it too.
+    clock_rec = torch.zeros(8, dtype=torch.int64, device=dev)
+    rc = tgemm.tgemm_debug_clock_record(clock_rec.data_ptr())
+    if rc != 0:
+        raise RuntimeError("tgemm_debug_clock_record: " + tgemm.status_string(rc))
+
+    def kernel_clock():
+        torch.cuda.synchronize(dev)
+        ns, cyc, n = clock_rec[0].item(), clock_rec[1].item(), clock_rec[2].item()
+        clock_rec.zero_()
+        torch.cuda.synchronize(dev)
+        return {"sm_mhz": cyc * 1e3 / ns if ns > 0 else None, "launches": n,
+                "how": "clock64 cycles over globaltimer time inside every GEMM launch (its first CTA, from the "
+                       "dependency wait to exit)"}
+
     cap = torch.cuda.Stream(dev)
     cap_h = ctypes.c_void_p(cap.cuda_stream)
 
@@ -520,6 +537,7 @@ def main():
         graph.replay()
         torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
+    kernel_clock()                                     # drop what warm-up and capture recorded
     # SM-clock probes (tgemm_debug_sm_clock: clock64 cycles over globaltimer
     # time on one SM) just before and just after the timed region, outside
     # its events, on the same stream.
@@ -563,19 +581,18 @@ def main():
     # draws 1.4 kW in it), so inside a region that short they show the state
     # before it: they are reported, but no per-clock efficiency is derived
     # from them.  The steady-state window below is long enough.
+    in_kernel = kernel_clock()
     mhz0, mhz1 = probe_mhz(0), probe_mhz(1)
     clocks["sm_mhz_probe"] = {"before": mhz0, "after": mhz1,
                               "how": "clock64 cycles over 20 us of globaltimer on one SM, just before and just "
                                      "after the timed region"}
+    clocks["sm_mhz_in_kernels"] = in_kernel
     if (t_host1 - t_host0) < 0.25:
         clocks["note"] = ("timed region shorter than NVML's update interval: its NVML samples show the clock "
-                          "before the region; the probes bracket it, and steady_state holds clocks under load")
-        mean_probe = (mhz0 + mhz1) / 2 if mhz0 and mhz1 else None
-        clocks["per_clock_efficiency"] = per_clock_efficiency(value, sms, flop_clk, mean_probe)
-        clocks["per_clock_basis"] = "mean of the two probes"
-    else:
-        clocks["per_clock_efficiency"] = per_clock_efficiency(value, sms, flop_clk, clocks.get("sm_mhz"))
-        clocks["per_clock_basis"] = "NVML median inside the region"
+                          "before the region; sm_mhz_in_kernels is the clock the GEMM launches themselves "
+                          "measured, and steady_state holds a second of clocks under load")
+    clocks["per_clock_efficiency"] = per_clock_efficiency(value, sms, flop_clk, in_kernel["sm_mhz"])
+    clocks["per_clock_basis"] = "sm_mhz_in_kernels"
 
     # Per-launch distribution: K more launches (graph mode: blocks of up to
     # 10 replayed launches), each bracketed by its own pair of events.
@@ -600,6 +617,7 @@ def main():
             e1.record(stream)
         torch.cuda.synchronize(dev)
         per = [e0.elapsed_time(e1) for e0, e1 in evs]
+    kernel_clock()
     kstats = launch_stats(per) or {}
     kernel_ms = {"mean": avg_launch, "median": kstats.get("median"), "best": kstats.get("best"),
                  "distribution": "%d %s, an event pair around each" % (
@@ -635,10 +653,13 @@ def main():
         # skip the first quarter: the clock falls from burst to its power-limited level
         ss_clk = sampler.window(t0 + 0.25 * (t1 - t0), t1)
         ss_clk["sm_mhz_probe_after"] = probe_mhz(2)
+        ss_clk["sm_mhz_in_kernels"] = kernel_clock()
         steady = {"steps": n_ss, "seconds": (t1 - t0), "ms_per_step": ss_ms, "value": ss_val, "unit": "TFLOPS",
                   "clocks": ss_clk,
-                  "per_clock_efficiency": per_clock_efficiency(ss_val, sms, flop_clk, ss_clk.get("sm_mhz"))}
+                  "per_clock_efficiency": per_clock_efficiency(ss_val, sms, flop_clk,
+                                                               ss_clk["sm_mhz_in_kernels"]["sm_mhz"])}
     sampler.stop()
+    tgemm.tgemm_debug_clock_record(None)
     rc = tgemm.tgemm_check(sh)
     if rc != 0:
         raise RuntimeError("distribution/steady-state launches failed: " + tgemm.status_string(rc))

@@ -36,6 +36,7 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     uint32_t *status = nullptr;     // device status word, lazily allocated
     std::map<const void *, int> pairs;   // resident CTA pairs per pair-kernel variant
+    std::atomic<uint64_t *> clock_rec{nullptr};   // tgemm_debug_clock_record's buffer, or null
 };
 
 std::mutex g_mu;
@@ -813,6 +814,7 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     p.group_m = 1;
     p.idesc = make_idesc(in_dtype == TGEMM_BF16, false, kSkinnyRows, npad, w_mn);
     p.status = dev->status;
+    p.clock_rec = dev->clock_rec.load(std::memory_order_relaxed);
     p.timeout_ns = wait_timeout_ns();
     p.c_ptr = C;
     p.ldc = ldc;
@@ -999,6 +1001,7 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     // kind::f16: type codes 0 F16 / 1 BF16; kind::f8f6f4: 0 E4M3 / 1 E5M2
     p.idesc = make_idesc(mma_type(in_dtype), b_mn, cfg.bm, cfg.bn);
     p.status = dev->status;
+    p.clock_rec = dev->clock_rec.load(std::memory_order_relaxed);
     p.timeout_ns = wait_timeout_ns();
     st = epilogue_params(ep, M, N, out_dtype, &p, bt);
     if (st != TGEMM_OK) return st;
@@ -1227,7 +1230,11 @@ TGEMM_EXPORT void tgemm_shutdown(void)
             cudaSetDevice(d);
             cudaFree(g_dev[d].status);
         }
-        g_dev[d] = DeviceState();
+        g_dev[d].ready = false;
+        g_dev[d].sm_count = g_dev[d].cc_major = g_dev[d].cc_minor = 0;
+        g_dev[d].status = nullptr;
+        g_dev[d].pairs.clear();
+        g_dev[d].clock_rec.store(nullptr);
     }
     if (cur >= 0) cudaSetDevice(cur);
     cudaGetLastError();
@@ -1320,5 +1327,15 @@ TGEMM_EXPORT tgemm_status tgemm_debug_sm_clock(uint64_t *out, uint32_t duration_
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
     }
+    return TGEMM_OK;
+}
+
+TGEMM_EXPORT tgemm_status tgemm_debug_clock_record(uint64_t *rec)
+{
+    if (((uintptr_t)rec % 8) != 0) return TGEMM_ERR_MISALIGNED;
+    DeviceState *dev = nullptr;
+    tgemm_status st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    dev->clock_rec.store(rec, std::memory_order_relaxed);
     return TGEMM_OK;
 }

@@ -131,6 +131,34 @@ struct SmemPlan {
     static constexpr uint32_t alloc_bytes = bytes + 1024;        // slack to align the base to 1024
 };
 
+// SM-clock record for benchmarks (tgemm_debug_clock_record): CTA 0's
+// thread 0 notes %globaltimer and %clock64 once its dependency wait returns
+// and, as the CTA leaves, adds the elapsed nanoseconds and SM cycles (and one
+// launch) to rec[0..2].  Launches on a stream never overlap between those
+// two points (the next launch's wait returns only once this one is
+// complete), so the sums give the average SM clock over the launches that
+// ran while the record was set.  One uniform branch when it is not set.
+__device__ __forceinline__ void clock_record_begin(const GemmParams &p)
+{
+    if (p.clock_rec != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        p.clock_rec[4] = ptx::globaltimer_ns();
+        p.clock_rec[5] = clock64();
+    }
+}
+
+__device__ __forceinline__ void clock_record_end(const GemmParams &p)
+{
+    if (p.clock_rec != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        const uint64_t t1 = ptx::globaltimer_ns();
+        const uint64_t c1 = clock64();
+        atomicAdd(reinterpret_cast<unsigned long long *>(&p.clock_rec[0]),
+                  (unsigned long long)(t1 - p.clock_rec[4]));
+        atomicAdd(reinterpret_cast<unsigned long long *>(&p.clock_rec[1]),
+                  (unsigned long long)(c1 - p.clock_rec[5]));
+        atomicAdd(reinterpret_cast<unsigned long long *>(&p.clock_rec[2]), 1ull);
+    }
+}
+
 template <int BN>
 struct TmemCols {
     static constexpr uint32_t value = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
@@ -461,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
     const int num_tiles = p.num_tiles;
     ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
+    clock_record_begin(p);
     ptx::launch_dependents();
 
     if (warp == 0) {
@@ -609,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
+    clock_record_end(p);
 }
 
 template <int BN, int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>

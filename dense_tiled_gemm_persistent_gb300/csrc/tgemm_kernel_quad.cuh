@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
     ptx::cluster_sync();          // all four CTAs' barriers initialised, both pairs' TMEM allocated
     ptx::tc_fence_after_sync();
     ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
+    clock_record_begin(p);
     ptx::launch_dependents();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
 
@@ -428,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
     }
+    clock_record_end(p);
 }
 
 template <int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>

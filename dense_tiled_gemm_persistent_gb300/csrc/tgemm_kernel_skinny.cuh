@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
     ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
+    clock_record_begin(p);
     ptx::launch_dependents();
 
     if (warp == 0) {
@@ -364,6 +365,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
+    clock_record_end(p);
 }
 
 template <int NPAD, int OUT, bool W_MN>

@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(base_ptr + Plan::slot_off);
     const WaitCtx wc{p.status, abort_flag, p.timeout_ns};
     ptx::grid_dependency_wait();   // inputs written and outputs read by earlier kernels are settled
+    clock_record_begin(p);
     // The next launch on the stream may start its prologue (and weight
     // prefetch) at once, or -- late_trigger -- once every CTA has issued its
     // last load (the first call in a CTA counts; the later ones in the other
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
+    clock_record_end(p);
 }
 
 template <int NPAD, int OUT, bool W_MN, int RING_KB>

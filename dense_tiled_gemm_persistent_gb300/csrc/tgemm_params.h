@@ -47,6 +47,7 @@ struct alignas(128) GemmParams {
     int32_t group_m;
     uint32_t idesc;         // tcgen05 instruction descriptor (kind::f16)
     uint32_t *status;       // device status word (first fault wins)
+    uint64_t *clock_rec;    // SM-clock record (tgemm_debug_clock_record), or null
     uint64_t timeout_ns;    // limit of every pipeline wait
     // swap-AB / split-K path only
     void *c_ptr;            // C, row-major M x ldc (written with plain stores)

@@ -24,7 +24,7 @@ EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
            "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_stream_k_plan", "tgemm_run_noalloc",
            "tgemm_run_ex", "tgemm_run_strided_batched", "tgemm_debug_noalloc_wait_timeout",
-           "tgemm_debug_sm_clock")
+           "tgemm_debug_sm_clock", "tgemm_debug_clock_record")
 
 ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH):
         lib.tgemm_debug_noalloc_wait_timeout.restype = _i
         lib.tgemm_debug_sm_clock.argtypes = [_p, ctypes.c_uint32, _p]
         lib.tgemm_debug_sm_clock.restype = _i
+        lib.tgemm_debug_clock_record.argtypes = [_p]
+        lib.tgemm_debug_clock_record.restype = _i
         lib.tgemm_debug_tile_order.argtypes = [_i64, _i64, _i, _i, _i, _p, _p, _p]
         lib.tgemm_debug_tile_order.restype = _i
         lib.tgemm_stream_k_plan.argtypes = [_i64, _i64, _i, _i, ctypes.POINTER(_i64), ctypes.POINTER(_i64),
@@ -186,6 +188,11 @@ def tgemm_debug_noalloc_wait_timeout(timeout_us: int, stream=None) -> int:
 def tgemm_debug_sm_clock(out, duration_us: int, stream=None) -> int:
     """out: device address of two uint64 (elapsed ns, SM cycles)."""
     return load().tgemm_debug_sm_clock(out, duration_us, stream)
+
+
+def tgemm_debug_clock_record(rec) -> int:
+    """rec: device address of eight uint64 (rec[0..2] zeroed), or None to stop."""
+    return load().tgemm_debug_clock_record(rec)
 
 
 def tgemm_debug_tile_order(M, N, bm, bn, group_m, rows, cols, stream=None) -> int:

@@ -289,6 +289,22 @@ tgemm_status tgemm_debug_noalloc_wait_timeout(uint32_t timeout_us, void *stream)
 tgemm_status tgemm_debug_sm_clock(uint64_t *out, uint32_t duration_us, void *stream);
 
 /*
+ * Diagnostic: record the SM clock inside the GEMM kernels of later calls on
+ * the current device.  With `rec` set (a caller-owned device array of eight
+ * uint64_t, 8-byte aligned, rec[0..2] zeroed by the caller), every GEMM
+ * kernel launched afterwards adds, from its first CTA, the nanoseconds of
+ * %globaltimer and the cycles of %clock64 between its dependency wait and its
+ * exit to rec[0] and rec[1], and 1 to rec[2] (rec[4..5] are its scratch), so
+ * rec[1] * 1000 / rec[0] is the mean SM clock in MHz over those launches.
+ * rec = NULL turns it off.  The cost is two stores and three atomics per
+ * launch.  Launches captured in a CUDA graph keep the setting they were
+ * captured with.  The pages report throughput only; this lets a benchmark set
+ * a throughput against the clock it actually ran at: a dense GEMM burst can
+ * run well below the clock read just before and just after it.
+ */
+tgemm_status tgemm_debug_clock_record(uint64_t *rec);
+
+/*
  * tgemm_run without any device allocation, for a skinny A (1..64 rows).
  *
  * The pages have no counterpart to this entry point; it exists for callers

@@ -164,6 +164,7 @@ ILLEGAL = [
     ("cta_stages_5", dict(stages=5), 256, tgemm.F16),                      # no such ring depth compiled
     ("cluster_3_tiles", dict(bm=256, stages=6, cluster_m=3), 256, tgemm.F16),
     ("pair_bn_128", dict(bm=256, bn=128, stages=6, cluster_m=2), 256, tgemm.F16),
+    ("cluster_8_tiles", dict(bm=256, stages=6, cluster_m=8), 256, tgemm.F16),   # no cluster-of-eight tile kernel
     ("workspace_stages", dict(bn=16, stages=6, group_m=1, split_k=5, swap_ab=1), 16, tgemm.F16),
     ("workspace_bn_below_m", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 32, tgemm.F16),
     ("cluster_mismatch", dict(bn=16, stages=12, cluster_m=2, group_m=1, split_k=3, swap_ab=2), 16, tgemm.F16),
@@ -340,3 +341,7 @@ def test_sm_clock_probe_checks_arguments_on_the_host(lib):
     assert tgemm.tgemm_debug_sm_clock(FAKE, 0) == tgemm.ERR_INVALID_ARG
     assert tgemm.tgemm_debug_sm_clock(FAKE, 100001) == tgemm.ERR_INVALID_ARG
     assert tgemm.tgemm_debug_sm_clock(FAKE + 4, 20) == tgemm.ERR_MISALIGNED
+
+
+def test_clock_record_checks_alignment_on_the_host(lib):
+    assert tgemm.tgemm_debug_clock_record(FAKE + 4) == tgemm.ERR_MISALIGNED

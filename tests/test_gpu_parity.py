@@ -208,11 +208,13 @@ def test_misaligned_rows_pick_the_quad_kernel():
     assert rc == 0 and (c.cluster_m, c.bm, c.bn, c.split_k) == (4, 256, 256, 0)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert c.grid == 4 * (sms // 4)          # stream-K tail: every quad
-    # FP8 rows of 5008 bytes (16-byte aligned, not 128) are misaligned too; 5120-byte rows are not
-    rc, c = tgemm.tgemm_query_config(4000, 3000, 5008, gen.B_NK, gen.E4M3, gen.BF16)
+    # FP8 rows of 1040 bytes (16-byte aligned, not 128) are misaligned too; 1024-byte rows are not.  At
+    # 1024 x 8192 x 1024 the FP8 rows of the measured table pick the CTA pair; only misaligned rows turn
+    # it into a quad.
+    rc, c = tgemm.tgemm_query_config(1024, 8192, 1040, gen.B_NK, gen.E4M3, gen.BF16)
     assert rc == 0 and c.cluster_m == 4
-    rc, c = tgemm.tgemm_query_config(4000, 3000, 5120, gen.B_NK, gen.E4M3, gen.BF16)
-    assert rc == 0 and c.cluster_m != 4
+    rc, c = tgemm.tgemm_query_config(1024, 8192, 1024, gen.B_NK, gen.E4M3, gen.BF16)
+    assert rc == 0 and c.cluster_m == 2
 
 
 def test_query_config_grid_is_the_launch_grid_for_quads():
@@ -580,3 +582,25 @@ def test_sm_clock_probe_reads_a_plausible_clock():
     assert ns >= 50_000
     mhz = cyc * 1e3 / ns
     assert 300 <= mhz <= 2070 * 1.05, mhz
+
+
+def test_clock_record_counts_launches_and_reads_a_plausible_clock():
+    """tgemm_debug_clock_record: every GEMM kernel launched while it is set
+    adds its elapsed time and SM cycles; none after it is cleared."""
+    rec = torch.zeros(8, dtype=torch.int64, device="cuda:0")
+    assert tgemm.tgemm_debug_clock_record(rec.data_ptr()) == 0
+    try:
+        M, N, K = 512, 512, 512
+        a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.ints(-2, 2), seed=3)
+        for name, kw in SHAPE_CFGS:
+            check_full(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32, exact=True, config=cfg(**kw), what=name)
+        a16, b16 = operands(16, 4096, 4096, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=4)
+        run_gpu(a16, b16, 16, 4096, 4096, gen.B_NK, gen.BF16, gen.BF16)    # a skinny kernel
+    finally:
+        assert tgemm.tgemm_debug_clock_record(None) == 0
+    ns, cyc, n = rec[:3].tolist()
+    assert n == len(SHAPE_CFGS) + 1
+    mhz = cyc * 1e3 / ns
+    assert 300 <= mhz <= 2070 * 1.05, mhz
+    run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32)
+    assert rec[2].item() == n
