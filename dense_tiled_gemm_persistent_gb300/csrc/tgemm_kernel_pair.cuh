@@ -45,22 +45,34 @@ struct PairWork {
     int tile;          // tile number in grouped order
     int k0, k1;        // k-blocks [k0, k1)
     bool partial;      // a stream-K segment: the tile is shared with other pairs
+    bool reverse;      // run the k-blocks from k1 - 1 down to k0 (odd waves of whole tiles)
     int64_t t_sk;      // tail tile index (partial segments)
     int64_t slot;      // workspace slot (partial segments)
 };
+
+// The k-block of step j (0 .. k1 - k0 - 1) of a work item.  Whole tiles of
+// odd waves run their K loop backwards: every wave of a persistent grid reads
+// the same band of A rows k-block by k-block, and a band larger than what L2
+// keeps is evicted in the order it was read, so a wave that starts where the
+// previous one ended finds that end still in L2 instead of re-reading the
+// whole band from HBM.  The sum's order changes with the direction, which
+// stays fixed per configuration and shape.
+__device__ __forceinline__ int work_kb(const PairWork &w, int j) { return w.reverse ? w.k1 - 1 - j : w.k0 + j; }
 
 // The items of pair `cid` of `P`: first the segments of its stream-K share
 // of the tail tiles, then whole tiles cid, cid + P, ... below dp_tiles.
 // Doing the shared tiles first lets their partial-sum hand-off and final
 // additions run in the epilogue warps while the whole tiles' MMAs proceed.
 struct PairWorkIter {
-    int next_dp, dp_tiles, P, kb;
+    int next_dp, dp_tiles, P, kb, waves;
     StreamK sk;
     int64_t unit, it, end;
+    bool alternate;
 
     __device__ PairWorkIter(const GemmParams &p, int cid, int num_pairs)
-        : next_dp(cid), dp_tiles(p.dp_tiles), P(num_pairs), kb(p.num_kb),
-          sk{p.sk_tiles, p.sk_units > 0 ? p.sk_units : 1, p.num_kb}, unit(cid), it(0), end(0)
+        : next_dp(cid), dp_tiles(p.dp_tiles), P(num_pairs), kb(p.num_kb), waves(0),
+          sk{p.sk_tiles, p.sk_units > 0 ? p.sk_units : 1, p.num_kb}, unit(cid), it(0), end(0),
+          alternate(p.k_alternate != 0)
     {
         if (p.sk_units > 0 && cid < p.sk_units) {
             it = sk.bound(cid);
@@ -78,6 +90,7 @@ struct PairWorkIter {
             w.k0 = (int)(it - t * kb);
             w.k1 = (int)(stop - t * kb);
             w.partial = !(w.k0 == 0 && w.k1 == kb);
+            w.reverse = false;
             w.t_sk = t;
             w.slot = sk.slot(unit, t);
             it = stop;
@@ -88,6 +101,8 @@ struct PairWorkIter {
             w.k0 = 0;
             w.k1 = kb;
             w.partial = false;
+            w.reverse = alternate && (waves & 1);
+            ++waves;
             next_dp += P;
             return true;
         }
@@ -182,14 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank;
                 const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
                 const int32_t za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-                for (int kb = w.k0; kb < w.k1; ++kb) {
+                for (int j = 0; j < w.k1 - w.k0; ++j) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = ptx::map_to_cta(full_bar(s), 0);   // the leader's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);
-                    const int32_t k0 = kb * KBlock<KIND>::elems;
+                    const int32_t k0 = work_kb(w, j) * KBlock<KIND>::elems;
                     ptx::tma_load_3d_pair(sA + s * Plan::a_stage, &p.tma_a, fb, k0, m0, za);
                     if (B_MN) {
 #pragma unroll
@@ -244,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     // both): the lone issuing thread's per-k-block overhead would
                     // otherwise idle the tensor pipe.  The second stage is only
                     // tested, never waited for, so a tile's first MMAs are not
-                    // held back while the ring fills.
+                    // held back while the ring fills.  (kb counts the steps of
+                    // the item; the producer decides which k-block each is.)
                     if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
                         ok = false;
                         break;

@@ -278,14 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_quad_kernel(const __grid_con
                 const int32_t m0 = (int32_t)tr * kPairBM + 128 * (int32_t)rank + 64 * (int32_t)q;
                 const int32_t n0 = (int32_t)tc * kPairBN + kHalfN * (int32_t)rank;
                 const int32_t za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-                for (int kb = w.k0; kb < w.k1; ++kb) {
+                for (int j = 0; j < w.k1 - w.k0; ++j) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, wc, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = ptx::map_to_cta(full_bar(s), pair_leader);
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);
-                    const int32_t k0 = kb * KBlock<KIND>::elems;
+                    const int32_t k0 = work_kb(w, j) * KBlock<KIND>::elems;
                     ptx::tma_load_3d_pair_mc(sA + s * Plan::a_stage + q * kAHalfBytes, &p.tma_a, fb, k0, m0, za,
                                              a_mask);
                     if (B_MN) {

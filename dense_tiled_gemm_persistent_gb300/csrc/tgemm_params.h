@@ -55,6 +55,7 @@ struct alignas(128) GemmParams {
     float *partials;        // [splits][tiles_n][128 rows][npad] FP32 partial sums
     uint32_t *counters;     // [tiles_n] arrival counters, zero between calls
     int32_t splits;         // K is cut into `splits` runs of whole k-blocks
+    int32_t k_alternate;    // pair/quad kernels: odd waves of whole tiles run their K loop backwards
     int32_t prefetch_kb;    // k-blocks of its weight slice a CTA prefetches into L2 before the dependency wait
     int32_t late_trigger;   // 1: let the next launch start once this CTA has issued its last load (else at once)
     // stream-K tail of the CTA-pair kernel (sk_units = 0: whole tiles only)
