@@ -201,7 +201,10 @@ void fill_config(tgemm_config *cfg, int cluster, int bn, int64_t tiles, int unit
     cfg->grid = (int)ctas;
 }
 
-int skinny_npad(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+// Rows of A a swap-AB kernel pads to (its MMA's N); 128 only in the
+// in-cluster kernel (65 to 128 rows).
+int skinny_npad(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
+constexpr int64_t kMaxSwapRows = 128;
 
 // Splits of the K loop for the swap-AB path: about two CTAs per SM stream
 // the weights, every split keeps at least one k-block.
@@ -266,9 +269,8 @@ bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, int
         cfg->swap_ab = r.c.swap_ab;
         cfg->grid = 0;
         if (cfg->swap_ab) {
-            if (M > 64) return false;
-            const int npad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-            if (npad != cfg->bn) return false;          // grid point of another padding class
+            if (M > kMaxSwapRows) return false;
+            if (skinny_npad(M) != cfg->bn) return false;   // grid point of another padding class
         } else if (M <= 64) {
             return false;
         }
@@ -290,12 +292,18 @@ int cluster_splits_limit_of(int stages)
 int cluster_splits_limit(int npad, int stages = 0)
 {
     return npad == 16 ? cluster_splits_limit_of<16>(stages)
-                      : npad == 32 ? cluster_splits_limit_of<32>(stages) : cluster_splits_limit_of<64>(stages);
+           : npad == 32 ? cluster_splits_limit_of<32>(stages)
+           : npad == 64 ? cluster_splits_limit_of<64>(stages) : ClusterSplitPlan<128>::max_splits;
 }
-int cluster_stages(int npad) { return npad == 16 ? ClusterSplitPlan<16>::stages
-                                    : npad == 32 ? ClusterSplitPlan<32>::stages : ClusterSplitPlan<64>::stages; }
+int cluster_stages(int npad)
+{
+    return npad == 16 ? ClusterSplitPlan<16>::stages
+           : npad == 32 ? ClusterSplitPlan<32>::stages
+           : npad == 64 ? ClusterSplitPlan<64>::stages : ClusterSplitPlan<128>::stages;
+}
 
-void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch = 1);
+void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch = 1,
+                         bool allow_swap = true);
 
 // CTAs of a quad launch (four per quad): one quad per 256 x 512 block with
 // whole blocks, every quad with a stream-K tail; resident limits apply later.
@@ -331,9 +339,36 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, in
     choose_config_model(M, N, K, sm_count, cfg);
 }
 
-void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch)
+void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch,
+                         bool allow_swap)
 {
-    if (M <= 64) {
+    if (allow_swap && M > 64 && M <= kMaxSwapRows && 2 * ceil_div(N, kSkinnyRows) <= sm_count) {
+        // 65-128 rows: the in-cluster kernel padded to 128 (one 128 x 128 x
+        // 16 MMA per 16 of K) where the weight's column tiles leave room for
+        // at least two splits each; the ring holds three 64 KiB partials, so
+        // at most four splits.  Measured on one GB300 (BF16, graph-replayed):
+        // 128 x 4096 x 4096 20.1 -> 14.6 us against 128 x 128 tiles,
+        // 128 x 4096 x 14336 51.4 -> 30.4 us against pair + stream-K, 128 x
+        // 1024 x 4096 19.7 -> 12.1 us; with one split (128 x 14336 x 4096,
+        // 112 column tiles) it was 11 % slower than the tiles.
+        const int64_t tiles = ceil_div(N, kSkinnyRows);
+        const int64_t kb = ceil_div(K, kBK);
+        int64_t cs = sm_count / tiles;
+        if (cs > ClusterSplitPlan<128>::max_splits) cs = ClusterSplitPlan<128>::max_splits;
+        if (cs > kb) cs = kb;
+        if (cs < 1) cs = 1;
+        cfg->bm = kSkinnyRows;
+        cfg->bn = 128;
+        cfg->bk = kBK;
+        cfg->stages = ClusterSplitPlan<128>::stages;
+        cfg->cluster_m = (int)cs;
+        cfg->group_m = 1;
+        cfg->split_k = (int)cs;
+        cfg->swap_ab = 2;
+        cfg->grid = (int)(tiles * cs);
+        return;
+    }
+    if (allow_swap && M <= 64) {
         const int npad = skinny_npad(M);
         const int64_t tiles = ceil_div(N, kSkinnyRows);
         const int64_t kb = ceil_div(K, kBK);
@@ -784,7 +819,7 @@ void log_call(const char *entry, int64_t batch, int64_t M, int64_t N, int64_t K,
                  epilogue ? 1 : 0, forced ? "caller" : "library", what, tgemm_status_string(st));
 }
 
-// C^T = B^T A^T on a swap-AB split-K kernel (M <= 64): the workspace
+// C^T = B^T A^T on a swap-AB split-K kernel (M <= 64, or M <= 128 in-cluster): the workspace
 // reduction (swap_ab = 1) or the in-cluster one (swap_ab = 2).
 tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
                         int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype, void *stream_ptr,
@@ -945,11 +980,11 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         if (bt.count > 1) {
             // The table was measured on single problems and the skinny kernels
             // are not batched: the wave model over the tiles of all batches.
-            choose_config_model(M > 64 ? M : 65, N, K, dev->sm_count, &cfg, bt.count);
+            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false);
         }
         if (tile_only(in_dtype) && cfg.swap_ab) {
             // the skinny kernels take 16-bit operands: the tile kernels for FP8 and TF32
-            choose_config_model(65, N, K, dev->sm_count, &cfg, bt.count);
+            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false);
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
         prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, dev->sm_count, bt.count > 1);
@@ -1148,7 +1183,8 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     if (st != TGEMM_OK) return st;
     choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, pick_class(in_dtype), dev->sm_count,
                   out_cfg);
-    if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(65, N, K, dev->sm_count, out_cfg);
+    if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(M > 0 ? M : 1, N, K, dev->sm_count, out_cfg, 1,
+                                                                      false);
     // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
     prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
     return TGEMM_OK;

@@ -3,7 +3,8 @@
 // (0 = B stored N x K, K-major; 1 = B stored K x N, MN-major); the pair
 // entries run 256 x 256 tiles on CTA pairs; the skinny entries are the
 // swap-AB split-K kernels for at most 64 rows of A (global-workspace and
-// in-cluster reductions), by padded row count; the quad entries run two pairs
+// in-cluster reductions) and the in-cluster one for 65-128 rows, by padded
+// row count; the quad entries run two pairs
 // that share A (clusters of four); the last eight take FP8 and FP32-as-TF32
 // operands (B stored N x K).
 #include "tgemm_kernel_quad.cuh"
@@ -31,6 +32,8 @@ const KernelVariant kVariantsF16[] = {
     TGEMM_CLUSTER_SPLIT_VARIANT(32, OUT_F16, 1),
     TGEMM_CLUSTER_SPLIT_VARIANT(64, OUT_F16, 0),
     TGEMM_CLUSTER_SPLIT_VARIANT(64, OUT_F16, 1),
+    TGEMM_CLUSTER_SPLIT_VARIANT_RING(128, OUT_F16, 0, 216),
+    TGEMM_CLUSTER_SPLIT_VARIANT_RING(128, OUT_F16, 1, 216),
     TGEMM_QUAD_VARIANT(6, OUT_F16, 0),
     TGEMM_QUAD_VARIANT(6, OUT_F16, 1),
     TGEMM_VARIANT_KIND(256, 4, OUT_F16, KIND_F8),

@@ -42,7 +42,7 @@ INC_PATH = os.path.join(HERE, "csrc", "tgemm_picker_table.inc")
 BIG_M = [8, 9, 10, 11, 12, 13, 14]          # 256 .. 16384
 BIG_N = [8, 9, 10, 11, 12, 13, 14]
 BIG_K = [10, 12, 13]                        # 1024, 4096, 8192
-SKINNY_M = [0, 3, 4, 5, 6]                  # 1, 8, 16, 32, 64
+SKINNY_M = [0, 3, 4, 5, 6, 7]               # 1, 8, 16, 32, 64, 128
 SKINNY_N = [10, 12, 14]                     # 1024, 4096, 16384
 SKINNY_K = [10, 12, 13]
 
@@ -75,6 +75,11 @@ def candidates(tg, M, N=0, dclass=0):
         for s in (4, 8, 16):
             out.append(("workspace%d" % s, C(bm=128, bn=npad, bk=64, stages=4, cluster_m=1, group_m=1,
                                              split_k=s, swap_ab=1, grid=0)))
+    elif M <= 128 and dclass == 0:
+        # 65-128 rows: the in-cluster kernel padded to 128 (full ring only, up to 4 splits)
+        for s in (1, 2, 3, 4):
+            out.append(("cluster%d" % s, C(bm=128, bn=128, bk=64, stages=6, cluster_m=s, group_m=1, split_k=s,
+                                           swap_ab=2, grid=0)))
     out.append(("pair256", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=1, swap_ab=0, grid=0)))
     out.append(("pair256sk", C(bm=256, bn=256, bk=64, stages=6, cluster_m=2, group_m=8, split_k=0, swap_ab=0,
                                grid=0)))

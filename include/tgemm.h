@@ -69,10 +69,11 @@ typedef enum {
  * pipeline stage; stages is the shared-memory ring depth; group_m is the
  * GROUP_SIZE_M of the grouped rasterisation ("Performance optimisation:
  * Swizzle" of the cuTile matrix multiplication tutorial); swap_ab != 0
- * computes C^T = B^T A^T so a short M (<= 64, padded to bn) becomes the MMA's
- * N, with the K loop split over split_k CTAs whose partial sums are added
- * through a global FP32 workspace (swap_ab = 1) or inside a thread-block
- * cluster of split_k CTAs (swap_ab = 2, cluster_m = split_k); grid is the
+ * computes C^T = B^T A^T so a short M (padded to bn) becomes the MMA's N,
+ * with the K loop split over split_k CTAs whose partial sums are added
+ * through a global FP32 workspace (swap_ab = 1: M <= 64, bn 16/32/64) or
+ * inside a thread-block cluster of split_k CTAs (swap_ab = 2, cluster_m =
+ * split_k: M <= 128, bn 16/32/64/128, at most 4 splits for 128); grid is the
  * number of CTAs launched (0 = the library's choice).  Tile kernels:
  * cluster_m = 1 (bm 128, bn 128 or 256), 2 (a CTA pair, 256 x 256) or 4
  * (two CTA pairs on neighbouring 256 x 256 tiles sharing their A rows); for

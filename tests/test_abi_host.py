@@ -153,6 +153,7 @@ LEGAL = [
     ("skinny_cluster_half_ring", dict(bn=16, stages=6, cluster_m=8, group_m=1, split_k=8, swap_ab=2), 16,
      tgemm.F16),
     ("skinny_cluster_64", dict(bn=64, stages=9, cluster_m=7, group_m=1, split_k=7, swap_ab=2), 64, tgemm.BF16),
+    ("skinny_cluster_128", dict(bn=128, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2), 100, tgemm.BF16),
 ]
 
 ILLEGAL = [
@@ -170,6 +171,10 @@ ILLEGAL = [
     ("cluster_mismatch", dict(bn=16, stages=12, cluster_m=2, group_m=1, split_k=3, swap_ab=2), 16, tgemm.F16),
     ("cluster_9_splits", dict(bn=16, stages=12, cluster_m=9, group_m=1, split_k=9, swap_ab=2), 16, tgemm.F16),
     ("half_ring_64_x5", dict(bn=64, stages=4, cluster_m=5, group_m=1, split_k=5, swap_ab=2), 64, tgemm.F16),
+    ("cluster_128_x5", dict(bn=128, stages=6, cluster_m=5, group_m=1, split_k=5, swap_ab=2), 100, tgemm.F16),
+    ("cluster_128_half_ring", dict(bn=128, stages=3, cluster_m=2, group_m=1, split_k=2, swap_ab=2), 100, tgemm.F16),
+    ("workspace_128", dict(bn=128, group_m=1, split_k=5, swap_ab=1), 100, tgemm.F16),
+    ("cluster_129_rows", dict(bn=128, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2), 129, tgemm.F16),
     ("swap_3", dict(bn=16, group_m=1, split_k=5, swap_ab=3), 16, tgemm.F16),
     ("fp8_swap", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 16, tgemm.E4M3),   # skinny kernels: 16-bit only
     ("fp8_cta_split", dict(split_k=2), 256, tgemm.E4M3),

@@ -312,8 +312,8 @@ def test_skinny_forced_splits_integers_exact(layout, splits):
                    what="splits=%d npad=%d" % (splits, npad))
 
 
-CLUSTER_STAGES = {16: 12, 32: 10, 64: 9}
-CLUSTER_MAX_SPLITS = {16: 8, 32: 8, 64: 7}
+CLUSTER_STAGES = {16: 12, 32: 10, 64: 9, 128: 6}
+CLUSTER_MAX_SPLITS = {16: 8, 32: 8, 64: 7, 128: 4}
 # the half-size ring: two CTAs per SM
 HALF_STAGES = {16: 6, 32: 5, 64: 4}
 HALF_MAX_SPLITS = {16: 8, 32: 7, 64: 4}
@@ -325,11 +325,11 @@ def cluster_cfg(npad, splits, half=False):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
-@pytest.mark.parametrize("npad", [16, 32, 64])
+@pytest.mark.parametrize("npad", [16, 32, 64, 128])
 def test_cluster_split_k_integers_exact(layout, npad):
     """Split-K reduced through distributed shared memory inside a cluster, for
-    every cluster size the leader can receive."""
-    M, N, K = min(npad, 40), 700, 1600
+    every cluster size the leader can receive (128 rows: up to 4)."""
+    M, N, K = (100 if npad == 128 else min(npad, 40)), 700, 1600
     a, b = operands(M, N, K, gen.BF16, layout, gen.ints(-2, 2), seed=41 + npad)
     for splits in range(1, CLUSTER_MAX_SPLITS[npad] + 1):
         check_full(a, b, M, N, K, layout, gen.BF16, gen.F32, exact=True, config=cluster_cfg(npad, splits),
@@ -604,3 +604,53 @@ def test_clock_record_counts_launches_and_reads_a_plausible_clock():
     assert 300 <= mhz <= 2070 * 1.05, mhz
     run_gpu(a, b, M, N, K, gen.B_NK, gen.F16, gen.F32)
     assert rec[2].item() == n
+
+
+@pytest.mark.parametrize("M", [65, 100, 128])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nk", "kn"])
+def test_swap_ab_128_rows(M, layout):
+    """65-128 rows of A on the in-cluster kernel padded to 128 (MMA N = 128):
+    the library's own pick on a weight whose column tiles alone do not fill
+    the GPU, random values against the oracle, both output widths."""
+    N, K = 4096, 2048
+    rc, c = tgemm.tgemm_query_config(M, N, K, layout, gen.BF16, gen.BF16)
+    assert rc == 0 and c.swap_ab == 2 and c.bn == 128 and 1 <= c.split_k <= 4
+    a, b = operands(M, N, K, gen.BF16, layout, gen.normal(0, 1), seed=M + 3, dist_b=gen.normal(0, 0.02))
+    for out in (gen.F32, gen.BF16):
+        check_full(a, b, M, N, K, layout, gen.BF16, out, what="swap-AB 128 rows M=%d" % M)
+
+
+def test_swap_ab_128_rows_with_epilogue_and_ragged_n():
+    """The fused epilogue (alpha, bias, GELU) on the 128-row kernel, with a
+    ragged last column tile."""
+    M, N, K = 96, 1000, 1024
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.normal(0, 1), seed=9, dist_b=gen.normal(0, 0.05))
+    A, B = a.to("cuda:0"), b.to("cuda:0")
+    ldc = 1000
+    Cd = torch.full((M, ldc), float("nan"), dtype=torch.float32, device="cuda:0")
+    bias = torch.randn(N).to("cuda:0")
+    ep = tgemm.Epilogue(alpha=0.5, beta=0.0, c_in=None, ldc_in=ldc, bias=bias.data_ptr(), bias_dtype=gen.F32,
+                        act=tgemm.ACT_GELU_TANH)
+    for splits in (1, 2, 4):
+        rc = tgemm.tgemm_run_ex(M, N, K, A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1], gen.B_NK, Cd.data_ptr(),
+                                ldc, gen.F16, gen.F32, None, ep, cluster_cfg(128, splits))
+        assert rc == 0, tgemm.status_string(rc)
+        assert tgemm.tgemm_check() == 0
+        acc, bound = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.F16)
+        bias64 = bias.double().cpu().numpy()
+        ref = oracle.epilogue(acc, 0.5, 0.0, None, bias64, oracle.ACT_GELU_TANH)
+        mag = np.abs(0.5 * acc) + np.abs(bias64)[None, :]
+        tol = 1.13 * (0.5 * 1e-3 * bound + 2.0 ** -20 * mag) + oracle.ulp(ref, gen.F32)
+        got = Cd.double().cpu().numpy()
+        assert np.all(np.abs(got - ref) <= tol), "splits=%d" % splits
+
+
+def test_swap_ab_128_rows_rejects_five_splits_and_the_workspace_kernel():
+    x = torch.empty(1 << 16, dtype=torch.bfloat16, device="cuda:0")
+    p = x.data_ptr()
+    rc = tgemm.tgemm_run_config(100, 256, 1024, p, 1024, p, 1024, gen.B_NK, p, 256, gen.BF16, gen.BF16, None,
+                                cluster_cfg(128, 5))
+    assert rc == tgemm.ERR_UNSUPPORTED
+    rc = tgemm.tgemm_run_config(100, 256, 1024, p, 1024, p, 1024, gen.B_NK, p, 256, gen.BF16, gen.BF16, None,
+                                skinny_cfg(128, 4))
+    assert rc == tgemm.ERR_UNSUPPORTED

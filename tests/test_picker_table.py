@@ -40,12 +40,14 @@ def test_every_row_is_a_legal_configuration():
             assert e["swap_ab"] == 0 and e["layout"] == 1 and e["em"] > 6
         if e["swap_ab"]:
             M = 1 << e["em"]
-            assert M <= 64 and e["bn"] >= M and e["bm"] == 128
+            assert M <= 128 and e["bn"] >= M and e["bm"] == 128
+            if M > 64:
+                assert e["swap_ab"] == 2 and e["stages"] == 6 and e["split_k"] <= 4
             if e["swap_ab"] == 2:
                 # the full ring (one CTA per SM) or the half ring (two per SM)
                 assert e["cluster_m"] == e["split_k"]
-                assert e["stages"] in ({16: 12, 32: 10, 64: 9}[e["bn"]], {16: 6, 32: 5, 64: 4}[e["bn"]])
-                if e["stages"] == {16: 6, 32: 5, 64: 4}[e["bn"]]:
+                assert e["stages"] in ({16: 12, 32: 10, 64: 9, 128: 6}[e["bn"]], {16: 6, 32: 5, 64: 4, 128: 3}[e["bn"]])
+                if e["bn"] < 128 and e["stages"] == {16: 6, 32: 5, 64: 4}[e["bn"]]:
                     assert e["split_k"] <= {16: 8, 32: 7, 64: 4}[e["bn"]]
         else:
             assert (e["cluster_m"], e["bm"]) in ((1, 128), (2, 256), (4, 256))   # 4: two pairs sharing A
