@@ -405,8 +405,20 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         cfg->grid = (int)(tiles * s);
         return;
     }
-    struct Cand { int cluster, bn; double per_tile; };
-    const Cand cands[] = {{2, 256, 0.85 * 256}, {1, 256, 256}, {1, 128, 1.25 * 128}};
+    // Time of one tile on its SM(s), in cycles: the mainloop (8 cycles per
+    // element of K for a 128 x 256 half-tile at full MMA rate, the pair's
+    // at 0.85 of that per SM, 128 x 128 tiles at 1.25x per column) or a
+    // floor for draining the accumulator and storing the tile (3000 cycles
+    // for 128 x 256, half for 128 x 128), whichever is longer: the two
+    // overlap through the double TMEM accumulator.  Short K (many small
+    // batched problems) hits the floor, where finer tiles fill the waves
+    // better.  The floor puts the crossover where batches of 512 x 512
+    // products measured it on a GB300: 128 x 128 tiles ahead at K = 128
+    // (12.5 against 14.0 us for 64 of them), CTA pairs ahead at K = 512
+    // (20.9 against 23.7 us).
+    struct Cand { int cluster, bn; double main_per_k, epi; };
+    // (on a tie the one-CTA tiles: more CTAs in flight for the same waves)
+    const Cand cands[] = {{1, 256, 8, 3000}, {1, 128, 1.25 * 4, 1500}, {2, 256, 0.85 * 8, 3000}};
     double best = 0;
     const Cand *pick = nullptr;
     int64_t pick_tiles = 0;
@@ -415,7 +427,8 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         const int bm = c.cluster == 2 ? kPairBM : kBM;
         const TileGrid g(M, N, bm, c.bn);
         const int units = c.cluster == 2 ? sm_count / 2 : sm_count;
-        const double cost = (double)ceil_div(g.count() * batch, units) * c.per_tile;
+        const double per_tile = std::max(c.main_per_k * (double)K, c.epi);
+        const double cost = (double)ceil_div(g.count() * batch, units) * per_tile;
         if (!pick || cost < best) {
             pick = &c;
             best = cost;

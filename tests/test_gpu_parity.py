@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
 
 LAYOUTS = [gen.B_NK, gen.B_KN]
 LNAME = {gen.B_NK: "nk", gen.B_KN: "kn"}
+DEV_ = "cuda:0"
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -654,3 +655,46 @@ def test_swap_ab_128_rows_rejects_five_splits_and_the_workspace_kernel():
     rc = tgemm.tgemm_run_config(100, 256, 1024, p, 1024, p, 1024, gen.B_NK, p, 256, gen.BF16, gen.BF16, None,
                                 skinny_cfg(128, 4))
     assert rc == tgemm.ERR_UNSUPPORTED
+
+
+# ---- maximum sizes ----------------------------------------------------------------
+
+@pytest.mark.parametrize("name,kw", SHAPE_CFGS + [("default", None)], ids=[n for n, _ in SHAPE_CFGS] + ["default"])
+def test_long_k_integers_exact(name, kw):
+    """K = 2^17: 2048 k-blocks, so the stage ring and its barrier phases wrap
+    hundreds of times inside one tile; small integers keep every partial sum
+    exact in FP32, so the result is bit-exact."""
+    M, N, K = 256, 256, 1 << 17
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.ints(-2, 2), seed=101)
+    check_full(a, b, M, N, K, gen.B_NK, gen.BF16, gen.F32, exact=True, config=None if kw is None else cfg(**kw),
+               what="K=2^17 %s" % name)
+
+
+def test_output_beyond_2_31_elements():
+    """C of 65536 x 65536 FP16 elements (8 GiB, 2^32 elements): offsets past
+    2^31 elements in every addressing path of the chosen kernel; sampled
+    elements (the last row and column included) against the oracle."""
+    M = N = 65536
+    K = 64
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.ints(-2, 2), seed=103)
+    A, B = a.to(DEV_), b.to(DEV_)
+    C = torch.empty((M, N), dtype=torch.float16, device=DEV_)
+    rc = tgemm.tgemm_run(M, N, K, A.data_ptr(), K, B.data_ptr(), K, gen.B_NK, C.data_ptr(), N, gen.F16, gen.F16, None)
+    assert rc == 0 and tgemm.tgemm_check() == 0
+    rng = np.random.default_rng(7)
+    ii = np.concatenate([rng.integers(0, M, 8192), np.full(N, M - 1), np.arange(M), [M - 1, 0, M - 1]])
+    jj = np.concatenate([rng.integers(0, N, 8192), np.arange(N), np.full(M, N - 1), [0, N - 1, N - 1]])
+    got = C[torch.from_numpy(ii).to(DEV_), torch.from_numpy(jj).to(DEV_)].cpu()
+    del C
+    ref, _ = oracle.gemm_elements(a, b, M, N, K, K, K, gen.B_NK, gen.F16, ii, jj)
+    want = oracle.round_bits(ref, gen.F16)
+    assert np.array_equal(bits(got, gen.F16), want)
+
+
+def test_skinny_widest_n():
+    """16 rows against a 524288 x 256 weight (4096 column tiles), on the
+    library's pick and on the workspace kernel; full comparison."""
+    M, N, K = 16, 1 << 19, 256
+    a, b = operands(M, N, K, gen.BF16, gen.B_NK, gen.normal(0, 1), seed=107, dist_b=gen.normal(0, 0.02))
+    for conf in (None, skinny_cfg(16, 2)):
+        check_full(a, b, M, N, K, gen.B_NK, gen.BF16, gen.BF16, config=conf, what="16 x 2^19 x 256")
