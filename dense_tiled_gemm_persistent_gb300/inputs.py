@@ -128,8 +128,9 @@ class Workload:
         return self.M * self.K * e_in + self.K * self.N * e_in + self.M * self.N * e_out
 
 
-# The five problem families the benchmark configuration lists, by shape, and
-# the FP8 and FP32 (multiplied as TF32) forms of the square one.
+# The five problem families the benchmark configuration lists, by shape, the
+# FP8 and FP32 (multiplied as TF32) forms of the square one, and two more
+# shapes (below).
 WORKLOADS = {
     w.name: w for w in [
         Workload("gemm_256x256x256_f16_kn_f32", 256, 256, 256, F16, F32, B_KN,
@@ -150,6 +151,13 @@ WORKLOADS = {
                  normal(0, 1), normal(0, 1), 5),
         Workload("gemm_8192x8192x8192_tf32_nk_f32", 8192, 8192, 8192, F32, F32, B_NK,
                  uniform(-0.5, 0.5), uniform(-0.5, 0.5), 6),
+        # a 128-token projection (the 65-128-row swap-AB kernel) and a short-K
+        # product (16 k-blocks per tile): shapes outside the benchmark
+        # configuration, named so that the benchmark can time and profile them
+        Workload("proj_128x4096x4096_bf16_nk_bf16", 128, 4096, 4096, BF16, BF16, B_NK,
+                 normal(0, 1), normal(0, 0.02), 7),
+        Workload("gemm_8192x4864x1024_f16_nk_f16", 8192, 4864, 1024, F16, F16, B_NK,
+                 uniform(-0.5, 0.5), uniform(-0.5, 0.5), 8),
     ]
 }
 

@@ -103,6 +103,8 @@ def test_arithmetic_intensity_classes():
             assert math.isclose(ai, 64.0)          # launch-latency bound, reported only
         elif name == "proj_16x4096x4096_bf16_nk_bf16":
             assert 15 < ai < 16 and ai < ridge
+        elif name == "proj_128x4096x4096_bf16_nk_bf16":
+            assert 110 < ai < 125 and ai < ridge       # 128 tokens: still below the ridge
         else:
             assert ai > ridge, name
 
