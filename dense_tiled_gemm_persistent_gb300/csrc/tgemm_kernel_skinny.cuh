@@ -35,7 +35,7 @@ struct SkinnyPlan {
     static constexpr uint32_t w_off = 0;
     static constexpr uint32_t x_off = w_off + kSkinnyStages * w_stage;
     static constexpr uint32_t bar_off = x_off + kSkinnyStages * x_stage;
-    static constexpr uint32_t n_bars = 2 * kSkinnyStages + 2;     // full, empty, tmem_full, drain
+    static constexpr uint32_t n_bars = 2 * kSkinnyStages + 3;     // full, empty, tmem_full, drain x 2
     static constexpr uint32_t slot_off = bar_off + 8 * n_bars;
     static constexpr uint32_t abort_off = slot_off + 4;
     static constexpr uint32_t last_off = abort_off + 4;
@@ -59,6 +59,113 @@ struct SkinnyPlan {
 // k-blocks +1.0 %, 8 +1.6 %, whole slices +2.4 % against 4); started once
 // the running launch has issued its last loads, the whole slice.
 constexpr int kSkinnyPrefetchKb = 4;
+
+// MMA issue of the swap-AB kernels.  With 128 weight rows x NPAD tokens per
+// instruction the tensor pipe finishes an MMA in about 40 SM cycles, and a
+// single issuing thread cannot keep up: measured on a GB300, one thread
+// spends about 45 cycles per tcgen05.mma with operands that are constant
+// offsets, about 64 when they come from a runtime stage index, and per
+// k-block another ~140 waiting on an already completed full barrier and ~45
+// committing to the empty one -- 450 to 550 cycles per 16 KiB k-block in
+// all, which bounded the kernel (a run with the loads taken out was as slow
+// as the whole kernel).  So two threads issue: warp 1 and warp 2 (lane 0),
+// the ring stages of even and odd index, each waiting for and committing
+// only its own stages (a stage is always served by the same thread, so its
+// full barrier's phases are waited on in order), the ring loop unrolled so
+// that stage offsets are constants.  Two issuers measured 57 cycles per MMA
+// against 93 for one with the same waits and commits.
+constexpr int kSkinnyIssuers = 2;
+
+// Each issuer adds into its own accumulators (NPAD TMEM columns apart): two
+// for NPAD <= 32 (k-step j into accumulator j mod 2), one for 64 and 128.
+// The epilogue adds them in a fixed order (0, 1, ...), so results do not
+// depend on timing.  Column budgets (64, 128, 128, 256 for NPAD 16, 32, 64,
+// 128) keep four CTAs per SM (two at NPAD 128) within 512 TMEM columns.
+template <int NPAD>
+struct SkinnyAcc {
+    static constexpr int per_issuer = NPAD <= 32 ? 2 : 1;
+    static constexpr int count = kSkinnyIssuers * per_issuer;
+    static constexpr uint32_t tmem_cols = count * NPAD < 32 ? 32u : (uint32_t)(count * NPAD);
+    static_assert((kBK / kUmmaK) % per_issuer == 0, "every k-block writes each of its issuer's accumulators");
+};
+
+// The MMA role of issuer `me` (0 or 1) over k-blocks kb0..kb1: full
+// barriers at bar + 8 s, empty ones at bar + 8 (S + s) for ring stage s; W
+// and X stages W_STAGE and X_STAGE bytes apart from sW and sX.  Ends with a
+// commit to tfull_bar (initialised for kSkinnyIssuers arrivals), or -- when
+// a wait ran out -- to the issuer's own drain barrier, waited on before
+// returning so that no MMA of this thread is still reading the ring.
+// Returns whether every wait completed.
+template <int NPAD, bool W_MN, int S, uint32_t W_STAGE, uint32_t X_STAGE>
+__device__ __forceinline__ bool skinny_mma_role(int me, uint32_t sW, uint32_t sX, uint32_t bar, uint32_t tfull_bar,
+                                                uint32_t drain_bar, int kb0, int kb1, uint32_t tmem_base,
+                                                uint32_t idesc, const WaitCtx &wc)
+{
+    constexpr int P = SkinnyAcc<NPAD>::per_issuer;
+    static_assert(S >= 2, "both issuers own a stage");
+    const uint32_t d0 = tmem_base + (uint32_t)(me * P * NPAD);
+    bool ok = true, fresh = true;
+    uint32_t ph = 0;
+    for (int kr = kb0; ok && kr < kb1; kr += S, ph ^= 1u) {   // one pass over the ring
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            if (kr + s >= kb1) break;
+            if ((s & 1) != me) continue;
+            if (!wait_bounded(bar + 8u * s, ph, wc, SITE_MMA_FULL)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            const uint32_t w_addr = sW + s * W_STAGE;
+            const uint32_t x_addr = sX + s * X_STAGE;
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+                const uint64_t ad = W_MN ? desc_at(kDescMNMajor, w_addr + k * (kUmmaK * 128))
+                                         : desc_at(kDescKMajor, w_addr + k * (kUmmaK * 2));
+                const uint64_t bd = desc_at(kDescKMajor, x_addr + k * (kUmmaK * 2));
+                // the issuer's first k-block overwrites each of its accumulators
+                ptx::mma_f16_ss(d0 + (uint32_t)((k % P) * NPAD), ad, bd, idesc, (fresh && k < P) ? 0u : 1u);
+            }
+            ptx::mma_commit(bar + 8u * (S + s));
+            fresh = false;
+        }
+    }
+    if (ok) {
+        ptx::mma_commit(tfull_bar);
+    } else {
+        ptx::mma_commit(drain_bar);
+        wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
+    }
+    return ok;
+}
+
+// This warp's 32 TMEM lanes (taddr carries the lane offset) of the summed
+// accumulators into v[0..NPAD).  A K range of one k-block (ring stage 0
+// only) leaves the second issuer's accumulators unwritten: only the first
+// issuer's are read then.
+template <int NPAD>
+__device__ __forceinline__ void load_skinny_acc(uint32_t taddr, int kblocks, float (&v)[NPAD])
+{
+    constexpr int A = SkinnyAcc<NPAD>::count;
+    constexpr int P = SkinnyAcc<NPAD>::per_issuer;
+    const bool second = kblocks >= 2;
+#pragma unroll
+    for (int c = 0; c < NPAD / 16; ++c) {
+        uint32_t r[A][16];
+#pragma unroll
+        for (int a = 0; a < A; ++a)
+            if (a < P || second) ptx::tmem_ld_32x32b_x16(taddr + a * NPAD + 16 * c, r[a]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float t = __uint_as_float(r[0][j]);
+#pragma unroll
+            for (int a = 1; a < A; ++a)
+                if (a < P || second) t += __uint_as_float(r[a][j]);
+            v[16 * c + j] = t;
+        }
+    }
+}
 
 template <bool W_MN>
 __device__ __forceinline__ void prefetch_weights_l2(const CUtensorMap *tma_b, int32_t n0, int kb0, int kb1,
@@ -152,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
     using Plan = SkinnyPlan<NPAD>;
     constexpr int S = kSkinnyStages;
     constexpr uint32_t kStageBytes = Plan::w_stage + Plan::x_stage;
-    constexpr uint32_t kTmemCols = NPAD < 32 ? 32 : NPAD;
+    constexpr uint32_t kTmemCols = SkinnyAcc<NPAD>::tmem_cols;
     static_assert(NPAD == 16 || NPAD == 32 || NPAD == 64, "NPAD must be 16, 32 or 64");
 
     extern __shared__ uint8_t smem_raw[];
@@ -165,7 +272,8 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
     auto full_bar = [&](int s) { return bar + 8u * s; };
     auto empty_bar = [&](int s) { return bar + 8u * (S + s); };
     const uint32_t tfull_bar = bar + 8u * (2 * S);
-    const uint32_t drain_bar = bar + 8u * (2 * S + 1);
+    const uint32_t drain_bar = bar + 8u * (2 * S + 1);    // first MMA issuer
+    const uint32_t drain2_bar = bar + 8u * (2 * S + 2);   // second MMA issuer
     const uint32_t slot = base + Plan::slot_off;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
     volatile int *last_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::last_off);
@@ -184,8 +292,9 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        ptx::mbar_init(tfull_bar, 1);
+        ptx::mbar_init(tfull_bar, kSkinnyIssuers);
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(drain2_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         *epi_fail = 0;
@@ -245,42 +354,19 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after_sync();
-                const uint32_t w_addr = sW + s * Plan::w_stage;
-                const uint32_t x_addr = sX + s * Plan::x_stage;
-#pragma unroll
-                for (int k = 0; k < kBK / kUmmaK; ++k) {
-                    const uint64_t ad = W_MN ? desc_at(kDescMNMajor, w_addr + k * (kUmmaK * 128))
-                                             : desc_at(kDescKMajor, w_addr + k * (kUmmaK * 2));
-                    const uint64_t bd = desc_at(kDescKMajor, x_addr + k * (kUmmaK * 2));
-                    ptx::mma_f16_ss(tmem_base, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                }
-                ptx::mma_commit(empty_bar(s));
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-            if (ok) {
-                ptx::mma_commit(tfull_bar);
-            } else {
-                ptx::mma_commit(drain_bar);
-                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
-            }
-        }
+        // ---------------------------------------------------- MMA, first issuer
+        if (lane == 0)
+            skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(0, sW, sX, bar, tfull_bar, drain_bar, kb0,
+                                                                         kb1, tmem_base, p.idesc, wc);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        if (warp == 2) {   // the second MMA issuer first
+            if (lane == 0)
+                skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(1, sW, sX, bar, tfull_bar, drain2_bar,
+                                                                             kb0, kb1, tmem_base, p.idesc, wc);
+            __syncwarp();
+        }
         const int q = warp & 3;                   // TMEM lanes 32q..32q+31 = weight rows
         const int nl = 32 * q + lane;             // row inside the 128-row tile
         const int64_t n = (int64_t)n0 + nl;
@@ -291,14 +377,7 @@ __global__ void __launch_bounds__(kThreads) gemm_skinny_kernel(const __grid_cons
         if (!*epi_fail) {
             ptx::tc_fence_after_sync();
             float v[NPAD];
-#pragma unroll
-            for (int c = 0; c < NPAD / 16; ++c) {
-                uint32_t r[16];
-                ptx::tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * q) << 16) + 16 * c, r);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[16 * c + j] = __uint_as_float(r[j]);
-            }
+            load_skinny_acc<NPAD>(tmem_base + ((uint32_t)(32 * q) << 16), kb1 - kb0, v);
             if (p.splits == 1) {
                 if (n < p.N) store_column<OUT, NPAD>(p, M, n, v);
             } else {

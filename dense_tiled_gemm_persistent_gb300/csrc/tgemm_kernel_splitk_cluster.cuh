@@ -49,13 +49,13 @@ struct ClusterSplitPlan {
     static constexpr uint32_t w_stage = kSkinnyRows * kBK * 2;
     static constexpr uint32_t x_stage = NPAD * kBK * 2;
     static constexpr uint32_t stage_bytes = w_stage + x_stage;
-    // 216 KiB: 12, 11, 9 stages for NPAD 16, 32, 64; 108 KiB: 6, 5, 4
+    // 216 KiB: 12, 10, 9 stages for NPAD 16, 32, 64 (6 for 128); 108 KiB: 6, 5, 4
     static constexpr int stages = (int)((RING_KB * 1024u) / stage_bytes);
     static constexpr int ctas_per_sm = RING_KB <= 108 ? 2 : 1;
     static constexpr uint32_t w_off = 0;
     static constexpr uint32_t x_off = w_off + stages * w_stage;
     static constexpr uint32_t bar_off = x_off + stages * x_stage;
-    static constexpr uint32_t n_bars = 2 * stages + 4;   // full, empty, tmem_full, drain, ring free, partials
+    static constexpr uint32_t n_bars = 2 * stages + 5;   // full, empty, tmem_full, drain, ring free, partials, drain 2
     static constexpr uint32_t slot_off = bar_off + 8 * n_bars;
     static constexpr uint32_t abort_off = slot_off + 4;
     static constexpr uint32_t bytes = abort_off + 4;
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
 {
     using Plan = ClusterSplitPlan<NPAD, RING_KB>;
     constexpr int S = Plan::stages;
-    constexpr uint32_t kTmemCols = NPAD < 32 ? 32 : NPAD;
+    constexpr uint32_t kTmemCols = SkinnyAcc<NPAD>::tmem_cols;
     static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
     static_assert(Plan::ctas_per_sm == 1 || Plan::alloc_bytes <= 232448 / 2 - 1024,
                   "two CTAs of this plan must fit one SM");
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     const uint32_t drain_bar = bar + 8u * (2 * S + 1);
     const uint32_t free_bar = bar + 8u * (2 * S + 2);   // ranks 1..S-1: the leader's ring may be filled
     const uint32_t part_bar = bar + 8u * (2 * S + 3);   // leader: the other ranks' partials have arrived
+    const uint32_t drain2_bar = bar + 8u * (2 * S + 4); // the second MMA issuer's wind-down
     const uint32_t slot = base + Plan::slot_off;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
 
@@ -107,8 +108,9 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        ptx::mbar_init(tfull_bar, 1);
+        ptx::mbar_init(tfull_bar, kSkinnyIssuers);
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(drain2_bar, 1);
         ptx::mbar_init(free_bar, 1);
         ptx::mbar_init(part_bar, 1);
         if (rank == 0 && splits > 1)
@@ -183,58 +185,27 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         __syncwarp();
         if (p.late_trigger) ptx::launch_dependents();
     } else if (warp == 1) {
-        // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bounded(full_bar(s), ph, wc, SITE_MMA_FULL)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after_sync();
-                const uint32_t w_addr = sW + s * Plan::w_stage;
-                const uint32_t x_addr = sX + s * Plan::x_stage;
-#pragma unroll
-                for (int k = 0; k < kBK / kUmmaK; ++k) {
-                    const uint64_t ad = W_MN ? desc_at(kDescMNMajor, w_addr + k * (kUmmaK * 128))
-                                             : desc_at(kDescKMajor, w_addr + k * (kUmmaK * 2));
-                    const uint64_t bd = desc_at(kDescKMajor, x_addr + k * (kUmmaK * 2));
-                    ptx::mma_f16_ss(tmem_base, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                }
-                ptx::mma_commit(empty_bar(s));
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-            if (ok) {
-                ptx::mma_commit(tfull_bar);
-                // The leader's ring is reused for the partials of the other
-                // ranks: make sure every MMA of this CTA is done reading it.
-                wait_bounded(tfull_bar, 0, wc, SITE_MMA_FULL, false);
-            } else {
-                ptx::mma_commit(drain_bar);
-                wait_bounded(drain_bar, 0, wc, SITE_DRAIN_MMA, false);
-            }
-        }
+        // ---------------------------------------------------- MMA, first issuer
+        // The leader's ring is reused for the partials of the other ranks:
+        // make sure every MMA of this CTA (both issuers) is done reading it.
+        if (lane == 0 && skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(
+                             0, sW, sX, bar, tfull_bar, drain_bar, kb0, kb1, tmem_base, p.idesc, wc))
+            wait_bounded(tfull_bar, 0, wc, SITE_MMA_FULL, false);
         __syncwarp();
         if (p.late_trigger) ptx::launch_dependents();
     } else {
         // -------------------------------------------------- epilogue: TMEM -> registers
+        if (warp == 2) {   // the second MMA issuer first
+            if (lane == 0)
+                skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(1, sW, sX, bar, tfull_bar, drain2_bar,
+                                                                             kb0, kb1, tmem_base, p.idesc, wc);
+            __syncwarp();
+        }
         const int q = warp & 3;
         const bool got = wait_bounded(tfull_bar, 0, wc, SITE_EPI_TMEM_FULL);
         if (__all_sync(0xffffffffu, got)) {
             ptx::tc_fence_after_sync();
-#pragma unroll
-            for (int c = 0; c < NPAD / 16; ++c) {
-                uint32_t r[16];
-                ptx::tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * q) << 16) + 16 * c, r);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[16 * c + j] = __uint_as_float(r[j]);
-            }
+            load_skinny_acc<NPAD>(tmem_base + ((uint32_t)(32 * q) << 16), kb1 - kb0, v);
             have = true;
         }
         if (p.late_trigger) ptx::launch_dependents();

@@ -349,6 +349,22 @@ def test_cluster_split_k_half_ring_integers_exact(layout, npad):
                    what="half ring splits=%d npad=%d" % (splits, npad))
 
 
+@pytest.mark.parametrize("npad", [16, 32, 64, 128])
+def test_cluster_split_k_one_k_block_per_cta(npad):
+    """K ranges of one k-block (ring stage 0 only: the second MMA issuer adds
+    nothing) and of one or two (a ragged K), full and half rings."""
+    M = 100 if npad == 128 else min(npad, 40)
+    for splits in (2, 4):
+        for K in (64 * splits, 64 * splits + 16):
+            a, b = operands(M, 384, K, gen.BF16, gen.B_NK, gen.ints(-2, 2), seed=59 + npad + K)
+            for half in ((False, True) if npad < 128 else (False,)):
+                if splits > (HALF_MAX_SPLITS if half else CLUSTER_MAX_SPLITS)[npad]:
+                    continue
+                check_full(a, b, M, 384, K, gen.B_NK, gen.BF16, gen.F32, exact=True,
+                           config=cluster_cfg(npad, splits, half),
+                           what="one k-block per CTA npad=%d splits=%d K=%d half=%s" % (npad, splits, K, half))
+
+
 def test_cluster_split_k_half_ring_two_ctas_per_sm():
     """More CTAs than SMs (128 tiles x 2 splits = 256), all resident two per
     SM, and a ragged last tile; sampled against the oracle."""
