@@ -280,9 +280,9 @@ bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, int
     return false;
 }
 
-// Largest split count of the in-cluster kernel: the leader's ring receives
-// the other ranks' partials (the half-size ring, named by its stage count,
-// holds fewer).
+// Largest split count of the in-cluster kernel: an owner's ring receives
+// the other ranks' partials of its quarters, bounded by S-1 whole partials
+// (the half-size ring, named by its stage count, holds fewer).
 template <int NPAD>
 int cluster_splits_limit_of(int stages)
 {

@@ -246,11 +246,16 @@ __device__ __forceinline__ void store_column(const GemmParams &p, int rows, int6
         for (int m = 0; m < NPAD; ++m)
             if (m < rows) v[m] = epi_apply<OUT>(p, m, n, v[m]);
     }
-    void *const c = p.c_ptr;
-    const int64_t ldc = p.ldc;
+    // a running row pointer: per-row offsets m * ldc held for all NPAD rows
+    // at once spilled at NPAD 128
+    constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
+    char *row = static_cast<char *>(p.c_ptr) + n * kOutBytes;
+    const int64_t pitch = p.ldc * kOutBytes;
 #pragma unroll
-    for (int m = 0; m < NPAD; ++m)
-        if (m < rows) store_out<OUT>(c, (int64_t)m * ldc + n, v[m]);
+    for (int m = 0; m < NPAD; ++m) {
+        if (m < rows) store_out<OUT>(row, 0, v[m]);
+        row += pitch;
+    }
 }
 
 template <int NPAD, int OUT, bool W_MN>

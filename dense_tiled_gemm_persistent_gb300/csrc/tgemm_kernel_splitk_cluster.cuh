@@ -1,36 +1,43 @@
 // Skinny GEMM with split-K reduced inside a thread-block cluster.
 //
 // Same swap-AB formulation as tgemm_kernel_skinny.cuh (C^T = B^T * A^T: 128
-// weight rows on the MMA's M side, the <= 64 rows of A padded to NPAD on its N
+// weight rows on the MMA's M side, the <= 128 rows of A padded to NPAD on its N
 // side), but the S CTAs that split the K loop of one 128-column tile of C
 // form one cluster and add their partial sums through distributed shared
 // memory instead of a global workspace:
 //
 //   1. every CTA runs its K range through a STAGES-deep TMA ring and reads
-//      its 128 x NPAD FP32 partial from tensor memory into registers;
-//   2. once the leader's (rank 0) MMAs are done reading its ring, its MMA
-//      thread arrives on a "ring free" mbarrier in each other rank;
-//   3. ranks 1..S-1 wait for that and send their partials into the leader's
-//      ring with st.async, each store counting its 16 bytes on the leader's
-//      "partials" mbarrier (which expects all (S-1) partials' bytes); chunk c
-//      of weight row r goes to ((rank - 1) * NPAD/4 + c) * 128 + r, so the 32
-//      lanes of a warp touch 512 consecutive bytes (no bank conflicts);
-//   4. the leader waits for the partials' bytes;
-//   5. the leader adds them to its own in rank order 0, 1, ..., S-1 (fixed,
-//      so results do not depend on timing), casts with round-to-nearest-even,
-//      stages the 128-column slice of C in its ring (row-major) and writes it
-//      with 16-byte stores along the rows of C.
+//      its 128 x NPAD FP32 partial from tensor memory into registers, one
+//      32-row quarter per epilogue warp;
+//   2. quarter q is reduced by rank q mod min(S, 4), its owner (so up to
+//      four CTAs of the cluster reduce and store at once, each receiving a
+//      quarter of what one leader would); once an owner's MMAs are done
+//      reading its ring, its MMA thread arrives on a "ring free" mbarrier in
+//      each other rank;
+//   3. the other ranks' warps q wait for that and send their quarter into
+//      the owner's ring with st.async, each store counting its 16 bytes on
+//      the owner's "partials" mbarrier (which expects the bytes of every
+//      quarter it owns from every other rank);
+//   4. the owner waits for those bytes;
+//   5. its warp q adds the partials of quarter q in rank order 0, 1, ...,
+//      S-1 (fixed, so results do not depend on timing), applies the fused
+//      epilogue, casts with round-to-nearest-even and stores from registers
+//      (32 consecutive columns of each row of C per warp).
+//
+// Measured on 16 x 4096 x 4096 (four ranks), the leader-only reduction
+// spent 0.4 us receiving 24 KiB through distributed shared memory, 0.3 us
+// summing and 0.25 us staging and storing the tile.
 //
 // No CTA waits for the whole cluster on the way: a cluster barrier's
 // release/acquire costs about a microsecond here, two of them a tenth of a
 // 32 MiB projection.  The barrier halves at start and exit only order the
 // mbarrier set-up and keep every CTA's shared memory alive while others may
 // write into it.  After a fault the ranks still send their (meaningless)
-// partials, so the leader never waits for bytes that will not come; the
+// partials, so an owner never waits for bytes that will not come; the
 // status word reports the fault.
 // No device memory besides A, B and C is touched, no atomics, no counters.
-// S is limited by the cluster size (8) and by the leader's ring holding
-// S-1 partials.
+// S is limited by the cluster size (8) and, conservatively, by a ring
+// holding S-1 whole partials.
 //
 // RING_KB is the operand ring's budget.  216 KiB keeps one CTA per SM with
 // the most weight bytes in flight; 108 KiB lets two CTAs share an SM, so the
@@ -55,15 +62,28 @@ struct ClusterSplitPlan {
     static constexpr uint32_t w_off = 0;
     static constexpr uint32_t x_off = w_off + stages * w_stage;
     static constexpr uint32_t bar_off = x_off + stages * x_stage;
-    static constexpr uint32_t n_bars = 2 * stages + 5;   // full, empty, tmem_full, drain, ring free, partials, drain 2
+    // full[S], empty[S], tmem_full, drain, partials, drain 2, ring free[4]
+    static constexpr uint32_t n_bars = 2 * stages + 8;
     static constexpr uint32_t slot_off = bar_off + 8 * n_bars;
     static constexpr uint32_t abort_off = slot_off + 4;
     static constexpr uint32_t bytes = abort_off + 4;
     static constexpr uint32_t alloc_bytes = bytes + 1024;
     static constexpr uint32_t partial_bytes = kSkinnyRows * NPAD * 4;   // one CTA's 128 x NPAD partial
-    // The leader's ring (from offset 0) receives the partials of ranks 1..S-1.
+    static constexpr uint32_t quarter_bytes = partial_bytes / 4;         // its 32 rows of one epilogue warp
+    // An owner's ring (from offset 0) receives, for each quarter it owns (at
+    // most two), the other ranks' partials of it; bounded here, more loosely,
+    // by S-1 whole partials.
     static constexpr int max_splits_by_ring = 1 + (int)((stages * stage_bytes) / partial_bytes);
     static constexpr int max_splits = max_splits_by_ring < kMaxClusterSplits ? max_splits_by_ring : kMaxClusterSplits;
+    // The slots an owner's ring holds at S splits: S per quarter it owns (at
+    // most 4 / min(S, 4), rounded up).
+    static constexpr bool slots_fit(int s)
+    {
+        return s > max_splits ||
+               (uint32_t)((4 + (s < 4 ? s : 4) - 1) / (s < 4 ? s : 4) * s) * quarter_bytes <= stages * stage_bytes;
+    }
+    static constexpr bool all_slots_fit(int s = 2) { return s > kMaxClusterSplits || (slots_fit(s) && all_slots_fit(s + 1)); }
+    static_assert(all_slots_fit(), "an owner's ring must hold the partials of its quarters");
 };
 
 template <int NPAD, int OUT, bool W_MN, int RING_KB>
@@ -88,9 +108,9 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     auto empty_bar = [&](int s) { return bar + 8u * (S + s); };
     const uint32_t tfull_bar = bar + 8u * (2 * S);
     const uint32_t drain_bar = bar + 8u * (2 * S + 1);
-    const uint32_t free_bar = bar + 8u * (2 * S + 2);   // ranks 1..S-1: the leader's ring may be filled
-    const uint32_t part_bar = bar + 8u * (2 * S + 3);   // leader: the other ranks' partials have arrived
-    const uint32_t drain2_bar = bar + 8u * (2 * S + 4); // the second MMA issuer's wind-down
+    const uint32_t part_bar = bar + 8u * (2 * S + 2);   // owners: the other ranks' partials have arrived
+    const uint32_t drain2_bar = bar + 8u * (2 * S + 3); // the second MMA issuer's wind-down
+    auto free_bar = [&](int o) { return bar + 8u * (2 * S + 4 + o); };   // owner o's ring may be filled
     const uint32_t slot = base + Plan::slot_off;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + Plan::abort_off);
 
@@ -102,6 +122,11 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     const int kb0 = (int)((int64_t)rank * p.num_kb / splits);
     const int kb1 = (int)((int64_t)(rank + 1) * p.num_kb / splits);
     const int32_t n0 = nt * kSkinnyRows;
+    // Quarter q of the tile (weight rows 32q..32q+31, epilogue warp q) is
+    // reduced and stored by rank q mod min(S, 4), its owner.
+    const int owners = splits < 4 ? splits : 4;
+    int owned = 0;                                  // quarters this rank owns
+    for (int q = 0; q < 4; ++q) owned += (q % owners == (int)rank) ? 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -111,10 +136,10 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         ptx::mbar_init(tfull_bar, kSkinnyIssuers);
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(drain2_bar, 1);
-        ptx::mbar_init(free_bar, 1);
+        for (int o = 0; o < 4; ++o) ptx::mbar_init(free_bar(o), 1);
         ptx::mbar_init(part_bar, 1);
-        if (rank == 0 && splits > 1)
-            ptx::mbar_arrive_expect_tx(part_bar, (uint32_t)(splits - 1) * Plan::partial_bytes);
+        if (owned > 0 && splits > 1)
+            ptx::mbar_arrive_expect_tx(part_bar, (uint32_t)(owned * (splits - 1)) * Plan::quarter_bytes);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -184,17 +209,33 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         }
         __syncwarp();
         if (p.late_trigger) ptx::launch_dependents();
+        ptx::cluster_wait();   // every CTA's barriers are initialised (the other roles wait before their loops)
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA, first issuer
-        // The leader's ring is reused for the partials of the other ranks:
-        // make sure every MMA of this CTA (both issuers) is done reading it.
-        if (lane == 0 && skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(
-                             0, sW, sX, bar, tfull_bar, drain_bar, kb0, kb1, tmem_base, p.idesc, wc))
-            wait_bounded(tfull_bar, 0, wc, SITE_MMA_FULL, false);
+        // Every CTA's barriers are initialised before the first remote
+        // access.  The MMA and epilogue warps take that wait now, where it
+        // overlaps the first loads, instead of after the K loop; the
+        // producer after its loop, so that its first loads go out at once.
+        ptx::cluster_wait();
+        if (lane == 0) {
+            // An owner's ring is reused for the partials of the other ranks:
+            // once every MMA of this CTA (both issuers) is done reading it
+            // (tfull, or the drain after a fault), the ranks that send to
+            // this one may fill it.  A relaxed arrive is enough: the hazard
+            // is write-after-read, the reads are done before the arrive is
+            // issued and no write is issued before a rank has seen it.
+            if (skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(0, sW, sX, bar, tfull_bar, drain_bar,
+                                                                             kb0, kb1, tmem_base, p.idesc, wc))
+                wait_bounded(tfull_bar, 0, wc, SITE_MMA_FULL, false);
+            if ((int)rank < owners)
+                for (int r = 0; r < splits; ++r)
+                    if (r != (int)rank)
+                        ptx::mbar_arrive_remote_relaxed(ptx::map_to_cta(free_bar(rank), (uint32_t)r));
+        }
         __syncwarp();
-        if (p.late_trigger) ptx::launch_dependents();
     } else {
         // -------------------------------------------------- epilogue: TMEM -> registers
+        ptx::cluster_wait();
         if (warp == 2) {   // the second MMA issuer first
             if (lane == 0)
                 skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(1, sW, sX, bar, tfull_bar, drain2_bar,
@@ -208,93 +249,83 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
             load_skinny_acc<NPAD>(tmem_base + ((uint32_t)(32 * q) << 16), kb1 - kb0, v);
             have = true;
         }
-        if (p.late_trigger) ptx::launch_dependents();
     }
 
-    ptx::cluster_wait();   // every CTA's barriers are initialised
     const bool epi = warp >= 2;
-    const int nl = 32 * (warp & 3) + lane;           // weight row inside the tile (epilogue warps)
-    constexpr uint32_t kChunkStride = kSkinnyRows * 16;   // bytes between chunk c and c + 1 of one partial
+    const int q = warp & 3;                          // quarter of the tile (epilogue warps)
+    const int owner = q % owners;
+    // Slot of quarter q's partial from rank `from` (the owner's own
+    // included) in its owner's ring: the owner's quarters in order, then the
+    // ranks in order; inside a slot, chunk c (4 floats) of row l at
+    // c * 512 + l * 16, so the 32 lanes of a warp touch 512 consecutive bytes.
+    auto slot_addr = [&](int from) {
+        const int idx = (q / owners) * splits + from;
+        return sW + (uint32_t)idx * Plan::quarter_bytes + (uint32_t)lane * 16u;
+    };
     bool received = true;
     if (splits > 1) {
-        if (rank == 0 && warp == 1 && lane == 0) {
-            // Every MMA of this CTA is complete (tfull or drain waited on
-            // above): the other ranks may fill the ring.  A relaxed arrive
-            // is enough: the hazard is write-after-read, the reads are done
-            // before the arrive is issued and no write is issued before a
-            // rank has seen it.
-            for (int r = 1; r < splits; ++r) ptx::mbar_arrive_remote_relaxed(ptx::map_to_cta(free_bar, (uint32_t)r));
-        }
-        if (epi && rank != 0) {
-            wait_bounded(free_bar, 0, wc, SITE_CLUSTER_EXCHANGE, false);
-            const uint32_t dst = ptx::map_to_cta(sW + (rank - 1) * (NPAD / 4) * kChunkStride + nl * 16, 0);
-            const uint32_t leader_bar = ptx::map_to_cta(part_bar, 0);
+        if (epi && owner != (int)rank) {
+            wait_bounded(free_bar(owner), 0, wc, SITE_CLUSTER_EXCHANGE, false);
+            const uint32_t dst = ptx::map_to_cta(slot_addr((int)rank), (uint32_t)owner);
+            const uint32_t owner_bar = ptx::map_to_cta(part_bar, (uint32_t)owner);
 #pragma unroll
             for (int c = 0; c < NPAD / 4; ++c)
-                ptx::st_async_v4(dst + c * kChunkStride, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3],
-                                 leader_bar);
+                ptx::st_async_v4(dst + c * 512u, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], owner_bar);
         }
-        if (epi && rank == 0) received = wait_bounded(part_bar, 0, wc, SITE_CLUSTER_EXCHANGE, false);
+        if (epi && owner == (int)rank) received = wait_bounded(part_bar, 0, wc, SITE_CLUSTER_EXCHANGE, false);
     }
-    // The leader's four epilogue warps decide together (a fault may be
-    // recorded by another warp while they read the flag).
-    const bool go = epi && rank == 0 && ptx::named_barrier_and(1, 4 * 32, have && received && *abort_flag == 0);
-    if (go) {
-        for (int r = 1; r < splits; ++r) {            // fixed order: rank 0 (own), 1, 2, ...
-            const uint32_t src = sW + (r - 1) * (NPAD / 4) * kChunkStride + nl * 16;
+    // Each owning warp decides for its quarter (all its lanes together).
+    const bool go = epi && owner == (int)rank && __all_sync(0xffffffffu, have && received && *abort_flag == 0);
+    if (go && splits > 1) {
+        // Rank order 0, 1, ..., S-1 (fixed, so results do not depend on
+        // timing): the owner's own partial goes to its slot first, then the
+        // slots are added in place, one rank at a time.  (Keeping the own
+        // partial in registers and reading the other slots all at once was
+        // slower at 16 columns, 0.48 against 0.32 us, and spilled at 128.)
+        const uint32_t own = slot_addr((int)rank);
+#pragma unroll
+        for (int c = 0; c < NPAD / 4; ++c)
+            ptx::st_shared_v4(own + c * 512u, __float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                              __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+        {
+            const uint32_t src = slot_addr(0);
 #pragma unroll
             for (int c = 0; c < NPAD / 4; ++c) {
-                const float4 t = ptx::ld_shared_v4(src + c * kChunkStride);
+                const float4 t = ptx::ld_shared_v4(src + c * 512u);
+                v[4 * c] = t.x;
+                v[4 * c + 1] = t.y;
+                v[4 * c + 2] = t.z;
+                v[4 * c + 3] = t.w;
+            }
+        }
+        for (int r = 1; r < splits; ++r) {
+            const uint32_t src = slot_addr(r);
+#pragma unroll
+            for (int c = 0; c < NPAD / 4; ++c) {
+                const float4 t = ptx::ld_shared_v4(src + c * 512u);
                 v[4 * c] += t.x;
                 v[4 * c + 1] += t.y;
                 v[4 * c + 2] += t.z;
                 v[4 * c + 3] += t.w;
             }
         }
-        // The partials are in registers: the ring now stages C's slice,
-        // [m][128 columns] of the output type, at its start.
-        constexpr int kOutBytes = OUT == OUT_F32 ? 4 : 2;
-        constexpr int kPerChunk = 16 / kOutBytes;               // output elements per 16-byte store
-        constexpr int kChunksPerRow = kSkinnyRows / kPerChunk;
-        const int64_t n = (int64_t)n0 + nl;
-        const int rows = p.M < NPAD ? (int)p.M : NPAD;
-        // The fused epilogue first, all in registers: stores between the
-        // parameter reads made the compiler re-read them per element (the
-        // staging loop then took 1.1 us for 16 rows, 5 us for 64).
-        if ((p.epi & 1) && n < p.N) {
-#pragma unroll
-            for (int m = 0; m < NPAD; ++m)
-                if (m < rows) v[m] = epi_apply<OUT>(p, m, n, v[m]);
-        }
-        ptx::named_barrier(1, 4 * 32);
-        const uint8_t *stg = base_ptr + Plan::w_off;
-        const uint32_t stg_row = sW + nl * kOutBytes;   // shared address of element (0, nl)
-#pragma unroll
-        for (int m = 0; m < NPAD; ++m) st_shared_out<OUT>(stg_row + m * kSkinnyRows * kOutBytes, v[m]);
-        ptx::named_barrier(1, 4 * 32);
-        char *const c_base = static_cast<char *>(p.c_ptr);
-        const int64_t ldc = p.ldc, N = p.N;
-        for (int c = nl; c < rows * kChunksPerRow; c += kSkinnyRows) {
-            const int m = c / kChunksPerRow, j = c % kChunksPerRow;
-            const int64_t col = (int64_t)n0 + j * kPerChunk;
-            const uint4 q = *reinterpret_cast<const uint4 *>(stg + (m * kSkinnyRows + j * kPerChunk) * kOutBytes);
-            // C and ldc * element size are 16-byte aligned (checked by the host)
-            char *dst = c_base + ((int64_t)m * ldc + col) * kOutBytes;
-            if (col + kPerChunk <= N) {
-                *reinterpret_cast<uint4 *>(dst) = q;
-            } else {
-                const char *qb = reinterpret_cast<const char *>(&q);
-                for (int e = 0; e < kPerChunk && col + e < N; ++e)
-                    for (int b = 0; b < kOutBytes; ++b) dst[e * kOutBytes + b] = qb[e * kOutBytes + b];
-            }
-        }
+    }
+    if (go) {
+        // The fused epilogue and the stores straight from registers: for
+        // each row of C the warp writes 32 consecutive columns.
+        const int64_t n = (int64_t)n0 + 32 * q + lane;
+        if (n < p.N) store_column<OUT, NPAD>(p, p.M < NPAD ? (int)p.M : NPAD, n, v);
     }
 
+    // The other roles' copies of the trigger, after the exchange and off
+    // its path.
+    if (p.late_trigger && warp != 0) ptx::launch_dependents();
+
     // No CTA leaves while another may still write into its shared memory:
-    // the leader arrives once every partial has landed, the others once
-    // their stores are issued; the leader's MMA thread releases its remote
-    // arrives.
-    if (rank == 0 && warp == 1) ptx::cluster_arrive_release();
+    // an owner arrives once every partial it expects has landed, the
+    // senders once their stores are issued; the MMA thread releases its
+    // remote arrives.
+    if (warp == 1) ptx::cluster_arrive_release();
     else ptx::cluster_arrive_relaxed();
     ptx::cluster_wait();
     ptx::tc_fence_before_sync();
@@ -339,7 +370,7 @@ int cluster_max_splits()
 
 // stages carries the ring depth (it tells the two ring budgets apart);
 // cluster = 3 marks these entries; max_active reports the largest split count
-// the leader's ring can receive.
+// (S-1 whole partials fit one ring).
 #define TGEMM_CLUSTER_SPLIT_VARIANT_RING(NPAD, OUT, BMN, RING)                                                  \
     {NPAD, ClusterSplitPlan<NPAD, RING>::stages, OUT, BMN, ClusterSplitPlan<NPAD, RING>::alloc_bytes,          \
      &launch_gemm_splitk_cluster<NPAD, OUT, (BMN) != 0, RING>, 3, &cluster_max_splits<NPAD, RING>}
