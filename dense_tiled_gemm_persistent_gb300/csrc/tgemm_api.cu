@@ -187,6 +187,12 @@ const KernelVariant *find_variant(int bn, int stages, int out, int b_mn, int clu
     return nullptr;
 }
 
+// CTAs of a one-CTA tile variant resident per SM (the kernels' TileResidency).
+int tile_ctas_per_sm(int bn, int stages)
+{
+    return (bn == 128 && stages <= 2) ? TileResidency<128, 2>::ctas_per_sm : 1;
+}
+
 void fill_config(tgemm_config *cfg, int cluster, int bn, int64_t tiles, int units)
 {
     cfg->bm = cluster == 2 ? kPairBM : kBM;
@@ -253,12 +259,32 @@ int round_log2(int64_t x)
 
 // The measured winner at the grid point nearest (in log2) to this shape, if
 // the table has one; its tile shape and split are kept, sizes re-derived.
+// Grid point -> table row, built once: a linear scan of the ~1500 rows cost
+// microseconds of host time per call.
+int table_row(int em, int en, int ek, int layout, int dclass)
+{
+    auto key = [](int em_, int en_, int ek_, int layout_, int dclass_) {
+        return ((((uint64_t)(uint32_t)dclass_ * 2 + (uint32_t)layout_) * 64 + (uint32_t)em_) * 64 + (uint32_t)en_) *
+                   64 + (uint32_t)ek_;
+    };
+    static const std::map<uint64_t, int> index = [&] {
+        std::map<uint64_t, int> m;
+        for (int i = 0; kPickTable[i].em >= 0; ++i) {
+            const PickRow &r = kPickTable[i];
+            m.emplace(key(r.em, r.en, r.ek, r.layout, r.dclass), i);
+        }
+        return m;
+    }();
+    if (em < 0 || em >= 64 || en < 0 || en >= 64 || ek < 0 || ek >= 64) return -1;
+    const auto it = index.find(key(em, en, ek, layout, dclass));
+    return it == index.end() ? -1 : it->second;
+}
+
 bool table_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, int sm_count, tgemm_config *cfg)
 {
-    const int em = round_log2(M), en = round_log2(N), ek = round_log2(K);
-    for (const PickRow &r : kPickTable) {
-        if (r.em < 0) break;
-        if (r.em != em || r.en != en || r.ek != ek || r.layout != b_layout || r.dclass != dclass) continue;
+    const int row = table_row(round_log2(M), round_log2(N), round_log2(K), b_layout, dclass);
+    if (row >= 0) {
+        const PickRow &r = kPickTable[row];
         cfg->bm = r.c.bm;
         cfg->bn = r.c.bn;
         cfg->bk = kBK;
@@ -303,7 +329,7 @@ int cluster_stages(int npad)
 }
 
 void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch = 1,
-                         bool allow_swap = true);
+                         bool allow_swap = true, bool two_stage = true);
 
 // CTAs of a quad launch (four per quad): one quad per 256 x 512 block with
 // whole blocks, every quad with a stream-K tail; resident limits apply later.
@@ -332,15 +358,16 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, in
             else if (cfg->cluster_m == 4)
                 cfg->grid = quad_grid(M, N, cfg->split_k, sm_count);
             else
-                cfg->grid = (int)std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(), sm_count);
+                cfg->grid = (int)std::min<int64_t>(TileGrid(M, N, cfg->bm, cfg->bn).count(),
+                                                   (int64_t)sm_count * tile_ctas_per_sm(cfg->bn, cfg->stages));
             return;
         }
     }
-    choose_config_model(M, N, K, sm_count, cfg);
+    choose_config_model(M, N, K, sm_count, cfg, 1, true, dclass == 0);
 }
 
 void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch,
-                         bool allow_swap)
+                         bool allow_swap, bool two_stage)
 {
     if (allow_swap && M > 64 && M <= kMaxSwapRows && 2 * ceil_div(N, kSkinnyRows) <= sm_count) {
         // 65-128 rows: the in-cluster kernel padded to 128 (one 128 x 128 x
@@ -416,17 +443,27 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
     // products measured it on a GB300: 128 x 128 tiles ahead at K = 128
     // (12.5 against 14.0 us for 64 of them), CTA pairs ahead at K = 512
     // (20.9 against 23.7 us).
-    struct Cand { int cluster, bn; double main_per_k, epi; };
+    //
+    // With one k-block per tile (K <= 64) the two-stage 128 x 128 ring, two
+    // CTAs per SM (each at half the SM's MMA rate), doubles the tiles in
+    // flight and the epilogue warps: measured on one GB300, 64 x 512x512x64
+    // 11.5 -> 9.6 us and 128 x 256x256x64 8.5 -> 7.3 us against the six-stage
+    // ring; at K = 128 the two were within 2 %, beyond it the six stages won
+    // (64 x 512x512x256 15.2 against 20.3 us).  16-bit operands only.
+    struct Cand { int cluster, bn; double main_per_k, epi; int stages, per_sm; };
     // (on a tie the one-CTA tiles: more CTAs in flight for the same waves)
-    const Cand cands[] = {{1, 256, 8, 3000}, {1, 128, 1.25 * 4, 1500}, {2, 256, 0.85 * 8, 3000}};
+    const Cand cands[] = {{1, 256, 8, 3000, 4, 1}, {1, 128, 1.25 * 4, 1500, 6, 1}, {2, 256, 0.85 * 8, 3000, 6, 1},
+                          {1, 128, 2 * 1.25 * 4, 1500, 2, 2}};
+    const int n_cands = (two_stage && K <= kBK) ? 4 : 3;
     double best = 0;
     const Cand *pick = nullptr;
     int64_t pick_tiles = 0;
     int pick_units = 0;
-    for (const Cand &c : cands) {
+    for (int ci = 0; ci < n_cands; ++ci) {
+        const Cand &c = cands[ci];
         const int bm = c.cluster == 2 ? kPairBM : kBM;
         const TileGrid g(M, N, bm, c.bn);
-        const int units = c.cluster == 2 ? sm_count / 2 : sm_count;
+        const int units = (c.cluster == 2 ? sm_count / 2 : sm_count) * c.per_sm;
         const double per_tile = std::max(c.main_per_k * (double)K, c.epi);
         const double cost = (double)ceil_div(g.count() * batch, units) * per_tile;
         if (!pick || cost < best) {
@@ -437,6 +474,7 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         }
     }
     fill_config(cfg, pick->cluster, pick->bn, pick_tiles, pick_units);
+    cfg->stages = pick->stages;
     // Few pair tiles over a deep K leave most pairs idle: share the K loop
     // out (stream-K) when at most half the pairs would get a tile.
     if (pick->cluster == 2 && 2 * pick_tiles <= pick_units && ceil_div(K, kBK) >= 64) {
@@ -993,11 +1031,11 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         if (bt.count > 1) {
             // The table was measured on single problems and the skinny kernels
             // are not batched: the wave model over the tiles of all batches.
-            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false);
+            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false, !tile_only(in_dtype));
         }
         if (tile_only(in_dtype) && cfg.swap_ab) {
             // the skinny kernels take 16-bit operands: the tile kernels for FP8 and TF32
-            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false);
+            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false, false);
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
         prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, dev->sm_count, bt.count > 1);
@@ -1093,7 +1131,7 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
             if (p.sk_units > 0 && p.dp_tiles == 0) g = 4 * p.sk_units;   // only the sharing quads have work
         }
     } else {
-        g = cfg.grid > 0 ? cfg.grid : dev->sm_count;
+        g = cfg.grid > 0 ? cfg.grid : dev->sm_count * tile_ctas_per_sm(cfg.bn, cfg.stages);
         if (g > p.num_tiles) g = p.num_tiles;
         if (g < 1) g = 1;
     }
@@ -1197,7 +1235,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, pick_class(in_dtype), dev->sm_count,
                   out_cfg);
     if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(M > 0 ? M : 1, N, K, dev->sm_count, out_cfg, 1,
-                                                                      false);
+                                                                      false, false);
     // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
     prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
     return TGEMM_OK;

@@ -18,6 +18,8 @@ const KernelVariant kVariantsF16[] = {
     TGEMM_VARIANT(256, 4, OUT_F16, 1),
     TGEMM_VARIANT(128, 6, OUT_F16, 0),
     TGEMM_VARIANT(128, 6, OUT_F16, 1),
+    TGEMM_VARIANT(128, 2, OUT_F16, 0),
+    TGEMM_VARIANT(128, 2, OUT_F16, 1),
     TGEMM_PAIR_VARIANT(6, OUT_F16, 0),
     TGEMM_PAIR_VARIANT(6, OUT_F16, 1),
     TGEMM_SKINNY_VARIANT(16, OUT_F16, 0),

@@ -427,8 +427,18 @@ __device__ __forceinline__ void epilogue_drain(const CUtensorMap *map, int32_t r
     }
 }
 
+// CTAs of the one-CTA tile kernel resident per SM: two for the two-stage
+// 128 x 128 ring (98 KB of shared memory and 256 TMEM columns each), one
+// otherwise.  Tiles with one or two k-blocks (K <= 128) spend most of their
+// time in the epilogue; a second CTA doubles the epilogue warps per SM.
+template <int BN, int STAGES>
+struct TileResidency {
+    static constexpr int ctas_per_sm = (BN == 128 && STAGES <= 2) ? 2 : 1;
+};
+
 template <int BN, int STAGES, int OUT, bool B_MN, int KIND = KIND_F16>
-__global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p)
+__global__ void __launch_bounds__(kThreads, TileResidency<BN, STAGES>::ctas_per_sm)
+    gemm_persistent_kernel(const __grid_constant__ GemmParams p)
 {
     static_assert(KIND == KIND_F16 || !B_MN, "FP8 and TF32 operands are K-major only");
     using Plan = SmemPlan<BN, STAGES>;
@@ -437,6 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
     static_assert(2 * BN <= 512, "two accumulator buffers must fit in tensor memory");
     static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
+    static_assert(TileResidency<BN, STAGES>::ctas_per_sm == 1 ||
+                      (Plan::alloc_bytes <= 232448 / 2 - 1024 && 2 * kTmemCols <= 512),
+                  "two CTAs of this plan must fit one SM");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -662,6 +675,8 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// max_active stays null: the one-CTA grid is sized from the SM count and
+// TileResidency (run_body).
 #define TGEMM_VARIANT(BN, ST, OUT, BMN) \
     {BN, ST, OUT, BMN, SmemPlan<BN, ST>::alloc_bytes, &launch_gemm<BN, ST, OUT, (BMN) != 0>, 1, nullptr}
 #define TGEMM_VARIANT_KIND(BN, ST, OUT, KIND) \

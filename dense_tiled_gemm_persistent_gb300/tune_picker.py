@@ -41,7 +41,7 @@ INC_PATH = os.path.join(HERE, "csrc", "tgemm_picker_table.inc")
 # grid exponents: large shapes and the skinny (M <= 64) band
 BIG_M = [8, 9, 10, 11, 12, 13, 14]          # 256 .. 16384
 BIG_N = [8, 9, 10, 11, 12, 13, 14]
-BIG_K = [10, 12, 13]                        # 1024, 4096, 8192
+BIG_K = [7, 8, 9, 10, 11, 12, 13]           # 128 .. 8192
 SKINNY_M = [0, 3, 4, 5, 6, 7]               # 1, 8, 16, 32, 64, 128
 SKINNY_N = [10, 12, 14]                     # 1024, 4096, 16384
 SKINNY_K = [10, 12, 13]
@@ -96,6 +96,10 @@ def candidates(tg, M, N=0, dclass=0):
                                     grid=0)))
     out.append(("cta256", C(bm=128, bn=256, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
     out.append(("cta128", C(bm=128, bn=128, bk=64, stages=6, cluster_m=1, group_m=8, split_k=1, swap_ab=0, grid=0)))
+    if dclass == 0:
+        # two-stage ring, two CTAs per SM (16-bit operands only)
+        out.append(("cta128s2", C(bm=128, bn=128, bk=64, stages=2, cluster_m=1, group_m=8, split_k=1, swap_ab=0,
+                                  grid=0)))
     return out
 
 
@@ -172,6 +176,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="a few grid points only (smoke)")
     ap.add_argument("--skinny-only", action="store_true",
                     help="re-measure the M <= 64 band only and merge it into the existing table and CSV")
+    ap.add_argument("--k-exps", default="",
+                    help="measure only these log2 K grid exponents (comma-separated); the others are kept")
     ap.add_argument("--classes", default="0,1,2",
                     help="operand classes to measure (0 FP16/BF16, 1 FP8, 2 TF32); the others are kept")
     ap.add_argument("--csv", default=CSV_PATH)
@@ -202,6 +208,9 @@ def main():
     points = [pt for pt in all_points if pt[4] in classes]
     if args.skinny_only:
         points = [pt for pt in points if pt[0] in SKINNY_M]
+    if args.k_exps:
+        kx = {int(x) for x in args.k_exps.split(",") if x}
+        points = [pt for pt in points if pt[2] in kx]
     if args.quick:
         points = points[::37]
 

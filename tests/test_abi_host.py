@@ -142,6 +142,7 @@ def _cfg(bm=128, bn=256, bk=64, stages=4, cluster_m=1, group_m=8, split_k=1, swa
 LEGAL = [
     ("cta256", dict(), 256, tgemm.F16),
     ("cta128", dict(bn=128, stages=6), 256, tgemm.F16),
+    ("cta128_2stage", dict(bn=128, stages=2), 256, tgemm.F16),
     ("pair", dict(bm=256, stages=6, cluster_m=2), 256, tgemm.F16),
     ("pair_streamk", dict(bm=256, stages=6, cluster_m=2, split_k=0), 256, tgemm.F16),
     ("quad", dict(bm=256, stages=6, cluster_m=4), 256, tgemm.F16),
@@ -163,6 +164,8 @@ ILLEGAL = [
     ("cta_split_2", dict(split_k=2), 256, tgemm.F16),
     ("cta_streamk", dict(split_k=0), 256, tgemm.F16),                      # stream-K: pair and quad only
     ("cta_stages_5", dict(stages=5), 256, tgemm.F16),                      # no such ring depth compiled
+    ("cta256_stages_2", dict(stages=2), 256, tgemm.F16),                   # two stages: 128 x 128 only
+    ("fp8_cta128_stages_2", dict(bn=128, stages=2), 256, tgemm.E4M3),      # and 16-bit operands only
     ("cluster_3_tiles", dict(bm=256, stages=6, cluster_m=3), 256, tgemm.F16),
     ("pair_bn_128", dict(bm=256, bn=128, stages=6, cluster_m=2), 256, tgemm.F16),
     ("cluster_8_tiles", dict(bm=256, stages=6, cluster_m=8), 256, tgemm.F16),   # no cluster-of-eight tile kernel

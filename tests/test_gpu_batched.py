@@ -32,6 +32,7 @@ CONFIGS = {
     "auto": None,
     "cta256": C(),
     "cta128": C(bn=128, stages=6),
+    "cta128_2stage": C(bn=128, stages=2),
     "pair": C(bm=256, stages=6, cluster_m=2),
     "pair_streamk": C(bm=256, stages=6, cluster_m=2, split_k=0),
     "quad": C(bm=256, stages=6, cluster_m=4),

@@ -48,6 +48,7 @@ def C(**kw):
 FAMILIES = {
     "cta256": (C(), 300, 520, 1500),
     "cta128": (C(bn=128, stages=6), 300, 520, 1500),
+    "cta128_2stage": (C(bn=128, stages=2), 300, 520, 1500),
     "pair": (C(bm=256, stages=6, cluster_m=2), 300, 520, 1500),
     "quad": (C(bm=256, stages=6, cluster_m=4), 300, 1100, 1500),
     # 5 x 6 pair tiles on 7 pairs: the 2 leftover tiles are shared by k-range

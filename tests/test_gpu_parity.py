@@ -39,7 +39,8 @@ def cfg(bn, stages=None, group_m=8, grid=0, pair=False, quad=False):
 
 # every compiled tile shape: 128 x 256 and 128 x 128 on one CTA, 256 x 256 on a CTA pair, and two
 # 256 x 256 pairs sharing A in a cluster of four
-SHAPE_CFGS = [("1cta_128x256", dict(bn=256)), ("1cta_128x128", dict(bn=128)), ("pair_256x256", dict(bn=256, pair=True)),
+SHAPE_CFGS = [("1cta_128x256", dict(bn=256)), ("1cta_128x128", dict(bn=128)),
+              ("1cta_128x128_2stage", dict(bn=128, stages=2)), ("pair_256x256", dict(bn=256, pair=True)),
               ("quad_256x512", dict(bn=256, quad=True))]
 
 
