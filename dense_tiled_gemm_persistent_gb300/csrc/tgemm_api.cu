@@ -89,6 +89,16 @@ bool is_f8(int dt) { return dt == TGEMM_E4M3 || dt == TGEMM_E5M2; }
 // Operands that only the tile kernels take (K-major B): FP8, and FP32 read as TF32.
 bool tile_only(int dt) { return is_f8(dt) || dt == TGEMM_F32; }
 int mma_kind(int in_dtype) { return is_f8(in_dtype) ? KIND_F8 : in_dtype == TGEMM_F32 ? KIND_TF32 : KIND_F16; }
+
+// Whether a swap-AB mode (0 none, 1 workspace, 2 in-cluster) has kernels for
+// this operand type: both for FP16/BF16, the in-cluster one for FP8, none for
+// FP32 read as TF32.
+bool swap_supported(int in_dtype, int swap_ab)
+{
+    if (swap_ab == 0) return true;
+    if (is_f8(in_dtype)) return swap_ab == 2;
+    return !tile_only(in_dtype);
+}
 // K elements in one 128-byte k-block row
 int kblock_elems(int in_dtype) { return (int)(128 / elem_size(in_dtype)); }
 // Instruction-descriptor operand type: kind::f16 0 F16 / 1 BF16, kind::f8f6f4
@@ -329,7 +339,7 @@ int cluster_stages(int npad)
 }
 
 void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch = 1,
-                         bool allow_swap = true, bool two_stage = true);
+                         bool allow_swap = true, int dclass = 0);
 
 // CTAs of a quad launch (four per quad): one quad per 256 x 512 block with
 // whole blocks, every quad with a stream-K tail; resident limits apply later.
@@ -363,12 +373,17 @@ void choose_config(int64_t M, int64_t N, int64_t K, int b_layout, int dclass, in
             return;
         }
     }
-    choose_config_model(M, N, K, sm_count, cfg, 1, true, dclass == 0);
+    choose_config_model(M, N, K, sm_count, cfg, 1, true, dclass);
 }
 
 void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_config *cfg, int64_t batch,
-                         bool allow_swap, bool two_stage)
+                         bool allow_swap, int dclass)
 {
+    // Operand classes: 0 FP16/BF16 (every kernel), 1 FP8 (the tile kernels
+    // and the in-cluster swap-AB kernel), 2 TF32 (the tile kernels).
+    if (dclass == 2) allow_swap = false;
+    const bool two_stage = dclass == 0;
+    const int64_t kbe = dclass == 1 ? KBlock<KIND_F8>::elems : kBK;   // K elements per 128-byte k-block
     if (allow_swap && M > 64 && M <= kMaxSwapRows && 2 * ceil_div(N, kSkinnyRows) <= sm_count) {
         // 65-128 rows: the in-cluster kernel padded to 128 (one 128 x 128 x
         // 16 MMA per 16 of K) where the weight's column tiles leave room for
@@ -379,7 +394,7 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         // 1024 x 4096 19.7 -> 12.1 us; with one split (128 x 14336 x 4096,
         // 112 column tiles) it was 11 % slower than the tiles.
         const int64_t tiles = ceil_div(N, kSkinnyRows);
-        const int64_t kb = ceil_div(K, kBK);
+        const int64_t kb = ceil_div(K, kbe);
         int64_t cs = sm_count / tiles;
         if (cs > ClusterSplitPlan<128>::max_splits) cs = ClusterSplitPlan<128>::max_splits;
         if (cs > kb) cs = kb;
@@ -398,7 +413,7 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
     if (allow_swap && M <= 64) {
         const int npad = skinny_npad(M);
         const int64_t tiles = ceil_div(N, kSkinnyRows);
-        const int64_t kb = ceil_div(K, kBK);
+        const int64_t kb = ceil_div(K, kbe);
         // In-cluster split-K: one CTA per SM, the splits of a tile reduce
         // through distributed shared memory.  Used unless the tiles are so few
         // that the cluster limit leaves most SMs idle.  For up to 16 rows the
@@ -416,7 +431,7 @@ void choose_config_model(int64_t M, int64_t N, int64_t K, int sm_count, tgemm_co
         cfg->bn = npad;
         cfg->bk = kBK;
         cfg->group_m = 1;
-        if (2 * tiles * cs >= sm_count || cs == kb) {
+        if (2 * tiles * cs >= sm_count || cs == kb || dclass == 1) {   // (no FP8 workspace kernel)
             cfg->stages = stages;
             cfg->cluster_m = (int)cs;
             cfg->split_k = (int)cs;
@@ -596,7 +611,17 @@ tgemm_status legal_config(const tgemm_config &c, int64_t M, int64_t K, int out_d
     if (c.bk != kBK || c.grid < 0 || c.group_m < 1) return TGEMM_ERR_UNSUPPORTED;
     if (tile_only(in_dtype)) {
         // FP8 / TF32: the tile kernels, K-major B (bk names the 128-byte k-block)
-        if (c.swap_ab != 0 || b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
+        if (b_layout != TGEMM_B_NK) return TGEMM_ERR_UNSUPPORTED;
+        if (c.swap_ab == 2 && is_f8(in_dtype)) {
+            // FP8 in-cluster swap-AB split-K (128 K elements per k-block)
+            const int64_t kb = ceil_div(K > 0 ? K : 1, (int64_t)KBlock<KIND_F8>::elems);
+            if (c.bm != kSkinnyRows || c.bn < M || c.cluster_m != c.split_k || c.split_k < 1 || c.split_k > kb)
+                return TGEMM_ERR_UNSUPPORTED;
+            *v = find_variant(c.bn, c.stages, out_dtype, 0, 3, KIND_F8);
+            if (!*v || c.split_k > (*v)->max_active()) return TGEMM_ERR_UNSUPPORTED;
+            return TGEMM_OK;
+        }
+        if (c.swap_ab != 0) return TGEMM_ERR_UNSUPPORTED;
         if (!(c.split_k == 1 || (c.split_k == 0 && (c.cluster_m == 2 || c.cluster_m == 4))))
             return TGEMM_ERR_UNSUPPORTED;
         if (!((c.cluster_m == 1 && c.bm == kBM) ||
@@ -884,11 +909,13 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     if (cfg.swap_ab == 1 && tiles_n > kMaxSkinnyTiles) splits = 1;
     GemmParams p;
     std::memset(&p, 0, sizeof p);
-    bool ok = encode_2d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kBK, (uint32_t)npad);
+    // K elements per 128-byte k-block row: 64 for FP16/BF16, 128 for FP8
+    const uint32_t kbe = (uint32_t)kblock_elems(in_dtype);
+    bool ok = encode_2d(&p.tma_a, in_dtype, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kbe, (uint32_t)npad);
     if (w_mn)
         ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, kBK);
     else
-        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kBK, kSkinnyRows);
+        ok = ok && encode_2d(&p.tma_b, in_dtype, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kbe, kSkinnyRows);
     if (!ok) return TGEMM_ERR_CUDA;
     p.M = (int32_t)M;
     p.N = (int32_t)N;
@@ -896,9 +923,9 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     p.tiles_m = 1;
     p.tiles_n = (int32_t)tiles_n;
     p.num_tiles = (int32_t)tiles_n;
-    p.num_kb = (int32_t)ceil_div(K, kBK);
+    p.num_kb = (int32_t)ceil_div(K, (int64_t)kbe);
     p.group_m = 1;
-    p.idesc = make_idesc(in_dtype == TGEMM_BF16, false, kSkinnyRows, npad, w_mn);
+    p.idesc = make_idesc(mma_type(in_dtype), false, kSkinnyRows, npad, w_mn);
     p.status = dev->status;
     p.clock_rec = dev->clock_rec.load(std::memory_order_relaxed);
     p.timeout_ns = wait_timeout_ns();
@@ -915,7 +942,7 @@ tgemm_status run_skinny(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
         // configuration per shape: 16x4096x4096 8.9 -> 8.2 us, 64x4096x4096
         // 11.5 -> 11.0, 32x4096x8192 14.9 -> 14.4, 16x14336x4096 20.8 -> 19.9;
         // 16x16384x1024 (256 CTAs of 8 k-blocks) stays early, 7.5 against 8.0.
-        const int64_t kb_per_cta = ceil_div(ceil_div(K, kBK), splits);
+        const int64_t kb_per_cta = ceil_div(ceil_div(K, (int64_t)kbe), splits);
         p.late_trigger = (kb_per_cta >= 12 || tiles_n * splits <= dev->sm_count) ? 1 : 0;
         p.prefetch_kb = p.late_trigger ? (int32_t)kb_per_cta : kSkinnyPrefetchKb;
     }
@@ -1031,11 +1058,11 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         if (bt.count > 1) {
             // The table was measured on single problems and the skinny kernels
             // are not batched: the wave model over the tiles of all batches.
-            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false, !tile_only(in_dtype));
+            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false, pick_class(in_dtype));
         }
-        if (tile_only(in_dtype) && cfg.swap_ab) {
-            // the skinny kernels take 16-bit operands: the tile kernels for FP8 and TF32
-            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false, false);
+        if (!swap_supported(in_dtype, cfg.swap_ab)) {
+            // a table entry of another operand class: the tile kernels
+            choose_config_model(M, N, K, dev->sm_count, &cfg, bt.count, false, pick_class(in_dtype));
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
         prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, dev->sm_count, bt.count > 1);
@@ -1234,8 +1261,8 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     if (st != TGEMM_OK) return st;
     choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, pick_class(in_dtype), dev->sm_count,
                   out_cfg);
-    if (tile_only(in_dtype) && out_cfg->swap_ab) choose_config_model(M > 0 ? M : 1, N, K, dev->sm_count, out_cfg, 1,
-                                                                      false, false);
+    if (!swap_supported(in_dtype, out_cfg->swap_ab))
+        choose_config_model(M > 0 ? M : 1, N, K, dev->sm_count, out_cfg, 1, false, pick_class(in_dtype));
     // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
     prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
     return TGEMM_OK;

@@ -42,6 +42,7 @@ const KernelVariant kVariantsBF16[] = {
     TGEMM_VARIANT_KIND(128, 6, OUT_BF16, KIND_F8),
     TGEMM_PAIR_VARIANT_KIND(6, OUT_BF16, KIND_F8),
     TGEMM_QUAD_VARIANT_KIND(6, OUT_BF16, KIND_F8),
+    TGEMM_CLUSTER_SPLIT_VARIANTS_F8(OUT_BF16),
     TGEMM_VARIANT_KIND(256, 4, OUT_BF16, KIND_TF32),
     TGEMM_VARIANT_KIND(128, 6, OUT_BF16, KIND_TF32),
     TGEMM_PAIR_VARIANT_KIND(6, OUT_BF16, KIND_TF32),

@@ -96,7 +96,7 @@ struct SkinnyAcc {
 // a wait ran out -- to the issuer's own drain barrier, waited on before
 // returning so that no MMA of this thread is still reading the ring.
 // Returns whether every wait completed.
-template <int NPAD, bool W_MN, int S, uint32_t W_STAGE, uint32_t X_STAGE>
+template <int NPAD, bool W_MN, int S, uint32_t W_STAGE, uint32_t X_STAGE, int KIND = KIND_F16>
 __device__ __forceinline__ bool skinny_mma_role(int me, uint32_t sW, uint32_t sX, uint32_t bar, uint32_t tfull_bar,
                                                 uint32_t drain_bar, int kb0, int kb1, uint32_t tmem_base,
                                                 uint32_t idesc, const WaitCtx &wc)
@@ -124,7 +124,9 @@ __device__ __forceinline__ bool skinny_mma_role(int me, uint32_t sW, uint32_t sX
                                          : desc_at(kDescKMajor, w_addr + k * (kUmmaK * 2));
                 const uint64_t bd = desc_at(kDescKMajor, x_addr + k * (kUmmaK * 2));
                 // the issuer's first k-block overwrites each of its accumulators
-                ptx::mma_f16_ss(d0 + (uint32_t)((k % P) * NPAD), ad, bd, idesc, (fresh && k < P) ? 0u : 1u);
+                const uint32_t acc = (fresh && k < P) ? 0u : 1u;
+                if constexpr (KIND == KIND_F8) ptx::mma_f8_ss(d0 + (uint32_t)((k % P) * NPAD), ad, bd, idesc, acc);
+                else ptx::mma_f16_ss(d0 + (uint32_t)((k % P) * NPAD), ad, bd, idesc, acc);
             }
             ptx::mma_commit(bar + 8u * (S + s));
             fresh = false;
@@ -167,13 +169,13 @@ __device__ __forceinline__ void load_skinny_acc(uint32_t taddr, int kblocks, flo
     }
 }
 
-template <bool W_MN>
+template <bool W_MN, int KE = kBK>
 __device__ __forceinline__ void prefetch_weights_l2(const CUtensorMap *tma_b, int32_t n0, int kb0, int kb1,
                                                     int depth)
 {
     const int kbe = kb1 - kb0 > depth ? kb0 + depth : kb1;
     for (int kb = kb0; kb < kbe; ++kb) {
-        const int32_t k0 = kb * kBK;
+        const int32_t k0 = kb * KE;   // KE elements per 128-byte k-block row
         if (W_MN) {
 #pragma unroll
             for (int j = 0; j < kSkinnyRows / 64; ++j) ptx::tma_prefetch_l2_2d(tma_b, n0 + 64 * j, k0);

@@ -86,12 +86,16 @@ struct ClusterSplitPlan {
     static_assert(all_slots_fit(), "an owner's ring must hold the partials of its quarters");
 };
 
-template <int NPAD, int OUT, bool W_MN, int RING_KB>
+template <int NPAD, int OUT, bool W_MN, int RING_KB, int KIND = KIND_F16>
 __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::ctas_per_sm)
     gemm_splitk_cluster_kernel(const __grid_constant__ GemmParams p)
 {
     using Plan = ClusterSplitPlan<NPAD, RING_KB>;
     constexpr int S = Plan::stages;
+    // FP16/BF16 (kind::f16, 64 elements per 128-byte k-block row) or FP8
+    // (kind::f8f6f4, 128 elements): the same bytes per stage and per MMA
+    static_assert(KIND == KIND_F16 || (KIND == KIND_F8 && !W_MN), "FP8 weights are K-major only");
+    constexpr int kKE = KBlock<KIND>::elems;
     constexpr uint32_t kTmemCols = SkinnyAcc<NPAD>::tmem_cols;
     static_assert(Plan::alloc_bytes <= 232448, "shared memory plan exceeds 227 KiB");
     static_assert(Plan::ctas_per_sm == 1 || Plan::alloc_bytes <= 232448 / 2 - 1024,
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&p.tma_a);
         ptx::prefetch_tensormap(&p.tma_b);
-        prefetch_weights_l2<W_MN>(&p.tma_b, n0, kb0, kb1, p.prefetch_kb);
+        prefetch_weights_l2<W_MN, kKE>(&p.tma_b, n0, kb0, kb1, p.prefetch_kb);
     }
     if (warp == 1) {
         ptx::tmem_alloc(slot, kTmemCols);
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
                 }
                 const uint32_t fb = full_bar(s);
                 ptx::mbar_arrive_expect_tx(fb, Plan::stage_bytes);
-                const int32_t k0 = kb * kBK;
+                const int32_t k0 = kb * kKE;
                 if (W_MN) {
 #pragma unroll
                     for (int j = 0; j < kSkinnyRows / 64; ++j)
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
             // this one may fill it.  A relaxed arrive is enough: the hazard
             // is write-after-read, the reads are done before the arrive is
             // issued and no write is issued before a rank has seen it.
-            if (skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(0, sW, sX, bar, tfull_bar, drain_bar,
+            if (skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage, KIND>(0, sW, sX, bar, tfull_bar, drain_bar,
                                                                              kb0, kb1, tmem_base, p.idesc, wc))
                 wait_bounded(tfull_bar, 0, wc, SITE_MMA_FULL, false);
             if ((int)rank < owners)
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
         ptx::cluster_wait();
         if (warp == 2) {   // the second MMA issuer first
             if (lane == 0)
-                skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage>(1, sW, sX, bar, tfull_bar, drain2_bar,
+                skinny_mma_role<NPAD, W_MN, S, Plan::w_stage, Plan::x_stage, KIND>(1, sW, sX, bar, tfull_bar, drain2_bar,
                                                                              kb0, kb1, tmem_base, p.idesc, wc);
             __syncwarp();
         }
@@ -337,10 +341,10 @@ __global__ void __launch_bounds__(kThreads, ClusterSplitPlan<NPAD, RING_KB>::cta
     clock_record_end(p);
 }
 
-template <int NPAD, int OUT, bool W_MN, int RING_KB>
+template <int NPAD, int OUT, bool W_MN, int RING_KB, int KIND = KIND_F16>
 cudaError_t launch_gemm_splitk_cluster(const GemmParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = gemm_splitk_cluster_kernel<NPAD, OUT, W_MN, RING_KB>;
+    auto kern = gemm_splitk_cluster_kernel<NPAD, OUT, W_MN, RING_KB, KIND>;
     constexpr uint32_t smem = ClusterSplitPlan<NPAD, RING_KB>::alloc_bytes;
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
@@ -376,5 +380,14 @@ int cluster_max_splits()
      &launch_gemm_splitk_cluster<NPAD, OUT, (BMN) != 0, RING>, 3, &cluster_max_splits<NPAD, RING>}
 #define TGEMM_CLUSTER_SPLIT_VARIANT(NPAD, OUT, BMN) TGEMM_CLUSTER_SPLIT_VARIANT_RING(NPAD, OUT, BMN, 216), \
                                                     TGEMM_CLUSTER_SPLIT_VARIANT_RING(NPAD, OUT, BMN, 108)
+// FP8 weights (B stored N x K) and activations, kind::f8f6f4
+#define TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(NPAD, OUT, RING)                                                    \
+    {NPAD, ClusterSplitPlan<NPAD, RING>::stages, OUT, 0, ClusterSplitPlan<NPAD, RING>::alloc_bytes,            \
+     &launch_gemm_splitk_cluster<NPAD, OUT, false, RING, KIND_F8>, 3, &cluster_max_splits<NPAD, RING>, KIND_F8}
+#define TGEMM_CLUSTER_SPLIT_VARIANTS_F8(OUT)                                                                     \
+    TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(16, OUT, 216), TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(16, OUT, 108),        \
+        TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(32, OUT, 216), TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(32, OUT, 108),    \
+        TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(64, OUT, 216), TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(64, OUT, 108),    \
+        TGEMM_CLUSTER_SPLIT_VARIANT_F8_RING(128, OUT, 216)
 
 }  // namespace tgemm

@@ -155,6 +155,9 @@ LEGAL = [
      tgemm.F16),
     ("skinny_cluster_64", dict(bn=64, stages=9, cluster_m=7, group_m=1, split_k=7, swap_ab=2), 64, tgemm.BF16),
     ("skinny_cluster_128", dict(bn=128, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2), 100, tgemm.BF16),
+    ("fp8_skinny_cluster", dict(bn=16, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2), 16, tgemm.E4M3),
+    ("fp8_skinny_cluster_128", dict(bn=128, stages=6, cluster_m=2, group_m=1, split_k=2, swap_ab=2), 100,
+     tgemm.E5M2),
 ]
 
 ILLEGAL = [
@@ -179,7 +182,10 @@ ILLEGAL = [
     ("workspace_128", dict(bn=128, group_m=1, split_k=5, swap_ab=1), 100, tgemm.F16),
     ("cluster_129_rows", dict(bn=128, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2), 129, tgemm.F16),
     ("swap_3", dict(bn=16, group_m=1, split_k=5, swap_ab=3), 16, tgemm.F16),
-    ("fp8_swap", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 16, tgemm.E4M3),   # skinny kernels: 16-bit only
+    ("fp8_swap", dict(bn=16, group_m=1, split_k=5, swap_ab=1), 16, tgemm.E4M3),   # workspace kernel: 16-bit only
+    ("tf32_swap", dict(bn=16, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2), 16, tgemm.F32),
+    ("fp8_cluster_5_splits_128", dict(bn=128, stages=6, cluster_m=5, group_m=1, split_k=5, swap_ab=2), 100,
+     tgemm.E4M3),
     ("fp8_cta_split", dict(split_k=2), 256, tgemm.E4M3),
 ]
 

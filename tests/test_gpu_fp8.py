@@ -120,8 +120,8 @@ def test_fp8_stream_k_integers_bit_exact(name, fp8):
 @pytest.mark.parametrize("M,N,K", [(1, 1, 16), (16, 4096, 4096), (64, 300, 2000), (129, 257, 4112),
                                    (1024, 1024, 16384)])
 def test_fp8_shapes(fp8, M, N, K):
-    # M <= 64 goes to the tile kernels (the swap-AB kernels take 16-bit
-    # operands); the deep-K case is the stream-K pick's home ground.
+    # M <= 128 goes to the in-cluster swap-AB kernel; the deep-K case is the
+    # stream-K pick's home ground.
     dt = FP8[fp8]
     a, b = fp8_operands(M, N, K, dt, gen.uniform(-1, 1), seed=13)
     out = run(a, b, M, N, K, dt, gen.F32)
@@ -192,11 +192,11 @@ def test_fp8_rejections():
     assert call(layout=gen.B_KN) == tgemm.ERR_UNSUPPORTED            # FP8 B must be K-major
     assert call(lda=K + 8) == tgemm.ERR_MISALIGNED                    # 72-byte rows
     skinny = C(bn=16, stages=4, group_m=1, split_k=2, swap_ab=1)
-    assert call(cfg=skinny) == tgemm.ERR_UNSUPPORTED                  # swap-AB kernels are 16-bit only
+    assert call(cfg=skinny) == tgemm.ERR_UNSUPPORTED                  # the workspace reduction is 16-bit only
     assert call(cfg=C(bn=128, stages=4)) == tgemm.ERR_UNSUPPORTED     # no such FP8 instantiation
     cfg = tgemm.Config()
     assert tgemm.load().tgemm_query_config(16, 4096, 4096, gen.B_NK, dt, gen.BF16, ctypes.byref(cfg)) == 0
-    assert cfg.swap_ab == 0 and cfg.bm in (128, 256)
+    assert cfg.swap_ab == 2 and cfg.bn == 16                          # the in-cluster swap-AB kernel
     assert tgemm.load().tgemm_query_config(16, 4096, 4096, gen.B_KN, dt, gen.BF16, ctypes.byref(cfg)) == \
         tgemm.ERR_UNSUPPORTED
     # noalloc entry: 16-bit operands only
@@ -212,3 +212,85 @@ def test_fp8_matmul_helper_defaults_to_bf16():
     assert out.dtype == torch.bfloat16
     ref, _ = oracle.gemm(a, b, 130, 72, 48, a.shape[1], b.shape[1], gen.B_NK, gen.E5M2)
     assert np.array_equal(bits(out.cpu(), gen.BF16), oracle.round_bits(ref, gen.BF16))
+
+
+# ---- few rows of A: the in-cluster swap-AB split-K kernel (kind::f8f6f4) ----
+
+CLUSTER_STAGES = {16: 12, 32: 10, 64: 9, 128: 6}
+CLUSTER_MAX_SPLITS = {16: 8, 32: 8, 64: 7, 128: 4}
+HALF_STAGES = {16: 6, 32: 5, 64: 4}
+HALF_MAX_SPLITS = {16: 8, 32: 7, 64: 4}
+
+
+def cluster_cfg(npad, splits, half=False):
+    return C(bm=128, bn=npad, stages=(HALF_STAGES if half else CLUSTER_STAGES)[npad], cluster_m=splits, group_m=1,
+             split_k=splits, swap_ab=2)
+
+
+@pytest.mark.parametrize("npad,half", [(16, False), (16, True), (32, False), (32, True), (64, False), (64, True),
+                                       (128, False)], ids=lambda v: str(v))
+@pytest.mark.parametrize("fp8", sorted(FP8))
+def test_fp8_cluster_split_k_integers_exact(npad, half, fp8):
+    """Every legal cluster size (first, second, middle, last), 8 ragged
+    128-element k-blocks, ragged N: bit-exact against the oracle."""
+    dt = FP8[fp8]
+    M, N, K = (100 if npad == 128 else min(npad, 40)), 700, 1000
+    a, b = fp8_operands(M, N, K, dt, gen.ints(-3, 3), seed=61 + npad)
+    ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, dt)
+    top = (HALF_MAX_SPLITS if half else CLUSTER_MAX_SPLITS)[npad]
+    for splits in sorted({1, 2, (top + 1) // 2, top}):
+        for out_dtype in (gen.F32, gen.BF16):
+            out = run(a, b, M, N, K, dt, out_dtype, cluster_cfg(npad, splits, half))
+            got = bits(out[:M, :N], out_dtype)
+            want = oracle.round_bits(ref, out_dtype)
+            assert np.array_equal(got, want), "splits=%d out=%d: %d bit mismatches" % (
+                splits, out_dtype, (got != want).sum())
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_fp8_cluster_split_k_one_k_block_per_cta(splits):
+    dt = gen.E4M3
+    M, N = 16, 384
+    for K in (128 * splits, 128 * splits + 48):
+        a, b = fp8_operands(M, N, K, dt, gen.ints(-3, 3), seed=67 + K)
+        out = run(a, b, M, N, K, dt, gen.F32, cluster_cfg(16, splits, True))
+        ref, _ = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, dt)
+        assert np.array_equal(bits(out[:M, :N], gen.F32), oracle.round_bits(ref, gen.F32)), "K=%d" % K
+
+
+@pytest.mark.parametrize("fp8", sorted(FP8))
+@pytest.mark.parametrize("M", [1, 7, 16, 33, 64, 100, 128])
+def test_fp8_skinny_default_pick_matches_oracle(fp8, M):
+    dt = FP8[fp8]
+    N, K = 4096, 4096
+    cfg = tgemm.Config()
+    assert tgemm.load().tgemm_query_config(M, N, K, gen.B_NK, dt, gen.BF16, ctypes.byref(cfg)) == 0
+    assert cfg.swap_ab == 2
+    a, b = fp8_operands(M, N, K, dt, gen.normal(0, 1), seed=70 + M, dist_b=gen.uniform(-1, 1))
+    for out_dtype in (gen.BF16, gen.F32):
+        out = run(a, b, M, N, K, dt, out_dtype)
+        ref, bound = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, dt)
+        assert_close(out[:M, :N].double().numpy(), ref, bound, out_dtype, "M=%d %s" % (M, fp8))
+
+
+def test_fp8_cluster_split_k_with_fused_epilogue():
+    """alpha, beta * C_in, bias and GELU applied by the owning ranks."""
+    dt = gen.E4M3
+    M, N, K = 24, 1000, 2048
+    a, b = fp8_operands(M, N, K, dt, gen.normal(0, 1), seed=73, dist_b=gen.uniform(-1, 1))
+    g = torch.Generator().manual_seed(74)
+    bias = torch.randn(N, generator=g).to(torch.bfloat16)
+    ldc = round_up(N, 8)
+    cin = torch.randn(M, ldc, generator=g).to(torch.bfloat16)
+    cin_d, bias_d = cin.to(DEV), bias.to(DEV)
+    alpha, beta, act = 0.5, -1.0, tgemm.ACT_GELU_TANH
+    ep = tgemm.Epilogue(alpha=alpha, beta=beta, c_in=cin_d.data_ptr(), ldc_in=ldc, bias=bias_d.data_ptr(),
+                        bias_dtype=gen.BF16, act=act)
+    out = run(a, b, M, N, K, dt, gen.BF16, cluster_cfg(32, 4), ep=ep)
+    acc, bound = oracle.gemm(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, dt)
+    cin64, bias64 = cin[:, :N].double().numpy(), bias.double().numpy()
+    want = oracle.epilogue(acc, alpha, beta, cin64, bias64, act)
+    mag = np.abs(alpha * acc) + np.abs(beta * cin64) + np.abs(bias64)[None, :]
+    tol = 1.13 * (abs(alpha) * 1e-3 * bound + 2.0 ** -20 * mag) + oracle.ulp(want, gen.BF16)
+    err = np.abs(out[:M, :N].double().numpy() - want)
+    assert (err <= tol).all(), "max excess %g" % float((err - tol).max())
