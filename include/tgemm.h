@@ -73,9 +73,11 @@ typedef enum {
  * with the K loop split over split_k CTAs whose partial sums are added
  * through a global FP32 workspace (swap_ab = 1: M <= 64, bn 16/32/64) or
  * inside a thread-block cluster of split_k CTAs (swap_ab = 2, cluster_m =
- * split_k: M <= 128, bn 16/32/64/128, at most 4 splits for 128); grid is the
- * number of CTAs launched (0 = the library's choice).  Tile kernels:
- * cluster_m = 1 (bm 128, bn 128 or 256), 2 (a CTA pair, 256 x 256) or 4
+ * split_k: M <= 128, bn 16/32/64/128, at most 4 splits for 128; FP16/BF16
+ * and FP8 operands, the workspace form FP16/BF16 only); grid is the number
+ * of CTAs launched (0 = the library's choice).  Tile kernels: cluster_m = 1
+ * (bm 128, bn 128 or 256; bn 128 also with stages = 2, two CTAs per SM,
+ * FP16/BF16 only), 2 (a CTA pair, 256 x 256) or 4
  * (two CTA pairs on neighbouring 256 x 256 tiles sharing their A rows); for
  * cluster_m = 2 and 4, split_k = 0 adds a stream-K tail (the last waves'
  * tiles, or the quad's 256 x 512 blocks, shared out by k-range and summed
