@@ -11,9 +11,10 @@ fastest, and writes
   * csrc/tgemm_picker_table.inc   the winner per grid point, as a C array.
 
 Operand classes: 0 = FP16/BF16 (measured FP16 in, FP16 out, both B
-layouts, the skinny band included), 1 = FP8 (E4M3 in, BF16 out) and 2 = FP32
-read as TF32 (FP32 in and out); the last two only with B stored N x K and
-more than 64 rows of A, which is all their kernels take.
+layouts, the skinny band included), 1 = FP8 (E4M3 in, BF16 out; the skinny
+band on the in-cluster kernel) and 2 = FP32 read as TF32 (FP32 in and out,
+more than 64 rows of A); the last two only with B stored N x K, which is all
+their kernels take.
 
 Launches are timed from a replayed CUDA graph.  tgemm_run rounds log2 of
 each of M, N and K to the nearest grid exponent and uses the winner of its
@@ -75,7 +76,21 @@ def candidates(tg, M, N=0, dclass=0):
         for s in (4, 8, 16):
             out.append(("workspace%d" % s, C(bm=128, bn=npad, bk=64, stages=4, cluster_m=1, group_m=1,
                                              split_k=s, swap_ab=1, grid=0)))
-    elif M <= 128 and dclass == 0:
+    elif M <= 64 and dclass == 1:
+        # FP8: the in-cluster kernel only (no FP8 workspace reduction)
+        npad = 16 if M <= 16 else (32 if M <= 32 else 64)
+        st = {16: 12, 32: 10, 64: 9}[npad]
+        mx = {16: 8, 32: 8, 64: 7}[npad]
+        st_h = {16: 6, 32: 5, 64: 4}[npad]
+        mx_h = {16: 8, 32: 7, 64: 4}[npad]
+        for s in (1, 2, 3, 4, 6, 8):
+            if s <= mx:
+                out.append(("cluster%d" % s, C(bm=128, bn=npad, bk=64, stages=st, cluster_m=s, group_m=1,
+                                             split_k=s, swap_ab=2, grid=0)))
+            if s <= mx_h:
+                out.append(("cluster%dh" % s, C(bm=128, bn=npad, bk=64, stages=st_h, cluster_m=s, group_m=1,
+                                              split_k=s, swap_ab=2, grid=0)))
+    elif M <= 128 and dclass in (0, 1):
         # 65-128 rows: the in-cluster kernel padded to 128 (full ring only, up to 4 splits)
         for s in (1, 2, 3, 4):
             out.append(("cluster%d" % s, C(bm=128, bn=128, bk=64, stages=6, cluster_m=s, group_m=1, split_k=s,
@@ -175,7 +190,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--quick", action="store_true", help="a few grid points only (smoke)")
     ap.add_argument("--skinny-only", action="store_true",
-                    help="re-measure the M <= 64 band only and merge it into the existing table and CSV")
+                    help="re-measure the M <= 128 band only and merge it into the existing table and CSV")
     ap.add_argument("--k-exps", default="",
                     help="measure only these log2 K grid exponents (comma-separated); the others are kept")
     ap.add_argument("--classes", default="0,1,2",
@@ -200,7 +215,7 @@ def main():
                 for en in BIG_N:
                     for ek in BIG_K:
                         all_points.append((em, en, ek, layout, dclass))
-            if dclass == 0:
+            if dclass in (0, 1):
                 for em in SKINNY_M:
                     for en in SKINNY_N:
                         for ek in SKINNY_K:
