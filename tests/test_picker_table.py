@@ -35,8 +35,11 @@ def test_every_row_is_a_legal_configuration():
         assert key not in seen, key
         seen.add(key)
         assert e["dclass"] in (0, 1, 2)
-        if e["dclass"] != 0:
-            # FP8 and TF32 operands: tile kernels only, B stored N x K, more than 64 rows of A
+        if e["dclass"] == 1:
+            # FP8 operands: B stored N x K; the tile kernels or the in-cluster swap-AB kernel
+            assert e["layout"] == 1 and e["swap_ab"] in (0, 2)
+        if e["dclass"] == 2:
+            # TF32 operands: tile kernels only, B stored N x K, more than 64 rows of A
             assert e["swap_ab"] == 0 and e["layout"] == 1 and e["em"] > 6
         if e["swap_ab"]:
             M = 1 << e["em"]
