@@ -151,13 +151,18 @@ WORKLOADS = {
                  normal(0, 1), normal(0, 1), 5),
         Workload("gemm_8192x8192x8192_tf32_nk_f32", 8192, 8192, 8192, F32, F32, B_NK,
                  uniform(-0.5, 0.5), uniform(-0.5, 0.5), 6),
-        # a 128-token projection (the 65-128-row swap-AB kernel) and a short-K
-        # product (16 k-blocks per tile): shapes outside the benchmark
-        # configuration, named so that the benchmark can time and profile them
+        # a 128-token projection (the 65-128-row swap-AB kernel), a short-K
+        # product (16 k-blocks per tile) and an FP8 projection: shapes outside
+        # the benchmark configuration, named so that the benchmark can time and
+        # profile them
         Workload("proj_128x4096x4096_bf16_nk_bf16", 128, 4096, 4096, BF16, BF16, B_NK,
                  normal(0, 1), normal(0, 0.02), 7),
         Workload("gemm_8192x4864x1024_f16_nk_f16", 8192, 4864, 1024, F16, F16, B_NK,
                  uniform(-0.5, 0.5), uniform(-0.5, 0.5), 8),
+        # an FP8 weight (E4M3) read by 16 tokens: the in-cluster swap-AB
+        # kernel on kind::f8f6f4, HBM-bound
+        Workload("proj_16x4096x4096_e4m3_nk_bf16", 16, 4096, 4096, E4M3, BF16, B_NK,
+                 normal(0, 1), normal(0, 0.5), 9),
     ]
 }
 

@@ -37,7 +37,8 @@ def run_default(wl, a, b):
     return C
 
 
-FULL = ["gemm_256x256x256_f16_kn_f32", "proj_16x4096x4096_bf16_nk_bf16", "proj_128x4096x4096_bf16_nk_bf16"]
+FULL = ["gemm_256x256x256_f16_kn_f32", "proj_16x4096x4096_bf16_nk_bf16", "proj_128x4096x4096_bf16_nk_bf16",
+        "proj_16x4096x4096_e4m3_nk_bf16"]
 SAMPLED = ["gemm_4000x3000x5000_bf16_nk_bf16", "gemm_4096x4096x4096_f16_kn_f16",
            "gemm_8192x8192x8192_f16_nk_f16", "proj_16384x14336x4096_bf16_nk_bf16",
            "gemm_8192x8192x8192_e4m3_nk_bf16", "gemm_8192x8192x8192_tf32_nk_f32", "gemm_8192x4864x1024_f16_nk_f16"]

@@ -105,6 +105,8 @@ def test_arithmetic_intensity_classes():
             assert 15 < ai < 16 and ai < ridge
         elif name == "proj_128x4096x4096_bf16_nk_bf16":
             assert 110 < ai < 125 and ai < ridge       # 128 tokens: still below the ridge
+        elif name == "proj_16x4096x4096_e4m3_nk_bf16":
+            assert 30 < ai < 32 and ai < ridge         # one byte per weight: twice the FLOP per byte
         else:
             assert ai > ridge, name
 
