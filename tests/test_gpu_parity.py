@@ -551,6 +551,56 @@ def test_chained_products_see_each_others_results(kinds):
     assert np.array_equal(bits(C3.cpu(), gen.F32), oracle.round_bits(r3, gen.F32))
 
 
+@pytest.mark.parametrize("graph", [False, True], ids=["stream", "graph"])
+def test_chained_skinny_products_see_each_others_results(graph):
+    """Eight 16-row projections X_{i+1} = X_i W_i^T launched back to back (the
+    in-cluster swap-AB kernel and its reduce-scatter exchange): each launch
+    may start early and must read the previous launch's owners' stores
+    complete.  Small integers keep every intermediate exact in BF16, so the
+    last product is compared bit for bit with the oracle's chain."""
+    M, N = 16, 1024
+    g = torch.Generator().manual_seed(79)
+    x0 = torch.randint(-1, 2, (M, N), generator=g).to(torch.bfloat16)
+    # weights with one +-1 per row, so every intermediate stays in {-1, 0, 1} x small
+    W = []
+    for i in range(8):
+        w = torch.zeros(N, N)
+        cols = torch.randperm(N, generator=g)[:N]
+        w[torch.arange(N), cols] = torch.randint(0, 2, (N,), generator=g).float() * 2 - 1
+        W.append(w.to(torch.bfloat16))
+    dev = "cuda:0"
+    Wd = [w.to(dev) for w in W]
+    X = [x0.to(dev)] + [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev) for _ in W]
+    s = torch.cuda.Stream()
+    sh = tgemm.ctypes.c_void_p(s.cuda_stream)
+    cfg = tgemm.Config(bm=128, bn=16, bk=64, stages=6, cluster_m=4, group_m=1, split_k=4, swap_ab=2, grid=0)
+
+    def launch_all():
+        for i, w in enumerate(Wd):
+            rc = tgemm.tgemm_run_config(M, N, N, X[i].data_ptr(), N, w.data_ptr(), N, gen.B_NK, X[i + 1].data_ptr(),
+                                        N, gen.BF16, gen.BF16, sh, cfg)
+            assert rc == tgemm.OK, tgemm.status_string(rc)
+
+    torch.cuda.synchronize()
+    if graph:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            launch_all()
+        for t in X[1:]:
+            t.fill_(float("nan"))
+        gr.replay()
+    else:
+        with torch.cuda.stream(s):
+            launch_all()
+    torch.cuda.synchronize()
+    assert tgemm.tgemm_check(sh) == tgemm.OK
+    ref = x0
+    for w in W:
+        r, _ = oracle.gemm(ref, w, M, N, N, N, N, gen.B_NK, gen.BF16)
+        ref = torch.from_numpy(oracle.round_bits(r, gen.BF16).astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+    assert np.array_equal(bits(X[-1].cpu(), gen.BF16), bits(ref, gen.BF16))
+
+
 LOG_RUN = r"""
 import sys, torch
 sys.path.insert(0, %r)
