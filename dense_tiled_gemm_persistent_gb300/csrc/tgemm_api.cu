@@ -991,6 +991,75 @@ void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, in
     cfg->grid = quad_grid(M, N, cfg->split_k, sm_count);
 }
 
+// GROUP_SIZE_M of the grouped order from the L2 footprint it implies.  A
+// band of group_m tile rows that spans several waves of resident tiles reads
+// all of B once, and its A rows again in every wave; they stay in L2 only
+// while they, the B columns of about two waves and one wave's C tiles fit in
+// what L2 keeps for them.  Fewer, taller bands read B fewer times.  Measured
+// with ncu (DRAM bytes per launch, pair kernel): 8192^3 FP16 2.87x the
+// algorithmic bytes at group 8 or 10, 2.56x at 12, 2.86x at 14 (bands 14,
+// 14, 4: the short last band reads B once more); 16384 x 14336 x 4096 BF16
+// 2.23x at 8, 1.75x at 16 and 1.97x at 24.  This footprint model with a
+// 64 MiB budget picks 16 there; for 8192^3 no band fits and the smallest
+// footprint, bands of 11, 11 and 10 rows, is taken.  The tutorial's group of 8 stays where A and B together are small
+// enough to stay in L2 (4000 x 3000 x 5000 reads about its algorithmic bytes
+// at group 8) and where a band of 8 rows holds less than two waves (there a
+// wave spans bands and B, not A, is what the next wave re-reads).
+constexpr double kL2BandBudget = 64.0 * 1024 * 1024;
+constexpr double kL2OperandsFit = 96.0 * 1024 * 1024;
+
+int l2_group_m(int64_t M, int64_t N, int64_t K, int bm, int unit_bn, int in_dtype, int out_dtype, int64_t resident)
+{
+    const int64_t tm = ceil_div(M, bm), tn = ceil_div(N, unit_bn);
+    const double e = (double)elem_size(in_dtype), eo = (double)elem_size(out_dtype);
+    const double row = (double)bm * (double)K * e, col = (double)unit_bn * (double)K * e;
+    if (resident < 1 || (double)tm * row + (double)tn * col <= kL2OperandsFit) return kDefaultGroupM;
+    if ((int64_t)kDefaultGroupM * tn < 2 * resident) return kDefaultGroupM;
+    const double c_wave = (double)resident * bm * unit_bn * eo;
+    int64_t best_gm = kDefaultGroupM, prev_gm = 0;
+    double best = 0;
+    for (int64_t nb = 1; nb <= tm; ++nb) {
+        const int64_t gm = ceil_div(tm, nb);                 // bands of near-equal height
+        if (gm == prev_gm) continue;
+        prev_gm = gm;
+        if (gm * tn < 2 * resident) break;                   // later bands are shorter still
+        const int64_t cols = std::min<int64_t>(tn, ceil_div(resident, gm));
+        const double f = (double)gm * row + 2.0 * (double)cols * col + c_wave;
+        if (f <= kL2BandBudget) return (int)gm;              // the fewest bands that fit
+        if (best == 0 || f < best) {
+            best = f;
+            best_gm = gm;
+        }
+    }
+    return (int)best_gm;
+}
+
+// The group for an automatically chosen tile configuration (single
+// problems; strided batches keep the default).  The picker table measured
+// groups of 8 and 16 for the pair kernel's whole tiles in the power-capped
+// steady state, and where 16 won it stays (also on shapes whose operands fit
+// in L2, where the model has no say); the model only makes a default group
+// of 8 taller.  On 8192^3 FP16 (pair, stream-K tail) that is 11: DRAM bytes
+// 2.77x -> 2.69x the algorithmic ones, per-clock tensor efficiency 0.959 ->
+// 0.966 in a 50-launch burst; on 8192^3 TF32 (quad) 11, within noise.
+void l2_group_config(tgemm_config *cfg, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype,
+                     int sm_count)
+{
+    if (cfg->swap_ab || cfg->group_m != kDefaultGroupM) return;
+    int64_t resident;
+    int unit_bn = cfg->bn;
+    if (cfg->cluster_m == 2) {
+        resident = sm_count / 2;
+    } else if (cfg->cluster_m == 4) {
+        resident = sm_count / 4;
+        unit_bn = 2 * cfg->bn;                                // a quad's block is two pair tiles wide
+    } else {
+        resident = (int64_t)sm_count * tile_ctas_per_sm(cfg->bn, cfg->stages);
+    }
+    const int g = l2_group_m(M, N, K, cfg->bm, unit_bn, in_dtype, out_dtype, resident);
+    if (g > cfg->group_m) cfg->group_m = g;
+}
+
 tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                       int64_t ldb, int b_layout, void *C, int64_t ldc, int in_dtype, int out_dtype,
                       void *stream_ptr, const tgemm_config *forced, const tgemm_epilogue *ep,
@@ -1066,6 +1135,7 @@ tgemm_status run_body(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         }
         if (bt.count > 1 && cfg.split_k == 0) cfg.split_k = 1;   // many batches fill the waves themselves
         prefer_quad_for_misaligned_rows(&cfg, M, N, lda, ldb, in_dtype, dev->sm_count, bt.count > 1);
+        if (bt.count == 1) l2_group_config(&cfg, M, N, K, in_dtype, out_dtype, dev->sm_count);
         cfg.grid = 0;   // sized below from the tiles of all batches
         st = legal_config(cfg, M, K, out_dtype, b_layout, &var, in_dtype);
         if (st != TGEMM_OK) return st;
@@ -1265,6 +1335,7 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
         choose_config_model(M > 0 ? M : 1, N, K, dev->sm_count, out_cfg, 1, false, pick_class(in_dtype));
     // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
     prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
+    l2_group_config(out_cfg, M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, in_dtype, out_dtype, dev->sm_count);
     return TGEMM_OK;
 }
 
@@ -1384,6 +1455,16 @@ namespace tgemm {
 cudaError_t launch_tile_order_probe(int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t count, int32_t *rows,
                                     int32_t *cols, cudaStream_t st);
 }  // namespace tgemm
+
+TGEMM_EXPORT tgemm_status tgemm_group_size(int64_t M, int64_t N, int64_t K, int bm, int unit_bn, int in_dtype,
+                                           int out_dtype, int resident, int *group_m)
+{
+    if (M < 1 || N < 1 || K < 1 || bm < 1 || unit_bn < 1 || resident < 1 || !group_m) return TGEMM_ERR_INVALID_ARG;
+    if (in_dtype < TGEMM_F16 || in_dtype > TGEMM_E5M2 || out_dtype < TGEMM_F16 || out_dtype > TGEMM_F32)
+        return TGEMM_ERR_INVALID_ARG;
+    *group_m = l2_group_m(M, N, K, bm, unit_bn, in_dtype, out_dtype, resident);
+    return TGEMM_OK;
+}
 
 TGEMM_EXPORT tgemm_status tgemm_stream_k_plan(int64_t items, int64_t k_blocks, int units, int tiles_per_item,
                                               int64_t *dp_items, int64_t *sk_items, int64_t *sk_units)

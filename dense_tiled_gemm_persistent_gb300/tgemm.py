@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 # Every symbol include/tgemm.h declares.
 EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
-           "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_stream_k_plan", "tgemm_run_noalloc",
+           "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_stream_k_plan", "tgemm_group_size",
+           "tgemm_run_noalloc",
            "tgemm_run_ex", "tgemm_run_strided_batched", "tgemm_debug_noalloc_wait_timeout",
            "tgemm_debug_sm_clock", "tgemm_debug_clock_record")
 
@@ -104,6 +105,8 @@ def load(path: str = LIB_PATH):
         lib.tgemm_stream_k_plan.argtypes = [_i64, _i64, _i, _i, ctypes.POINTER(_i64), ctypes.POINTER(_i64),
                                             ctypes.POINTER(_i64)]
         lib.tgemm_stream_k_plan.restype = _i
+        lib.tgemm_group_size.argtypes = [_i64, _i64, _i64, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]
+        lib.tgemm_group_size.restype = _i
         _lib = lib
         return lib
 
@@ -167,6 +170,13 @@ def tgemm_tile_coord(M, N, bm, bn, group_m, bid):
     r, c = _i64(), _i64()
     rc = load().tgemm_tile_coord(M, N, bm, bn, group_m, bid, ctypes.byref(r), ctypes.byref(c))
     return rc, r.value, c.value
+
+
+def tgemm_group_size(M, N, K, bm, unit_bn, in_dtype, out_dtype, resident):
+    """(status, group_m) the library picks for a single problem on the tile kernels."""
+    g = _i()
+    rc = load().tgemm_group_size(M, N, K, bm, unit_bn, in_dtype, out_dtype, resident, ctypes.byref(g))
+    return rc, g.value
 
 
 def tgemm_stream_k_plan(items, k_blocks, units, tiles_per_item=1):

@@ -224,6 +224,25 @@ tgemm_status tgemm_tile_coord(int64_t M, int64_t N, int bm, int bn, int group_m,
                               int64_t *bid_m, int64_t *bid_n);
 
 /*
+ * The group_m (bands of tile rows of the grouped order above) that an L2
+ * footprint model gives for a single problem on the tile kernels, exposed
+ * for host-side tests; no device is touched.  tgemm_run and
+ * tgemm_query_config use it in place of a default group of 8 when it is
+ * taller; a group the picker table measured stays.  bm x unit_bn is the
+ * unit the order deals out (a tile, or a quad's 256 x 512 block) and
+ * `resident` how many units run at once.  The tutorial's group of 8 is kept
+ * while A and B together fit in 96 MiB of L2 or a band of 8 rows holds fewer
+ * than two waves of units; otherwise the fewest bands of near-equal height
+ * whose A rows, two waves' B columns and one wave's C fit in 64 MiB, or the
+ * band with the smallest such footprint.  That section of the tutorial
+ * explains the order by L2 reuse; the sizes are this library's.  Returns
+ * TGEMM_ERR_INVALID_ARG for a size below 1, an unknown dtype or a NULL
+ * output.
+ */
+tgemm_status tgemm_group_size(int64_t M, int64_t N, int64_t K, int bm, int unit_bn, int in_dtype, int out_dtype,
+                              int resident, int *group_m);
+
+/*
  * The stream-K plan of a pair (tiles_per_item = 1) or quad (2: its 256 x 512
  * blocks) launch, exposed for host-side tests; no device is touched.  `items`
  * work items of `k_blocks` k-blocks each run on `units` resident CTA pairs or

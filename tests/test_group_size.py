@@ -1,0 +1,147 @@
+"""Host-side tests of the grouped order's band height (no GPU needed).
+
+tgemm_run and tgemm_query_config make a default GROUP_SIZE_M of 8 (the bands
+of tile rows of the grouped order of "Writing high-performance matrix
+multiplication with NVIDIA CUDA Tile", section "Performance optimisation:
+Swizzle") taller where an L2 footprint model asks for it: a band's A rows
+over K, the B columns of two waves of resident units and one wave's C tiles.
+These tests check the model (tgemm_group_size, the function both calls use)
+against that description by brute force over the candidate band heights, pin
+it on the measured workloads, and check that the calls keep a group the
+picker table measured.
+"""
+import itertools
+
+import pytest
+
+from dense_tiled_gemm_persistent_gb300 import build as libbuild
+from dense_tiled_gemm_persistent_gb300 import inputs as gen
+from dense_tiled_gemm_persistent_gb300 import tgemm
+
+MIB = 1024 * 1024
+BUDGET = 64 * MIB        # A band + two waves of B + one wave of C
+OPERANDS_FIT = 96 * MIB  # A and B together at most this: the tutorial's group of 8
+DEFAULT = 8
+ESIZE = {gen.F16: 2, gen.BF16: 2, gen.F32: 4, gen.E4M3: 1, gen.E5M2: 1}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    libbuild.build()
+    return tgemm.load()
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def expected(M, N, K, bm, ubn, ind, outd, resident):
+    """The band height the description above asks for, by enumeration."""
+    tm, tn = cdiv(M, bm), cdiv(N, ubn)
+    a_rows = bm * K * ESIZE[ind]                 # bytes of one tile row of A over K
+    b_cols = ubn * K * ESIZE[ind]                # bytes of one unit column of B over K
+    if tm * a_rows + tn * b_cols <= OPERANDS_FIT or DEFAULT * tn < 2 * resident:
+        return DEFAULT
+    # heights of near-equal bands, fewest bands first, each band holding at
+    # least two waves of units
+    heights = []
+    for nb in range(1, tm + 1):
+        h = cdiv(tm, nb)
+        if h * tn < 2 * resident:
+            break
+        if h not in heights:
+            heights.append(h)
+
+    def footprint(h):
+        return h * a_rows + 2 * min(tn, cdiv(resident, h)) * b_cols + resident * bm * ubn * ESIZE[outd]
+
+    fitting = [h for h in heights if footprint(h) <= BUDGET]
+    if fitting:
+        return fitting[0]
+    if not heights:
+        return DEFAULT
+    return min(heights, key=lambda h: (footprint(h), heights.index(h)))
+
+
+def pick(M, N, K, bm=256, ubn=256, ind=gen.F16, outd=gen.F16, resident=76):
+    rc, g = tgemm.tgemm_group_size(M, N, K, bm, ubn, ind, outd, resident)
+    assert rc == 0
+    return g
+
+
+# (M, N, K, bm, unit width, in, out, resident units) -> band height, on the
+# workloads whose DRAM bytes per launch were measured at several heights.
+PINNED = [
+    # 2.23x the algorithmic bytes at 8, 1.75x at 16, 1.97x at 24
+    ((16384, 14336, 4096, 256, 256, gen.BF16, gen.BF16, 76), 16),
+    # 1.37x at 16 (FP8 operands: half the bytes of a band)
+    ((8192, 8192, 8192, 256, 256, gen.E4M3, gen.BF16, 76), 16),
+    # no band fits: 2.87x at 8 and 10, 2.69x at 11, 2.56x at 12, 2.86x at 14;
+    # the model takes the smallest footprint, 11
+    ((8192, 8192, 8192, 256, 256, gen.F16, gen.F16, 76), 11),
+    # the quad's 256 x 512 blocks, 38 resident
+    ((8192, 8192, 8192, 256, 512, gen.F32, gen.F32, 38), 11),
+    # operands stay in L2 (DRAM bytes about the algorithmic ones at 8)
+    ((4000, 3000, 5000, 256, 512, gen.BF16, gen.BF16, 38), 8),
+    ((4096, 4096, 4096, 256, 256, gen.F16, gen.F16, 76), 8),
+    ((8192, 4864, 1024, 256, 256, gen.F16, gen.F16, 76), 8),
+    # a band of 8 rows is less than two waves: B is what the next wave re-reads
+    ((8192, 2048, 8192, 256, 256, gen.F16, gen.F16, 76), 8),
+]
+
+
+@pytest.mark.parametrize("args,want", PINNED, ids=["x".join(map(str, a[:3])) for a, _ in PINNED])
+def test_pinned_workloads(args, want):
+    assert pick(*args[:3], bm=args[3], ubn=args[4], ind=args[5], outd=args[6], resident=args[7]) == want
+    assert expected(*args) == want
+
+
+def test_matches_the_description_over_a_grid():
+    sizes = [256, 1000, 2048, 4096, 6144, 8192, 12288, 16384, 32768]
+    ks = [64, 1024, 4096, 8192, 16384]
+    n = 0
+    for M, N, K in itertools.product(sizes, sizes, ks):
+        for bm, ubn, res in ((256, 256, 76), (256, 512, 38), (128, 256, 152), (128, 128, 304)):
+            for ind, outd in ((gen.F16, gen.F16), (gen.E4M3, gen.BF16), (gen.F32, gen.F32)):
+                got = pick(M, N, K, bm, ubn, ind, outd, res)
+                assert got == expected(M, N, K, bm, ubn, ind, outd, res), (M, N, K, bm, ubn, ind, outd, res)
+                n += 1
+    assert n == len(sizes) ** 2 * len(ks) * 12
+
+
+def test_changed_heights_cover_two_waves_in_near_equal_bands():
+    for M, N, K in itertools.product([8192, 16384, 24576, 65536], [8192, 14336, 32768], [4096, 8192, 16384]):
+        tm, tn = cdiv(M, 256), cdiv(N, 256)
+        g = pick(M, N, K)
+        assert 1 <= g <= max(tm, DEFAULT)
+        if g != DEFAULT:
+            assert g * tn >= 2 * 76                      # a band spans at least two waves
+            assert g == cdiv(tm, cdiv(tm, g))            # the bands differ by at most one row
+
+
+def test_rejects_bad_arguments():
+    for args in ((0, 1, 1, 256, 256, gen.F16, gen.F16, 76), (1, 1, 0, 256, 256, gen.F16, gen.F16, 76),
+                 (1, 1, 1, 0, 256, gen.F16, gen.F16, 76), (1, 1, 1, 256, 256, 9, gen.F16, 76),
+                 (1, 1, 1, 256, 256, gen.F16, gen.E4M3, 76), (1, 1, 1, 256, 256, gen.F16, gen.F16, 0)):
+        assert tgemm.tgemm_group_size(*args)[0] == tgemm.ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_calls_keep_measured_groups_and_raise_default_ones():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cases = [
+        # the picker table measured group 16 (pair, whole tiles) at these grid points
+        ((16384, 14336, 4096, gen.B_NK, gen.BF16, gen.BF16), 16),
+        ((8192, 8192, 8192, gen.B_NK, gen.E4M3, gen.BF16), 16),
+        ((4096, 8192, 1024, gen.B_NK, gen.F16, gen.F16), 16),
+        # a default group of 8 made taller by the footprint model
+        ((8192, 8192, 8192, gen.B_NK, gen.F16, gen.F16), 11),
+        # operands that stay in L2 keep the default
+        ((4096, 4096, 4096, gen.B_KN, gen.F16, gen.F16), 8),
+    ]
+    for (M, N, K, layout, ind, outd), want in cases:
+        rc, cfg = tgemm.tgemm_query_config(M, N, K, layout, ind, outd)
+        assert rc == 0 and cfg.swap_ab == 0
+        assert cfg.group_m == want, (M, N, K, cfg)
