@@ -15,7 +15,7 @@ import oracle
 from dense_tiled_gemm_persistent_gb300 import inputs as gen
 from dense_tiled_gemm_persistent_gb300 import tgemm
 
-from gpu_util import assert_close, bits, ensure_built, sampled_points
+from gpu_util import assert_close, bits, ensure_built, operands, sampled_points
 
 pytestmark = pytest.mark.gpu
 
@@ -84,3 +84,22 @@ def test_config_sampled(name):
 def gpu_boundary_rows(M):
     from gpu_util import boundary_indices
     return boundary_indices(M, 128)
+
+
+def test_taller_band_sampled():
+    """16384 x 8192 x 8192 FP16: a shape whose default band of 8 tile rows the
+    L2 footprint model makes 13 rows tall (bands 13, 13, 13, 13, 12 of the 64
+    pair-tile rows), sampled against the oracle in tgemm_run's launch."""
+    M, N, K = 16384, 8192, 8192
+    rc, cfg = tgemm.tgemm_query_config(M, N, K, gen.B_NK, gen.F16, gen.F16)
+    assert rc == 0 and cfg.cluster_m == 2 and cfg.group_m == 13
+    a, b = operands(M, N, K, gen.F16, gen.B_NK, gen.uniform(-0.5, 0.5), seed=73)
+    A, B = a.to("cuda:0"), b.to("cuda:0")
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda:0")
+    rc = tgemm.tgemm_run(M, N, K, A.data_ptr(), a.shape[1], B.data_ptr(), b.shape[1], gen.B_NK, C.data_ptr(), N,
+                         gen.F16, gen.F16, None)
+    assert rc == 0 and tgemm.tgemm_check() == 0
+    ii, jj = sampled_points(M, N, seed=73)
+    got = C[torch.from_numpy(ii).to("cuda:0"), torch.from_numpy(jj).to("cuda:0")].double().cpu().numpy()
+    ref, bound = oracle.gemm_elements(a, b, M, N, K, a.shape[1], b.shape[1], gen.B_NK, gen.F16, ii, jj)
+    assert_close(got, ref, bound, gen.F16, "16384x8192x8192")
