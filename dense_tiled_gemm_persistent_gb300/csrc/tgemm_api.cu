@@ -1315,9 +1315,11 @@ TGEMM_EXPORT tgemm_status tgemm_run_strided_batched(int64_t batch, int64_t M, in
                     stream, cfg, ep, bt);
 }
 
-TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
-                                             tgemm_dtype in_dtype, tgemm_dtype out_dtype,
-                                             tgemm_config *out_cfg)
+namespace tgemm {
+namespace {
+
+tgemm_status query_args(int64_t M, int64_t N, int64_t K, int b_layout, int in_dtype, int out_dtype,
+                        const tgemm_config *out_cfg)
 {
     if (!out_cfg) return TGEMM_ERR_INVALID_ARG;
     if (b_layout != TGEMM_B_KN && b_layout != TGEMM_B_NK) return TGEMM_ERR_INVALID_ARG;
@@ -1326,16 +1328,46 @@ TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tg
     if (out_dtype != TGEMM_F16 && out_dtype != TGEMM_BF16 && out_dtype != TGEMM_F32)
         return TGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
-    DeviceState *dev = nullptr;
-    tgemm_status st = device_state(&dev);
+    return TGEMM_OK;
+}
+
+// The configuration tgemm_run chooses for a single problem with tightly
+// packed rows (lda = K, ldb = K for N x K or N for K x N) on a GPU with
+// sm_count SMs: the same steps as its own choice, in the same order.
+void auto_config(int64_t M, int64_t N, int64_t K, int b_layout, int in_dtype, int out_dtype, int sm_count,
+                 tgemm_config *cfg)
+{
+    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, pick_class(in_dtype), sm_count, cfg);
+    if (!swap_supported(in_dtype, cfg->swap_ab))
+        choose_config_model(M > 0 ? M : 1, N, K, sm_count, cfg, 1, false, pick_class(in_dtype));
+    prefer_quad_for_misaligned_rows(cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, sm_count);
+    l2_group_config(cfg, M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, in_dtype, out_dtype, sm_count);
+}
+
+}  // namespace
+}  // namespace tgemm
+
+TGEMM_EXPORT tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
+                                             tgemm_dtype in_dtype, tgemm_dtype out_dtype,
+                                             tgemm_config *out_cfg)
+{
+    tgemm_status st = query_args(M, N, K, b_layout, in_dtype, out_dtype, out_cfg);
     if (st != TGEMM_OK) return st;
-    choose_config(M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, b_layout, pick_class(in_dtype), dev->sm_count,
-                  out_cfg);
-    if (!swap_supported(in_dtype, out_cfg->swap_ab))
-        choose_config_model(M > 0 ? M : 1, N, K, dev->sm_count, out_cfg, 1, false, pick_class(in_dtype));
-    // tightly packed rows assumed: lda = K, ldb = K (N x K) or N (K x N)
-    prefer_quad_for_misaligned_rows(out_cfg, M, N, K, b_layout == TGEMM_B_KN ? N : K, in_dtype, dev->sm_count);
-    l2_group_config(out_cfg, M > 0 ? M : 1, N > 0 ? N : 1, K > 0 ? K : 1, in_dtype, out_dtype, dev->sm_count);
+    DeviceState *dev = nullptr;
+    st = device_state(&dev);
+    if (st != TGEMM_OK) return st;
+    auto_config(M, N, K, b_layout, in_dtype, out_dtype, dev->sm_count, out_cfg);
+    return TGEMM_OK;
+}
+
+TGEMM_EXPORT tgemm_status tgemm_query_config_sms(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
+                                                 tgemm_dtype in_dtype, tgemm_dtype out_dtype, int sm_count,
+                                                 tgemm_config *out_cfg)
+{
+    tgemm_status st = query_args(M, N, K, b_layout, in_dtype, out_dtype, out_cfg);
+    if (st != TGEMM_OK) return st;
+    if (sm_count < 1 || sm_count > 4096) return TGEMM_ERR_INVALID_ARG;
+    auto_config(M, N, K, b_layout, in_dtype, out_dtype, sm_count, out_cfg);
     return TGEMM_OK;
 }
 

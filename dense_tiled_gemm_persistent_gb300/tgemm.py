@@ -20,7 +20,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_OO
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libtgemm.so")
 
 # Every symbol include/tgemm.h declares.
-EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_run_config", "tgemm_check",
+EXPORTS = ("tgemm_run", "tgemm_query_config", "tgemm_query_config_sms", "tgemm_run_config", "tgemm_check",
            "tgemm_last_fault_code", "tgemm_status_string", "tgemm_shutdown", "tgemm_tile_coord",
            "tgemm_debug_wait_timeout", "tgemm_debug_tile_order", "tgemm_stream_k_plan", "tgemm_group_size",
            "tgemm_run_noalloc",
@@ -105,6 +105,8 @@ def load(path: str = LIB_PATH):
         lib.tgemm_stream_k_plan.argtypes = [_i64, _i64, _i, _i, ctypes.POINTER(_i64), ctypes.POINTER(_i64),
                                             ctypes.POINTER(_i64)]
         lib.tgemm_stream_k_plan.restype = _i
+        lib.tgemm_query_config_sms.argtypes = [_i64, _i64, _i64, _i, _i, _i, _i, ctypes.POINTER(Config)]
+        lib.tgemm_query_config_sms.restype = _i
         lib.tgemm_group_size.argtypes = [_i64, _i64, _i64, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]
         lib.tgemm_group_size.restype = _i
         _lib = lib
@@ -147,6 +149,13 @@ def tgemm_run_config(M, N, K, A, lda, B, ldb, b_layout, C, ldc, in_dtype, out_dt
 def tgemm_query_config(M, N, K, b_layout, in_dtype, out_dtype):
     cfg = Config()
     rc = load().tgemm_query_config(M, N, K, b_layout, in_dtype, out_dtype, ctypes.byref(cfg))
+    return rc, cfg
+
+
+def tgemm_query_config_sms(M, N, K, b_layout, in_dtype, out_dtype, sm_count):
+    """(status, Config) tgemm_run would choose on a GPU with sm_count SMs (no device touched)."""
+    cfg = Config()
+    rc = load().tgemm_query_config_sms(M, N, K, b_layout, in_dtype, out_dtype, sm_count, ctypes.byref(cfg))
     return rc, cfg
 
 

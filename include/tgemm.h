@@ -168,6 +168,18 @@ tgemm_status tgemm_query_config(int64_t M, int64_t N, int64_t K, tgemm_b_layout 
                                 tgemm_dtype in_dtype, tgemm_dtype out_dtype,
                                 tgemm_config *out_cfg);
 
+/* tgemm_query_config for a GPU with `sm_count` SMs given by the caller
+ * (1..4096), touching no device: for planning and host-side tests.  The
+ * choice assumes tightly packed rows (lda = K; ldb = K for TGEMM_B_NK, N for
+ * TGEMM_B_KN), as tgemm_query_config does; with the current device's SM
+ * count the two return the same configuration.  Returns
+ * TGEMM_ERR_INVALID_ARG or TGEMM_ERR_UNSUPPORTED for the arguments
+ * tgemm_query_config rejects, and TGEMM_ERR_INVALID_ARG for an SM count
+ * outside that range. */
+tgemm_status tgemm_query_config_sms(int64_t M, int64_t N, int64_t K, tgemm_b_layout b_layout,
+                                    tgemm_dtype in_dtype, tgemm_dtype out_dtype, int sm_count,
+                                    tgemm_config *out_cfg);
+
 /* tgemm_run with an explicit configuration, for tuning and tests: the
  * measurement side of the autotuning the pages describe (the Tile
  * programming model overview, section 7, times candidate tile shapes; the
