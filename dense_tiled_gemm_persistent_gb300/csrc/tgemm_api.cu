@@ -1001,10 +1001,11 @@ void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, in
 // 14, 4: the short last band reads B once more); 16384 x 14336 x 4096 BF16
 // 2.23x at 8, 1.75x at 16 and 1.97x at 24.  This footprint model with a
 // 64 MiB budget picks 16 there; for 8192^3 no band fits and the smallest
-// footprint, bands of 11, 11 and 10 rows, is taken.  The tutorial's group of 8 stays where A and B together are small
-// enough to stay in L2 (4000 x 3000 x 5000 reads about its algorithmic bytes
-// at group 8) and where a band of 8 rows holds less than two waves (there a
-// wave spans bands and B, not A, is what the next wave re-reads).
+// footprint, bands of 11, 11 and 10 rows, is taken.  The tutorial's group of
+// 8 stays where A and B together are small enough to stay in L2 (4000 x 3000
+// x 5000 reads about its algorithmic bytes at group 8) and where a band of 8
+// rows holds less than two waves (there a wave spans bands and B, not A, is
+// what the next wave re-reads).
 constexpr double kL2BandBudget = 64.0 * 1024 * 1024;
 constexpr double kL2OperandsFit = 96.0 * 1024 * 1024;
 
