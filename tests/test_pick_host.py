@@ -110,14 +110,12 @@ def test_sm_count_shapes_the_grid_not_the_tile_choice_on_the_table():
 
 
 def test_rejects_bad_arguments():
-    cfg = tgemm.Config()
     assert tgemm.tgemm_query_config_sms(64, 64, 64, gen.B_NK, gen.F16, gen.F16, 0)[0] == tgemm.ERR_INVALID_ARG
     assert tgemm.tgemm_query_config_sms(64, 64, 64, gen.B_NK, gen.F16, gen.F16, 5000)[0] == tgemm.ERR_INVALID_ARG
     assert tgemm.tgemm_query_config_sms(-1, 64, 64, gen.B_NK, gen.F16, gen.F16, 152)[0] == tgemm.ERR_INVALID_ARG
     assert tgemm.tgemm_query_config_sms(64, 64, 64, 7, gen.F16, gen.F16, 152)[0] == tgemm.ERR_INVALID_ARG
     assert tgemm.tgemm_query_config_sms(64, 64, 64, gen.B_KN, gen.E4M3, gen.F16, 152)[0] == tgemm.ERR_UNSUPPORTED
     assert tgemm.tgemm_query_config_sms(64, 64, 64, gen.B_NK, gen.F16, gen.E4M3, 152)[0] == tgemm.ERR_INVALID_ARG
-    del cfg
 
 
 @pytest.mark.gpu
