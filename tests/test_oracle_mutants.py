@@ -39,6 +39,13 @@ MUTANTS = {
     "tf32_keeps_low_bits": ("uint32_t t = u & 0xffffe000u;", "uint32_t t = u;"),
     "tf32_nine_fraction_bits": ("uint32_t t = u & 0xffffe000u;", "uint32_t t = u & 0xffffc000u;"),
     "tf32_read_as_16bit": ("if (p->esz == 4) return", "if (p->esz == 5) return"),
+    "alpha_dropped": ("double x = alpha * D[i * ldd + j];", "double x = D[i * ldd + j];"),
+    "relu_passes_magnitude": ("if (act == 1) return x > 0.0 ? x : 0.0;", "if (act == 1) return fabs(x);"),
+    "gelu_sqrt_pi_over_2": ("const double c = 0.7978845608028654;", "const double c = 1.2533141373155003;"),
+    "overflow_saturates": ("    if (r >= limit)\n        return sign_bit | (exp_all_ones << fbits);",
+                           "    if (r >= limit)\n        return sign_bit | (((exp_all_ones - 1u) << fbits) | ((1u << fbits) - 1u));"),
+    "subnormals_flushed": ("        uint32_t frac = (uint32_t)(r / ldexp(1.0, emin - fbits));\n        return sign_bit | frac;",
+                           "        uint32_t frac = 0u * (uint32_t)(r / ldexp(1.0, emin - fbits));\n        return sign_bit | frac;"),
 }
 
 
