@@ -44,6 +44,12 @@ MUTANTS = {
     "gelu_sqrt_pi_over_2": ("const double c = 0.7978845608028654;", "const double c = 1.2533141373155003;"),
     "overflow_saturates": ("    if (r >= limit)\n        return sign_bit | (exp_all_ones << fbits);",
                            "    if (r >= limit)\n        return sign_bit | (((exp_all_ones - 1u) << fbits) | ((1u << fbits) - 1u));"),
+    "fp32_accumulator": ("double s = 0.0, r = 0.0;", "float s = 0.0f; double r = 0.0;"),
+    "thread_shares_drop_a_row": ("w[t].last = first + total * (t + 1) / nt;",
+                                 "w[t].last = first + total * (t + 1) / nt - (t + 1 < nt);"),
+    "element_indices_swapped": ("dot(w->p, w->ii[t], w->jj[t], &w->out[t], &w->out_bound[t]);",
+                                "dot(w->p, w->jj[t], w->ii[t], &w->out[t], &w->out_bound[t]);"),
+    "row_range_offset_ignored": ("w->C[(i - w->row0) * w->ldc + j] = c;", "w->C[i * w->ldc + j] = c;"),
     "subnormals_flushed": ("        uint32_t frac = (uint32_t)(r / ldexp(1.0, emin - fbits));\n        return sign_bit | frac;",
                            "        uint32_t frac = 0u * (uint32_t)(r / ldexp(1.0, emin - fbits));\n        return sign_bit | frac;"),
 }
