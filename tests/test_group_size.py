@@ -53,7 +53,8 @@ def expected(M, N, K, bm, ubn, ind, outd, resident):
             heights.append(h)
 
     def footprint(h):
-        return h * a_rows + 2 * min(tn, cdiv(resident, h)) * b_cols + resident * bm * ubn * ESIZE[outd]
+        # the B columns of two waves, a wave spanning resident / h columns
+        return h * a_rows + 2 * min(tn, resident / h) * b_cols + resident * bm * ubn * ESIZE[outd]
 
     fitting = [h for h in heights if footprint(h) <= BUDGET]
     if fitting:
@@ -87,6 +88,10 @@ PINNED = [
     ((8192, 4864, 1024, 256, 256, gen.F16, gen.F16, 76), 8),
     # a band of 8 rows is less than two waves: B is what the next wave re-reads
     ((8192, 2048, 8192, 256, 256, gen.F16, gen.F16, 76), 8),
+    # 48 tile rows, no band fits: 12 (bands of 12); an LRU model of the
+    # schedule puts it at its best height for these shapes
+    ((12288, 12288, 8192, 256, 256, gen.F16, gen.F16, 76), 12),
+    ((12288, 16384, 16384, 256, 256, gen.F16, gen.F16, 76), 12),
 ]
 
 
