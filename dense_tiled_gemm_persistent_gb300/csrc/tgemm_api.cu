@@ -1002,7 +1002,8 @@ void prefer_quad_for_misaligned_rows(tgemm_config *cfg, int64_t M, int64_t N, in
 // 2.23x at 8, 1.75x at 16 and 1.97x at 24.  This footprint model with a
 // 64 MiB budget picks 16 there; for 8192^3 no band fits and the smallest
 // footprint, bands of 11, 11 and 10 rows, is taken.  An LRU model of the
-// schedule (a 64 MiB cache, each wave's pairs in lockstep over k) puts this
+// schedule (l2_schedule_model.py: a 64 MiB cache, each wave's pairs in
+// lockstep over k, which ranks the measured heights as ncu did) puts this
 // choice within 1 % of its best height in DRAM reads on 44 of 48 shapes
 // from 8192 to 24576 rows and columns and K 4096-16384, at most 4.6 % above
 // it (8192^3, where 12 is best), and above a group of 8 on two shapes, by at

@@ -150,3 +150,14 @@ def test_calls_keep_measured_groups_and_raise_default_ones():
         rc, cfg = tgemm.tgemm_query_config(M, N, K, layout, ind, outd)
         assert rc == 0 and cfg.swap_ab == 0
         assert cfg.group_m == want, (M, N, K, cfg)
+
+
+def test_lru_model_ranks_heights_as_measured_and_prefers_the_pick():
+    """The schedule model (l2_schedule_model) against the ncu-measured order
+    of band heights on 8192^3 FP16 (DRAM reads 1.01 / 0.94 / 0.885 / 1.006 GB
+    at groups 8 / 11 / 12 / 14), and the library's pick against a group of 8
+    in it."""
+    from dense_tiled_gemm_persistent_gb300 import l2_schedule_model as model
+    reads = {g: model.dram_read_bytes(8192, 8192, 8192, g) for g in (8, 11, 12, 14)}
+    assert reads[12] < reads[11] < reads[14] < reads[8]
+    assert pick(8192, 8192, 8192) == 11
